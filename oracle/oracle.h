@@ -1,0 +1,85 @@
+/*
+ * oracle.h -- plain, slow CPU reference for the W4A4 MXFP4 linear layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link,
+ * load or call this code; only the tests, the package smoke check and the
+ * benchmark's CPU-baseline leg use it.  It shares no code, header, table or
+ * constant generator with the CUDA library.
+ *
+ * Pages followed (cited by title and section):
+ *   [AMD]   "Efficiently Serving NVFP4 Models on AMD Instinct MI350X/MI355X
+ *            Accelerators via Online NVFP4 to Quark MXFP4 Requantization"
+ *   [OMNI]  "W4A4 MXFP4 Quantization" (vllm-omni user guide, mxfp4.md)
+ *   [SGL]   "[SGLang] FP4: 4-bit floating point quantization (NVIDIA NF4)"
+ *
+ * Every routine works element by element in the order the pages describe,
+ * with double precision wherever the pages do not fix a precision.  Scale
+ * factors are produced row-major ([rows][K/32]); the swizzled layout the
+ * tensor cores read is a separate index function (orc_sf_swizzled_offset).
+ *
+ * Parity status: every function here is pinned by the CPU tests except the
+ * UOS scale rule (orc_mx_shared_exp with alg = 2), which follows one reading
+ * of [OMNI] "Single-Scale Block Scaling (OCP / UOS)" and is parity unpinned
+ * beyond the two inequalities that reading implies.
+ */
+#ifndef FP4_ORACLE_H
+#define FP4_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- element codecs, from the bit definitions of each format ---------- */
+double orc_e2m1_value(unsigned code4);        /* 4-bit code -> value      */
+double orc_e4m3_value(unsigned byte);         /* float8_e4m3fn -> value   */
+double orc_e8m0_value(unsigned byte);         /* E8M0 -> 2^(b-127) or NaN */
+double orc_bf16_value(uint16_t bits);         /* bf16 -> value            */
+unsigned orc_e2m1_encode(double q);           /* nearest, ties to even code, saturating, sign copied */
+unsigned orc_e4m3_encode(float t);            /* t >= 0: nearest finite, ties to even code, saturating at 448 */
+
+/* ---- MX shared exponent ([OMNI] Single-Scale Block Scaling) ----------- */
+#define ORC_SCALE_OCP 0
+#define ORC_SCALE_UOS 2
+int orc_mx_shared_exp(double amax, int alg);  /* clamped to [-127, 127]   */
+
+/* One 32-element block -> 16 packed bytes + one E8M0 byte. */
+void orc_mx_quantize_block(const float v[32], int alg, uint8_t packed[16], uint8_t* sf);
+
+/* ---- the three hot-path computations (row-major scale output) --------- */
+/* NVFP4 decode: v = fp32((E2M1(c) * E4M3(s)) * g)  ([SGL] sections 3-4). */
+void orc_nvfp4_dequant(const uint8_t* w_packed, const uint8_t* w_scale, float g,
+                       int64_t rows, int64_t K, float* out);
+/* NVFP4 -> MXFP4 requantization ([AMD] online requantization pipeline).   */
+void orc_requant(const uint8_t* w_packed, const uint8_t* w_scale, float g,
+                 int64_t row0, int64_t row1, int64_t K, int alg,
+                 uint8_t* out_packed, uint8_t* out_sf);
+/* Dynamic MXFP4 quantization of bf16 activations ([AMD] serve-time path).  */
+void orc_act_quant(const uint16_t* x_bf16, int64_t row0, int64_t row1, int64_t K,
+                   int alg, uint8_t* out_packed, uint8_t* out_sf);
+
+/* W4A4 GEMM over dequantized MXFP4 operands, float64 accumulation.
+ * Computes ref[i][j] = sum_k A[rows[i]][k] * B[cols[j]][k] + bias[cols[j]]
+ * and absum[i][j] = sum_k |A*B| for the listed rows and columns. bias may be
+ * NULL.  sa / sb are row-major E8M0 ([rows][K/32]).                          */
+void orc_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+              const uint16_t* bias_bf16, int64_t K,
+              const int64_t* rows, int64_t n_rows, const int64_t* cols, int64_t n_cols,
+              double* ref, double* absum);
+
+/* ---- input preparation (NVFP4 producer used to build test inputs) ----- */
+float orc_nvfp4_global_scale(const uint16_t* x_bf16, int64_t n);   /* amax/(6*448) */
+void orc_nvfp4_quantize(const uint16_t* x_bf16, float g, int64_t row0, int64_t row1,
+                        int64_t K, uint8_t* out_packed, uint8_t* out_scale);
+
+/* ---- scale-factor layout the block-scaled MMA reads ------------------- */
+int64_t orc_sf_swizzled_bytes(int64_t rows, int64_t kblocks);
+int64_t orc_sf_swizzled_offset(int64_t r, int64_t c, int64_t kblocks);
+/* Scatter a row-major [rows][kblocks] scale array into the swizzled layout
+ * (pad bytes are zero). */
+void orc_sf_swizzle(const uint8_t* rowmajor, int64_t rows, int64_t kblocks, uint8_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

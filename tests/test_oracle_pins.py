@@ -1,0 +1,380 @@
+"""Pins for the CPU oracle: each test checks the oracle against something
+other than itself -- hand-derived worked examples (tests/golden), library
+codecs (torch's float8 types), closed forms, invariants and brute force.
+
+A plausible slip in the oracle (a swapped nibble order, a k/16 vs k/32 scale
+index, a wrong exponent offset, a transposed GEMM operand, a dropped bias)
+fails at least one test here.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import GOLDEN
+
+# ------------------------------------------------------------------ helpers
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+def _e2m1_table():
+    """code -> value from the hand-written fixture (independent of the oracle)."""
+    t = {}
+    for code, val in _golden_lines("e2m1_values.txt"):
+        t[int(code, 16)] = float(val)
+    return t
+
+
+def _hex_bytes(s):
+    return np.frombuffer(bytes.fromhex(s), dtype=np.uint8).copy()
+
+
+def _unpack(packed):
+    """packed u8 [..., K/2] -> 4-bit codes [..., K]; element 2j in the low nibble."""
+    lo = packed & 0xF
+    hi = packed >> 4
+    return np.stack([lo, hi], axis=-1).reshape(*packed.shape[:-1], -1)
+
+
+def _torch_e4m3(bytes_u8):
+    return torch.from_numpy(np.asarray(bytes_u8, np.uint8)).view(torch.float8_e4m3fn).float().numpy()
+
+
+# ------------------------------------------------------------------ codecs
+
+
+def test_e2m1_decode_matches_hand_table(orc):
+    table = _e2m1_table()
+    assert len(table) == 16
+    for code, val in table.items():
+        got = orc.e2m1_value(code)
+        assert got == val and math.copysign(1, got) == math.copysign(1, val), code
+    assert max(table.values()) == 6.0          # largest finite E2M1 value is 6
+
+
+def test_e4m3_decode_matches_torch(orc):
+    ref = _torch_e4m3(np.arange(256))
+    got = np.array([orc.e4m3_value(b) for b in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.nanmax(got) == 448.0
+
+
+def test_e8m0_decode_matches_torch(orc):
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).double().numpy()
+    got = np.array([orc.e8m0_value(b) for b in range(256)])
+    assert np.isnan(got[255]) and np.isnan(ref[255])
+    assert np.array_equal(got[:255], ref[:255])
+
+
+def test_bf16_decode_matches_torch(orc):
+    bits = np.array([0x0000, 0x8000, 0x3F80, 0xBF80, 0x0001, 0x0080, 0x7F7F, 0x7F80, 0x4049, 0x3E4D],
+                    dtype=np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    got = np.array([orc.bf16_value(int(b)) for b in bits])
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_encode_matches_torch(orc):
+    # every E4M3 magnitude, every midpoint between neighbours, and points just off them
+    vals = np.array(sorted({abs(v) for v in _torch_e4m3(np.arange(0x7F))}), dtype=np.float64)
+    mids = (vals[:-1] + vals[1:]) / 2
+    pts = np.concatenate([vals, mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+                          np.nextafter(mids.astype(np.float32), np.float32(1e9))])
+    pts = pts.astype(np.float32)
+    rng = np.random.default_rng(7)
+    pts = np.concatenate([pts, rng.uniform(0, 448, 5000).astype(np.float32),
+                          np.exp(rng.uniform(np.log(1e-4), np.log(448), 5000)).astype(np.float32)])
+    ref = torch.from_numpy(pts).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([orc.e4m3_encode(float(p)) for p in pts], dtype=np.uint8)
+    assert np.array_equal(got, ref)
+    # saturation beyond the largest finite value (0x7E = 448)
+    for t in (449.0, 464.0, 1000.0, 1e30):
+        assert orc.e4m3_encode(t) == 0x7E
+
+
+def test_e2m1_encode_matches_per_binade_rint(orc):
+    """Round to nearest, ties to even code, written as np.rint on each binade:
+    the E2M1 grid is uniform with step 0.5 on [0,2], 1 on [2,4], 2 on [4,6];
+    the even grid index is the even code."""
+    grid = np.unique(np.concatenate([np.arange(0, 8.0001, 1 / 64.0), [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]]))
+    qs = np.concatenate([grid, -grid])
+
+    def expect(q):
+        m = abs(q)
+        if m <= 2:
+            code = int(np.rint(m * 2))                   # codes 0..4 at step 0.5
+        elif m <= 4:
+            code = 4 + int(np.rint(m - 2))               # codes 4..6 at step 1
+        else:
+            code = 6 + int(min(np.rint((m - 4) / 2), 1))  # codes 6..7 at step 2, saturating
+        return (8 if math.copysign(1, q) < 0 else 0) | code
+
+    for q in qs:
+        assert orc.e2m1_encode(float(q)) == expect(float(q)), q
+    assert orc.e2m1_encode(-0.0) == 0x8
+
+
+# ------------------------------------------------------ shared exponent rule
+
+
+def _amax_samples():
+    rng = np.random.default_rng(11)
+    a = list(np.exp(rng.uniform(np.log(1e-38), np.log(1e38), 4000)))
+    for k in range(-120, 120, 7):
+        for m in (1.0, 1.8125, np.nextafter(1.8125, 2), 1.9999999, 1.5, np.nextafter(2.0, 0)):
+            a.append(m * 2.0 ** k)
+    return [float(np.float32(x)) for x in a if x > 0]
+
+
+def test_ocp_exponent_closed_form(orc):
+    # OCP MX: amax / 2^e lies in [4, 8) (E2M1's largest exponent is 2)
+    for amax in _amax_samples():
+        e = orc.mx_shared_exp(amax, orc.SCALE_OCP)
+        r = amax / 2.0 ** e
+        if e == -127:                                    # clamped at E8M0's smallest scale
+            assert r < 8.0 and math.floor(math.log2(amax)) - 2 <= -127, (amax, e)
+        else:
+            assert 4.0 <= r < 8.0, (amax, e)
+    assert orc.mx_shared_exp(0.0, orc.SCALE_OCP) == -127
+    assert orc.mx_shared_exp(2.0 ** -140, orc.SCALE_OCP) == -127      # clamped
+    assert orc.mx_shared_exp(float(np.finfo(np.float32).max), orc.SCALE_OCP) == 125
+
+
+def test_uos_exponent_reading(orc):
+    # UOS (Qmax = 7.25), reading: smallest e with amax <= 7.25 * 2^e
+    for amax in _amax_samples():
+        e = orc.mx_shared_exp(amax, orc.SCALE_UOS)
+        assert amax <= 7.25 * 2.0 ** e, (amax, e)
+        assert e == -127 or amax > 7.25 * 2.0 ** (e - 1), (amax, e)
+    assert orc.mx_shared_exp(7.25, orc.SCALE_UOS) == 0       # the boundary itself keeps the smaller e
+    assert orc.mx_shared_exp(float(np.nextafter(np.float32(7.25), np.float32(8))), orc.SCALE_UOS) == 1
+
+
+# ------------------------------------------------------ worked examples
+
+
+@pytest.mark.parametrize("row", _golden_lines("requant_examples.txt"), ids=lambda r: r[0])
+def test_requant_worked_examples(orc, row):
+    name, g_hex, codes, scales, ocp_sf, ocp_codes, uos_sf, uos_codes = row
+    g = float(np.frombuffer(bytes.fromhex(g_hex)[::-1], dtype=np.float32)[0])
+    packed = _hex_bytes(codes).reshape(1, 16)
+    sc = _hex_bytes(scales).reshape(1, 2)
+    for alg, sf, out in ((orc.SCALE_OCP, ocp_sf, ocp_codes), (orc.SCALE_UOS, uos_sf, uos_codes)):
+        p, s = orc.requant(packed, sc, g, alg)
+        assert s[0, 0] == int(sf, 16), (name, alg)
+        assert p.tobytes().hex() == out, (name, alg)
+
+
+@pytest.mark.parametrize("row", _golden_lines("act_quant_examples.txt"), ids=lambda r: r[0])
+def test_act_quant_worked_examples(orc, row):
+    name, xs, ocp_sf, ocp_codes, uos_sf, uos_codes = row
+    x = np.array([int(h, 16) for h in xs.split(",")], np.uint16).reshape(1, 32)
+    for alg, sf, out in ((orc.SCALE_OCP, ocp_sf, ocp_codes), (orc.SCALE_UOS, uos_sf, uos_codes)):
+        p, s = orc.act_quant(x, alg)
+        assert s[0, 0] == int(sf, 16), (name, alg)
+        assert p.tobytes().hex() == out, (name, alg)
+
+
+# ------------------------------------------------------ NVFP4 decode
+
+
+def test_nvfp4_dequant_matches_float32_products(orc):
+    """v = fp32((E2M1(c) * E4M3(s)) * g): checked with numpy float32 products
+    over the hand E2M1 table and torch's E4M3 decode, per-16 scale index."""
+    rng = np.random.default_rng(3)
+    N, K = 5, 96
+    packed = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scale = rng.integers(0, 0x7F, (N, K // 16), dtype=np.uint8)       # finite, positive
+    scale[0, 1] |= 0x80                                                  # one negative scale
+    table = _e2m1_table()
+    codes = _unpack(packed)
+    cval = np.vectorize(lambda c: table[int(c)])(codes).astype(np.float32)
+    sval = _torch_e4m3(scale).astype(np.float32)
+    for g in (1.0, 0.0001234, 3.7e-3, 2.0 ** -20):
+        g32 = np.float32(g)
+        expect = (cval * np.repeat(sval, 16, axis=1)) * g32
+        got = orc.nvfp4_dequant(packed, scale, float(g32))
+        assert np.array_equal(got.view(np.uint32), expect.astype(np.float32).view(np.uint32))
+
+
+# ------------------------------------------------------ invariants
+
+
+def _rand_roundtrip_case(orc, rng, g_log2, k):
+    """An NVFP4 block with both half-scales times g equal to 2^k and largest
+    magnitude code 6 or 7: requant must return the same codes bit for bit."""
+    s_log2 = k - g_log2
+    s_byte = (s_log2 + 7) << 3                                          # E4M3 power of two (normal)
+    codes = rng.integers(0, 16, 32)
+    codes[rng.integers(0, 32)] = rng.choice([6, 7, 14, 15])
+    codes = np.where((codes & 7) == 7, codes - 1, codes) if rng.random() < 0.5 else codes
+    if not np.any((codes & 7) >= 6):
+        codes[0] = 6
+    packed = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8).reshape(1, 16)
+    scale = np.array([[s_byte, s_byte]], np.uint8)
+    return packed, scale, float(2.0 ** g_log2)
+
+
+def test_roundtrip_bit_identical(orc):
+    rng = np.random.default_rng(5)
+    n = 0
+    for g_log2 in (-12, -3, 0, 4):
+        for k in range(g_log2 - 6, g_log2 + 8):
+            s_log2 = k - g_log2
+            if not -6 <= s_log2 <= 8:
+                continue
+            for _ in range(8):
+                packed, scale, g = _rand_roundtrip_case(orc, rng, g_log2, k)
+                for alg in (orc.SCALE_OCP, orc.SCALE_UOS):
+                    p, s = orc.requant(packed, scale, g, alg)
+                    assert np.array_equal(p, packed) and s[0, 0] == k + 127, (g_log2, k, alg)
+                n += 1
+    assert n > 100
+
+
+def test_emitted_codes_are_nearest(orc):
+    """Brute force over all 16 codes: each emitted element is a nearest
+    representable value under its block scale (ties to the even code)."""
+    rng = np.random.default_rng(9)
+    table = _e2m1_table()
+    grid = np.array([table[c] for c in range(16)])
+    for trial in range(300):
+        v = (rng.standard_normal(32) * 10.0 ** rng.uniform(-6, 6)).astype(np.float32)
+        if trial % 3 == 0:
+            v[rng.integers(0, 32, 4)] *= 16
+        for alg in (orc.SCALE_OCP, orc.SCALE_UOS):
+            packed, sf = orc.mx_quantize_block(v, alg)
+            scale = 2.0 ** (sf - 127)
+            codes = _unpack(packed.reshape(1, 16))[0]
+            for x, c in zip(v.astype(np.float64), codes):
+                d = np.abs(grid * scale - x)
+                best = d.min()
+                assert d[c] == best, (x, c)
+                ties = np.nonzero(d == best)[0]
+                if len({abs(grid[t]) for t in ties}) > 1:     # a real tie between magnitudes
+                    assert (c & 7) % 2 == 0
+
+
+def test_requant_error_bound(orc):
+    """|dq_mx - v| is at most half the local E2M1 step times 2^e, or the
+    saturation error for |q| > 6."""
+    rng = np.random.default_rng(13)
+    N, K = 16, 256
+    packed = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scale = rng.integers(0x20, 0x7E, (N, K // 16), dtype=np.uint8)
+    g = 0.0037
+    v = orc.nvfp4_dequant(packed, scale, g).astype(np.float64)
+    p, s = orc.requant(packed, scale, g)
+    table = _e2m1_table()
+    dq = np.vectorize(lambda c: table[int(c)])(_unpack(p)) * np.repeat(2.0 ** (s.astype(np.float64) - 127), 32, axis=1)
+    e = np.repeat(s.astype(np.float64) - 127, 32, axis=1)
+    q = np.abs(v) / 2.0 ** e
+    half_step = np.where(q <= 2, 0.25, np.where(q <= 4, 0.5, 1.0)) * 2.0 ** e
+    sat = np.maximum(q - 6.0, 0) * 2.0 ** e
+    assert np.all(np.abs(dq - v) <= np.maximum(half_step, sat))
+
+
+# ------------------------------------------------------ GEMM
+
+
+def _dequant_indep(packed, sf_rowmajor):
+    table = _e2m1_table()
+    codes = _unpack(packed)
+    vals = np.vectorize(lambda c: table[int(c)])(codes)
+    return vals * np.repeat(2.0 ** (sf_rowmajor.astype(np.float64) - 127), 32, axis=1)
+
+
+def test_gemm_matches_numpy_matmul(orc):
+    rng = np.random.default_rng(17)
+    M, N, K = 7, 13, 160
+    a = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = rng.integers(110, 140, (M, K // 32), dtype=np.uint8)
+    sb = rng.integers(110, 140, (N, K // 32), dtype=np.uint8)
+    bias = torch.randn(N).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    A = _dequant_indep(a, sa)
+    B = _dequant_indep(b, sb)
+    bias_f = torch.from_numpy(bias.view(np.int16)).view(torch.bfloat16).double().numpy()
+    expect = A @ B.T + bias_f
+    ref, absum = orc.gemm(a, sa, b, sb, bias)
+    assert np.allclose(ref, expect, rtol=1e-12, atol=1e-12 * np.abs(A) @ np.abs(B).T + 1e-300)
+    assert np.allclose(absum, np.abs(A) @ np.abs(B).T, rtol=1e-12)
+    # a row/column subset gives the same entries
+    rows, cols = np.array([5, 0, 3]), np.array([12, 1])
+    r2, _ = orc.gemm(a, sa, b, sb, bias, rows=rows, cols=cols)
+    assert np.array_equal(r2, ref[np.ix_(rows, cols)])
+
+
+def test_gemm_one_hot_selects_columns(orc):
+    """B rows one-hot with code 1.0 under scale 2^0: out[:, n] = A[:, sel[n]] exactly."""
+    rng = np.random.default_rng(19)
+    M, N, K = 6, 10, 128
+    a = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    sa = rng.integers(120, 135, (M, K // 32), dtype=np.uint8)
+    sel = rng.integers(0, K, N)
+    codes = np.zeros((N, K), np.uint8)
+    codes[np.arange(N), sel] = 0x2
+    b = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    sb = np.full((N, K // 32), 127, np.uint8)
+    ref, _ = orc.gemm(a, sa, b, sb)
+    A = _dequant_indep(a, sa)
+    assert np.array_equal(ref, A[:, sel])
+
+
+# ------------------------------------------------------ SF layout
+
+
+def test_sf_swizzle_hand_offsets(orc):
+    rows = _golden_lines("sf_swizzle_offsets.txt")
+    assert orc.sf_swizzled_bytes(200, 6) == 2048
+    for r, c, off in rows:
+        assert orc.sf_swizzled_offset(int(r), int(c), 6) == int(off)
+
+
+def test_sf_swizzle_is_injective_and_pads_zero(orc):
+    for rows, kb in ((200, 6), (128, 4), (1, 1), (300, 224)):
+        rm = np.arange(rows * kb, dtype=np.int64).reshape(rows, kb)
+        offs = {orc.sf_swizzled_offset(r, c, kb) for r in range(rows) for c in range(kb)}
+        assert len(offs) == rows * kb
+        assert max(offs) < orc.sf_swizzled_bytes(rows, kb)
+    rm = (np.arange(200 * 6) % 251 + 1).astype(np.uint8).reshape(200, 6)
+    sw = orc.sf_swizzle(rm)
+    assert np.count_nonzero(sw) == 200 * 6
+
+
+# ------------------------------------------------------ NVFP4 producer
+
+
+def test_nvfp4_quantize_against_float32_recipe(orc):
+    """Block scale = torch's E4M3 rounding of fp32(bamax / fp32(6 g)); codes
+    are nearest E2M1 values of fp32(x / fp32(scale * g)); dequantization error
+    within half a grid step."""
+    rng = np.random.default_rng(23)
+    N, K = 9, 128
+    x = torch.from_numpy(rng.standard_normal((N, K)).astype(np.float32) * 0.02).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    xf = x.float().numpy()
+    g = orc.nvfp4_global_scale(bits)
+    assert np.float32(g) == np.float32(np.abs(xf).max()) / np.float32(2688.0)
+    p, s = orc.nvfp4_quantize(bits, g)
+    bamax = np.abs(xf).reshape(N, K // 16, 16).max(-1).astype(np.float32)
+    t = bamax / (np.float32(6.0) * np.float32(g))
+    s_ref = torch.from_numpy(t.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(s, s_ref)
+    den = (_torch_e4m3(s).astype(np.float32) * np.float32(g)).astype(np.float32)
+    q = (xf.reshape(N, K // 16, 16) / den[..., None]).astype(np.float32).reshape(N, K)
+    table = _e2m1_table()
+    grid = np.array([table[c] for c in range(8)])
+    codes = _unpack(p)
+    dq = np.vectorize(lambda c: table[int(c)])(codes)
+    err = np.abs(dq - q)
+    nearest = np.min(np.abs(grid[None, None, :] - np.abs(q)[..., None]), axis=-1)
+    assert np.all(err <= nearest + 1e-12)
