@@ -1,0 +1,209 @@
+/*
+ * fp4lin.h -- C ABI of libfp4lin, the W4A4 MXFP4 linear layer on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer has three parts, all on the GPU:
+ *   1. load-time NVFP4 -> MXFP4 weight requantization,
+ *   2. dynamic per-batch MXFP4 quantization of bf16 activations,
+ *   3. the block-scaled FP4 GEMM over two MXFP4 operands with a bf16
+ *      (+ optional bf16 bias) epilogue, dense and grouped (MoE).
+ *
+ * Pages that define the operations (cited by title and section):
+ *   [AMD]  "Efficiently Serving NVFP4 Models on AMD Instinct MI350X/MI355X
+ *           Accelerators via Online NVFP4 to Quark MXFP4 Requantization"
+ *   [OMNI] "W4A4 MXFP4 Quantization" (vllm-omni user guide)
+ *   [SGL]  "[SGLang] FP4: 4-bit floating point quantization (NVIDIA NF4)"
+ *
+ * Conventions for every call
+ *   - Pointers are DEVICE pointers unless the comment says "host".  The
+ *     caller owns every buffer; the library allocates no device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; no call synchronizes.
+ *   - Argument checks (null pointers, shapes, alignment, device support)
+ *     run on the host before any launch and return an error status with
+ *     nothing enqueued.  A failed launch returns FP4_ERR_CUDA.
+ *   - Device-side waits are bounded.  A wait that gives up records
+ *     FP4_ERR_TIMEOUT in a library-owned device status word, which
+ *     fp4_get_device_status() reads (that call synchronizes the device).
+ *   - Packed FP4 tensors: two E2M1 codes per byte, K-contiguous, element 2j
+ *     of a row in the low nibble of byte j, element 2j+1 in the high nibble.
+ *   - MXFP4 scale factors are E8M0 bytes (2^(b-127), 0xFF = NaN), one per
+ *     32 consecutive K-elements ([OMNI] Overview).  They come in two
+ *     layouts:
+ *       FP4_SF_ROWMAJOR  [rows][K/32] bytes, as checkpoints store them
+ *                        ([OMNI] "Pre-Quantized Single-Scale Weights").
+ *       FP4_SF_SWIZZLED  the layout the block-scaled tensor-core MMA reads:
+ *                        rows padded to 128, K/32 padded to 4; byte of
+ *                        (row r, block c) at
+ *                        ((r/128)*ceil(Kb/4) + c/4)*512 + (r%32)*16
+ *                          + ((r%128)/32)*4 + c%4,      Kb = K/32.
+ *                        Pad bytes are written as 0.
+ *     fp4_sf_bytes() gives the size of either layout.
+ */
+#ifndef FP4LIN_H
+#define FP4LIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP4LIN_API __attribute__((visibility("default")))
+#else
+#define FP4LIN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP4_OK = 0,
+    FP4_ERR_INVALID_ARG = 1,   /* null pointer, bad enum value            */
+    FP4_ERR_SHAPE = 2,         /* dimension not allowed for this call     */
+    FP4_ERR_ALIGNMENT = 3,     /* pointer not aligned as required         */
+    FP4_ERR_UNSUPPORTED = 4,   /* device is not compute capability 10.3  */
+    FP4_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed    */
+    FP4_ERR_TIMEOUT = 6        /* a bounded device wait expired           */
+} fp4_status;
+
+/* Block scaling rule ([OMNI] "Single-Scale Block Scaling (OCP / UOS)",
+ * same numbering as the page's mxfp4_scale_alg setting).
+ *   OCP: shared exponent e = floor(log2(amax)) - 2.
+ *   UOS: e = the smallest integer with amax <= 7.25 * 2^e; elements still
+ *        saturate at 6.  (The page gives only the 7.25 boundary; this is
+ *        the reading the library implements.)                              */
+typedef enum { FP4_SCALE_OCP = 0, FP4_SCALE_UOS = 2 } fp4_scale_alg;
+
+typedef enum { FP4_SF_SWIZZLED = 0, FP4_SF_ROWMAJOR = 1 } fp4_sf_layout;
+
+/* Options for the quantizers.  A NULL pointer means {OCP, SWIZZLED}. */
+typedef struct {
+    int32_t scale_alg;   /* fp4_scale_alg */
+    int32_t sf_layout;   /* fp4_sf_layout */
+} fp4_quant_opts;
+
+/* ------------------------------------------------------------------ sizes */
+
+/* Bytes of an E8M0 scale array for `rows` x K elements in the given layout
+ * (K must be a multiple of 32; returns 0 otherwise).                      */
+FP4LIN_API size_t fp4_sf_bytes(int64_t rows, int64_t K, int32_t sf_layout);
+
+/* Upper bound on the swizzled scale bytes of a grouped activation tensor
+ * of total_M rows split into E groups (each group padded to 128 rows).    */
+FP4LIN_API size_t fp4_sf_bytes_grouped(int64_t total_M, int32_t E, int64_t K);
+
+/* Human-readable name of a status code (static string). */
+FP4LIN_API const char* fp4_status_string(fp4_status s);
+
+/* Reads and clears the device status word on the current device after a
+ * device synchronize.  Returns FP4_OK or FP4_ERR_TIMEOUT (or FP4_ERR_CUDA
+ * if the synchronize itself failed).  For tests and diagnostics.           */
+FP4LIN_API fp4_status fp4_get_device_status(void);
+
+/* ------------------------------------------------------- requantization */
+
+/* NVFP4 -> MXFP4 weight requantization ([AMD] online requantization
+ * pipeline: run once per layer at load; the dequantized intermediate never
+ * leaves registers, the result goes straight into a preallocated
+ * destination).  NVFP4 layout per [SGL] sections 3-4.
+ *
+ *   w_packed      [N, K/2] u8    NVFP4 codes (device)
+ *   w_scale_e4m3  [N, K/16] u8   float8_e4m3fn block scales (device)
+ *   w_global      f32, by value  per-tensor scale; MULTIPLIES the decoded
+ *                                values (a loader holding the divisor form
+ *                                passes its reciprocal)
+ *   out_packed    [N, K/2] u8    MXFP4 codes (device, caller-allocated)
+ *   out_scale     E8M0 bytes     fp4_sf_bytes(N, K, layout) (device)
+ *
+ * Decoding: v = fp32((E2M1(c) * E4M3(s)) * w_global) (one rounding).
+ * Encoding per 32-block: amax, shared exponent by the chosen rule clamped
+ * to [-127, 127], codes = nearest E2M1 of v / 2^e with ties to the even
+ * code, saturating at +-6, sign always kept (-0 -> 0x8).  A block holding
+ * NaN or Inf gets scale byte 0xFF and zero codes.
+ * Requires N >= 1, K a positive multiple of 32, 16-byte aligned packed
+ * pointers.  Outputs must not overlap inputs.
+ * fp4_requant_nvfp4_to_mxfp4 uses {OCP, SWIZZLED}.                        */
+FP4LIN_API fp4_status fp4_requant_nvfp4_to_mxfp4(const uint8_t* w_packed, const uint8_t* w_scale_e4m3,
+                                      float w_global, uint8_t* out_packed, uint8_t* out_scale,
+                                      int64_t N, int64_t K, void* stream);
+FP4LIN_API fp4_status fp4_requant_nvfp4_to_mxfp4_ex(const uint8_t* w_packed, const uint8_t* w_scale_e4m3,
+                                         float w_global, uint8_t* out_packed, uint8_t* out_scale,
+                                         int64_t N, int64_t K, const fp4_quant_opts* opts,
+                                         void* stream);
+
+/* ------------------------------------------------- activation quantizer */
+
+/* Dynamic MXFP4 quantization of bf16 activations ([AMD] serve-time path:
+ * the activation scales are computed for every batch; none are stored or
+ * calibrated).  Same block rule as the requantization.
+ *   x_bf16     [M, K] bf16 (device, 16-byte aligned)
+ *   out_packed [M, K/2] u8; out_scale fp4_sf_bytes(M, K, layout) bytes.
+ * Requires M >= 0 (M = 0 is a no-op), K a positive multiple of 32.          */
+FP4LIN_API fp4_status fp4_quant_act_mxfp4(const void* x_bf16, uint8_t* out_packed, uint8_t* out_scale,
+                               int64_t M, int64_t K, const fp4_quant_opts* opts, void* stream);
+
+/* Grouped variant for MoE: rows [row_offsets[e], row_offsets[e+1]) belong
+ * to group e.  Scales are always SWIZZLED; group e's scale rows start at
+ * sum_{j<e} ceil(rows_j/128)*128, so every group begins on a 128-row tile.
+ *   row_offsets  [E+1] int32 (device), non-decreasing, row_offsets[0] = 0,
+ *                row_offsets[E] = total_M
+ *   out_scale    fp4_sf_bytes_grouped(total_M, E, K) bytes (device)
+ * Only the scale-row tiles a group uses are written (pad rows as 0).       */
+FP4LIN_API fp4_status fp4_quant_act_mxfp4_grouped(const void* x_bf16, const int32_t* row_offsets, int32_t E,
+                                       int64_t total_M, int64_t K, uint8_t* out_packed,
+                                       uint8_t* out_scale, const fp4_quant_opts* opts,
+                                       void* stream);
+
+/* ----------------------------------------------------------- NVFP4 producer */
+
+/* bf16 -> NVFP4 with a caller-given global scale g (the NVFP4 quantize
+ * step of [SGL] section 6, used to build NVFP4 weights from bf16).  Per
+ * 16-element block, in float32, one IEEE operation at a time:
+ *   s = E4M3_rne_satfinite(bamax / (6*g)); den = E4M3(s) * g;
+ *   code_i = E2M1 nearest of x_i / den (ties to even, saturating),
+ * signed-zero codes where den is 0 or NaN.  The usual g is
+ * amax(x) / (6 * 448), computed by the caller.
+ *   out_packed [M, K/2] u8, out_scale_e4m3 [M, K/16] u8 (row-major).
+ * Requires K a positive multiple of 16 and 16-byte aligned pointers.       */
+FP4LIN_API fp4_status fp4_quant_nvfp4(const void* x_bf16, float g, uint8_t* out_packed,
+                           uint8_t* out_scale_e4m3, int64_t M, int64_t K, void* stream);
+
+/* ------------------------------------------------------------------ GEMM */
+
+/* W4A4 GEMM on block-scaled FP4 tensor cores ([AMD] "Native FP4 matmul":
+ * both operands MXFP4; [OMNI] Configuration: bf16 output with a bf16
+ * per-output-channel bias; [SGL] section 6: bias added to the output):
+ *   out[m, n] = bf16_rne( sum_k A[m,k] * B[n,k] + bias[n] )
+ * with fp32 accumulation.
+ *   a     [M, K/2] u8, sa = SWIZZLED scales of A (fp4_sf_bytes(M, K, 0))
+ *   b     [N, K/2] u8, sb = SWIZZLED scales of B (fp4_sf_bytes(N, K, 0))
+ *   bias  [N] bf16 or NULL
+ *   out   [M, N] bf16, row-major
+ * Requires K a positive multiple of 128, N a positive multiple of 8,
+ * M >= 0 (M = 0 is a no-op), 16-byte aligned a, b, out, sa, sb.            */
+FP4LIN_API fp4_status fp4_gemm_mxfp4(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                          const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K,
+                          void* stream);
+
+/* Grouped (MoE) W4A4 GEMM ([AMD] "Native FP4 matmul": MoE experts on
+ * MXFP4): for every expert e and every row m in [row_offsets[e],
+ * row_offsets[e+1]):  out[m, :] = A[m, :] . B_e^T (+ bias_e).
+ *   a            [total_M, K/2] u8, rows grouped by expert
+ *   sa           grouped SWIZZLED scales as written by
+ *                fp4_quant_act_mxfp4_grouped
+ *   b            [E][N][K/2] u8; sb: E consecutive SWIZZLED arrays of
+ *                fp4_sf_bytes(N, K, 0) bytes each
+ *   bias         [E][N] bf16 or NULL
+ *   row_offsets  [E+1] int32 (device); the tile walk is derived on the
+ *                device, so no host synchronization is needed
+ *   out          [total_M, N] bf16
+ * Same shape and alignment rules as fp4_gemm_mxfp4.                        */
+FP4LIN_API fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
+                                  const uint8_t* sb, const void* bias_bf16, void* out_bf16,
+                                  const int32_t* row_offsets, int32_t E, int64_t total_M,
+                                  int64_t N, int64_t K, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP4LIN_H */

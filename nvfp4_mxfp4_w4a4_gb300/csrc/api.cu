@@ -1,0 +1,279 @@
+// api.cu -- the extern "C" boundary of libfp4lin.  Validates arguments on
+// the host, then enqueues the kernels on the caller's stream.  No call
+// allocates device memory and none synchronizes (except
+// fp4_get_device_status, which exists to read the device status word).
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/fp4lin.h"
+#include "internal.h"
+
+namespace {
+
+// Library-owned device status word: kernels OR flags into it when a
+// bounded wait gives up.  One copy per device that loads the library.
+__device__ unsigned int g_fp4_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool checked = false;
+    bool supported = false;
+    unsigned int* status = nullptr;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+// Resolves the current device's support and status-word address (once).
+fp4_status current_device(unsigned int** status)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return FP4_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.checked) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FP4_ERR_CUDA;
+        // The kernels are built for sm_103a only.
+        d.supported = (major == 10 && minor == 3);
+        if (d.supported) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_fp4_device_status) != cudaSuccess)
+                return FP4_ERR_CUDA;
+            d.status = static_cast<unsigned int*>(p);
+        }
+        d.checked = true;
+    }
+    if (!d.supported)
+        return FP4_ERR_UNSUPPORTED;
+    if (status)
+        *status = d.status;
+    return FP4_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline fp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP4_OK : FP4_ERR_CUDA; }
+
+fp4_status check_opts(const fp4_quant_opts* opts, int* alg, int* swizzled)
+{
+    *alg = FP4_SCALE_OCP;
+    *swizzled = 1;
+    if (!opts)
+        return FP4_OK;
+    if (opts->scale_alg != FP4_SCALE_OCP && opts->scale_alg != FP4_SCALE_UOS)
+        return FP4_ERR_INVALID_ARG;
+    if (opts->sf_layout != FP4_SF_SWIZZLED && opts->sf_layout != FP4_SF_ROWMAJOR)
+        return FP4_ERR_INVALID_ARG;
+    *alg = opts->scale_alg;
+    *swizzled = opts->sf_layout == FP4_SF_SWIZZLED ? 1 : 0;
+    return FP4_OK;
+}
+
+constexpr int64_t kMaxDim = int64_t(1) << 31;
+
+}  // namespace
+
+extern "C" {
+
+size_t fp4_sf_bytes(int64_t rows, int64_t K, int32_t sf_layout)
+{
+    if (rows < 0 || K <= 0 || K % 32 != 0)
+        return 0;
+    const int64_t kb = K / 32;
+    if (sf_layout == FP4_SF_ROWMAJOR)
+        return static_cast<size_t>(rows * kb);
+    return static_cast<size_t>(((rows + 127) / 128) * 128 * ((kb + 3) / 4) * 4);
+}
+
+size_t fp4_sf_bytes_grouped(int64_t total_M, int32_t E, int64_t K)
+{
+    if (total_M < 0 || E <= 0 || K <= 0 || K % 32 != 0)
+        return 0;
+    const int64_t tiles = (total_M + static_cast<int64_t>(E) * 127) / 128;
+    return static_cast<size_t>(tiles * 128 * ((K / 32 + 3) / 4) * 4);
+}
+
+const char* fp4_status_string(fp4_status s)
+{
+    switch (s) {
+    case FP4_OK: return "FP4_OK";
+    case FP4_ERR_INVALID_ARG: return "FP4_ERR_INVALID_ARG: null pointer or invalid option";
+    case FP4_ERR_SHAPE: return "FP4_ERR_SHAPE: dimension not supported by this call";
+    case FP4_ERR_ALIGNMENT: return "FP4_ERR_ALIGNMENT: pointer not 16-byte aligned";
+    case FP4_ERR_UNSUPPORTED: return "FP4_ERR_UNSUPPORTED: device is not sm_103";
+    case FP4_ERR_CUDA: return "FP4_ERR_CUDA: CUDA runtime call or launch failed";
+    case FP4_ERR_TIMEOUT: return "FP4_ERR_TIMEOUT: a bounded device wait expired";
+    }
+    return "FP4_ERR_UNKNOWN";
+}
+
+fp4_status fp4_get_device_status(void)
+{
+    unsigned int* status = nullptr;
+    fp4_status st = current_device(&status);
+    if (st != FP4_OK)
+        return st;
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        return FP4_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_fp4_device_status, sizeof v) != cudaSuccess)
+        return FP4_ERR_CUDA;
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_fp4_device_status, &zero, sizeof zero) != cudaSuccess)
+        return FP4_ERR_CUDA;
+    return (v & fp4lin::kStatusTimeout) ? FP4_ERR_TIMEOUT : FP4_OK;
+}
+
+fp4_status fp4_requant_nvfp4_to_mxfp4_ex(const uint8_t* w_packed, const uint8_t* w_scale_e4m3, float w_global,
+                                         uint8_t* out_packed, uint8_t* out_scale, int64_t N, int64_t K,
+                                         const fp4_quant_opts* opts, void* stream)
+{
+    int alg, swz;
+    fp4_status st = check_opts(opts, &alg, &swz);
+    if (st != FP4_OK)
+        return st;
+    if (!w_packed || !w_scale_e4m3 || !out_packed || !out_scale)
+        return FP4_ERR_INVALID_ARG;
+    if (N <= 0 || K <= 0 || K % 32 != 0 || N >= kMaxDim || K >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    if (!aligned16(w_packed) || !aligned16(out_packed) || (reinterpret_cast<uintptr_t>(w_scale_e4m3) & 1u) ||
+        (swz && (reinterpret_cast<uintptr_t>(out_scale) & 3u)))
+        return FP4_ERR_ALIGNMENT;
+    if ((st = current_device(nullptr)) != FP4_OK)
+        return st;
+    return from_cuda(fp4lin::launch_requant(w_packed, w_scale_e4m3, w_global, out_packed, out_scale, N, K, alg, swz,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status fp4_requant_nvfp4_to_mxfp4(const uint8_t* w_packed, const uint8_t* w_scale_e4m3, float w_global,
+                                      uint8_t* out_packed, uint8_t* out_scale, int64_t N, int64_t K, void* stream)
+{
+    return fp4_requant_nvfp4_to_mxfp4_ex(w_packed, w_scale_e4m3, w_global, out_packed, out_scale, N, K, nullptr,
+                                         stream);
+}
+
+fp4_status fp4_quant_act_mxfp4(const void* x_bf16, uint8_t* out_packed, uint8_t* out_scale, int64_t M, int64_t K,
+                               const fp4_quant_opts* opts, void* stream)
+{
+    int alg, swz;
+    fp4_status st = check_opts(opts, &alg, &swz);
+    if (st != FP4_OK)
+        return st;
+    if (M < 0 || K <= 0 || K % 32 != 0 || M >= kMaxDim || K >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    if (M == 0)
+        return FP4_OK;
+    if (!x_bf16 || !out_packed || !out_scale)
+        return FP4_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(out_packed) || (swz && (reinterpret_cast<uintptr_t>(out_scale) & 3u)))
+        return FP4_ERR_ALIGNMENT;
+    if ((st = current_device(nullptr)) != FP4_OK)
+        return st;
+    return from_cuda(
+        fp4lin::launch_act_quant(x_bf16, out_packed, out_scale, M, K, alg, swz, static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status fp4_quant_act_mxfp4_grouped(const void* x_bf16, const int32_t* row_offsets, int32_t E, int64_t total_M,
+                                       int64_t K, uint8_t* out_packed, uint8_t* out_scale,
+                                       const fp4_quant_opts* opts, void* stream)
+{
+    int alg, swz;
+    fp4_status st = check_opts(opts, &alg, &swz);
+    if (st != FP4_OK)
+        return st;
+    if (opts && !swz)
+        return FP4_ERR_INVALID_ARG;  // grouped scales are always swizzled
+    if (E <= 0 || E > 4096 || total_M < 0 || K <= 0 || K % 32 != 0 || total_M >= kMaxDim || K >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    if (total_M == 0)
+        return FP4_OK;
+    if (!x_bf16 || !row_offsets || !out_packed || !out_scale)
+        return FP4_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(out_packed) || (reinterpret_cast<uintptr_t>(out_scale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(row_offsets) & 3u))
+        return FP4_ERR_ALIGNMENT;
+    if ((st = current_device(nullptr)) != FP4_OK)
+        return st;
+    return from_cuda(fp4lin::launch_act_quant_grouped(x_bf16, row_offsets, E, total_M, K, out_packed, out_scale, alg,
+                                                      static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status fp4_quant_nvfp4(const void* x_bf16, float g, uint8_t* out_packed, uint8_t* out_scale_e4m3, int64_t M,
+                           int64_t K, void* stream)
+{
+    if (M < 0 || K <= 0 || K % 16 != 0 || M >= kMaxDim || K >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    if (M == 0)
+        return FP4_OK;
+    if (!x_bf16 || !out_packed || !out_scale_e4m3)
+        return FP4_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || (reinterpret_cast<uintptr_t>(out_packed) & 3u))
+        return FP4_ERR_ALIGNMENT;
+    fp4_status st;
+    if ((st = current_device(nullptr)) != FP4_OK)
+        return st;
+    return from_cuda(
+        fp4lin::launch_quant_nvfp4(x_bf16, g, out_packed, out_scale_e4m3, M, K, static_cast<cudaStream_t>(stream)));
+}
+
+static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                              const void* bias, void* out, const int32_t* offsets, int32_t E, int64_t M, int64_t N,
+                              int64_t K, void* stream)
+{
+    if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 8 != 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    if (static_cast<int64_t>(E) * N >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    if (M == 0)
+        return FP4_OK;
+    if (!a || !sa || !b || !sb || !out)
+        return FP4_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(out) ||
+        (bias && !aligned16(bias)))
+        return FP4_ERR_ALIGNMENT;
+    unsigned int* status = nullptr;
+    fp4_status st = current_device(&status);
+    if (st != FP4_OK)
+        return st;
+    fp4lin::GemmArgs args;
+    args.a = a;
+    args.sa = sa;
+    args.b = b;
+    args.sb = sb;
+    args.bias = bias;
+    args.out = out;
+    args.row_offsets = offsets;
+    args.E = offsets ? E : 1;
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.status = status;
+    return from_cuda(fp4lin::launch_gemm(args, static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status fp4_gemm_mxfp4(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                          const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, void* stream)
+{
+    return gemm_common(a, sa, b, sb, bias_bf16, out_bf16, nullptr, 1, M, N, K, stream);
+}
+
+fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                                  const void* bias_bf16, void* out_bf16, const int32_t* row_offsets, int32_t E,
+                                  int64_t total_M, int64_t N, int64_t K, void* stream)
+{
+    if (E <= 0 || E > 4096)
+        return FP4_ERR_SHAPE;
+    if (total_M > 0 && !row_offsets)
+        return FP4_ERR_INVALID_ARG;
+    if (row_offsets && (reinterpret_cast<uintptr_t>(row_offsets) & 3u))
+        return FP4_ERR_ALIGNMENT;
+    return gemm_common(a, sa, b, sb, bias_bf16, out_bf16, row_offsets, E, total_M, N, K, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// formats.cuh -- device-side element codecs for the quantizers.
+//
+// E2M1 grid (magnitudes, code 0..7): 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+// MX block rule ("W4A4 MXFP4 Quantization", Single-Scale Block Scaling):
+// 32 elements share one E8M0 exponent; OCP picks floor(log2 amax) - 2,
+// UOS (Qmax = 7.25) the smallest e with amax <= 7.25 * 2^e; elements are
+// rounded to the nearest E2M1 value ("rint", ties to even) and saturate at 6.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace fp4lin {
+
+// x + kMagic (|x| < 2^22) leaves rint(x) (nearest, ties to even) in the low
+// mantissa bits of the float sum; the low byte of the sum's bit pattern is
+// that integer for 0 <= rint(x) < 256.
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+
+// Nearest E2M1 magnitude code of z * 2^j (z >= 0, not NaN), returned as
+// kMagic + code.  The code of a value y is the lower envelope of the three
+// lines 2y (step-0.5 part of the grid), 2 + y (step-1 part) and 4 + y/2
+// (step-2 part), capped at 7; rint is monotone, so it commutes with the min
+// and each line is rounded on its own (the even offsets keep ties on even
+// codes).  The scaling by 2^j happens inside the fused multiply-adds, so it
+// is exact.
+template <int J>
+__device__ __forceinline__ float e2m1_code_scaled(float z)
+{
+    constexpr float s2 = (J == 0) ? 2.0f : (J == 1) ? 4.0f : 8.0f;
+    constexpr float s1 = (J == 0) ? 1.0f : (J == 1) ? 2.0f : 4.0f;
+    constexpr float s0 = (J == 0) ? 0.5f : (J == 1) ? 1.0f : 2.0f;
+    const float a = __fmaf_rn(z, s2, kMagic);
+    const float b = __fmaf_rn(z, s1, kMagic + 2.0f);
+    const float c = __fmaf_rn(z, s0, kMagic + 4.0f);
+    return fminf(fminf(a, b), fminf(c, kMagic + 7.0f));
+}
+
+__device__ __forceinline__ uint32_t e2m1_code(float z)
+{
+    return __float_as_uint(e2m1_code_scaled<0>(z)) & 0xFFu;
+}
+
+// Shared exponent from the fp32 bit pattern of a finite, non-negative amax.
+// For a normal amax = (1 + f) * 2^E the OCP exponent is E - 2 (biased field
+// minus 129); UOS adds one when 1 + f > 1.8125 (mantissa field > 0x680000).
+// Subnormal and zero amax give <= -128, which the clamp turns into -127.
+__device__ __forceinline__ int mx_shared_exp(uint32_t amax_bits, int uos)
+{
+    int e = static_cast<int>(amax_bits >> 23) - 129;
+    if (uos)
+        e += (amax_bits & 0x7FFFFFu) > 0x680000u ? 1 : 0;
+    return max(-127, min(127, e));
+}
+
+// 2^-e as a float (e in [-127, 126]).
+__device__ __forceinline__ float exp2_neg(int e)
+{
+    return __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+}
+
+// E2M1 value of a magnitude code 0..7 (exact float).
+__device__ __forceinline__ float e2m1_mag_value(uint32_t m)
+{
+    if (m < 2)
+        return 0.5f * static_cast<float>(m);
+    return __uint_as_float((((m >> 1) + 126u) << 23) | ((m & 1u) << 22));
+}
+
+// Two float8_e4m3fn bytes (low byte first) -> two floats, exactly.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_bytes)
+{
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_bytes & 0xFFFFu),
+                                                     __NV_E4M3);
+    return make_float2(__half2float(__ushort_as_half(h.x)), __half2float(__ushort_as_half(h.y)));
+}
+
+// float -> float8_e4m3fn, round to nearest even, saturating to +-448, NaN -> 0x7F.
+__device__ __forceinline__ uint32_t float_to_e4m3_satfinite(float t)
+{
+    const __nv_fp8x2_storage_t v = __nv_cvt_float2_to_fp8x2(make_float2(t, t), __NV_SATFINITE, __NV_E4M3);
+    return static_cast<uint32_t>(v) & 0xFFu;
+}
+
+// Scale-factor byte offset of (row r, 32-block c) in the swizzled layout the
+// block-scaled MMA reads; kb4 = ceil(K/32 / 4).
+__device__ __forceinline__ int64_t sf_swizzled_offset(int64_t r, int64_t c, int64_t kb4)
+{
+    return ((r >> 7) * kb4 + (c >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
+}
+
+}  // namespace fp4lin

@@ -1,0 +1,46 @@
+// internal.h -- host-side launchers shared between the C ABI layer and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp4lin {
+
+// Status word bits a kernel sets in the library-owned device status word.
+constexpr unsigned int kStatusTimeout = 1u;
+
+// Upper bound of every bounded device wait (nanoseconds of wall time).
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+cudaError_t launch_requant(const uint8_t* wp, const uint8_t* ws, float g, uint8_t* op, uint8_t* osf,
+                           int64_t N, int64_t K, int alg, int swizzled, cudaStream_t stream);
+
+cudaError_t launch_act_quant(const void* x, uint8_t* op, uint8_t* osf, int64_t M, int64_t K, int alg,
+                             int swizzled, cudaStream_t stream);
+
+cudaError_t launch_act_quant_grouped(const void* x, const int32_t* offsets, int E, int64_t total_M,
+                                     int64_t K, uint8_t* op, uint8_t* osf, int alg, cudaStream_t stream);
+
+cudaError_t launch_quant_nvfp4(const void* x, float g, uint8_t* op, uint8_t* osf, int64_t M, int64_t K,
+                               cudaStream_t stream);
+
+// Dense (offsets == nullptr) or grouped GEMM.
+struct GemmArgs {
+    const uint8_t* a;
+    const uint8_t* sa;
+    const uint8_t* b;
+    const uint8_t* sb;
+    const void* bias;
+    void* out;
+    const int32_t* row_offsets;  // grouped only
+    int E;                       // grouped only (1 for dense)
+    int64_t M;                   // rows of A (total rows when grouped)
+    int64_t N;
+    int64_t K;
+    unsigned int* status;
+};
+
+cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
+
+}  // namespace fp4lin

@@ -1,0 +1,166 @@
+"""ctypes binding of libfp4lin (argument marshalling only).
+
+Every function here has the name and argument order of the C entry point
+declared in include/fp4lin.h.  Tensor arguments may be torch tensors (their
+data pointers are passed), plain integers (raw device pointers) or None
+(NULL).  `stream` defaults to torch's current CUDA stream.  A non-OK status
+raises Fp4Error.  There is no fallback: if the library is missing or the
+GPU is not sm_103, calls fail.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp4lin.so")
+
+FP4_OK = 0
+FP4_SCALE_OCP = 0
+FP4_SCALE_UOS = 2
+FP4_SF_SWIZZLED = 0
+FP4_SF_ROWMAJOR = 1
+
+# every symbol the header declares
+SYMBOLS = (
+    "fp4_sf_bytes", "fp4_sf_bytes_grouped", "fp4_status_string", "fp4_get_device_status",
+    "fp4_requant_nvfp4_to_mxfp4", "fp4_requant_nvfp4_to_mxfp4_ex", "fp4_quant_act_mxfp4",
+    "fp4_quant_act_mxfp4_grouped", "fp4_quant_nvfp4", "fp4_gemm_mxfp4", "fp4_gemm_mxfp4_grouped",
+)
+
+
+class Fp4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)}")
+        self.status = status
+
+
+class fp4_quant_opts(ctypes.Structure):
+    _fields_ = [("scale_alg", ctypes.c_int32), ("sf_layout", ctypes.c_int32)]
+
+
+_lib = None
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+
+
+def load(path: str = LIB_PATH):
+    """Loads the shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise FileNotFoundError(f"{path} is missing: build it with nvfp4_mxfp4_w4a4_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        sig = {
+            "fp4_sf_bytes": (ctypes.c_size_t, [_i64, _i64, _i32]),
+            "fp4_sf_bytes_grouped": (ctypes.c_size_t, [_i64, _i32, _i64]),
+            "fp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+            "fp4_get_device_status": (ctypes.c_int, []),
+            "fp4_requant_nvfp4_to_mxfp4": (ctypes.c_int, [_p, _p, ctypes.c_float, _p, _p, _i64, _i64, _p]),
+            "fp4_requant_nvfp4_to_mxfp4_ex": (ctypes.c_int, [_p, _p, ctypes.c_float, _p, _p, _i64, _i64,
+                                                             ctypes.POINTER(fp4_quant_opts), _p]),
+            "fp4_quant_act_mxfp4": (ctypes.c_int, [_p, _p, _p, _i64, _i64, ctypes.POINTER(fp4_quant_opts), _p]),
+            "fp4_quant_act_mxfp4_grouped": (ctypes.c_int, [_p, _p, _i32, _i64, _i64, _p, _p,
+                                                           ctypes.POINTER(fp4_quant_opts), _p]),
+            "fp4_quant_nvfp4": (ctypes.c_int, [_p, ctypes.c_float, _p, _p, _i64, _i64, _p]),
+            "fp4_gemm_mxfp4": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p]),
+            "fp4_gemm_mxfp4_grouped": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _opts(scale_alg, sf_layout):
+    if scale_alg is None and sf_layout is None:
+        return None
+    o = fp4_quant_opts(FP4_SCALE_OCP if scale_alg is None else scale_alg,
+                       FP4_SF_SWIZZLED if sf_layout is None else sf_layout)
+    return ctypes.byref(o)
+
+
+def _check(status: int, where: str):
+    if status != FP4_OK:
+        raise Fp4Error(status, where)
+
+
+def status_string(status: int) -> str:
+    return load().fp4_status_string(status).decode()
+
+
+def fp4_sf_bytes(rows: int, K: int, sf_layout: int = FP4_SF_SWIZZLED) -> int:
+    return load().fp4_sf_bytes(rows, K, sf_layout)
+
+
+def fp4_sf_bytes_grouped(total_M: int, E: int, K: int) -> int:
+    return load().fp4_sf_bytes_grouped(total_M, E, K)
+
+
+def fp4_get_device_status() -> int:
+    return load().fp4_get_device_status()
+
+
+def fp4_requant_nvfp4_to_mxfp4(w_packed, w_scale_e4m3, w_global, out_packed, out_scale, N, K, stream=None,
+                               scale_alg=None, sf_layout=None):
+    L = load()
+    if scale_alg is None and sf_layout is None:
+        st = L.fp4_requant_nvfp4_to_mxfp4(_ptr(w_packed), _ptr(w_scale_e4m3), float(w_global), _ptr(out_packed),
+                                          _ptr(out_scale), N, K, _stream(stream))
+    else:
+        st = L.fp4_requant_nvfp4_to_mxfp4_ex(_ptr(w_packed), _ptr(w_scale_e4m3), float(w_global),
+                                             _ptr(out_packed), _ptr(out_scale), N, K,
+                                             _opts(scale_alg, sf_layout), _stream(stream))
+    _check(st, "fp4_requant_nvfp4_to_mxfp4")
+
+
+def fp4_quant_act_mxfp4(x_bf16, out_packed, out_scale, M, K, stream=None, scale_alg=None, sf_layout=None):
+    st = load().fp4_quant_act_mxfp4(_ptr(x_bf16), _ptr(out_packed), _ptr(out_scale), M, K,
+                                    _opts(scale_alg, sf_layout), _stream(stream))
+    _check(st, "fp4_quant_act_mxfp4")
+
+
+def fp4_quant_act_mxfp4_grouped(x_bf16, row_offsets, E, total_M, K, out_packed, out_scale, stream=None,
+                                scale_alg=None):
+    st = load().fp4_quant_act_mxfp4_grouped(_ptr(x_bf16), _ptr(row_offsets), E, total_M, K, _ptr(out_packed),
+                                            _ptr(out_scale), _opts(scale_alg, None), _stream(stream))
+    _check(st, "fp4_quant_act_mxfp4_grouped")
+
+
+def fp4_quant_nvfp4(x_bf16, g, out_packed, out_scale_e4m3, M, K, stream=None):
+    st = load().fp4_quant_nvfp4(_ptr(x_bf16), float(g), _ptr(out_packed), _ptr(out_scale_e4m3), M, K,
+                                _stream(stream))
+    _check(st, "fp4_quant_nvfp4")
+
+
+def fp4_gemm_mxfp4(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, stream=None):
+    st = load().fp4_gemm_mxfp4(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias_bf16), _ptr(out_bf16), M, N, K,
+                               _stream(stream))
+    _check(st, "fp4_gemm_mxfp4")
+
+
+def fp4_gemm_mxfp4_grouped(a, sa, b, sb, bias_bf16, out_bf16, row_offsets, E, total_M, N, K, stream=None):
+    st = load().fp4_gemm_mxfp4_grouped(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias_bf16), _ptr(out_bf16),
+                                       _ptr(row_offsets), E, total_M, N, K, _stream(stream))
+    _check(st, "fp4_gemm_mxfp4_grouped")

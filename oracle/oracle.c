@@ -81,15 +81,19 @@ unsigned orc_e2m1_encode(double q)
     double best_d = INFINITY;
     if (isnan(q))
         return 0u;
-    for (unsigned i = 0; i < 8; ++i) {
-        double d = fabs(orc_e2m1_value(i) - mag);
-        if (d < best_d || (d == best_d && (i & 1u) == 0 && (best & 1u) == 1)) {
-            best = i;
-            best_d = d;
+    if (mag > 6.0) {
+        /* beyond the largest value every distance is largest-first; decide it
+         * directly (a brute-force distance would be absorbed for huge |q|) */
+        best = 7;
+    } else {
+        for (unsigned i = 0; i < 8; ++i) {
+            double d = fabs(orc_e2m1_value(i) - mag);
+            if (d < best_d || (d == best_d && (i & 1u) == 0 && (best & 1u) == 1)) {
+                best = i;
+                best_d = d;
+            }
         }
     }
-    if (isinf(mag))
-        best = 7;
     return (signbit(q) ? 8u : 0u) | best;
 }
 

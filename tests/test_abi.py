@@ -1,0 +1,85 @@
+"""CPU checks of the C ABI: the library builds, loads without a GPU, exports
+every symbol include/fp4lin.h declares, and rejects bad arguments before it
+touches a device (no compute call runs here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "fp4lin.h")
+
+
+def _declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"FP4LIN_API\s+[\w\s\*]+?\b(fp4_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from _util import lib
+
+    return lib()
+
+
+def test_header_declares_the_boundary():
+    syms = _declared_symbols()
+    for name in ("fp4_requant_nvfp4_to_mxfp4", "fp4_quant_act_mxfp4", "fp4_gemm_mxfp4",
+                 "fp4_gemm_mxfp4_grouped", "fp4_quant_act_mxfp4_grouped"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(L):
+    lib = ctypes.CDLL(L.LIB_PATH)
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(_declared_symbols()) == set(L.SYMBOLS)
+
+
+def test_sf_sizes(L):
+    assert L.fp4_sf_bytes(256, 512, L.FP4_SF_ROWMAJOR) == 256 * 16
+    assert L.fp4_sf_bytes(256, 512, L.FP4_SF_SWIZZLED) == 256 * 16
+    assert L.fp4_sf_bytes(200, 192, L.FP4_SF_SWIZZLED) == 256 * 8          # rows -> 256, 6 blocks -> 8
+    assert L.fp4_sf_bytes(1, 32, L.FP4_SF_SWIZZLED) == 128 * 4
+    assert L.fp4_sf_bytes(0, 32, L.FP4_SF_SWIZZLED) == 0
+    assert L.fp4_sf_bytes(5, 48, L.FP4_SF_SWIZZLED) == 0                   # K not a multiple of 32
+    # grouped bound: sum over groups of ceil(rows/128) <= (total + E*127) / 128
+    assert L.fp4_sf_bytes_grouped(32768, 64, 4096) == ((32768 + 64 * 127) // 128) * 128 * 128
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert L.status_string(s).startswith("FP4_")
+    assert "UNKNOWN" in L.status_string(99)
+
+
+def test_argument_checks_precede_device_use(L):
+    raw = L.load()
+    # shapes
+    assert raw.fp4_gemm_mxfp4(16, 16, 16, 16, None, 16, 1, 8, 100, None) == 2      # K % 128
+    assert raw.fp4_gemm_mxfp4(16, 16, 16, 16, None, 16, 1, 12, 128, None) == 2     # N % 8
+    assert raw.fp4_quant_act_mxfp4(16, 16, 16, 4, 48, None, None) == 2             # K % 32
+    assert raw.fp4_requant_nvfp4_to_mxfp4(16, 16, 1.0, 16, 16, 0, 32, None) == 2   # N = 0
+    # null pointers
+    assert raw.fp4_gemm_mxfp4(None, 16, 16, 16, None, 16, 1, 8, 128, None) == 1
+    assert raw.fp4_requant_nvfp4_to_mxfp4(None, 16, 1.0, 16, 16, 4, 32, None) == 1
+    # alignment
+    assert raw.fp4_gemm_mxfp4(17, 16, 16, 16, None, 16, 1, 8, 128, None) == 3
+    assert raw.fp4_quant_act_mxfp4(24, 16, 16, 4, 32, None, None) == 3
+    # bad option values
+    from nvfp4_mxfp4_w4a4_gb300.fp4lin import fp4_quant_opts
+
+    bad = fp4_quant_opts(1, 0)
+    assert raw.fp4_quant_act_mxfp4(16, 16, 16, 4, 32, ctypes.byref(bad), None) == 1
+    # empty problems are no-ops that need no device
+    assert raw.fp4_quant_act_mxfp4(None, None, None, 0, 32, None, None) == 0
+    assert raw.fp4_gemm_mxfp4(None, None, None, None, None, None, 0, 8, 128, None) == 0
+
+
+@pytest.mark.skipif(__import__("_util").gpu_available(), reason="CPU-only check")
+def test_valid_call_without_gpu_reports_cuda_error(L):
+    raw = L.load()
+    st = raw.fp4_quant_act_mxfp4(16, 16, 16, 4, 32, None, None)
+    assert st in (4, 5)   # no usable device: UNSUPPORTED or CUDA, never a silent success

@@ -1,0 +1,217 @@
+"""GPU parity of the quantizers against the CPU oracle: bit-exact codes and
+scale bytes, through the C ABI, on small ragged shapes, edge values and the
+full sizes of the decode / prefill / MoE / layer-stream workloads."""
+import numpy as np
+import pytest
+
+import synth
+from _util import THREADS, bf16_bits_host, dev, dev_bf16, empty_u8, host, lib
+
+pytestmark = pytest.mark.gpu
+
+OCP, UOS = 0, 2
+SWZ, ROW = 0, 1
+
+
+@pytest.fixture(scope="module")
+def L():
+    return lib()
+
+
+def _kernel_requant(L, packed, scale, g, alg, layout):
+    N, half = packed.shape
+    K = 2 * half
+    dp, ds = dev(packed), dev(scale)
+    op = empty_u8(N * K // 2)
+    osf = empty_u8(L.fp4_sf_bytes(N, K, layout))
+    L.fp4_requant_nvfp4_to_mxfp4(dp, ds, g, op, osf, N, K, scale_alg=alg, sf_layout=layout)
+    assert L.fp4_get_device_status() == 0
+    return host(op)[: N * K // 2].reshape(N, K // 2), host(osf)[: L.fp4_sf_bytes(N, K, layout)]
+
+
+def _check_requant(orc, L, packed, scale, g, alg=OCP, layout=SWZ):
+    kp, ks = _kernel_requant(L, packed, scale, g, alg, layout)
+    rp, rs = orc.requant(packed, scale, g, alg, threads=THREADS)
+    assert np.array_equal(kp, rp), f"codes differ at {np.argwhere(kp != rp)[:5]}"
+    expect_sf = orc.sf_swizzle(rs) if layout == SWZ else rs.reshape(-1)
+    assert np.array_equal(ks, expect_sf), f"scales differ at {np.argwhere(ks != expect_sf)[:5]}"
+
+
+def _random_nvfp4(rng, N, K, scale_lo=0, scale_hi=256):
+    packed = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scale = rng.integers(scale_lo, scale_hi, (N, K // 16), dtype=np.uint8)
+    return packed, scale
+
+
+@pytest.mark.parametrize("N,K", [(1, 32), (5, 96), (130, 64), (256, 512), (300, 224), (129, 1056)])
+@pytest.mark.parametrize("alg", [OCP, UOS])
+@pytest.mark.parametrize("layout", [SWZ, ROW])
+def test_requant_random_bytes(orc, L, N, K, alg, layout):
+    rng = np.random.default_rng(N * 7919 + K)
+    packed, scale = _random_nvfp4(rng, N, K)          # every code and every scale byte incl. NaN / negative
+    for g in (1.0, 0.0037, 2.0 ** -20, -0.25):
+        _check_requant(orc, L, packed, scale, float(np.float32(g)), alg, layout)
+
+
+def test_requant_special_global_scales(orc, L):
+    rng = np.random.default_rng(3)
+    packed, scale = _random_nvfp4(rng, 64, 256, 0, 0x7F)
+    for g in (0.0, -0.0, float("inf"), float("nan"), 3.0e38, 1.0e-38, 1.0e-45):
+        _check_requant(orc, L, packed, scale, g)
+
+
+def test_requant_tiny_workload_recipe(orc, L):
+    w = synth.workload0()
+    g = orc.nvfp4_global_scale(w["W"])
+    packed, scale = orc.nvfp4_quantize(w["W"], g)
+    for alg in (OCP, UOS):
+        for layout in (SWZ, ROW):
+            _check_requant(orc, L, packed, scale, g, alg, layout)
+
+
+# ---------------------------------------------------------------- activations
+def _kernel_act(L, x_bits, alg, layout):
+    M, K = x_bits.shape
+    op = empty_u8(M * K // 2)
+    osf = empty_u8(L.fp4_sf_bytes(M, K, layout))
+    L.fp4_quant_act_mxfp4(dev_bf16(x_bits), op, osf, M, K, scale_alg=alg, sf_layout=layout)
+    return host(op)[: M * K // 2].reshape(M, K // 2), host(osf)[: L.fp4_sf_bytes(M, K, layout)]
+
+
+def _check_act(orc, L, x_bits, alg=OCP, layout=SWZ):
+    kp, ks = _kernel_act(L, x_bits, alg, layout)
+    rp, rs = orc.act_quant(x_bits, alg, threads=THREADS)
+    assert np.array_equal(kp, rp), f"codes differ at {np.argwhere(kp != rp)[:5]}"
+    expect_sf = orc.sf_swizzle(rs) if layout == SWZ else rs.reshape(-1)
+    assert np.array_equal(ks, expect_sf), f"scales differ at {np.argwhere(ks != expect_sf)[:5]}"
+
+
+@pytest.mark.parametrize("M,K", [(1, 32), (3, 96), (16, 512), (129, 256), (200, 1056), (64, 4096)])
+@pytest.mark.parametrize("alg", [OCP, UOS])
+@pytest.mark.parametrize("layout", [SWZ, ROW])
+def test_act_quant_random_bits(orc, L, M, K, alg, layout):
+    rng = np.random.default_rng(M * 31 + K)
+    x = rng.integers(0, 1 << 16, (M, K), dtype=np.uint16)      # every bf16 pattern, incl. Inf/NaN/subnormal
+    _check_act(orc, L, x, alg, layout)
+    y = synth.bf16_normal(M + K, synth.S_ACT, (M, K), 1.0, 0.01, 20.0)
+    _check_act(orc, L, y, alg, layout)
+
+
+def test_act_quant_edge_blocks(orc, L):
+    K = 128
+    rows = [np.zeros(K, np.uint16), np.full(K, 0x8000, np.uint16), np.full(K, 0x0001, np.uint16),
+            np.full(K, 0x0100, np.uint16), np.full(K, 0x7F7F, np.uint16), np.full(K, 0xFF7F, np.uint16),
+            np.full(K, 0x40F0, np.uint16)]
+    r = np.zeros(K, np.uint16)
+    r[5] = 0x7F80                      # +Inf in block 0
+    r[40] = 0xFFC1                     # NaN in block 1
+    rows.append(r)
+    x = np.stack(rows)
+    for alg in (OCP, UOS):
+        _check_act(orc, L, x, alg, SWZ)
+
+
+def test_act_quant_zero_rows_is_noop(L):
+    L.fp4_quant_act_mxfp4(None, None, None, 0, 64)
+
+
+# ---------------------------------------------------------------- grouped
+def _expected_grouped_sf(orc, rowmajor_sf, offsets, K):
+    kb4 = (K // 32 + 3) // 4
+    parts, tiles = [], 0
+    for e in range(len(offsets) - 1):
+        rows = rowmajor_sf[offsets[e]:offsets[e + 1]]
+        if len(rows):
+            parts.append(orc.sf_swizzle(rows))
+            tiles += (len(rows) + 127) // 128
+    used = tiles * kb4 * 512
+    return (np.concatenate(parts) if parts else np.zeros(0, np.uint8)), used
+
+
+@pytest.mark.parametrize("counts,K", [([3, 0, 130, 1, 200], 256), ([0, 0, 5], 96), ([128, 128], 64),
+                                      ([1] * 40, 32)])
+def test_act_quant_grouped(orc, L, counts, K):
+    rng = np.random.default_rng(len(counts) * 100 + K)
+    offsets = np.zeros(len(counts) + 1, np.int32)
+    offsets[1:] = np.cumsum(counts)
+    total = int(offsets[-1])
+    x = synth.bf16_normal(11, synth.S_ACT, (total, K), 1.0, 0.02, 16.0)
+    x[rng.integers(0, total, 3), rng.integers(0, K, 3)] = 0x0001
+    E = len(counts)
+    op = empty_u8(total * K // 2)
+    osf = empty_u8(L.fp4_sf_bytes_grouped(total, E, K))
+    L.fp4_quant_act_mxfp4_grouped(dev_bf16(x), dev(offsets), E, total, K, op, osf)
+    rp, rs = orc.act_quant(x, OCP)
+    assert np.array_equal(host(op)[: total * K // 2].reshape(total, K // 2), rp)
+    expect, used = _expected_grouped_sf(orc, rs, offsets, K)
+    assert np.array_equal(host(osf)[:used], expect)
+
+
+# ---------------------------------------------------------------- NVFP4 producer
+@pytest.mark.parametrize("M,K", [(1, 16), (7, 48), (256, 512), (300, 1024)])
+def test_nvfp4_producer(orc, L, M, K):
+    x = synth.bf16_normal(M, synth.S_WEIGHT, (M, K), 0.02, 0.01, 8.0)
+    g = orc.nvfp4_global_scale(x)
+    op = empty_u8(M * K // 2)
+    osc = empty_u8(M * K // 16)
+    L.fp4_quant_nvfp4(dev_bf16(x), g, op, osc, M, K)
+    rp, rs = orc.nvfp4_quantize(x, g)
+    assert np.array_equal(host(op)[: M * K // 2].reshape(M, K // 2), rp)
+    assert np.array_equal(host(osc)[: M * K // 16].reshape(M, K // 16), rs)
+
+
+def test_nvfp4_producer_special_scales(orc, L):
+    x = synth.bf16_normal(5, synth.S_WEIGHT, (32, 64), 1.0)
+    x[0, :16] = 0
+    for g in (1.0, 0.0, 1e-30, 5.0, -0.5):
+        op = empty_u8(32 * 32)
+        osc = empty_u8(32 * 4)
+        L.fp4_quant_nvfp4(dev_bf16(x), g, op, osc, 32, 64)
+        rp, rs = orc.nvfp4_quantize(x, float(np.float32(g)))
+        assert np.array_equal(host(op).reshape(32, 32), rp), g
+        assert np.array_equal(host(osc).reshape(32, 4), rs), g
+
+
+# ---------------------------------------------------------------- full sizes
+def _nvfp4_from_recipe(orc, W):
+    g = orc.nvfp4_global_scale(W)
+    packed, scale = orc.nvfp4_quantize(W, g, threads=THREADS)
+    return packed, scale, g
+
+
+@pytest.mark.slow
+def test_full_decode_workload_quant(orc, L):
+    w = synth.workload1()
+    packed, scale, g = _nvfp4_from_recipe(orc, w["W"])
+    _check_requant(orc, L, packed, scale, g)
+    for M, X in w["X"].items():
+        _check_act(orc, L, X)
+
+
+@pytest.mark.slow
+def test_full_prefill_workload_quant(orc, L):
+    w = synth.workload2()
+    packed, scale, g = _nvfp4_from_recipe(orc, w["W"])
+    _check_requant(orc, L, packed, scale, g)
+    for M, X in w["X"].items():
+        _check_act(orc, L, X)
+
+
+@pytest.mark.slow
+def test_full_moe_workload_quant(orc, L):
+    w = synth.workload3(experts=[0, 31, 63])
+    for e in (0, 31, 63):
+        for W in (w["W_gu"][e], w["W_down"][e]):
+            packed, scale, g = _nvfp4_from_recipe(orc, W)
+            _check_requant(orc, L, packed, scale, g)
+    offsets = w["row_offsets"]
+    for A in (w["A_gu"], w["A_down"]):
+        total, K = A.shape
+        E = len(offsets) - 1
+        op = empty_u8(total * K // 2)
+        osf = empty_u8(L.fp4_sf_bytes_grouped(total, E, K))
+        L.fp4_quant_act_mxfp4_grouped(dev_bf16(A), dev(offsets), E, total, K, op, osf)
+        rp, rs = orc.act_quant(A, OCP, threads=THREADS)
+        assert np.array_equal(host(op)[: total * K // 2].reshape(total, K // 2), rp)
+        expect, used = _expected_grouped_sf(orc, rs, offsets, K)
+        assert np.array_equal(host(osf)[:used], expect)

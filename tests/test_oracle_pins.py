@@ -120,6 +120,9 @@ def test_e2m1_encode_matches_per_binade_rint(orc):
     for q in qs:
         assert orc.e2m1_encode(float(q)) == expect(float(q)), q
     assert orc.e2m1_encode(-0.0) == 0x8
+    # saturation holds for every magnitude above 6, however large
+    for q in (6.0000001, 1e3, 1e17, 1e27, 3.4e38, float("inf")):
+        assert orc.e2m1_encode(q) == 0x7 and orc.e2m1_encode(-q) == 0xF, q
 
 
 # ------------------------------------------------------ shared exponent rule
