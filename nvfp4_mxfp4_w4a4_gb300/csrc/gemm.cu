@@ -345,9 +345,23 @@ cudaError_t launch_tile_kernel(const GemmArgs& a, cudaStream_t stream)
         return cudaSuccess;
     const size_t smem = C::SMEM_FIXED + (kGrouped ? sizeof(int32_t) * (a.E + 1) : 0);
     auto kern = gemm_mxfp4_kernel<BN, STAGES, kGrouped>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (err != cudaSuccess)
-        return err;
+    // The shared-memory opt-in is a per-device function attribute: set it
+    // once per device (and grow it if a larger grouped prefix needs more).
+    static std::mutex mu;
+    static size_t configured[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess || dev < 0 || dev >= 64)
+        return err != cudaSuccess ? err : cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (configured[dev] < smem) {
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (err != cudaSuccess)
+                return err;
+            configured[dev] = smem;
+        }
+    }
     kern<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmA, tmB, p);
     return cudaGetLastError();
 }

@@ -126,9 +126,11 @@ def bf16_normal(seed, stream, shape, sigma=1.0, outlier_p=0.0, outlier_mul=1.0):
     return to_bf16_bits(x).reshape(shape)
 
 
-def weight_with_column_outliers(seed, shape, sigma, n_cols, mul):
-    """Weight ~N(0, sigma) with n_cols seeded K-columns (all rows) scaled by mul."""
+def weight_with_column_outliers(seed, shape, sigma, n_cols, mul, rows=None):
+    """Weight ~N(0, sigma) with n_cols seeded K-columns (all rows) scaled by mul.
+    `rows` limits generation to the first rows (same values as the full tensor)."""
     N, K = shape
+    N = N if rows is None else rows
     x = normal(seed, S_WEIGHT, N * K, sigma).reshape(N, K)
     cols = np.sort(np.argsort(uniform(seed, S_OUTLIER, K), kind="stable")[:n_cols])
     x[:, cols] *= mul
@@ -141,8 +143,8 @@ def workload0():
     return {"W": W, "X": X, "bias": None}
 
 
-def workload1(Ms=(1, 8, 32, 64)):
-    W, cols = weight_with_column_outliers(1, (14336, 4096), 0.02, 4, 8.0)
+def workload1(Ms=(1, 8, 32, 64), rows=None):
+    W, cols = weight_with_column_outliers(1, (14336, 4096), 0.02, 4, 8.0, rows)
     Xs = {M: bf16_normal(1, S_ACT * 1000 + M, (M, 4096), 1.0) for M in Ms}
     bias = bf16_normal(1, S_BIAS, (14336,), 0.01)
     return {"W": W, "X": Xs, "bias": bias, "outlier_cols": cols}
