@@ -5,9 +5,11 @@ One step = one pass of the whole hot path on the decode-shaped layer
 x8; bias ~N(0,0.01); activations M in {1, 8, 32, 64}, K=4096 ~N(0,1)):
   requantize the NVFP4 weight to MXFP4, then for each M quantize the
   activations and run the W4A4 GEMM with bias.
-The step is captured once as a CUDA graph (9 kernel launches) and replayed;
-L2 is flushed (a 512 MiB write) before every timed step, outside the timed
-events.  `value` = GEMM FLOPs of the step / device time of the step.
+The step is captured once as a CUDA graph (9 kernel launches) and replayed.
+Before every timed step L2 is flushed outside the timed events: a 512 MiB
+buffer is written, then a second 512 MiB buffer is read, so the previous
+step's lines are gone and the write-backs of the flush itself are paid before
+the events start.  `value` = GEMM FLOPs of the step / device time of the step.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs its own replica (the path has no exchange
@@ -44,6 +46,7 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--breakdown-reps", type=int, default=200)
+    ap.add_argument("--flush-mib", type=int, default=512, help="L2 flush buffer size (0 = no flush)")
     return ap.parse_args()
 
 
@@ -165,7 +168,7 @@ def max_over_ranks(pg, x, device=None):
 class Layer:
     """Device buffers and the captured step for the decode-shaped layer."""
 
-    def __init__(self, L, torch, seed=1):
+    def __init__(self, L, torch, flush_mib=512):
         import synth
 
         self.L, self.torch = L, torch
@@ -187,7 +190,9 @@ class Layer:
         self.a_packed = {M: torch.empty((M, K_W // 2), dtype=torch.uint8, device=dev) for M in MS}
         self.a_scale = {M: torch.empty(L.fp4_sf_bytes(M, K_W), dtype=torch.uint8, device=dev) for M in MS}
         self.out = {M: torch.empty((M, N_W), dtype=torch.bfloat16, device=dev) for M in MS}
-        self.flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        self.flush_mib = flush_mib
+        self.flush_w = torch.empty(max(1, flush_mib) << 20, dtype=torch.uint8, device=dev)
+        self.flush_r = torch.ones(max(1, flush_mib) << 20, dtype=torch.uint8, device=dev)
         self.stream = torch.cuda.Stream()
 
     # the kernels of one step
@@ -220,8 +225,11 @@ class Layer:
         return g
 
     def flush(self):
-        with self.torch.cuda.stream(self.stream):
-            self.flush_buf.fill_(1)
+        """Evict L2: write one buffer larger than L2, then read another one."""
+        if self.flush_mib > 0:
+            with self.torch.cuda.stream(self.stream):
+                self.flush_w.fill_(1)
+                self.flush_r.sum(dtype=self.torch.int32)
 
     def time_graph(self, g, reps, flush=True):
         """Mean device ms of one replay, L2 flushed before each replay (outside the events)."""
@@ -231,7 +239,7 @@ class Layer:
         with torch.cuda.stream(self.stream):
             for i in range(reps):
                 if flush:
-                    self.flush_buf.fill_(1)
+                    self.flush()
                 starts[i].record(self.stream)
                 g.replay()
                 ends[i].record(self.stream)
@@ -249,7 +257,7 @@ def run_ours(args):
     __graft_entry__.build()
     from nvfp4_mxfp4_w4a4_gb300 import fp4lin as L
 
-    layer = Layer(L, torch)
+    layer = Layer(L, torch, args.flush_mib)
     step_graph = layer.graph(layer.step)
     for _ in range(max(3, args.warmup)):
         layer.flush()
@@ -311,7 +319,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp4 e2m1 (mxfp4) x fp4 -> fp32 acc -> bf16", "data": "synthetic (seeded)",
         "config": {"workload": WORKLOAD, "N": N_W, "K": K_W, "M": list(MS), "global_batch": sum(MS),
-                   "l2": "flushed before every timed step (512 MiB write, outside the events)",
+                   "l2": f"flushed before every timed step ({args.flush_mib} MiB write + {args.flush_mib} MiB "
+                         "read of another buffer, outside the events)",
                    "parallelism": f"replicas x{world}", "cuda_graph": True},
         "requant_GBps": breakdown["requant"]["GBps"],
         "gemm_TFLOPS": {M: breakdown[f"gemm_M{M}"]["TFLOPS"] for M in MS},
@@ -371,8 +380,8 @@ def _e2e(layer, torch, L, reps):
     for _ in range(reps):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
+        layer.flush()
         with torch.cuda.stream(s):
-            layer.flush_buf.fill_(1)
             a.record(s)
             once()
             b.record(s)
