@@ -1,17 +1,26 @@
 """Benchmark of the W4A4 MXFP4 linear layer (libfp4lin) on GB300.
 
-One step = one pass of the whole hot path on the decode-shaped layer
-(weight N=14336, K=4096, NVFP4 from bf16 ~N(0,0.02) with 4 outlier K-columns
-x8; bias ~N(0,0.01); activations M in {1, 8, 32, 64}, K=4096 ~N(0,1)):
-  requantize the NVFP4 weight to MXFP4, then for each M quantize the
-  activations and run the W4A4 GEMM with bias.
-The step is captured once as a CUDA graph (9 kernel launches) and replayed.
-Before every timed step L2 is flushed outside the timed events: a 512 MiB
-buffer is written, then a second 512 MiB buffer is read, so the previous
-step's lines are gone and the write-backs of the flush itself are paid before
-the events start.  `value` = GEMM FLOPs of the step / device time of the step.
+One step = one pass of the whole hot path over one batch of a workload:
+requantize the NVFP4 weight(s) to MXFP4, quantize the activations, run the
+W4A4 GEMM(s).  Workloads (seeded synthetic inputs, see synth/):
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  decode  (default) W[14336,4096] NVFP4 (bf16 ~N(0,0.02), 4 outlier
+          K-columns x8); M in {1,8,32,64} activation batches ~N(0,1); bias.
+  prefill W[18432,7168] (~N(0,0.015)); M in {2048, 8192} (0.5 % outliers x16).
+  moe     64 experts, gate_up [2048,4096] and down [4096,1024]; 4096 tokens
+          routed top-8 -> 32768 grouped rows per projection.
+
+Timing: the inputs and outputs of a step are replicated into S buffer sets
+whose total exceeds twice the 129 MB L2, and one CUDA graph runs S
+consecutive steps, set after set, so every step starts with its data out of
+L2 and no flush kernel or launch gap sits inside the timed events.  The
+graph is replayed until K steps ran; CUDA events on the launching stream
+bracket the whole region.  `value` = GEMM FLOPs of a step / device time of a
+step.  Per-kernel times use the same rotation (one kernel type, S launches
+per graph).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload W]
+                       [--impl ours|reference]
 Under torchrun each rank runs its own replica (the path has no exchange
 step); rank 0 prints one JSON line.
 """
@@ -32,10 +41,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MXFP4 W4A4 GEMM TFLOPS & % FP4 peak; NVFP4→MXFP4 requant GB/s"
-N_W, K_W = 14336, 4096
-MS = (1, 8, 32, 64)
-FP4_NOMINAL_TFLOPS = 15000.0      # dense block-scaled FP4, Blackwell Ultra public figure
-WORKLOAD = "decode layer: W[14336,4096] NVFP4->MXFP4 requant + MXFP4 act-quant + W4A4 GEMM (+bias), M in {1,8,32,64}"
+FP4_NOMINAL_TFLOPS = 15000.0      # dense block-scaled FP4, public Blackwell Ultra figure
+FP4_PER_BF16_NOMINAL = 13.5 / 2.25
+REQ_B = 0.5625 + 0.53125          # requant bytes per element (NVFP4 in, MXFP4 out)
+ACT_B = 2 + 0.53125               # activation-quant bytes per element
 
 
 def parse():
@@ -43,10 +52,10 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", choices=("decode", "prefill", "moe"), default="decode")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--breakdown-reps", type=int, default=200)
-    ap.add_argument("--flush-mib", type=int, default=512, help="L2 flush buffer size (0 = no flush)")
     return ap.parse_args()
 
 
@@ -54,24 +63,8 @@ def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
-
-
-def step_flops():
-    return sum(2.0 * M * N_W * K_W for M in MS)
-
-
-def requant_bytes():
-    return N_W * K_W * (0.5625 + 0.53125)
-
-
-def act_bytes(M):
-    return M * K_W * (2 + 0.53125)
-
-
-def gemm_bytes(M):
-    return 0.53125 * (M + N_W) * K_W + 2.0 * M * N_W + 2.0 * N_W
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
 
 
 # ------------------------------------------------------------------ clocks
@@ -164,87 +157,215 @@ def max_over_ranks(pg, x, device=None):
     return float(t.item())
 
 
-# ------------------------------------------------------------------ our arm
-class Layer:
-    """Device buffers and the captured step for the decode-shaped layer."""
+# ------------------------------------------------------------------ workloads
+class Weight:
+    """NVFP4 weight(s) made on the device by the library's NVFP4 producer
+    from the seeded bf16 tensors (setup, not timed) and the MXFP4
+    destination.  E > 1 stacks E tensors of [N, K], one global scale each."""
 
-    def __init__(self, L, torch, flush_mib=512):
+    def __init__(self, L, torch, bf16_list, N, K, bias=None):
         import synth
 
-        self.L, self.torch = L, torch
         dev = torch.device("cuda")
-        W = synth.workload1()
-        self.inputs_host = W
-        wb = torch.from_numpy(W["W"].view(np.int16)).to(dev).view(torch.bfloat16)
-        amax = float(torch.from_numpy(synth.bf16_bits_to_f32(W["W"])).abs().max())
-        self.g = float(np.float32(amax) / np.float32(6.0 * 448.0))
-        # NVFP4 weight made on the device by the library's NVFP4 producer (setup, not timed)
-        self.w_packed = torch.empty((N_W, K_W // 2), dtype=torch.uint8, device=dev)
-        self.w_scale = torch.empty((N_W, K_W // 16), dtype=torch.uint8, device=dev)
-        L.fp4_quant_nvfp4(wb, self.g, self.w_packed, self.w_scale, N_W, K_W)
-        del wb
-        self.bias = torch.from_numpy(W["bias"].view(np.int16)).to(dev).view(torch.bfloat16)
-        self.x = {M: torch.from_numpy(W["X"][M].view(np.int16)).to(dev).view(torch.bfloat16) for M in MS}
-        self.b_packed = torch.empty((N_W, K_W // 2), dtype=torch.uint8, device=dev)
-        self.b_scale = torch.empty(L.fp4_sf_bytes(N_W, K_W), dtype=torch.uint8, device=dev)
-        self.a_packed = {M: torch.empty((M, K_W // 2), dtype=torch.uint8, device=dev) for M in MS}
-        self.a_scale = {M: torch.empty(L.fp4_sf_bytes(M, K_W), dtype=torch.uint8, device=dev) for M in MS}
-        self.out = {M: torch.empty((M, N_W), dtype=torch.bfloat16, device=dev) for M in MS}
-        self.flush_mib = flush_mib
-        self.flush_w = torch.empty(max(1, flush_mib) << 20, dtype=torch.uint8, device=dev)
-        self.flush_r = torch.ones(max(1, flush_mib) << 20, dtype=torch.uint8, device=dev)
-        self.stream = torch.cuda.Stream()
+        self.L, self.N, self.K, self.E = L, N, K, len(bf16_list)
+        self.packed = torch.empty((self.E * N, K // 2), dtype=torch.uint8, device=dev)
+        self.scale = torch.empty((self.E * N, K // 16), dtype=torch.uint8, device=dev)
+        self.g = []
+        for e, W in enumerate(bf16_list):
+            wb = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+            amax = float(np.abs(synth.bf16_bits_to_f32(W)).max())
+            g = float(np.float32(amax) / np.float32(6.0 * 448.0))
+            self.g.append(g)
+            L.fp4_quant_nvfp4(wb, g, self.packed[e * N:(e + 1) * N], self.scale[e * N:(e + 1) * N], N, K)
+        self.b_packed = torch.empty((self.E * N, K // 2), dtype=torch.uint8, device=dev)
+        self.sf_bytes = L.fp4_sf_bytes(N, K)
+        self.b_scale = torch.empty(self.E * self.sf_bytes, dtype=torch.uint8, device=dev)
+        self.bias = None if bias is None else torch.from_numpy(bias.view(np.int16)).to(dev).view(torch.bfloat16)
 
-    # the kernels of one step
+    def clone(self):
+        c = object.__new__(Weight)
+        c.__dict__.update(self.__dict__)
+        for k in ("packed", "scale", "b_packed", "b_scale"):
+            setattr(c, k, getattr(self, k).clone())
+        return c
+
     def requant(self, s):
-        self.L.fp4_requant_nvfp4_to_mxfp4(self.w_packed, self.w_scale, self.g, self.b_packed, self.b_scale,
-                                          N_W, K_W, stream=s)
+        N, K = self.N, self.K
+        for e in range(self.E):
+            self.L.fp4_requant_nvfp4_to_mxfp4(self.packed[e * N:(e + 1) * N], self.scale[e * N:(e + 1) * N],
+                                              self.g[e], self.b_packed[e * N:(e + 1) * N],
+                                              self.b_scale[e * self.sf_bytes:(e + 1) * self.sf_bytes], N, K,
+                                              stream=s)
 
-    def act(self, M, s):
-        self.L.fp4_quant_act_mxfp4(self.x[M], self.a_packed[M], self.a_scale[M], M, K_W, stream=s)
 
-    def gemm(self, M, s):
-        self.L.fp4_gemm_mxfp4(self.a_packed[M], self.a_scale[M], self.b_packed, self.b_scale, self.bias,
-                              self.out[M], M, N_W, K_W, stream=s)
+class Act:
+    """bf16 activations of one GEMM (dense, or grouped by `offsets`)."""
 
-    def step(self, s):
-        self.requant(s)
-        for M in MS:
-            self.act(M, s)
-            self.gemm(M, s)
+    def __init__(self, L, torch, bits, weight, offsets=None):
+        dev = torch.device("cuda")
+        self.L, self.w = L, weight
+        self.M, self.K = bits.shape
+        self.x = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+        self.a_packed = torch.empty((self.M, self.K // 2), dtype=torch.uint8, device=dev)
+        self.offsets = None if offsets is None else torch.from_numpy(offsets.astype(np.int32)).to(dev)
+        self.E = 0 if offsets is None else len(offsets) - 1
+        sfb = (L.fp4_sf_bytes(self.M, self.K) if offsets is None
+               else L.fp4_sf_bytes_grouped(self.M, self.E, self.K))
+        self.a_scale = torch.empty(sfb, dtype=torch.uint8, device=dev)
+        self.out = torch.empty((self.M, weight.N), dtype=torch.bfloat16, device=dev)
+
+    def clone(self, weight):
+        c = object.__new__(Act)
+        c.__dict__.update(self.__dict__)
+        c.w = weight
+        for k in ("x", "a_packed", "a_scale", "out"):
+            setattr(c, k, getattr(self, k).clone())
+        return c
+
+    @property
+    def set_bytes(self):
+        return sum(t.numel() * t.element_size() for t in (self.x, self.a_packed, self.a_scale, self.out))
+
+    @property
+    def flops(self):
+        return 2.0 * self.M * self.w.N * self.K
+
+    @property
+    def gemm_bytes(self):
+        w = self.w
+        bias = 2.0 * w.E * w.N if w.bias is not None else 0.0
+        return 0.53125 * (self.M + w.E * w.N) * self.K + 2.0 * self.M * w.N + bias
+
+    def quant(self, s):
+        if self.offsets is None:
+            self.L.fp4_quant_act_mxfp4(self.x, self.a_packed, self.a_scale, self.M, self.K, stream=s)
+        else:
+            self.L.fp4_quant_act_mxfp4_grouped(self.x, self.offsets, self.E, self.M, self.K, self.a_packed,
+                                               self.a_scale, stream=s)
+
+    def gemm(self, s):
+        w = self.w
+        if self.offsets is None:
+            self.L.fp4_gemm_mxfp4(self.a_packed, self.a_scale, w.b_packed, w.b_scale, w.bias, self.out, self.M,
+                                  w.N, self.K, stream=s)
+        else:
+            self.L.fp4_gemm_mxfp4_grouped(self.a_packed, self.a_scale, w.b_packed, w.b_scale, w.bias, self.out,
+                                          self.offsets, self.E, self.M, w.N, self.K, stream=s)
+
+
+def make_workload(name, L, torch):
+    import synth
+
+    if name == "decode":
+        d = synth.workload1()
+        w = Weight(L, torch, [d["W"]], 14336, 4096, bias=d["bias"])
+        acts = [Act(L, torch, d["X"][M], w) for M in (1, 8, 32, 64)]
+        return DECODE_DESC, [w], acts
+    if name == "prefill":
+        d = synth.workload2()
+        w = Weight(L, torch, [d["W"]], 18432, 7168)
+        acts = [Act(L, torch, d["X"][M], w) for M in (2048, 8192)]
+        return "prefill layer: W[18432,7168] requant + act-quant + W4A4 GEMM, M in {2048, 8192}", [w], acts
+    d = synth.workload3()
+    E = len(d["row_offsets"]) - 1
+    wgu = Weight(L, torch, [d["W_gu"][e] for e in range(E)], 2048, 4096)
+    wdn = Weight(L, torch, [d["W_down"][e] for e in range(E)], 4096, 1024)
+    acts = [Act(L, torch, d["A_gu"], wgu, d["row_offsets"]), Act(L, torch, d["A_down"], wdn, d["row_offsets"])]
+    desc = ("MoE: 64 experts gate_up[2048,4096] + down[4096,1024] requant, grouped act-quant and grouped W4A4 "
+            "GEMM over 4096 tokens x top-8 (32768 rows)")
+    return desc, [wgu, wdn], acts
+
+
+class Bench:
+    """A workload replicated into S buffer sets (> 2 x L2 in total)."""
+
+    L2_BYTES = 129 * 2 ** 20
+
+    def __init__(self, name, L, torch):
+        self.L, self.torch = L, torch
+        self.desc, weights, acts = make_workload(name, L, torch)
+        set_bytes = sum(w.packed.numel() + w.scale.numel() + w.b_packed.numel() + w.b_scale.numel()
+                        for w in weights) + sum(a.set_bytes for a in acts)
+        self.n_sets = max(2, -(-2 * self.L2_BYTES // set_bytes))
+        self.sets = [(weights, acts)]
+        for _ in range(self.n_sets - 1):
+            wmap = {id(w): w.clone() for w in weights}
+            self.sets.append(([wmap[id(w)] for w in weights], [a.clone(wmap[id(a.w)]) for a in acts]))
+        self.set_bytes = set_bytes
+        self.stream = torch.cuda.Stream()
+        self.side = torch.cuda.Stream()
+
+    @property
+    def weights(self):
+        return self.sets[0][0]
+
+    @property
+    def acts(self):
+        return self.sets[0][1]
+
+    @property
+    def launches_per_step(self):
+        return sum(w.E for w in self.weights) + 2 * len(self.acts)
+
+    def step(self, s, i=0):
+        """Requant on `s`; the activation quantizers (independent of it) on a
+        side stream; the GEMMs on `s` once both are done."""
+        weights, acts = self.sets[i]
+        side = self.side
+        side.wait_stream(s)
+        for a in acts:
+            a.quant(side)
+        for w in weights:
+            w.requant(s)
+        s.wait_stream(side)
+        for a in acts:
+            a.gemm(s)
+
+    def step_flops(self):
+        return sum(a.flops for a in self.acts)
 
     def graph(self, fn):
+        """fn(stream, set_index) for every buffer set, captured as one graph."""
         torch = self.torch
         with torch.cuda.stream(self.stream):
-            fn(self.stream)                      # warm (function attributes, module load)
+            fn(self.stream, 0)                   # warm (function attributes, module load)
         torch.cuda.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=self.stream):
-            fn(self.stream)
+            for i in range(self.n_sets):
+                fn(self.stream, i)
         torch.cuda.synchronize()
         return g
 
-    def flush(self):
-        """Evict L2: write one buffer larger than L2, then read another one."""
-        if self.flush_mib > 0:
-            with self.torch.cuda.stream(self.stream):
-                self.flush_w.fill_(1)
-                self.flush_r.sum(dtype=self.torch.int32)
-
-    def time_graph(self, g, reps, flush=True):
-        """Mean device ms of one replay, L2 flushed before each replay (outside the events)."""
+    def time_graph(self, g, replays):
+        """Device ms of `replays` back-to-back replays (one event pair around all)."""
         torch = self.torch
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(self.stream):
-            for i in range(reps):
-                if flush:
-                    self.flush()
-                starts[i].record(self.stream)
+            a.record(self.stream)
+            for _ in range(replays):
                 g.replay()
-                ends[i].record(self.stream)
+            b.record(self.stream)
         torch.cuda.synchronize()
-        return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return a.elapsed_time(b)
+
+    def kernels(self):
+        """(group, label, fn(stream, set), bytes, flops) per launch group of the step."""
+        out = []
+        for wi, w in enumerate(self.weights):
+            out.append(("requant", f"requant_w{wi}",
+                        lambda s, i, wi=wi: self.sets[i][0][wi].requant(s), w.E * w.N * w.K * REQ_B, 0.0))
+        for ai, a in enumerate(self.acts):
+            tag = f"M{a.M}_N{a.w.N}_K{a.K}" + (f"_E{a.E}" if a.E else "")
+            out.append(("act_quant", f"act_quant_{tag}",
+                        lambda s, i, ai=ai: self.sets[i][1][ai].quant(s), a.M * a.K * ACT_B, 0.0))
+            out.append(("gemm", f"gemm_{tag}", lambda s, i, ai=ai: self.sets[i][1][ai].gemm(s), a.gemm_bytes,
+                        a.flops))
+        return out
+
+
+KERNEL_NAMES = {"gemm": "gemm_mxfp4_kernel", "requant": "requant_kernel", "act_quant": "act_quant_kernel"}
 
 
 def run_ours(args):
@@ -256,14 +377,13 @@ def run_ours(args):
 
     __graft_entry__.build()
     from nvfp4_mxfp4_w4a4_gb300 import fp4lin as L
+    from nvfp4_mxfp4_w4a4_gb300 import peak as P
 
-    layer = Layer(L, torch, args.flush_mib)
-    step_graph = layer.graph(layer.step)
-    for _ in range(max(3, args.warmup)):
-        layer.flush()
-        with torch.cuda.stream(layer.stream):
-            step_graph.replay()
-    torch.cuda.synchronize()
+    b = Bench(args.workload, L, torch)
+    step_graph = b.graph(b.step)
+    replays = max(1, -(-args.steps // b.n_sets))
+    steps = replays * b.n_sets
+    b.time_graph(step_graph, max(1, -(-max(3, args.warmup) // b.n_sets)))
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -271,65 +391,88 @@ def run_ours(args):
     barrier(pg)
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
-    times = layer.time_graph(step_graph, args.steps)
+    total_ms = b.time_graph(step_graph, replays)
     torch.cuda.synchronize()
     barrier(pg)
     t_wall = time.perf_counter() - t_wall0
     clk = clocks.stop()
     if L.fp4_get_device_status() != 0:
         raise RuntimeError("device status reports a timeout")
+    times = [total_ms / steps]
 
     ms = statistics.fmean(times)
     ms_max = max_over_ranks(pg, ms, device="cuda")
-    value = world * step_flops() / (ms_max * 1e-3) / 1e12
+    value = world * b.step_flops() / (ms_max * 1e-3) / 1e12
 
-    # per-kernel breakdown: each kernel alone as a graph, L2 flushed before each replay
-    reps = args.breakdown_reps
-    kern = {"requant": (layer.graph(layer.requant), requant_bytes(), 0.0)}
-    for M in MS:
-        kern[f"act_quant_M{M}"] = (layer.graph(lambda s, M=M: layer.act(M, s)), act_bytes(M), 0.0)
-        kern[f"gemm_M{M}"] = (layer.graph(lambda s, M=M: layer.gemm(M, s)), gemm_bytes(M), 2.0 * M * N_W * K_W)
-    hbm_peak, peak_kind = peaks()
-    breakdown = {}
-    for name, (g, nbytes, flops) in kern.items():
-        t = statistics.fmean(layer.time_graph(g, reps))
-        breakdown[name] = {"us": round(t * 1e3, 2), "GBps": round(nbytes / (t * 1e-3) / 1e9, 1),
-                           "hbm_frac": round(nbytes / (t * 1e-3) / 1e9 / hbm_peak, 3)}
+    # per-kernel breakdown: each launch group alone, rotated over the buffer sets in one graph
+    hbm_peak, bf16_peak, peak_kind = peaks()
+    fp4_peak = bf16_peak * FP4_PER_BF16_NOMINAL
+    breakdown, groups = {}, {}
+    for group, label, fn, nbytes, flops in b.kernels():
+        g = b.graph(fn)
+        reps = max(1, -(-args.breakdown_reps // b.n_sets))
+        b.time_graph(g, 1)
+        t = b.time_graph(g, reps) / (reps * b.n_sets) * 1e-3
+        e = {"us": round(t * 1e6, 2), "GBps": round(nbytes / t / 1e9, 1),
+             "hbm_frac": round(nbytes / t / 1e9 / hbm_peak, 3)}
         if flops:
-            breakdown[name]["TFLOPS"] = round(flops / (t * 1e-3) / 1e12, 2)
-            breakdown[name]["pct_fp4_nominal"] = round(100 * flops / (t * 1e-3) / 1e12 / FP4_NOMINAL_TFLOPS, 3)
-    total_us = sum(v["us"] for v in breakdown.values())
-    for v in breakdown.values():
-        v["share"] = round(v["us"] / total_us, 3)
-    dom = max(breakdown, key=lambda k: breakdown[k]["us"])
-    dom_bytes = kern[dom][1]
-    achieved = dom_bytes / (breakdown[dom]["us"] * 1e-6) / 1e9
-    traffic = _committed_traffic(dom)
-    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
-                "unit": "GB/s", "frac": round(achieved / hbm_peak, 3), "traffic": traffic,
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                else "fallback 6800 GB/s"}
+            e["TFLOPS"] = round(flops / t / 1e12, 2)
+            e["tensor_frac"] = round(flops / t / 1e12 / fp4_peak, 4)
+        breakdown[label] = e
+        gsum = groups.setdefault(group, {"s": 0.0, "bytes": 0.0, "flops": 0.0, "n": 0})
+        gsum["s"] += t
+        gsum["bytes"] += nbytes
+        gsum["flops"] += flops
+        gsum["n"] += 1
+    total = sum(v["s"] for v in groups.values())
+    shares = {k: round(v["s"] / total, 3) for k, v in groups.items()}
+    dom = max(groups, key=lambda k: groups[k]["s"])
+    gd = groups[dom]
+    tensor_bound = dom == "gemm" and (gd["flops"] / (fp4_peak * 1e12)) > (gd["bytes"] / (hbm_peak * 1e9))
+    if tensor_bound:
+        achieved = gd["flops"] / gd["s"] / 1e12
+        roofline = {"kernel": KERNEL_NAMES[dom], "bound": "tensor", "achieved": round(achieved, 1),
+                    "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 3),
+                    "peak_source": f"MEASURED_PEAKS bf16_tflops {bf16_peak} x nominal fp4/bf16 ratio 6 "
+                                   f"(of {peak_kind})"}
+    else:
+        achieved = gd["bytes"] / gd["s"] / 1e9
+        roofline = {"kernel": KERNEL_NAMES[dom], "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+                    "unit": "GB/s", "frac": round(achieved / hbm_peak, 3),
+                    "peak_source": f"MEASURED_PEAKS hbm_gbs (of {peak_kind})"}
+    roofline["traffic"] = _committed_traffic(args.workload, roofline["kernel"])
+    roofline["launches_averaged"] = gd["n"]
+    roofline["algorithmic"] = ("bytes: requant 1.09375 B/elem, act-quant 2.53125 B/elem, "
+                               "GEMM 0.53125(M+N)K+2MN(+2N bias); flops 2MNK")
 
-    # end to end through the C ABI from pinned host buffers: H2D of the NVFP4
-    # weight and the activations, the step, D2H of the outputs
-    e2e = _e2e(layer, torch, L, min(args.steps, 50))
+    try:
+        probe = P.measure(n=256, iters=4000)
+        fp4_probe = {"tflops": round(probe["tflops"], 1), "cycles_per_mma": round(probe["cycles_per_mma"], 1),
+                     "what": "tcgen05.mma kind::mxf4 128x256x64 issue-rate probe, all SMs"}
+    except Exception as exc:  # noqa: BLE001
+        fp4_probe = {"error": str(exc)}
 
+    e2e = _e2e(b, torch, L, min(args.steps, 50))
+
+    req = [breakdown[k] for k in breakdown if k.startswith("requant")]
     result = {
-        "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp4 e2m1 (mxfp4) x fp4 -> fp32 acc -> bf16", "data": "synthetic (seeded)",
-        "config": {"workload": WORKLOAD, "N": N_W, "K": K_W, "M": list(MS), "global_batch": sum(MS),
-                   "l2": f"flushed before every timed step ({args.flush_mib} MiB write + {args.flush_mib} MiB "
-                         "read of another buffer, outside the events)",
+        "config": {"workload": b.desc, "name": args.workload, "global_batch": sum(a.M for a in b.acts),
+                   "l2": f"inputs larger than L2: {b.n_sets} rotating buffer sets of "
+                         f"{b.set_bytes / 2 ** 20:.0f} MiB, one graph of {b.n_sets} consecutive steps",
                    "parallelism": f"replicas x{world}", "cuda_graph": True},
-        "requant_GBps": breakdown["requant"]["GBps"],
-        "gemm_TFLOPS": {M: breakdown[f"gemm_M{M}"]["TFLOPS"] for M in MS},
-        "pct_fp4_peak_step": round(100 * value / world / FP4_NOMINAL_TFLOPS, 3),
-        "fp4_peak_used": "15000 TFLOPS nominal dense block-scaled FP4 (public Blackwell Ultra figure)",
-        "breakdown": breakdown, "roofline": roofline, "e2e": e2e, "gpu_launches": 9 * args.steps,
-        "clocks": clk, "wall_s_timed_region": round(t_wall, 3),
+        "requant_GBps": round(sum(r["GBps"] * r["us"] for r in req) / max(1e-9, sum(r["us"] for r in req)), 1),
+        "gemm_TFLOPS": {k: v["TFLOPS"] for k, v in breakdown.items() if "TFLOPS" in v},
+        "pct_fp4_peak_step": {"of_nominal_15PF": round(100 * value / world / FP4_NOMINAL_TFLOPS, 3),
+                              "of_probe": (round(100 * value / world / fp4_probe["tflops"], 3)
+                                           if "tflops" in fp4_probe else None)},
+        "fp4_probe_peak": fp4_probe,
+        "breakdown": breakdown, "shares": shares, "roofline": roofline, "e2e": e2e,
+        "gpu_launches": b.launches_per_step * steps, "clocks": clk, "wall_s_timed_region": round(t_wall, 3),
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and args.workload == "decode":
         result["cpu_baseline"] = cpu_baseline(budget_s=12.0)
     if rank == 0:
         print(json.dumps(result))
@@ -337,40 +480,47 @@ def run_ours(args):
         pg.destroy_process_group()
 
 
-def _committed_traffic(kernel):
-    """DRAM bytes per launch from the committed ncu summary of this kernel, if any."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(p):
-        d = json.load(open(p))
-        return d.get(kernel)
+def _committed_traffic(workload, kernel):
+    """DRAM bytes per launch of `kernel` on `workload` from profiles/traffic.md
+    (table rows `| workload | kernel | source sha256 prefix | bytes |`), if
+    the kernel's source file still matches the recorded hash; else None."""
+    import hashlib
+
+    p = os.path.join(ROOT, "profiles", "traffic.md")
+    src = {"gemm_mxfp4_kernel": "gemm.cu", "requant_kernel": "quant.cu", "act_quant_kernel": "quant.cu"}.get(kernel)
+    if not os.path.exists(p) or src is None:
+        return None
+    sha = hashlib.sha256(open(os.path.join(ROOT, "nvfp4_mxfp4_w4a4_gb300", "csrc", src), "rb").read()).hexdigest()
+    for ln in open(p):
+        f = [x.strip() for x in ln.strip().strip("|").split("|")]
+        if len(f) == 4 and f[0] == workload and f[1] == kernel and f[2] and sha.startswith(f[2]):
+            try:
+                return float(f[3])
+            except ValueError:
+                return None
     return None
 
 
-def _e2e(layer, torch, L, reps):
-    dev = torch.device("cuda")
-    wp_h = layer.w_packed.cpu().pin_memory()
-    ws_h = layer.w_scale.cpu().pin_memory()
-    x_h = {M: layer.x[M].cpu().pin_memory() for M in MS}
-    out_h = {M: torch.empty((M, N_W), dtype=torch.bfloat16).pin_memory() for M in MS}
-    wp_d = torch.empty_like(layer.w_packed)
-    ws_d = torch.empty_like(layer.w_scale)
-    x_d = {M: torch.empty_like(layer.x[M]) for M in MS}
-    s = layer.stream
-    h2d = wp_h.numel() + ws_h.numel() + sum(x.numel() * 2 for x in x_h.values())
-    d2h = sum(o.numel() * 2 for o in out_h.values())
+def _e2e(b, torch, L, reps):
+    """The same step through the C ABI with host buffers: H2D of the NVFP4
+    weights and the activations from pinned memory, the step, D2H of the
+    outputs, all inside the timed events."""
+    s = b.stream
+    host_w = [(w.packed.cpu().pin_memory(), w.scale.cpu().pin_memory()) for w in b.weights]
+    host_x = [a.x.cpu().pin_memory() for a in b.acts]
+    host_o = [torch.empty(a.out.shape, dtype=torch.bfloat16).pin_memory() for a in b.acts]
+    h2d = sum(p.numel() + q.numel() for p, q in host_w) + sum(x.numel() * 2 for x in host_x)
+    d2h = sum(o.numel() * 2 for o in host_o)
 
     def once():
-        wp_d.copy_(wp_h, non_blocking=True)
-        ws_d.copy_(ws_h, non_blocking=True)
-        for M in MS:
-            x_d[M].copy_(x_h[M], non_blocking=True)
-        L.fp4_requant_nvfp4_to_mxfp4(wp_d, ws_d, layer.g, layer.b_packed, layer.b_scale, N_W, K_W, stream=s)
-        for M in MS:
-            L.fp4_quant_act_mxfp4(x_d[M], layer.a_packed[M], layer.a_scale[M], M, K_W, stream=s)
-            L.fp4_gemm_mxfp4(layer.a_packed[M], layer.a_scale[M], layer.b_packed, layer.b_scale, layer.bias,
-                             layer.out[M], M, N_W, K_W, stream=s)
-        for M in MS:
-            out_h[M].copy_(layer.out[M], non_blocking=True)
+        for w, (p, q) in zip(b.weights, host_w):
+            w.packed.copy_(p, non_blocking=True)
+            w.scale.copy_(q, non_blocking=True)
+        for a, x in zip(b.acts, host_x):
+            a.x.copy_(x, non_blocking=True)
+        b.step(s)
+        for a, o in zip(b.acts, host_o):
+            o.copy_(a.out, non_blocking=True)
 
     with torch.cuda.stream(s):
         for _ in range(3):
@@ -379,22 +529,29 @@ def _e2e(layer, torch, L, reps):
     ts = []
     for _ in range(reps):
         a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        layer.flush()
+        e = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(s):
             a.record(s)
             once()
-            b.record(s)
-        b.synchronize()
-        ts.append(a.elapsed_time(b))
+            e.record(s)
+        e.synchronize()
+        ts.append(a.elapsed_time(e))
     ms = statistics.fmean(ts)
-    return {"value": round(step_flops() / (ms * 1e-3) / 1e12, 4), "unit": "TFLOPS", "ms_per_step": round(ms, 4),
+    return {"value": round(b.step_flops() / (ms * 1e-3) / 1e12, 4), "unit": "TFLOPS", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "path": "C ABI, pinned host buffers, H2D + step + D2H inside the events"}
 
 
 # ------------------------------------------------------------------ CPU oracle
+N_W, K_W = 14336, 4096
+MS = (1, 8, 32, 64)
+DECODE_DESC = ("decode layer: W[14336,4096] NVFP4->MXFP4 requant + MXFP4 act-quant + W4A4 GEMM (+bias), "
+               "M in {1,8,32,64}")
 _SAMPLE_CACHE = {}
+
+
+def _decode_flops():
+    return sum(2.0 * M * N_W * K_W for M in MS)
 
 
 def _oracle_inputs(rows_w, threads):
@@ -415,9 +572,10 @@ def _oracle_inputs(rows_w, threads):
 
 
 def _oracle_sample(rows_w, threads):
-    """The oracle on a bounded sample of the step: `rows_w` weight rows are
-    requantized and multiplied with all activation rows (M = 1+8+32+64), and
-    all activations are quantized.  Returns (seconds, fraction of the step)."""
+    """The oracle on a bounded sample of the decode step: `rows_w` weight
+    rows are requantized and multiplied with all activation rows
+    (M = 1+8+32+64), and all activations are quantized.  Returns (seconds,
+    fraction of the step)."""
     import oracle
 
     g, (W, wp, ws) = _oracle_inputs(rows_w, threads)
@@ -439,7 +597,7 @@ def cpu_baseline(budget_s=12.0):
         rows = max(128, rows // 128 * 128)
         dt, frac = _oracle_sample(rows, threads)
     full_s = dt / frac
-    return {"value": round(step_flops() / full_s / 1e12, 6), "unit": "TFLOPS", "cores": threads,
+    return {"value": round(_decode_flops() / full_s / 1e12, 6), "unit": "TFLOPS", "cores": threads,
             "kind": "oracle",
             "sample": f"{rows} of {N_W} weight rows requantized and multiplied with all {sum(MS)} activation "
                       f"rows, all activations quantized; step time extrapolated by {N_W}/{rows} "
@@ -460,12 +618,12 @@ def run_reference(args):
         dt, frac = _oracle_sample(rows, threads)
         ts.append(dt / frac)
     full_s = statistics.fmean(ts)
-    value = step_flops() / full_s / 1e12
+    value = _decode_flops() / full_s / 1e12
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(full_s * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
-        "config": {"workload": WORKLOAD, "N": N_W, "K": K_W, "M": list(MS)},
+        "config": {"workload": DECODE_DESC, "name": "decode"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
                          "sample": f"{rows} of {N_W} weight rows per step, extrapolated"},
         "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

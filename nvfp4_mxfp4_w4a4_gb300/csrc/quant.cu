@@ -14,7 +14,11 @@
 // loads in flight per thread), and writes packed codes with 128/32-bit
 // stores.  Scale bytes for the swizzled layout are gathered with shuffles so
 // that one lane writes the four bytes of a 4-block group as one 32-bit store.
+#include <algorithm>
+#include <mutex>
+
 #include "formats.cuh"
+#include "ptx.cuh"
 #include "internal.h"
 
 namespace fp4lin {
@@ -40,149 +44,309 @@ __device__ __forceinline__ uint32_t ld_stream_u16(const void* p)
 }
 
 // ------------------------------------------------------------ requant
-// One NVFP4 half-block (16 codes in two 32-bit words, one E4M3 scale)
-// contributes its largest magnitude to the block amax.  The largest
-// magnitude code is found with a byte-permute one-hot lookup: each 3-bit
-// magnitude selects byte m of the constant 0x80..01, the OR of all results
-// is the set of magnitudes present.
-__device__ __forceinline__ uint32_t max_magnitude_code(uint32_t w0, uint32_t w1)
+//
+// Work split: a lane owns 4 consecutive 32-element blocks of a row (64 code
+// bytes, 8 E4M3 bytes); a warp owns a chunk of 128 blocks of one row; the
+// grid is persistent and walks (row, chunk) items with the next item's loads
+// in flight while the current one is converted.  The 4 scale bytes a lane
+// produces are one 32-bit word of the swizzled layout.
+//
+// Per half-block (16 codes, one scale s) the output codes come from an
+// 8-entry map magnitude -> code, applied to 8 nibbles at once with byte
+// permutes.  The maps depend only on (s, e - er(s)) for a tensor (fixed g)
+// and are tabulated per CTA in shared memory at kernel start.
+
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint32_t (&r)[8])
 {
-    constexpr uint32_t kOneHotLo = 0x08040201u, kOneHotHi = 0x80402010u;
-    const uint32_t m0 = w0 & 0x77777777u, m1 = w1 & 0x77777777u;
-    uint32_t p = __byte_perm(kOneHotLo, kOneHotHi, m0) | __byte_perm(kOneHotLo, kOneHotHi, m0 >> 16) |
-                 __byte_perm(kOneHotLo, kOneHotHi, m1) | __byte_perm(kOneHotLo, kOneHotHi, m1 >> 16);
-    p |= p >> 16;
-    p |= p >> 8;
-    return 31u - __clz(p & 0xFFu);
+    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "l"(p));
 }
 
-// Output codes of one half-block as an 8-entry map magnitude -> code.  With
-// S = |E4M3 scale| and ag = |g|, the decoded magnitude of code m is
-// RN(G[m] * S * ag).  The products with G in {0.5, 1, 1.5} are each rounded
-// once (H, P, Q); G in {2, 4} and {3, 6} are exact doublings of P and Q
-// (their overflow matches that of the direct product).  Multiplying by 2^-e
-// is exact except in deep underflow, where every code is 0 anyway.  The map
-// is returned as bytes 0..7 of (t0, t1) for byte-permute lookups.
-__device__ __forceinline__ void half_block_code_map(float S, float ag, float se, uint32_t& t0, uint32_t& t1)
+__device__ __forceinline__ void st_v8(void* p, const uint32_t (&r)[8])
 {
-    const float H = __fmul_rn(0.5f * S, ag);
-    const float P = __fmul_rn(S, ag);
-    const float Q = __fmul_rn(1.5f * S, ag);
-    const float h = __fmul_rn(H, se), x = __fmul_rn(P, se), y = __fmul_rn(Q, se);
-    const uint32_t r1 = __float_as_uint(e2m1_code_scaled<0>(h));
-    const uint32_t r2 = __float_as_uint(e2m1_code_scaled<0>(x));
-    const uint32_t r3 = __float_as_uint(e2m1_code_scaled<0>(y));
-    const uint32_t r4 = __float_as_uint(e2m1_code_scaled<1>(x));
-    const uint32_t r5 = __float_as_uint(e2m1_code_scaled<1>(y));
-    const uint32_t r6 = __float_as_uint(e2m1_code_scaled<2>(x));
-    const uint32_t r7 = __float_as_uint(e2m1_code_scaled<2>(y));
-    // byte 1 of kMagic + code is 0x00: use it for the code of magnitude 0
-    const uint32_t a = __byte_perm(r1, r2, 0x1401u);  // [0, r1, r2, -]
-    t0 = __byte_perm(a, r3, 0x4210u);                  // [0, r1, r2, r3]
-    const uint32_t b = __byte_perm(r4, r5, 0x0040u);  // [r4, r5, -, -]
-    const uint32_t c = __byte_perm(r6, r7, 0x4000u);  // [-, -, r6, r7]
-    t1 = __byte_perm(b, c, 0x7610u);                   // [r4, r5, r6, r7]
+    asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
-// Apply the magnitude map to 8 codes in one word and restore the signs
-// (flipped when the scale times g is negative).
-__device__ __forceinline__ uint32_t apply_code_map(uint32_t w, uint32_t t0, uint32_t t1, uint32_t flip)
+__device__ __forceinline__ uint2 ld_nc_u64(const void* p)
 {
-    const uint32_t m = w & 0x77777777u;
-    const uint32_t lo = __byte_perm(t0, t1, m);
-    const uint32_t hi = __byte_perm(t0, t1, m >> 16);
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_nc_u4_cached(const void* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+// Packs the codes of magnitudes 1..7 (each the low byte of kMagic + code)
+// into the two permute-table words [0, r1, r2, r3], [r4, r5, r6, r7].  Byte 1
+// of kMagic + code is 0x00 and supplies the code of magnitude 0.
+__device__ __forceinline__ uint2 pack_code_map(uint32_t r1, uint32_t r2, uint32_t r3, uint32_t r4, uint32_t r5,
+                                               uint32_t r6, uint32_t r7)
+{
+    const uint32_t a = __byte_perm(r1, r2, 0x1401u);
+    const uint32_t b = __byte_perm(r4, r5, 0x0040u);
+    const uint32_t c = __byte_perm(r6, r7, 0x4000u);
+    return make_uint2(__byte_perm(a, r3, 0x4210u), __byte_perm(b, c, 0x7610u));
+}
+
+// Code maps for one tensor (fixed global scale g).  Entry (s, d) holds the
+// map of a half-block with E4M3 scale byte s (sign cleared) when the block
+// exponent is e = er(s) + d, er(s) the unbiased exponent of P = RN(S |g|),
+// d in [-3, 5].  With S = value(s): the decoded magnitudes are H = RN(S/2 |g|),
+// P, Q = RN(1.5 S |g|) for codes 1..3 and the exact doublings 2P, 2Q, 4P, 4Q
+// for codes 4..7 (their overflow matches that of the direct product);
+// multiplying by 2^-e is exact except in deep underflow, where every code
+// is 0 anyway.  A half whose largest code is m >= 1 has amax >= H, so its
+// block exponent is >= er - 3; at d >= 6 every magnitude is below 2^(e-2)
+// and maps to 0 (entry 9).  A half of zero codes reads 0 from any entry.
+// Exponents outside [-127, 126] never occur for a finite block and stay 0.
+// The doubling codes of entry d are the plain codes of entry d - 1
+// (2 x_d = x_{d-1}), so each further entry costs three roundings.
+constexpr int kMapD = 10;
+constexpr int kMapEntries = 128 * kMapD;
+
+__device__ void build_code_maps(float ag, uint2* __restrict__ map)
+{
+    for (int sb = threadIdx.x; sb < 128; sb += blockDim.x) {
+        const float S = e4m3x2_to_float2(static_cast<uint32_t>(sb)).x;
+        const float H = __fmul_rn(0.5f * S, ag);
+        const float P = __fmul_rn(S, ag);
+        const float Q = __fmul_rn(1.5f * S, ag);
+        const int er = static_cast<int>(__float_as_uint(P) >> 23) - 127;
+        uint32_t p2 = 0u, p3 = 0u, p4 = 0u, p5 = 0u;
+        bool prev = false;
+        for (int di = 0; di < 9; ++di) {
+            const int e = er + di - 3;
+            uint2 m = make_uint2(0u, 0u);
+            if (e >= -127 && e <= 126) {
+                const float se = exp2_neg(e);
+                const float h = __fmul_rn(H, se), x = __fmul_rn(P, se), y = __fmul_rn(Q, se);
+                const uint32_t r1 = __float_as_uint(e2m1_code_scaled<0>(h));
+                const uint32_t r2 = __float_as_uint(e2m1_code_scaled<0>(x));
+                const uint32_t r3 = __float_as_uint(e2m1_code_scaled<0>(y));
+                uint32_t r4, r5, r6, r7;
+                if (prev) {
+                    r4 = p2;
+                    r5 = p3;
+                    r6 = p4;
+                    r7 = p5;
+                } else {
+                    r4 = __float_as_uint(e2m1_code_scaled<1>(x));
+                    r5 = __float_as_uint(e2m1_code_scaled<1>(y));
+                    r6 = __float_as_uint(e2m1_code_scaled<2>(x));
+                    r7 = __float_as_uint(e2m1_code_scaled<2>(y));
+                }
+                m = pack_code_map(r1, r2, r3, r4, r5, r6, r7);
+                p2 = r2;
+                p3 = r3;
+                p4 = r4;
+                p5 = r5;
+                prev = true;
+            } else {
+                prev = false;
+            }
+            map[sb * kMapD + di] = m;
+        }
+        map[sb * kMapD + 9] = make_uint2(0u, 0u);
+    }
+}
+
+// Largest magnitude code of each half of a block (words w0,w1 and w2,w3 as
+// magnitude-only nibbles m0..m3, with m0h..m3h = m >> 16): a byte-permute
+// one-hot lookup turns every nibble into bit (1 << m); the OR over a half is
+// the set of magnitudes present and its top bit the largest code.
+__device__ __forceinline__ void max_codes(uint32_t m0, uint32_t m0h, uint32_t m1, uint32_t m1h, uint32_t m2,
+                                          uint32_t m2h, uint32_t m3, uint32_t m3h, uint32_t& mm0, uint32_t& mm1)
+{
+    constexpr uint32_t kLo = 0x08040201u, kHi = 0x80402010u;
+    const uint32_t p0 = __byte_perm(kLo, kHi, m0) | __byte_perm(kLo, kHi, m0h) | __byte_perm(kLo, kHi, m1) |
+                        __byte_perm(kLo, kHi, m1h);
+    const uint32_t p1 = __byte_perm(kLo, kHi, m2) | __byte_perm(kLo, kHi, m2h) | __byte_perm(kLo, kHi, m3) |
+                        __byte_perm(kLo, kHi, m3h);
+    // fold 4 bytes of each half: z = [p0.b0|p0.b2, p1.b0|p1.b2, p0.b1|p0.b3, p1.b1|p1.b3]
+    const uint32_t z = __byte_perm(p0, p1, 0x5140u) | __byte_perm(p0, p1, 0x7362u);
+    const uint32_t w = z | (z >> 16);
+    mm0 = 31u - __clz((w & 0xFFu) | 1u);
+    mm1 = 31u - __clz(((w >> 8) & 0xFFu) | 1u);
+}
+
+// Applies a magnitude map to 8 codes (m = magnitudes, mh = m >> 16) and
+// restores the signs of w (flipped when the scale times g is negative).
+__device__ __forceinline__ uint32_t apply_map(uint32_t w, uint32_t m, uint32_t mh, uint2 t, uint32_t flip)
+{
+    const uint32_t lo = __byte_perm(t.x, t.y, m);
+    const uint32_t hi = __byte_perm(t.x, t.y, mh);
     const uint32_t a = lo | (lo >> 4);
     const uint32_t b = hi | (hi >> 4);
     return __byte_perm(a, b, 0x6420u) | ((w & 0x88888888u) ^ flip);
 }
 
-// One 32-element NVFP4 block (16 code bytes, two E4M3 scales) -> MXFP4.
-__device__ __forceinline__ void requant_block(uint4 codes, uint32_t scales, float ag, uint32_t gsign, int uos,
-                                              uint4& out, uint32_t& sf)
+// One block: codes in 4 words, its two E4M3 scale bytes in `sc` (low byte =
+// elements 0..15).  Returns the scale byte; writes the 4 output words.
+__device__ __forceinline__ uint32_t requant_block(const uint32_t* w, uint32_t sc, float ag, uint32_t gsign, int uos,
+                                                  const uint2* __restrict__ map, uint32_t* out)
 {
-    const float2 s = e4m3x2_to_float2(scales);
+    const float2 s = e4m3x2_to_float2(sc);
     const float S0 = fabsf(s.x), S1 = fabsf(s.y);
-    const uint32_t mm0 = max_magnitude_code(codes.x, codes.y);
-    const uint32_t mm1 = max_magnitude_code(codes.z, codes.w);
+    const uint32_t m0 = w[0] & 0x77777777u, m1 = w[1] & 0x77777777u;
+    const uint32_t m2 = w[2] & 0x77777777u, m3 = w[3] & 0x77777777u;
+    const uint32_t m0h = m0 >> 16, m1h = m1 >> 16, m2h = m2 >> 16, m3h = m3 >> 16;
+    uint32_t mm0, mm1;
+    max_codes(m0, m0h, m1, m1h, m2, m2h, m3, m3h, mm0, mm1);
     const float amax0 = __fmul_rn(__fmul_rn(e2m1_mag_value(mm0), S0), ag);
     const float amax1 = __fmul_rn(__fmul_rn(e2m1_mag_value(mm1), S1), ag);
     const uint32_t ab = max(__float_as_uint(amax0), __float_as_uint(amax1));
     if (ab >= 0x7F800000u) {  // NaN or Inf somewhere in the block
-        out = make_uint4(0u, 0u, 0u, 0u);
-        sf = 0xFFu;
-        return;
+        out[0] = out[1] = out[2] = out[3] = 0u;
+        return 0xFFu;
     }
     const int e = mx_shared_exp(ab, uos);
-    sf = static_cast<uint32_t>(e + 127);
-    const float se = exp2_neg(e);
+    // d + 3 = e - er + 3 = e + 130 - biased exponent of RN(S |g|)
+    const int i0 = min(max(e + 130 - static_cast<int>(__float_as_uint(__fmul_rn(S0, ag)) >> 23), 0), kMapD - 1);
+    const int i1 = min(max(e + 130 - static_cast<int>(__float_as_uint(__fmul_rn(S1, ag)) >> 23), 0), kMapD - 1);
+    const uint2 t0 = map[(sc & 0x7Fu) * kMapD + i0];
+    const uint2 t1 = map[((sc >> 8) & 0x7Fu) * kMapD + i1];
     const uint32_t f0 = ((__float_as_uint(s.x) >> 31) ^ gsign) ? 0x88888888u : 0u;
     const uint32_t f1 = ((__float_as_uint(s.y) >> 31) ^ gsign) ? 0x88888888u : 0u;
-    uint32_t t0, t1;
-    half_block_code_map(S0, ag, se, t0, t1);
-    out.x = apply_code_map(codes.x, t0, t1, f0);
-    out.y = apply_code_map(codes.y, t0, t1, f0);
-    half_block_code_map(S1, ag, se, t0, t1);
-    out.z = apply_code_map(codes.z, t0, t1, f1);
-    out.w = apply_code_map(codes.w, t0, t1, f1);
+    out[0] = apply_map(w[0], m0, m0h, t0, f0);
+    out[1] = apply_map(w[1], m1, m1h, t0, f0);
+    out[2] = apply_map(w[2], m2, m2h, t1, f1);
+    out[3] = apply_map(w[3], m3, m3h, t1, f1);
+    return static_cast<uint32_t>(e + 127);
 }
 
-// Work item = (row, chunk of 32*U consecutive blocks); lane owns block
-// c = chunk*32*U + 32*u + lane.  Rows run over the padded row count when the
-// scales are swizzled so that pad rows and pad block columns get zero bytes.
-template <int U>
+struct RequantLane {
+    uint32_t w[16];  // 4 blocks x 4 code words
+    uint32_t sc[4];  // per block: its two E4M3 bytes
+};
+
+// kFast: the lane's 64 code bytes are 32-byte aligned and its 8 scale bytes
+// 8-byte aligned (K % 128 == 0 and aligned bases) and all 4 blocks exist.
+template <bool kFast>
+__device__ __forceinline__ void requant_lane_load(RequantLane& L, const uint8_t* __restrict__ wp,
+                                                  const uint8_t* __restrict__ ws, int64_t row, int c0, int nreal,
+                                                  int64_t K)
+{
+    const uint8_t* cp = wp + row * (K / 2) + static_cast<int64_t>(c0) * 16;
+    const uint8_t* sp = ws + row * (K / 16) + static_cast<int64_t>(c0) * 2;
+    if (kFast && nreal == 4) {
+        uint32_t a[8], b[8];
+        ld_nc_v8(cp, a);
+        ld_nc_v8(cp + 32, b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            L.w[i] = a[i];
+            L.w[8 + i] = b[i];
+        }
+        const uint2 s2 = ld_nc_u64(sp);
+        L.sc[0] = s2.x & 0xFFFFu;
+        L.sc[1] = s2.x >> 16;
+        L.sc[2] = s2.y & 0xFFFFu;
+        L.sc[3] = s2.y >> 16;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            uint32_t sc = 0u;
+            if (j < nreal) {
+                v = ld_nc_u4_cached(cp + 16 * j);
+                sc = ld_stream_u16(sp + 2 * j);
+            }
+            L.w[4 * j] = v.x;
+            L.w[4 * j + 1] = v.y;
+            L.w[4 * j + 2] = v.z;
+            L.w[4 * j + 3] = v.w;
+            L.sc[j] = sc;
+        }
+    }
+}
+
+template <bool kFast>
 __global__ void __launch_bounds__(kThreads) requant_kernel(const uint8_t* __restrict__ wp,
                                                            const uint8_t* __restrict__ ws, float g,
                                                            uint8_t* __restrict__ op, uint8_t* __restrict__ osf,
                                                            int64_t N, int64_t K, int64_t rows, int kb, int kbp,
                                                            int nch, int uos, int swizzled)
 {
-    const int lane = threadIdx.x & 31;
-    const int64_t item = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-    const int64_t row = item / nch;
-    if (row >= rows)
-        return;
-    const int c0 = static_cast<int>(item - row * nch) * 32 * U + lane;
-    const bool row_real = row < N;
+    __shared__ uint2 map[kMapEntries];
     const float ag = fabsf(g);
     const uint32_t gsign = __float_as_uint(g) >> 31;
-    const uint8_t* wrow = wp + row * (K / 2);
-    const uint8_t* srow = ws + row * (K / 16);
+    build_code_maps(ag, map);  // needs no global memory: overlaps the previous kernel
+    __syncthreads();
+    grid_dependency_wait();
+    launch_dependents();
 
-    uint4 codes[U];
-    uint32_t sc[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int c = c0 + 32 * u;
-        if (row_real && c < kb) {
-            codes[u] = ld_stream_u4(wrow + static_cast<int64_t>(c) * 16);
-            sc[u] = ld_stream_u16(srow + static_cast<int64_t>(c) * 2);
-        } else {
-            codes[u] = make_uint4(0u, 0u, 0u, 0u);
-            sc[u] = 0u;
-        }
-    }
+    const int lane = threadIdx.x & 31;
+    const int64_t n_items = rows * nch;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+    int64_t item = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+    if (item >= n_items)
+        return;
     const int64_t kb4 = kbp >> 2;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int c = c0 + 32 * u;
-        const bool real = row_real && c < kb;
-        uint4 out;
-        uint32_t sf;
-        requant_block(codes[u], sc[u], ag, gsign, uos, out, sf);
-        if (real)
-            *reinterpret_cast<uint4*>(op + row * (K / 2) + static_cast<int64_t>(c) * 16) = out;
-        if (!real)
-            sf = 0u;
-        if (swizzled) {
-            const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sf, 1);
-            const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sf, 2);
-            const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sf, 3);
-            if ((lane & 3) == 0 && c < kbp)
-                *reinterpret_cast<uint32_t*>(osf + sf_swizzled_offset(row, c, kb4)) =
-                    sf | (b1 << 8) | (b2 << 16) | (b3 << 24);
-        } else if (real) {
-            osf[row * kb + c] = static_cast<uint8_t>(sf);
+    int64_t row = item / nch;
+    int c0 = static_cast<int>(item - row * nch) * 128 + 4 * lane;
+    int nreal = row < N ? min(max(kb - c0, 0), 4) : 0;
+    RequantLane cur;
+    requant_lane_load<kFast>(cur, wp, ws, row, c0, nreal, K);
+    while (true) {
+        const int64_t next = item + stride;
+        int64_t nrow = 0;
+        int nc0 = 0, nnreal = 0;
+        RequantLane nxt;
+        if (next < n_items) {
+            nrow = next / nch;
+            nc0 = static_cast<int>(next - nrow * nch) * 128 + 4 * lane;
+            nnreal = nrow < N ? min(max(kb - nc0, 0), 4) : 0;
+            requant_lane_load<kFast>(nxt, wp, ws, nrow, nc0, nnreal, K);
         }
+        uint32_t out[16];
+        uint32_t sfw = 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t sf = requant_block(cur.w + 4 * j, cur.sc[j], ag, gsign, uos, map, out + 4 * j);
+            if (j < nreal)
+                sfw |= sf << (8 * j);
+        }
+        uint8_t* dst = op + row * (K / 2) + static_cast<int64_t>(c0) * 16;
+        if (kFast && nreal == 4) {
+            uint32_t a[8], b[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                a[i] = out[i];
+                b[i] = out[8 + i];
+            }
+            st_v8(dst, a);
+            st_v8(dst + 32, b);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < nreal)
+                    *reinterpret_cast<uint4*>(dst + 16 * j) =
+                        make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
+        }
+        if (swizzled) {
+            if (c0 < kbp)  // pad block columns and pad rows get zero bytes
+                *reinterpret_cast<uint32_t*>(osf + sf_swizzled_offset(row, c0, kb4)) = sfw;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < nreal)
+                    osf[row * kb + c0 + j] = static_cast<uint8_t>(sfw >> (8 * j));
+        }
+        if (next >= n_items)
+            break;
+        item = next;
+        row = nrow;
+        c0 = nc0;
+        nreal = nnreal;
+        cur = nxt;
     }
 }
 
@@ -255,6 +419,8 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
                                                              const int32_t* __restrict__ offsets, int E)
 {
     extern __shared__ int32_t tiles_before[];
+    grid_dependency_wait();
+    launch_dependents();
     if (kGrouped) {
         if (threadIdx.x < 32)
             group_tile_prefix(offsets, E, tiles_before);
@@ -327,6 +493,8 @@ __global__ void __launch_bounds__(kThreads) quant_nvfp4_kernel(const uint16_t* _
                                                                uint8_t* __restrict__ osf, int64_t groups,
                                                                int64_t K)
 {
+    grid_dependency_wait();
+    launch_dependents();
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
     // both threads of a block stay active for the shuffle; t / 2 indexes blocks
     const bool active = t < groups;
@@ -369,21 +537,49 @@ __global__ void __launch_bounds__(kThreads) quant_nvfp4_kernel(const uint16_t* _
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// CTAs of `kern` that fit on the whole GPU at once (per device, cached).
+template <typename Kern>
+int64_t resident_ctas(Kern kern)
+{
+    static std::mutex mu;
+    static int64_t cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 1 << 20;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
+        int sms = 0, per_sm = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0);
+        cached[dev] = std::max<int64_t>(1, static_cast<int64_t>(sms) * std::max(per_sm, 1));
+    }
+    return cached[dev];
+}
+
 }  // namespace
 
 // ------------------------------------------------------------- launchers
 cudaError_t launch_requant(const uint8_t* wp, const uint8_t* ws, float g, uint8_t* op, uint8_t* osf, int64_t N,
                            int64_t K, int alg, int swizzled, cudaStream_t stream)
 {
-    constexpr int U = 4;
     const int kb = static_cast<int>(K / 32);
     const int kbp = swizzled ? static_cast<int>(ceil_div(kb, 4) * 4) : kb;
     const int64_t rows = swizzled ? ceil_div(N, 128) * 128 : N;
-    const int nch = static_cast<int>(ceil_div(kbp, 32 * U));
+    const int nch = static_cast<int>(ceil_div(kbp, 128));
     const int64_t warps = rows * nch;
-    const int64_t blocks = ceil_div(warps * 32, kThreads);
-    requant_kernel<U><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        wp, ws, g, op, osf, N, K, rows, kb, kbp, nch, alg == 2 ? 1 : 0, swizzled);
+    const bool fast = K % 128 == 0 && (reinterpret_cast<uintptr_t>(wp) & 31u) == 0 &&
+                      (reinterpret_cast<uintptr_t>(op) & 31u) == 0 && (reinterpret_cast<uintptr_t>(ws) & 7u) == 0;
+    const int uos = alg == 2 ? 1 : 0;
+    if (fast) {
+        const int64_t blocks = std::min<int64_t>(ceil_div(warps * 32, kThreads), resident_ctas(requant_kernel<true>));
+        return launch_pdl(requant_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, wp, ws,
+                          g, op, osf, N, K, rows, kb, kbp, nch, uos, swizzled);
+    } else {
+        const int64_t blocks =
+            std::min<int64_t>(ceil_div(warps * 32, kThreads), resident_ctas(requant_kernel<false>));
+        return launch_pdl(requant_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, wp,
+                          ws, g, op, osf, N, K, rows, kb, kbp, nch, uos, swizzled);
+    }
     return cudaGetLastError();
 }
 
@@ -398,10 +594,9 @@ cudaError_t launch_act_quant(const void* x, uint8_t* op, uint8_t* osf, int64_t M
     const int64_t blocks = ceil_div(rows * nch * 32, kThreads);
     if (blocks == 0)
         return cudaSuccess;
-    act_quant_kernel<U, false><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        static_cast<const uint16_t*>(x), op, osf, M, K, rows, kb, kbp, nch, alg == 2 ? 1 : 0, swizzled, nullptr,
-        0);
-    return cudaGetLastError();
+    return launch_pdl(act_quant_kernel<U, false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream,
+                      static_cast<const uint16_t*>(x), op, osf, M, K, rows, kb, kbp, nch, alg == 2 ? 1 : 0, swizzled,
+                      static_cast<const int32_t*>(nullptr), 0);
 }
 
 cudaError_t launch_act_quant_grouped(const void* x, const int32_t* offsets, int E, int64_t total_M, int64_t K,
@@ -416,10 +611,9 @@ cudaError_t launch_act_quant_grouped(const void* x, const int32_t* offsets, int 
     if (blocks == 0)
         return cudaSuccess;
     const size_t smem = sizeof(int32_t) * static_cast<size_t>(E + 1);
-    act_quant_kernel<U, true><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(
-        static_cast<const uint16_t*>(x), op, osf, total_M, K, rows, kb, kbp, nch, alg == 2 ? 1 : 0, 1, offsets,
-        E);
-    return cudaGetLastError();
+    return launch_pdl(act_quant_kernel<U, true>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), smem, stream,
+                      static_cast<const uint16_t*>(x), op, osf, total_M, K, rows, kb, kbp, nch, alg == 2 ? 1 : 0, 1,
+                      offsets, E);
 }
 
 cudaError_t launch_quant_nvfp4(const void* x, float g, uint8_t* op, uint8_t* osf, int64_t M, int64_t K,
@@ -429,9 +623,8 @@ cudaError_t launch_quant_nvfp4(const void* x, float g, uint8_t* op, uint8_t* osf
     const int64_t blocks = ceil_div(groups, kThreads);
     if (blocks == 0)
         return cudaSuccess;
-    quant_nvfp4_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(static_cast<const uint16_t*>(x), g,
-                                                                                op, osf, groups, K);
-    return cudaGetLastError();
+    return launch_pdl(quant_nvfp4_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream,
+                      static_cast<const uint16_t*>(x), g, op, osf, groups, K);
 }
 
 }  // namespace fp4lin

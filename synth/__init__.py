@@ -112,8 +112,11 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 
 
 def random_bytes(seed: int, stream: int, n: int, start: int = 0) -> np.ndarray:
-    """n uniform bytes (the low byte of each 64-bit draw)."""
-    return (bits64(seed, stream, start, n) & np.uint64(0xFF)).astype(np.uint8)
+    """n uniform bytes: the 8 bytes of each 64-bit draw, little-endian, in
+    order (byte i is byte i % 8 of draw i // 8).  `start` must be a multiple of 8."""
+    assert start % 8 == 0
+    draws = bits64(seed, stream, start // 8, (n + 7) // 8)
+    return draws.view(np.uint8)[:n].copy()
 
 
 # ---------------------------------------------------------------- tensors
