@@ -43,6 +43,48 @@ __device__ __forceinline__ uint32_t e2m1_code(float z)
     return __float_as_uint(e2m1_code_scaled<0>(z)) & 0xFFu;
 }
 
+// Packed bf16 pairs (two values per 32-bit word, low half first), with
+// round-to-nearest-even and subnormals kept.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_add(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// E2M1 magnitude codes of two non-negative bf16 values q < 8 in one word:
+// the same lower-envelope rounding as e2m1_code_scaled, in bf16 pairs.  The
+// magic constant is 192 = 1.5 * 2^7, whose bf16 ulp is 1, so 192 + y rounds
+// y to an integer (nearest even) for 0 <= y < 64; each half of the result
+// holds 192 + code, i.e. the code in its 3 low mantissa bits.
+__device__ __forceinline__ uint32_t e2m1_codes_bf16x2(uint32_t q)
+{
+    constexpr uint32_t kTwo = 0x40004000u, kHalf = 0x3F003F00u;
+    constexpr uint32_t kM0 = 0x43404340u, kM2 = 0x43424342u, kM4 = 0x43444344u, kM7 = 0x43474347u;
+    const uint32_t a = bf16x2_fma(q, kTwo, kM0);   // 192 + rint(2q)
+    const uint32_t b = bf16x2_add(q, kM2);         // 194 + rint(q)
+    const uint32_t c = bf16x2_fma(q, kHalf, kM4);  // 196 + rint(q/2)
+    return bf16x2_min(bf16x2_min(a, b), bf16x2_min(c, kM7));
+}
+
 // Shared exponent from the fp32 bit pattern of a finite, non-negative amax.
 // For a normal amax = (1 + f) * 2^E the OCP exponent is E - 2 (biased field
 // minus 129); UOS adds one when 1 + f > 1.8125 (mantissa field > 0x680000).

@@ -106,6 +106,13 @@ def test_act_quant_edge_blocks(orc, L):
     r[5] = 0x7F80                      # +Inf in block 0
     r[40] = 0xFFC1                     # NaN in block 1
     rows.append(r)
+    # blocks of subnormals only: the exponent clamps at -127 and the scaled
+    # values reach the codes 1..4 (the kernel must keep subnormal inputs)
+    sub = (np.arange(K) * 5 % 0x80).astype(np.uint16)
+    sub[1::3] |= 0x8000
+    rows.append(sub)
+    rows.append(np.full(K, 0x007F, np.uint16))
+    rows.append((np.arange(K) % 0x81).astype(np.uint16))   # subnormals and the smallest normal
     x = np.stack(rows)
     for alg in (OCP, UOS):
         _check_act(orc, L, x, alg, SWZ)
