@@ -197,7 +197,8 @@ FP4LIN_API fp4_status fp4_gemm_mxfp4(const uint8_t* a, const uint8_t* sa, const 
  *   row_offsets  [E+1] int32 (device); the tile walk is derived on the
  *                device, so no host synchronization is needed
  *   out          [total_M, N] bf16
- * Same shape and alignment rules as fp4_gemm_mxfp4.                        */
+ * Same shape and alignment rules as fp4_gemm_mxfp4, and 1 <= E <= 1024
+ * (FP4_ERR_SHAPE otherwise).                                                */
 FP4LIN_API fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
                                   const uint8_t* sb, const void* bias_bf16, void* out_bf16,
                                   const int32_t* row_offsets, int32_t E, int64_t total_M,

@@ -267,7 +267,7 @@ fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uin
                                   const void* bias_bf16, void* out_bf16, const int32_t* row_offsets, int32_t E,
                                   int64_t total_M, int64_t N, int64_t K, void* stream)
 {
-    if (E <= 0 || E > 4096)
+    if (E <= 0 || E > fp4lin::kMaxGroupedExperts)
         return FP4_ERR_SHAPE;
     if (total_M > 0 && !row_offsets)
         return FP4_ERR_INVALID_ARG;

@@ -10,22 +10,31 @@
 // MXFP4 Quantization" (Configuration) and "[SGLang] FP4 ..." (section 6).
 //
 // Design: one persistent CTA per SM walks output tiles (the MMA-M operand's
-// 128-row tile fastest).  10 warps:
-//   warp 0      TMA producer: for every (tile, 256-element K stage) the two
-//               operand tiles (tensor maps, 128-byte swizzle) and the matching
-//               512-byte scale chunks (bulk copies) into a ring of smem stages
-//               that runs on across tile boundaries.
-//   warp 1      TMEM owner and MMA issuer: per stage, tcgen05.cp moves the
-//               scale chunks into TMEM and four tcgen05.mma kind::mxf4 (K = 64,
-//               two E8M0 scales per row each) accumulate into a 128 x BN fp32
-//               TMEM tile; tcgen05.commit frees the stage, and at the end of
-//               a tile signals the epilogue.
-//   warps 2-9   epilogue: each warp reads 32 TMEM lanes x BN/2 columns into
+// 128-row tile fastest).  A pipeline stage holds KC slabs of 128 packed
+// bytes (256 elements) of K for both operands.  12 warps:
+//   warp 0      TMA producer: per (tile, stage) one tensor-map load per
+//               operand (a 3-D box spanning the KC slabs when KC > 1: the
+//               TMA unit keeps only a few copies in flight per SM, so fewer,
+//               larger copies stream faster) plus one bulk copy of the
+//               matching scale chunks per 128-row scale tile, into a ring of
+//               smem stages that runs on across tile boundaries.
+//   warp 1      TMEM owner and MMA issuer: per stage, 4 * KC tcgen05.mma
+//               kind::mxf4 (K = 64, two E8M0 scales per row each) accumulate
+//               into a 128 x BN fp32 TMEM tile; tcgen05.commit frees the
+//               stage, and at the end of a tile signals the epilogue.
+//   warps 2-3   scale movers: per stage, tcgen05.cp of the scale chunks from
+//               smem into that stage's TMEM scale columns, split between the
+//               two warps.  A thread's copies run one after another at about
+//               a hundred cycles each, so one thread issuing both copies and
+//               MMAs would serialise them; on separate threads they overlap
+//               the MMAs of the previous stage.
+//   warps 4-11  epilogue: each warp reads 32 TMEM lanes x BN/2 columns into
 //               registers, releases the accumulator at once (so the next
-//               tile's MMAs start), then adds bias, rounds to bf16 and stores.
+//               tile's MMAs start), adds bias, rounds to bf16, stages the
+//               tile in shared memory and writes it with TMA tensor stores.
 // Orientation: the MMA-M operand is A (activations) in the normal mode and
 // the weights in the swapped mode used for small M (decode); there the
-// tokens are the MMA N dimension and the epilogue writes the transpose.
+// tokens are the MMA N dimension and the staged tile is the transpose.
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the status word and winds down.
 #include <cuda_bf16.h>
@@ -41,9 +50,12 @@ namespace fp4lin {
 namespace {
 
 constexpr int BM = 128;
-constexpr int kStageKBytes = 128;  // packed bytes of K per row per stage (256 elements)
+constexpr int kSlabBytes = 128;  // packed bytes of K per row per slab (256 elements)
+constexpr int kCpWarps = 2;
+constexpr int kFirstEpiWarp = 2 + kCpWarps;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
+constexpr int kChunk = 32;      // normal-mode store chunk: 32 rows x 32 columns per warp
 
 struct GemmParams {
     const uint8_t* sfa;         // swizzled scales of the MMA-M operand
@@ -63,30 +75,36 @@ struct GemmParams {
     unsigned int* status;
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int KC, bool kSwap>
 struct Cfg {
-    static constexpr int A_BYTES = BM * kStageKBytes;
-    static constexpr int B_BYTES = BN * kStageKBytes;
+    static constexpr int GROUPS = 2 * KC;  // 128-element scale groups per stage
+    static constexpr int A_BYTES = BM * kSlabBytes * KC;
+    static constexpr int B_BYTES = BN * kSlabBytes * KC;
     static constexpr int SFB_TILES = (BN + 127) / 128;
-    static constexpr int SFA_BYTES = 1024;  // 2 groups x 512 B
-    static constexpr int SFB_BYTES = SFB_TILES * 1024;
+    static constexpr int SFA_BYTES = GROUPS * 512;
+    static constexpr int SFB_BYTES = SFB_TILES * GROUPS * 512;
+    static constexpr int EPI_BYTES = kSwap ? BN * BM * 2 : kEpiWarps * kChunk * kChunk * 2;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-    static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 2;
+    static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
+    static constexpr int NUM_BARS = 3 * STAGES + 4;
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_PREFIX = OFF_TMEM_SLOT + 16;
     static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;  // + 1 KB alignment slack
-    static constexpr int SF_COLS_A = 8;
+    static constexpr int SF_COLS_A = 4 * GROUPS;
     static constexpr int SF_COLS_B_GROUP = 4 * SFB_TILES;
-    static constexpr int SF_COLS = SF_COLS_A + 2 * SF_COLS_B_GROUP;
-    static constexpr int TMEM_USED = BN + 2 * SF_COLS;
+    static constexpr int SF_COLS = SF_COLS_A + GROUPS * SF_COLS_B_GROUP;
+    static constexpr int TMEM_USED = BN + STAGES * SF_COLS;  // one scale buffer per smem stage
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                      : TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= 512, "TMEM overflow");
+    static_assert(OFF_EPI % 1024 == 0, "staging alignment (swizzled store boxes)");
+    static_assert(SMEM_FIXED <= 232448, "shared memory budget");
     static constexpr int CW = BN / 2;  // accumulator columns per epilogue warp
+    static_assert(kSwap || CW % kChunk == 0, "normal-mode columns per warp must be whole store chunks");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
@@ -97,7 +115,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 
 struct Tile {
     int64_t a_row0;  // first MMA-M row
-    int rows_valid;  // MMA-M rows of this tile inside the problem
+    int rows_valid;  // MMA-M rows of this tile inside the problem (inside the expert when grouped)
     int sfa_rt;      // scale row tile of the MMA-M operand
     int n0;          // first MMA-N row
     int expert;
@@ -152,25 +170,37 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* v)
     }
 }
 
-template <int BN, int STAGES, bool kSwap, bool kGrouped>
+template <int KC>
+__device__ __forceinline__ void load_operand(void* dst, const CUtensorMap* map, uint64_t* bar, int kb, int64_t row0)
+{
+    if constexpr (KC == 1)
+        tma_load_2d(dst, map, bar, kb * kSlabBytes, static_cast<int32_t>(row0));
+    else
+        tma_load_3d(dst, map, bar, 0, static_cast<int32_t>(row0), kb * KC);
+}
+
+template <int BN, int STAGES, int KC, bool kSwap, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const GemmParams p)
+                      const __grid_constant__ CUtensorMap tmO, const GemmParams p)
 {
-    using C = Cfg<BN, STAGES>;
+    using C = Cfg<BN, STAGES, KC, kSwap>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     uint64_t* empty = full + STAGES;
-    uint64_t* accum_full = empty + STAGES;
+    uint64_t* sf_full = empty + STAGES;
+    uint64_t* accum_full = sf_full + STAGES;
     uint64_t* accum_empty = accum_full + 1;
+    uint64_t* epi_full = accum_empty + 1;  // swapped mode: the staged tile is complete
+    uint64_t* epi_free = epi_full + 1;     // swapped mode: the staged tile has been read by its store
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
     int32_t* tiles_before = reinterpret_cast<int32_t*>(smem + C::OFF_PREFIX);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int total_tiles = p.m_tiles * p.n_tiles;
-    const int nkb = (p.K + 255) / 256;
+    const int nkb = (p.kb4 + C::GROUPS - 1) / C::GROUPS;  // stages per tile
 
     // ------------------------------------------------------------ setup
     // (no global memory is touched before the dependency wait: this part
@@ -179,12 +209,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_full[s], kCpWarps);
         }
         mbar_init(accum_full, 1);
         mbar_init(accum_empty, kEpiWarps);
+        mbar_init(epi_full, kEpiWarps);
+        mbar_init(epi_free, 1);
         fence_mbar_init();
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
+        tma_prefetch_map(&tmO);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -239,19 +273,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const int groups = min(2, p.kb4 - 2 * kb);
+                    const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
                     const uint32_t sf_bytes = static_cast<uint32_t>(groups) * 512u;
+                    // boxes past the end of K or of the rows are zero-filled and still counted
                     mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES + sf_bytes * (1u + nsfb));
-                    tma_load_2d(smem + C::OFF_A + s * C::A_BYTES, &tmA, &full[s], kb * kStageKBytes,
-                                static_cast<int32_t>(T.a_row0));
-                    tma_load_2d(smem + C::OFF_B + s * C::B_BYTES, &tmB, &full[s], kb * kStageKBytes,
-                                static_cast<int32_t>(b_row0));
+                    load_operand<KC>(smem + C::OFF_A + s * C::A_BYTES, &tmA, &full[s], kb, T.a_row0);
+                    load_operand<KC>(smem + C::OFF_B + s * C::B_BYTES, &tmB, &full[s], kb, b_row0);
                     bulk_load(smem + C::OFF_SFA + s * C::SFA_BYTES,
-                              p.sfa + (static_cast<int64_t>(T.sfa_rt) * p.kb4 + 2 * kb) * 512, sf_bytes, &full[s]);
+                              p.sfa + (static_cast<int64_t>(T.sfa_rt) * p.kb4 + C::GROUPS * kb) * 512, sf_bytes,
+                              &full[s]);
                     for (int j = 0; j < nsfb; ++j)
-                        bulk_load(smem + C::OFF_SFB + s * C::SFB_BYTES + j * 1024,
-                                  sfb + (static_cast<int64_t>(T.n0 / 128 + j) * p.kb4 + 2 * kb) * 512, sf_bytes,
-                                  &full[s]);
+                        bulk_load(smem + C::OFF_SFB + s * C::SFB_BYTES + j * C::GROUPS * 512,
+                                  sfb + (static_cast<int64_t>(T.n0 / 128 + j) * p.kb4 + C::GROUPS * kb) * 512,
+                                  sf_bytes, &full[s]);
                 }
             }
         }
@@ -274,31 +308,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = static_cast<int>(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
-                    if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, kWaitLimitNs)) {
+                    if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, kWaitLimitNs) ||
+                        !mbar_wait_bounded(&sf_full[s], ph, p.status, kStatusTimeout, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const int groups = min(2, p.kb4 - 2 * kb);
-                    const uint32_t sfa_t = tmem_base + BN + (it & 1u) * C::SF_COLS;
+                    const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
+                    const uint32_t sfa_t = tmem_base + BN + s * C::SF_COLS;
                     const uint32_t sfb_t = sfa_t + C::SF_COLS_A;
-                    const uint32_t sfa_s = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
-                    const uint32_t sfb_s = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
-                    for (int g = 0; g < groups; ++g) {
-                        tc_cp_32x128b_warpx4(sfa_t + 4 * g, smem_desc(sfa_s + 512 * g, 0, 128, 0));
-#pragma unroll
-                        for (int j = 0; j < C::SFB_TILES; ++j)
-                            tc_cp_32x128b_warpx4(sfb_t + g * C::SF_COLS_B_GROUP + 4 * j,
-                                                 smem_desc(sfb_s + 1024 * j + 512 * g, 0, 128, 0));
-                    }
                     const uint32_t a_s = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
                     const uint32_t b_s = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
                     for (int k = 0; k < 2 * groups; ++k) {
+                        // k-th 64-element step: slab k / 4, 32-byte column k % 4, scale group k / 2
+                        const int slab = k >> 2;
                         const int g = k >> 1;
                         const uint32_t sf_id = static_cast<uint32_t>(k & 1) * 2u;
-                        tc_mma_mxf4(tmem_base, smem_desc(a_s + 32 * k, 16, 1024, 2),
-                                    smem_desc(b_s + 32 * k, 16, 1024, 2), idesc_with_sf_id(idesc, sf_id),
-                                    sfa_t + 4 * g, sfb_t + g * C::SF_COLS_B_GROUP, (kb | k) != 0 ? 1u : 0u);
+                        tc_mma_mxf4(tmem_base, smem_desc(a_s + slab * (BM * kSlabBytes) + 32 * (k & 3), 16, 1024, 2),
+                                    smem_desc(b_s + slab * (BN * kSlabBytes) + 32 * (k & 3), 16, 1024, 2),
+                                    idesc_with_sf_id(idesc, sf_id), sfa_t + 4 * g, sfb_t + g * C::SF_COLS_B_GROUP,
+                                    (kb | k) != 0 ? 1u : 0u);
                     }
                     tc_commit(&empty[s]);
                 }
@@ -306,12 +335,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++tcount;
             }
         }
+    } else if (warp < kFirstEpiWarp) {
+        if (lane == 0) {
+            // ------------------------------------------------ scale movers
+            // Copy q of a stage (q = g * (1 + SFB_TILES) + i: i = 0 the
+            // MMA-M operand's chunk of group g, i = 1 + j the MMA-N
+            // operand's row tile j) belongs to warp 2 + q % kCpWarps.
+            const int me = warp - 2;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                const Tile T = decode_tile<BN, kGrouped>(t, p, tiles_before);
+                if (!T.valid)
+                    continue;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = static_cast<int>(it % STAGES);
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
+                    const uint32_t sfa_t = tmem_base + BN + s * C::SF_COLS;
+                    const uint32_t sfb_t = sfa_t + C::SF_COLS_A;
+                    const uint32_t sfa_s = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
+                    const uint32_t sfb_s = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
+#pragma unroll
+                    for (int q = me; q < C::GROUPS * (1 + C::SFB_TILES); q += kCpWarps) {
+                        const int g = q / (1 + C::SFB_TILES);
+                        const int i = q % (1 + C::SFB_TILES);
+                        if (g >= groups)
+                            break;
+                        if (i == 0)
+                            tc_cp_32x128b_warpx4(sfa_t + 4 * g, smem_desc(sfa_s + 512 * g, 0, 128, 0));
+                        else
+                            tc_cp_32x128b_warpx4(sfb_t + g * C::SF_COLS_B_GROUP + 4 * (i - 1),
+                                                 smem_desc(sfb_s + (i - 1) * C::GROUPS * 512 + 512 * g, 0, 128, 0));
+                    }
+                    tc_commit(&sf_full[s]);  // arrives once this thread's copies have landed
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------ epilogue
-        const int quad = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int ew = warp - kFirstEpiWarp;
+        const int quad = warp & 3;  // TMEM lanes 32 * quad ... (a warp reaches only its own quarter)
+        const int half = ew >> 2;
         constexpr int CW = C::CW;
+        uint8_t* epi = smem + C::OFF_EPI;
         uint32_t tcount = 0;
+        bool stored = false;  // this thread has bulk stores in flight
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
             const Tile T = decode_tile<BN, kGrouped>(t, p, tiles_before);
             if (!T.valid)
@@ -330,21 +404,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             const int r = quad * 32 + lane;
             const __nv_bfloat16* bias = p.bias ? p.bias + static_cast<int64_t>(T.expert) * p.ldo : nullptr;
-            if constexpr (!kSwap) {
-                // lane = output row; columns n0 + half*CW + [0, CW)
-                if (r < T.rows_valid) {
-                    __nv_bfloat16* orow = p.out + (T.a_row0 + r) * static_cast<int64_t>(p.ldo);
+            if constexpr (kSwap) {
+                // lane = output column n (weight row); tile columns = tokens.
+                // Stage [BN tokens][128 n] and store the box in one copy,
+                // handed between the warps by two mbarriers (bounded waits).
+                const uint32_t eph = (tcount - 1) & 1u;
+                if (!mbar_wait_bounded(epi_free, eph ^ 1u, p.status, kStatusTimeout, kWaitLimitNs))
+                    break;
+                const int64_t n = T.a_row0 + r;
+                const float bn = (bias && r < T.rows_valid) ? __bfloat162float(bias[n]) : 0.0f;
+                __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(epi);
 #pragma unroll
-                    for (int j = 0; j < CW; j += 8) {
-                        const int col = T.n0 + half * CW + j;
-                        if (col >= p.ldo)
-                            break;
+                for (int j = 0; j < CW; ++j)
+                    stg[(half * CW + j) * BM + r] = __float2bfloat16_rn(__uint_as_float(v[j]) + bn);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(epi_full);
+                if (ew == 0 && lane == 0) {
+                    if (mbar_wait_bounded(epi_full, eph, p.status, kStatusTimeout, kWaitLimitNs)) {
+                        tma_store_2d(&tmO, stg, static_cast<int32_t>(T.a_row0), T.n0);
+                        bulk_commit_group();
+                        bulk_wait_group_read0();
+                        stored = true;
+                    }
+                    mbar_arrive(epi_free);
+                }
+            } else {
+                // lane = output row; this warp's columns n0 + half*CW + [0, CW)
+                // go out in 32 x 32 chunks through its own staging area, in the
+                // 64-byte swizzled layout of the output map (16-byte piece q of
+                // row i sits at piece position q ^ ((i / 2) % 4)), which keeps
+                // the rows of one store phase on different banks.
+                uint8_t* stg = epi + ew * (kChunk * kChunk * 2);
+                uint8_t* my_row = stg + lane * (kChunk * 2);
+                const int rot = (lane >> 1) & 3;
+                // rows past the end of this expert belong to the next one:
+                // there a chunk is stored row by row instead
+                const bool whole = !kGrouped || quad * 32 + 31 < T.rows_valid;
+#pragma unroll
+                for (int c = 0; c < CW; c += kChunk) {
+                    const int col0 = T.n0 + half * CW + c;
+                    if (whole) {
+                        if (lane == 0 && stored)
+                            bulk_wait_group_read0();  // the previous chunk has left the staging area
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int j = 0; j < kChunk; j += 8) {
                         float f[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            f[i] = __uint_as_float(v[j + i]);
-                        if (bias) {
-                            const uint4 bb = *reinterpret_cast<const uint4*>(bias + col);
+                            f[i] = __uint_as_float(v[c + j + i]);
+                        if (bias && col0 + j < p.ldo) {
+                            const uint4 bb = *reinterpret_cast<const uint4*>(bias + col0 + j);
                             const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
@@ -352,29 +465,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 f[2 * i + 1] += __uint_as_float(bw[i] & 0xFFFF0000u);
                             }
                         }
-                        uint4 o;
-                        o.x = pack_bf16x2(f[0], f[1]);
-                        o.y = pack_bf16x2(f[2], f[3]);
-                        o.z = pack_bf16x2(f[4], f[5]);
-                        o.w = pack_bf16x2(f[6], f[7]);
-                        *reinterpret_cast<uint4*>(orow + col) = o;
+                        const uint4 o = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                                   pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+                        if (whole)
+                            *reinterpret_cast<uint4*>(my_row + (((j >> 3) ^ rot) << 4)) = o;
+                        else if (r < T.rows_valid && col0 + j < p.ldo)
+                            *reinterpret_cast<uint4*>(p.out + (T.a_row0 + r) * static_cast<int64_t>(p.ldo) + col0 + j) = o;
                     }
-                }
-            } else {
-                // lane = output column (weight row n); columns of the tile = tokens
-                const int64_t n = T.a_row0 + r;
-                if (r < T.rows_valid) {
-                    const float bn = bias ? __bfloat162float(bias[n]) : 0.0f;
-#pragma unroll
-                    for (int j = 0; j < CW; ++j) {
-                        const int tok = T.n0 + half * CW + j;
-                        if (tok < p.rows_b)
-                            p.out[static_cast<int64_t>(tok) * p.ldo + n] =
-                                __float2bfloat16_rn(__uint_as_float(v[j]) + bn);
+                    if (whole) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmO, stg, col0, static_cast<int32_t>(T.a_row0 + quad * 32));
+                            bulk_commit_group();
+                            stored = true;
+                        }
                     }
                 }
             }
         }
+        if (stored)
+            bulk_wait_group0();  // stores complete before the CTA exits
     }
 
     tc_fence_before_sync();
@@ -405,18 +516,48 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// [rows, K/2] packed bytes, box = 128 bytes x box_rows, 128-byte swizzle.
-bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows)
+// Packed operand [rows, K/2] bytes, 128-byte swizzle.  KC == 1: 2-D boxes of
+// 128 bytes x box_rows.  KC > 1 (needs K % 256 == 0): the rows viewed as
+// K/256 slabs of 128 bytes, 3-D boxes of 128 bytes x box_rows x KC slabs,
+// which land in shared memory as KC consecutive [box_rows][128 B] slabs.
+bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows, int kc)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kStageKBytes), static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (kc == 1) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kSlabBytes), static_cast<cuuint32_t>(box_rows)};
+        return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kSlabBytes), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(K / 256)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(kSlabBytes)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kSlabBytes), static_cast<cuuint32_t>(box_rows),
+                               static_cast<cuuint32_t>(kc)};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 output [rows, cols] (row stride cols), boxes of box_cols x box_rows
+// taken from shared memory with the given swizzle.
+bool make_output_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int box_cols, int box_rows,
+                     CUtensorMapSwizzle swizzle)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -434,19 +575,22 @@ int sm_count()
     return cached[dev];
 }
 
-template <int BN, int STAGES, bool kSwap, bool kGrouped>
+template <int BN, int STAGES, int KC, bool kSwap, bool kGrouped>
 cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
 {
-    using C = Cfg<BN, STAGES>;
+    using C = Cfg<BN, STAGES, KC, kSwap>;
     // MMA-M operand / MMA-N operand
     const uint8_t* opA = kSwap ? a.b : a.a;
     const uint8_t* opB = kSwap ? a.a : a.b;
     const int64_t rows_a = kSwap ? a.N : a.M;
     const int64_t rows_b = kSwap ? a.M : a.N;
-    CUtensorMap tmA, tmB;
-    if (!make_operand_map(&tmA, opA, rows_a, a.K, BM))
+    CUtensorMap tmA, tmB, tmO;
+    if (!make_operand_map(&tmA, opA, rows_a, a.K, BM, KC))
         return cudaErrorInvalidValue;
-    if (!make_operand_map(&tmB, opB, static_cast<int64_t>(a.E) * rows_b, a.K, BN))
+    if (!make_operand_map(&tmB, opB, static_cast<int64_t>(a.E) * rows_b, a.K, BN, KC))
+        return cudaErrorInvalidValue;
+    if (!(kSwap ? make_output_map(&tmO, a.out, a.M, a.N, BM, BN, CU_TENSOR_MAP_SWIZZLE_NONE)
+                : make_output_map(&tmO, a.out, a.M, a.N, kChunk, kChunk, CU_TENSOR_MAP_SWIZZLE_64B)))
         return cudaErrorInvalidValue;
     GemmParams p;
     p.sfa = kSwap ? a.sb : a.sa;
@@ -470,7 +614,7 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
         return cudaSuccess;
     const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count()));
     const size_t smem = C::SMEM_FIXED + (kGrouped ? sizeof(int32_t) * (a.E + 1) : 0);
-    auto kern = gemm_mxfp4_kernel<BN, STAGES, kSwap, kGrouped>;
+    auto kern = gemm_mxfp4_kernel<BN, STAGES, KC, kSwap, kGrouped>;
     // The shared-memory opt-in is a per-device function attribute: set it
     // once per device (and grow it if a larger grouped prefix needs more).
     static std::mutex mu;
@@ -488,26 +632,36 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
             configured[dev] = smem;
         }
     }
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, tmA, tmB, p);
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, tmA, tmB, tmO, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream)
 {
+    // Stages of two slabs need the 3-D operand view, which needs
+    // K % 256 == 0; otherwise the one-slab configurations run.
+    const bool k256 = a.K % 256 == 0;
+    const int64_t m_tiles =
+        a.row_offsets != nullptr ? (a.M + static_cast<int64_t>(a.E) * 127) / 128 : (a.M + 127) / 128;
+    const bool wide = a.N >= 256 && m_tiles * ((a.N + 255) / 256) >= 148;
     if (a.row_offsets != nullptr) {
-        const int64_t m_tiles = (a.M + static_cast<int64_t>(a.E) * 127) / 128;
-        const bool wide = a.N >= 256 && m_tiles * ((a.N + 255) / 256) >= 148;
-        return wide ? launch_kernel<256, 4, false, true>(a, stream) : launch_kernel<128, 6, false, true>(a, stream);
+        if (wide)
+            return launch_kernel<256, 4, 1, false, true>(a, stream);
+        return k256 ? launch_kernel<128, 3, 2, false, true>(a, stream)
+                    : launch_kernel<128, 6, 1, false, true>(a, stream);
     }
     // decode-sized batches: weights on the 128-row MMA side, tokens as N
-    if (a.M <= 32)
-        return launch_kernel<32, 8, true, false>(a, stream);
-    if (a.M <= 64)
-        return launch_kernel<64, 8, true, false>(a, stream);
-    const int64_t m_tiles = (a.M + 127) / 128;
-    const bool wide = a.N >= 256 && m_tiles * ((a.N + 255) / 256) >= 148;
-    return wide ? launch_kernel<256, 4, false, false>(a, stream) : launch_kernel<128, 6, false, false>(a, stream);
+    if (a.M <= 64) {
+        if (!k256)
+            return launch_kernel<64, 8, 1, true, false>(a, stream);
+        return a.M <= 32 ? launch_kernel<32, 4, 2, true, false>(a, stream)
+                         : launch_kernel<64, 4, 2, true, false>(a, stream);
+    }
+    if (wide)
+        return launch_kernel<256, 4, 1, false, false>(a, stream);
+    return k256 ? launch_kernel<128, 3, 2, false, false>(a, stream)
+                : launch_kernel<128, 6, 1, false, false>(a, stream);
 }
 
 }  // namespace fp4lin

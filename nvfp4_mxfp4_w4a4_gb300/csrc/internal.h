@@ -32,6 +32,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // Status word bits a kernel sets in the library-owned device status word.
 constexpr unsigned int kStatusTimeout = 1u;
 
+// Largest expert count of the grouped GEMM (its tile walk keeps a per-expert
+// prefix in shared memory).
+constexpr int kMaxGroupedExperts = 1024;
+
 // Upper bound of every bounded device wait (nanoseconds of wall time).
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
