@@ -181,6 +181,8 @@ class Weight:
         self.sf_bytes = L.fp4_sf_bytes(N, K)
         self.b_scale = torch.empty(self.E * self.sf_bytes, dtype=torch.uint8, device=dev)
         self.bias = None if bias is None else torch.from_numpy(bias.view(np.int16)).to(dev).view(torch.bfloat16)
+        # per-expert global scales on the device for the grouped requant
+        self.g_dev = torch.tensor(np.float32(self.g), dtype=torch.float32, device=dev)
 
     def clone(self):
         c = object.__new__(Weight)
@@ -191,6 +193,10 @@ class Weight:
 
     def requant(self, s):
         N, K = self.N, self.K
+        if self.E > 1:  # all experts in one launch
+            self.L.fp4_requant_nvfp4_to_mxfp4_grouped(self.packed, self.scale, self.g_dev, self.b_packed,
+                                                      self.b_scale, self.E, N, K, stream=s)
+            return
         for e in range(self.E):
             self.L.fp4_requant_nvfp4_to_mxfp4(self.packed[e * N:(e + 1) * N], self.scale[e * N:(e + 1) * N],
                                               self.g[e], self.b_packed[e * N:(e + 1) * N],
@@ -305,7 +311,7 @@ class Bench:
 
     @property
     def launches_per_step(self):
-        return sum(w.E for w in self.weights) + 2 * len(self.acts)
+        return len(self.weights) + 2 * len(self.acts)
 
     def step(self, s, i=0):
         """Requant on `s`; the activation quantizers (independent of it) on a

@@ -131,6 +131,23 @@ FP4LIN_API fp4_status fp4_requant_nvfp4_to_mxfp4_ex(const uint8_t* w_packed, con
                                          int64_t N, int64_t K, const fp4_quant_opts* opts,
                                          void* stream);
 
+/* The same requantization for E tensors of one shape in one launch (all
+ * experts of a MoE layer at load time, [AMD] "Native FP4 matmul": MoE
+ * experts on MXFP4), each with its own global scale.
+ *   w_packed      [E][N][K/2] u8, w_scale_e4m3 [E][N][K/16] u8 (device)
+ *   w_global      [E] f32 (DEVICE array), multiplicative as above
+ *   out_packed    [E][N][K/2] u8
+ *   out_scale     E consecutive arrays of fp4_sf_bytes(N, K, layout) bytes
+ *                 (the per-expert scale layout fp4_gemm_mxfp4_grouped reads)
+ * Tensor e is bit-identical to fp4_requant_nvfp4_to_mxfp4_ex on its slices
+ * with w_global[e].  Requires 1 <= E <= 4096, N >= 1, K a positive multiple
+ * of 128, 32-byte aligned packed pointers, an 8-byte aligned w_scale_e4m3,
+ * a 4-byte aligned out_scale (swizzled) and w_global.                       */
+FP4LIN_API fp4_status fp4_requant_nvfp4_to_mxfp4_grouped(const uint8_t* w_packed, const uint8_t* w_scale_e4m3,
+                                              const float* w_global, uint8_t* out_packed,
+                                              uint8_t* out_scale, int32_t E, int64_t N, int64_t K,
+                                              const fp4_quant_opts* opts, void* stream);
+
 /* ------------------------------------------------- activation quantizer */
 
 /* Dynamic MXFP4 quantization of bf16 activations ([AMD] serve-time path:

@@ -158,6 +158,29 @@ fp4_status fp4_requant_nvfp4_to_mxfp4(const uint8_t* w_packed, const uint8_t* w_
                                          stream);
 }
 
+fp4_status fp4_requant_nvfp4_to_mxfp4_grouped(const uint8_t* w_packed, const uint8_t* w_scale_e4m3,
+                                              const float* w_global, uint8_t* out_packed, uint8_t* out_scale,
+                                              int32_t E, int64_t N, int64_t K, const fp4_quant_opts* opts,
+                                              void* stream)
+{
+    int alg, swz;
+    fp4_status st = check_opts(opts, &alg, &swz);
+    if (st != FP4_OK)
+        return st;
+    if (!w_packed || !w_scale_e4m3 || !w_global || !out_packed || !out_scale)
+        return FP4_ERR_INVALID_ARG;
+    if (E <= 0 || E > 4096 || N <= 0 || K <= 0 || K % 128 != 0 || N >= kMaxDim || K >= kMaxDim ||
+        static_cast<int64_t>(E) * N >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    if (!fp4lin::requant_flat_ok(w_packed, w_scale_e4m3, out_packed, out_scale, K, swz) ||
+        (reinterpret_cast<uintptr_t>(w_global) & 3u))
+        return FP4_ERR_ALIGNMENT;
+    if ((st = current_device(nullptr)) != FP4_OK)
+        return st;
+    return from_cuda(fp4lin::launch_requant_grouped(w_packed, w_scale_e4m3, w_global, out_packed, out_scale, E, N, K,
+                                                    alg, swz, static_cast<cudaStream_t>(stream)));
+}
+
 fp4_status fp4_quant_act_mxfp4(const void* x_bf16, uint8_t* out_packed, uint8_t* out_scale, int64_t M, int64_t K,
                                const fp4_quant_opts* opts, void* stream)
 {

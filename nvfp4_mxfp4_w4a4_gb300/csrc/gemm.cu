@@ -22,16 +22,18 @@
 //               kind::mxf4 (K = 64, two E8M0 scales per row each) accumulate
 //               into a 128 x BN fp32 TMEM tile; tcgen05.commit frees the
 //               stage, and at the end of a tile signals the epilogue.
-//   warps 2-3   scale movers: per stage, tcgen05.cp of the scale chunks from
-//               smem into that stage's TMEM scale columns, split between the
-//               two warps.  A thread's copies run one after another at about
+//   CPW warps   scale movers (warps 2 .. 1+CPW; 4, or 2 where the epilogue
+//               needs the registers): per stage, tcgen05.cp of the scale
+//               chunks from smem into that stage's TMEM scale columns, split
+//               between the warps.  A thread's copies run one after another at about
 //               a hundred cycles each, so one thread issuing both copies and
 //               MMAs would serialise them; on separate threads they overlap
 //               the MMAs of the previous stage.
-//   warps 4-11  epilogue: each warp reads 32 TMEM lanes x BN/2 columns into
+//   8 warps     epilogue (the last eight): each warp reads 32 TMEM lanes x BN/2 columns into
 //               registers, releases the accumulator at once (so the next
-//               tile's MMAs start), adds bias, rounds to bf16, stages the
-//               tile in shared memory and writes it with TMA tensor stores.
+//               tile's MMAs start), adds bias, rounds to bf16, stages its
+//               part of the tile in its own shared-memory area and writes it
+//               with TMA tensor stores.
 // Orientation: the MMA-M operand is A (activations) in the normal mode and
 // the weights in the swapped mode used for small M (decode); there the
 // tokens are the MMA N dimension and the staged tile is the transpose.
@@ -51,10 +53,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int kSlabBytes = 128;  // packed bytes of K per row per slab (256 elements)
-constexpr int kCpWarps = 2;
-constexpr int kFirstEpiWarp = 2 + kCpWarps;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (kFirstEpiWarp + kEpiWarps);
 constexpr int kChunk = 32;      // normal-mode store chunk: 32 rows x 32 columns per warp
 
 struct GemmParams {
@@ -75,22 +74,25 @@ struct GemmParams {
     unsigned int* status;
 };
 
-template <int BN, int STAGES, int KC, bool kSwap>
+template <int BN, int STAGES, int KC, int CPW, bool kSwap>
 struct Cfg {
+    static constexpr int FIRST_EPI_WARP = 2 + CPW;
+    static constexpr int THREADS = 32 * (FIRST_EPI_WARP + kEpiWarps);
     static constexpr int GROUPS = 2 * KC;  // 128-element scale groups per stage
     static constexpr int A_BYTES = BM * kSlabBytes * KC;
     static constexpr int B_BYTES = BN * kSlabBytes * KC;
     static constexpr int SFB_TILES = (BN + 127) / 128;
     static constexpr int SFA_BYTES = GROUPS * 512;
     static constexpr int SFB_BYTES = SFB_TILES * GROUPS * 512;
-    static constexpr int EPI_BYTES = kSwap ? BN * BM * 2 : kEpiWarps * kChunk * kChunk * 2;
+    static constexpr int EPI_WARP_BYTES = kSwap ? 32 * (BN / 2) * 2 : kChunk * kChunk * 2;
+    static constexpr int EPI_BYTES = kEpiWarps * EPI_WARP_BYTES;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    static constexpr int NUM_BARS = 3 * STAGES + 4;
+    static constexpr int NUM_BARS = 3 * STAGES + 2;
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_PREFIX = OFF_TMEM_SLOT + 16;
     static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;  // + 1 KB alignment slack
@@ -179,12 +181,13 @@ __device__ __forceinline__ void load_operand(void* dst, const CUtensorMap* map, 
         tma_load_3d(dst, map, bar, 0, static_cast<int32_t>(row0), kb * KC);
 }
 
-template <int BN, int STAGES, int KC, bool kSwap, bool kGrouped>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped>
+__global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
     gemm_mxfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmO, const GemmParams p)
 {
-    using C = Cfg<BN, STAGES, KC, kSwap>;
+    using C = Cfg<BN, STAGES, KC, CPW, kSwap>;
+    constexpr int kFirstEpiWarp = C::FIRST_EPI_WARP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -192,8 +195,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* sf_full = empty + STAGES;
     uint64_t* accum_full = sf_full + STAGES;
     uint64_t* accum_empty = accum_full + 1;
-    uint64_t* epi_full = accum_empty + 1;  // swapped mode: the staged tile is complete
-    uint64_t* epi_free = epi_full + 1;     // swapped mode: the staged tile has been read by its store
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
     int32_t* tiles_before = reinterpret_cast<int32_t*>(smem + C::OFF_PREFIX);
 
@@ -209,12 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&sf_full[s], kCpWarps);
+            mbar_init(&sf_full[s], CPW);
         }
         mbar_init(accum_full, 1);
         mbar_init(accum_empty, kEpiWarps);
-        mbar_init(epi_full, kEpiWarps);
-        mbar_init(epi_free, 1);
         fence_mbar_init();
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
@@ -340,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ------------------------------------------------ scale movers
             // Copy q of a stage (q = g * (1 + SFB_TILES) + i: i = 0 the
             // MMA-M operand's chunk of group g, i = 1 + j the MMA-N
-            // operand's row tile j) belongs to warp 2 + q % kCpWarps.
+            // operand's row tile j) belongs to warp 2 + q % CPW.
             const int me = warp - 2;
             uint32_t it = 0;
             bool ok = true;
@@ -362,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sfa_s = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
                     const uint32_t sfb_s = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
 #pragma unroll
-                    for (int q = me; q < C::GROUPS * (1 + C::SFB_TILES); q += kCpWarps) {
+                    for (int q = me; q < C::GROUPS * (1 + C::SFB_TILES); q += CPW) {
                         const int g = q / (1 + C::SFB_TILES);
                         const int i = q % (1 + C::SFB_TILES);
                         if (g >= groups)
@@ -404,39 +403,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             const int r = quad * 32 + lane;
             const __nv_bfloat16* bias = p.bias ? p.bias + static_cast<int64_t>(T.expert) * p.ldo : nullptr;
+            uint8_t* stg = epi + ew * C::EPI_WARP_BYTES;  // this warp's staging area
+            if (lane == 0 && stored)
+                bulk_wait_group_read0();  // the previous store has left the staging area
+            __syncwarp();
             if constexpr (kSwap) {
                 // lane = output column n (weight row); tile columns = tokens.
-                // Stage [BN tokens][128 n] and store the box in one copy,
-                // handed between the warps by two mbarriers (bounded waits).
-                const uint32_t eph = (tcount - 1) & 1u;
-                if (!mbar_wait_bounded(epi_free, eph ^ 1u, p.status, kStatusTimeout, kWaitLimitNs))
-                    break;
+                // This warp's 32 columns x CW tokens go out as one box,
+                // staged as [CW tokens][32 n].
                 const int64_t n = T.a_row0 + r;
                 const float bn = (bias && r < T.rows_valid) ? __bfloat162float(bias[n]) : 0.0f;
-                __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(epi);
+                __nv_bfloat16* srow = reinterpret_cast<__nv_bfloat16*>(stg) + lane;
 #pragma unroll
                 for (int j = 0; j < CW; ++j)
-                    stg[(half * CW + j) * BM + r] = __float2bfloat16_rn(__uint_as_float(v[j]) + bn);
+                    srow[j * 32] = __float2bfloat16_rn(__uint_as_float(v[j]) + bn);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(epi_full);
-                if (ew == 0 && lane == 0) {
-                    if (mbar_wait_bounded(epi_full, eph, p.status, kStatusTimeout, kWaitLimitNs)) {
-                        tma_store_2d(&tmO, stg, static_cast<int32_t>(T.a_row0), T.n0);
-                        bulk_commit_group();
-                        bulk_wait_group_read0();
-                        stored = true;
-                    }
-                    mbar_arrive(epi_free);
+                if (lane == 0) {
+                    tma_store_2d(&tmO, stg, static_cast<int32_t>(T.a_row0 + quad * 32), T.n0 + half * CW);
+                    bulk_commit_group();
+                    stored = true;
                 }
             } else {
                 // lane = output row; this warp's columns n0 + half*CW + [0, CW)
-                // go out in 32 x 32 chunks through its own staging area, in the
+                // go out in 32 x 32 chunks through its staging area, in the
                 // 64-byte swizzled layout of the output map (16-byte piece q of
                 // row i sits at piece position q ^ ((i / 2) % 4)), which keeps
                 // the rows of one store phase on different banks.
-                uint8_t* stg = epi + ew * (kChunk * kChunk * 2);
                 uint8_t* my_row = stg + lane * (kChunk * 2);
                 const int rot = (lane >> 1) & 3;
                 // rows past the end of this expert belong to the next one:
@@ -445,8 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < CW; c += kChunk) {
                     const int col0 = T.n0 + half * CW + c;
-                    if (whole) {
-                        if (lane == 0 && stored)
+                    if (whole && c > 0) {
+                        if (lane == 0)
                             bulk_wait_group_read0();  // the previous chunk has left the staging area
                         __syncwarp();
                     }
@@ -485,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (stored)
-            bulk_wait_group0();  // stores complete before the CTA exits
+            bulk_wait_group_read0();  // shared memory stays valid until the last store has read it
     }
 
     tc_fence_before_sync();
@@ -575,10 +568,10 @@ int sm_count()
     return cached[dev];
 }
 
-template <int BN, int STAGES, int KC, bool kSwap, bool kGrouped>
+template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped>
 cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
 {
-    using C = Cfg<BN, STAGES, KC, kSwap>;
+    using C = Cfg<BN, STAGES, KC, CPW, kSwap>;
     // MMA-M operand / MMA-N operand
     const uint8_t* opA = kSwap ? a.b : a.a;
     const uint8_t* opB = kSwap ? a.a : a.b;
@@ -589,7 +582,7 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
         return cudaErrorInvalidValue;
     if (!make_operand_map(&tmB, opB, static_cast<int64_t>(a.E) * rows_b, a.K, BN, KC))
         return cudaErrorInvalidValue;
-    if (!(kSwap ? make_output_map(&tmO, a.out, a.M, a.N, BM, BN, CU_TENSOR_MAP_SWIZZLE_NONE)
+    if (!(kSwap ? make_output_map(&tmO, a.out, a.M, a.N, 32, BN / 2, CU_TENSOR_MAP_SWIZZLE_NONE)
                 : make_output_map(&tmO, a.out, a.M, a.N, kChunk, kChunk, CU_TENSOR_MAP_SWIZZLE_64B)))
         return cudaErrorInvalidValue;
     GemmParams p;
@@ -614,7 +607,7 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
         return cudaSuccess;
     const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count()));
     const size_t smem = C::SMEM_FIXED + (kGrouped ? sizeof(int32_t) * (a.E + 1) : 0);
-    auto kern = gemm_mxfp4_kernel<BN, STAGES, KC, kSwap, kGrouped>;
+    auto kern = gemm_mxfp4_kernel<BN, STAGES, KC, CPW, kSwap, kGrouped>;
     // The shared-memory opt-in is a per-device function attribute: set it
     // once per device (and grow it if a larger grouped prefix needs more).
     static std::mutex mu;
@@ -632,7 +625,7 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
             configured[dev] = smem;
         }
     }
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, tmA, tmB, tmO, p);
+    return launch_pdl(kern, dim3(grid), dim3(C::THREADS), smem, stream, tmA, tmB, tmO, p);
 }
 
 }  // namespace
@@ -647,21 +640,21 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream)
     const bool wide = a.N >= 256 && m_tiles * ((a.N + 255) / 256) >= 148;
     if (a.row_offsets != nullptr) {
         if (wide)
-            return launch_kernel<256, 4, 1, false, true>(a, stream);
-        return k256 ? launch_kernel<128, 3, 2, false, true>(a, stream)
-                    : launch_kernel<128, 6, 1, false, true>(a, stream);
+            return launch_kernel<256, 4, 1, 2, false, true>(a, stream);
+        return k256 ? launch_kernel<128, 3, 2, 4, false, true>(a, stream)
+                    : launch_kernel<128, 6, 1, 4, false, true>(a, stream);
     }
     // decode-sized batches: weights on the 128-row MMA side, tokens as N
     if (a.M <= 64) {
         if (!k256)
-            return launch_kernel<64, 8, 1, true, false>(a, stream);
-        return a.M <= 32 ? launch_kernel<32, 4, 2, true, false>(a, stream)
-                         : launch_kernel<64, 4, 2, true, false>(a, stream);
+            return launch_kernel<64, 8, 1, 4, true, false>(a, stream);
+        return a.M <= 32 ? launch_kernel<32, 4, 2, 4, true, false>(a, stream)
+                         : launch_kernel<64, 4, 2, 4, true, false>(a, stream);
     }
     if (wide)
-        return launch_kernel<256, 4, 1, false, false>(a, stream);
-    return k256 ? launch_kernel<128, 3, 2, false, false>(a, stream)
-                : launch_kernel<128, 6, 1, false, false>(a, stream);
+        return launch_kernel<256, 4, 1, 2, false, false>(a, stream);
+    return k256 ? launch_kernel<128, 3, 2, 4, false, false>(a, stream)
+                : launch_kernel<128, 6, 1, 4, false, false>(a, stream);
 }
 
 }  // namespace fp4lin

@@ -227,48 +227,32 @@ struct RequantLane {
     uint32_t sc[4];  // per block: its two E4M3 bytes
 };
 
-// kFast: the lane's 64 code bytes are 32-byte aligned and its 8 scale bytes
-// 8-byte aligned (K % 128 == 0 and aligned bases) and all 4 blocks exist.
-template <bool kFast>
+// Loads a lane's blocks c0 .. c0 + nreal - 1 of a row (16-byte code
+// accesses, 2-byte scale accesses: any K % 32 == 0 and 16-byte alignment).
 __device__ __forceinline__ void requant_lane_load(RequantLane& L, const uint8_t* __restrict__ wp,
                                                   const uint8_t* __restrict__ ws, int64_t row, int c0, int nreal,
                                                   int64_t K)
 {
     const uint8_t* cp = wp + row * (K / 2) + static_cast<int64_t>(c0) * 16;
     const uint8_t* sp = ws + row * (K / 16) + static_cast<int64_t>(c0) * 2;
-    if (kFast && nreal == 4) {
-        uint32_t a[8], b[8];
-        ld_nc_v8(cp, a);
-        ld_nc_v8(cp + 32, b);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            L.w[i] = a[i];
-            L.w[8 + i] = b[i];
+    for (int j = 0; j < 4; ++j) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        uint32_t sc = 0u;
+        if (j < nreal) {
+            v = ld_nc_u4_cached(cp + 16 * j);
+            sc = ld_stream_u16(sp + 2 * j);
         }
-        const uint2 s2 = ld_nc_u64(sp);
-        L.sc[0] = s2.x & 0xFFFFu;
-        L.sc[1] = s2.x >> 16;
-        L.sc[2] = s2.y & 0xFFFFu;
-        L.sc[3] = s2.y >> 16;
-    } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            uint32_t sc = 0u;
-            if (j < nreal) {
-                v = ld_nc_u4_cached(cp + 16 * j);
-                sc = ld_stream_u16(sp + 2 * j);
-            }
-            L.w[4 * j] = v.x;
-            L.w[4 * j + 1] = v.y;
-            L.w[4 * j + 2] = v.z;
-            L.w[4 * j + 3] = v.w;
-            L.sc[j] = sc;
-        }
+        L.w[4 * j] = v.x;
+        L.w[4 * j + 1] = v.y;
+        L.w[4 * j + 2] = v.z;
+        L.w[4 * j + 3] = v.w;
+        L.sc[j] = sc;
     }
 }
 
-template <bool kFast>
+// Row-based kernel for the shapes the flat kernel below does not take
+// (K % 128 != 0 or arrays aligned to 16 bytes only).
 __global__ void __launch_bounds__(kThreads) requant_kernel(const uint8_t* __restrict__ wp,
                                                            const uint8_t* __restrict__ ws, float g,
                                                            uint8_t* __restrict__ op, uint8_t* __restrict__ osf,
@@ -294,7 +278,7 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const uint8_t* __rest
     int c0 = static_cast<int>(item - row * nch) * 128 + 4 * lane;
     int nreal = row < N ? min(max(kb - c0, 0), 4) : 0;
     RequantLane cur;
-    requant_lane_load<kFast>(cur, wp, ws, row, c0, nreal, K);
+    requant_lane_load(cur, wp, ws, row, c0, nreal, K);
     while (true) {
         const int64_t next = item + stride;
         int64_t nrow = 0;
@@ -304,7 +288,7 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const uint8_t* __rest
             nrow = next / nch;
             nc0 = static_cast<int>(next - nrow * nch) * 128 + 4 * lane;
             nnreal = nrow < N ? min(max(kb - nc0, 0), 4) : 0;
-            requant_lane_load<kFast>(nxt, wp, ws, nrow, nc0, nnreal, K);
+            requant_lane_load(nxt, wp, ws, nrow, nc0, nnreal, K);
         }
         uint32_t out[16];
         uint32_t sfw = 0u;
@@ -315,22 +299,11 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const uint8_t* __rest
                 sfw |= sf << (8 * j);
         }
         uint8_t* dst = op + row * (K / 2) + static_cast<int64_t>(c0) * 16;
-        if (kFast && nreal == 4) {
-            uint32_t a[8], b[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                a[i] = out[i];
-                b[i] = out[8 + i];
-            }
-            st_v8(dst, a);
-            st_v8(dst + 32, b);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (j < nreal)
-                    *reinterpret_cast<uint4*>(dst + 16 * j) =
-                        make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
-        }
+        for (int j = 0; j < 4; ++j)
+            if (j < nreal)
+                *reinterpret_cast<uint4*>(dst + 16 * j) =
+                    make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
         if (swizzled) {
             if (c0 < kbp)  // pad block columns and pad rows get zero bytes
                 *reinterpret_cast<uint32_t*>(osf + sf_swizzled_offset(row, c0, kb4)) = sfw;
@@ -346,6 +319,132 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const uint8_t* __rest
         row = nrow;
         c0 = nc0;
         nreal = nnreal;
+        cur = nxt;
+    }
+}
+
+// Flat variant for K % 128 == 0 with 32-byte aligned code arrays and 8-byte
+// aligned scales.  Rows are then back to back in memory and a row's block
+// count is a multiple of 4, so a tensor is one run of 32-element blocks and a
+// warp item is 128 consecutive blocks whatever K is (a lane's 4 blocks never
+// straddle rows).  Rows are counted up to rows_pad (the 128-row padding of a
+// swizzled scale array; pad rows get zero scale bytes).  Grouped: E tensors of
+// the same shape stored back to back, each with its own global scale g[e]
+// (device array); a run of ctas_per_e CTAs serves one tensor, so a CTA builds
+// the code maps of one g only.
+template <bool kGrouped>
+__global__ void __launch_bounds__(kThreads) requant_flat_kernel(const uint8_t* __restrict__ wp,
+                                                                const uint8_t* __restrict__ ws, float g_dense,
+                                                                const float* __restrict__ g_dev,
+                                                                uint8_t* __restrict__ op, uint8_t* __restrict__ osf,
+                                                                int64_t N, int64_t K, int64_t rows_pad, int kb,
+                                                                int64_t items, int ctas_per_e, int64_t sf_e_bytes,
+                                                                int uos, int swizzled)
+{
+    __shared__ uint2 map[kMapEntries];
+    const int e = kGrouped ? static_cast<int>(blockIdx.x) / ctas_per_e : 0;
+    const int local = kGrouped ? static_cast<int>(blockIdx.x) - e * ctas_per_e : static_cast<int>(blockIdx.x);
+    float g = g_dense;
+    if (!kGrouped)
+        build_code_maps(fabsf(g), map);  // needs no global memory: overlaps the previous kernel
+    grid_dependency_wait();
+    launch_dependents();
+    if (kGrouped) {
+        g = __ldg(g_dev + e);
+        build_code_maps(fabsf(g), map);
+    }
+    __syncthreads();
+    const float ag = fabsf(g);
+    const uint32_t gsign = __float_as_uint(g) >> 31;
+
+    const int lane = threadIdx.x & 31;
+    const int64_t stride = static_cast<int64_t>(ctas_per_e) * (kThreads / 32);
+    int64_t item = static_cast<int64_t>(local) * (kThreads / 32) + (threadIdx.x >> 5);
+    if (item >= items)
+        return;
+    const int64_t nblocks = rows_pad * kb;  // blocks of one tensor, pad rows included
+    const int64_t kb4 = kb >> 2;
+    const uint8_t* wpe = wp + static_cast<int64_t>(e) * N * (K / 2);
+    const uint8_t* wse = ws + static_cast<int64_t>(e) * N * (K / 16);
+    uint8_t* ope = op + static_cast<int64_t>(e) * N * (K / 2);
+    uint8_t* osfe = osf + (swizzled ? static_cast<int64_t>(e) * sf_e_bytes : static_cast<int64_t>(e) * N * kb);
+    // lane's first block and whether it holds real data (4 blocks of one row)
+    auto locate = [&](int64_t it, int64_t& f, bool& real) {
+        f = it * 128 + 4 * lane;
+        real = f < N * kb;  // rows are contiguous: the first N*kb blocks are the tensor's
+    };
+    int64_t f;
+    bool real;
+    locate(item, f, real);
+    RequantLane cur;
+    auto load = [&](RequantLane& L, int64_t fb, bool r) {
+        if (r) {
+            uint32_t a[8], b[8];
+            ld_nc_v8(wpe + fb * 16, a);
+            ld_nc_v8(wpe + fb * 16 + 32, b);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                L.w[i] = a[i];
+                L.w[8 + i] = b[i];
+            }
+            const uint2 s2 = ld_nc_u64(wse + fb * 2);
+            L.sc[0] = s2.x & 0xFFFFu;
+            L.sc[1] = s2.x >> 16;
+            L.sc[2] = s2.y & 0xFFFFu;
+            L.sc[3] = s2.y >> 16;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                L.w[i] = 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                L.sc[j] = 0u;
+        }
+    };
+    load(cur, f, real);
+    while (true) {
+        const int64_t next = item + stride;
+        int64_t nf = 0;
+        bool nreal = false;
+        RequantLane nxt;
+        const bool more = next < items;
+        if (more) {
+            locate(next, nf, nreal);
+            load(nxt, nf, nreal);
+        }
+        if (f < nblocks) {
+            uint32_t out[16];
+            uint32_t sfw = 0u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                sfw |= requant_block(cur.w + 4 * j, cur.sc[j], ag, gsign, uos, map, out + 4 * j) << (8 * j);
+            const int64_t row = f / kb;
+            const int c0 = static_cast<int>(f - row * kb);
+            if (real) {
+                uint32_t a[8], b[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    a[i] = out[i];
+                    b[i] = out[8 + i];
+                }
+                st_v8(ope + f * 16, a);
+                st_v8(ope + f * 16 + 32, b);
+            } else {
+                sfw = 0u;  // pad rows
+            }
+            if (swizzled) {
+                *reinterpret_cast<uint32_t*>(osfe + sf_swizzled_offset(row, c0, kb4)) = sfw;
+            } else if (real) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    osfe[f + j] = static_cast<uint8_t>(sfw >> (8 * j));
+            }
+        }
+        if (!more)
+            break;
+        item = next;
+        f = nf;
+        real = nreal;
         cur = nxt;
     }
 }
@@ -561,6 +660,35 @@ int64_t resident_ctas(Kern kern)
 }  // namespace
 
 // ------------------------------------------------------------- launchers
+bool requant_flat_ok(const uint8_t* wp, const uint8_t* ws, const uint8_t* op, const uint8_t* osf, int64_t K,
+                     int swizzled)
+{
+    return K % 128 == 0 && (reinterpret_cast<uintptr_t>(wp) & 31u) == 0 && (reinterpret_cast<uintptr_t>(op) & 31u) == 0 &&
+           (reinterpret_cast<uintptr_t>(ws) & 7u) == 0 && (!swizzled || (reinterpret_cast<uintptr_t>(osf) & 3u) == 0);
+}
+
+// Flat kernel over E tensors (E = 1: dense, g_dev unused).
+cudaError_t launch_requant_flat(const uint8_t* wp, const uint8_t* ws, float g, const float* g_dev, uint8_t* op,
+                                uint8_t* osf, int E, int64_t N, int64_t K, int alg, int swizzled, cudaStream_t stream)
+{
+    const int kb = static_cast<int>(K / 32);
+    const int64_t rows_pad = swizzled ? ceil_div(N, 128) * 128 : N;
+    const int64_t items = ceil_div(rows_pad * kb, 128);  // warp items per tensor
+    const int64_t sf_e_bytes = rows_pad * kb;            // swizzled bytes per tensor (kb % 4 == 0)
+    const int uos = alg == 2 ? 1 : 0;
+    const int64_t want = ceil_div(items * 32, kThreads);  // CTAs that give every warp one item
+    if (g_dev == nullptr) {
+        const int64_t blocks = std::min<int64_t>(want, resident_ctas(requant_flat_kernel<false>));
+        return launch_pdl(requant_flat_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream,
+                          wp, ws, g, static_cast<const float*>(nullptr), op, osf, N, K, rows_pad, kb, items,
+                          static_cast<int>(blocks), sf_e_bytes, uos, swizzled);
+    }
+    const int64_t per_e = std::max<int64_t>(1, std::min<int64_t>(want, resident_ctas(requant_flat_kernel<true>) / E));
+    return launch_pdl(requant_flat_kernel<true>, dim3(static_cast<unsigned>(per_e * E)), dim3(kThreads), 0, stream, wp,
+                      ws, 0.0f, g_dev, op, osf, N, K, rows_pad, kb, items, static_cast<int>(per_e), sf_e_bytes, uos,
+                      swizzled);
+}
+
 cudaError_t launch_requant(const uint8_t* wp, const uint8_t* ws, float g, uint8_t* op, uint8_t* osf, int64_t N,
                            int64_t K, int alg, int swizzled, cudaStream_t stream)
 {
@@ -569,20 +697,23 @@ cudaError_t launch_requant(const uint8_t* wp, const uint8_t* ws, float g, uint8_
     const int64_t rows = swizzled ? ceil_div(N, 128) * 128 : N;
     const int nch = static_cast<int>(ceil_div(kbp, 128));
     const int64_t warps = rows * nch;
-    const bool fast = K % 128 == 0 && (reinterpret_cast<uintptr_t>(wp) & 31u) == 0 &&
-                      (reinterpret_cast<uintptr_t>(op) & 31u) == 0 && (reinterpret_cast<uintptr_t>(ws) & 7u) == 0;
     const int uos = alg == 2 ? 1 : 0;
-    if (fast) {
-        const int64_t blocks = std::min<int64_t>(ceil_div(warps * 32, kThreads), resident_ctas(requant_kernel<true>));
-        return launch_pdl(requant_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, wp, ws,
-                          g, op, osf, N, K, rows, kb, kbp, nch, uos, swizzled);
+    if (requant_flat_ok(wp, ws, op, osf, K, swizzled)) {
+        return launch_requant_flat(wp, ws, g, nullptr, op, osf, 1, N, K, alg, swizzled, stream);
     } else {
         const int64_t blocks =
-            std::min<int64_t>(ceil_div(warps * 32, kThreads), resident_ctas(requant_kernel<false>));
-        return launch_pdl(requant_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, wp,
+            std::min<int64_t>(ceil_div(warps * 32, kThreads), resident_ctas(requant_kernel));
+        return launch_pdl(requant_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, wp,
                           ws, g, op, osf, N, K, rows, kb, kbp, nch, uos, swizzled);
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_requant_grouped(const uint8_t* wp, const uint8_t* ws, const float* g_dev, uint8_t* op,
+                                   uint8_t* osf, int E, int64_t N, int64_t K, int alg, int swizzled,
+                                   cudaStream_t stream)
+{
+    return launch_requant_flat(wp, ws, 0.0f, g_dev, op, osf, E, N, K, alg, swizzled, stream);
 }
 
 cudaError_t launch_act_quant(const void* x, uint8_t* op, uint8_t* osf, int64_t M, int64_t K, int alg,

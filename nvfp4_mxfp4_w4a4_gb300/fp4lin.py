@@ -24,7 +24,8 @@ FP4_SF_ROWMAJOR = 1
 # every symbol the header declares
 SYMBOLS = (
     "fp4_sf_bytes", "fp4_sf_bytes_grouped", "fp4_status_string", "fp4_get_device_status",
-    "fp4_requant_nvfp4_to_mxfp4", "fp4_requant_nvfp4_to_mxfp4_ex", "fp4_quant_act_mxfp4",
+    "fp4_requant_nvfp4_to_mxfp4", "fp4_requant_nvfp4_to_mxfp4_ex", "fp4_requant_nvfp4_to_mxfp4_grouped",
+    "fp4_quant_act_mxfp4",
     "fp4_quant_act_mxfp4_grouped", "fp4_quant_nvfp4", "fp4_gemm_mxfp4", "fp4_gemm_mxfp4_grouped",
 )
 
@@ -60,6 +61,8 @@ def load(path: str = LIB_PATH):
             "fp4_requant_nvfp4_to_mxfp4": (ctypes.c_int, [_p, _p, ctypes.c_float, _p, _p, _i64, _i64, _p]),
             "fp4_requant_nvfp4_to_mxfp4_ex": (ctypes.c_int, [_p, _p, ctypes.c_float, _p, _p, _i64, _i64,
                                                              ctypes.POINTER(fp4_quant_opts), _p]),
+            "fp4_requant_nvfp4_to_mxfp4_grouped": (ctypes.c_int, [_p, _p, _p, _p, _p, _i32, _i64, _i64,
+                                                                  ctypes.POINTER(fp4_quant_opts), _p]),
             "fp4_quant_act_mxfp4": (ctypes.c_int, [_p, _p, _p, _i64, _i64, ctypes.POINTER(fp4_quant_opts), _p]),
             "fp4_quant_act_mxfp4_grouped": (ctypes.c_int, [_p, _p, _i32, _i64, _i64, _p, _p,
                                                            ctypes.POINTER(fp4_quant_opts), _p]),
@@ -133,6 +136,15 @@ def fp4_requant_nvfp4_to_mxfp4(w_packed, w_scale_e4m3, w_global, out_packed, out
                                              _ptr(out_packed), _ptr(out_scale), N, K,
                                              _opts(scale_alg, sf_layout), _stream(stream))
     _check(st, "fp4_requant_nvfp4_to_mxfp4")
+
+
+def fp4_requant_nvfp4_to_mxfp4_grouped(w_packed, w_scale_e4m3, w_global, out_packed, out_scale, E, N, K,
+                                       stream=None, scale_alg=None, sf_layout=None):
+    """w_global: device array of E float32 global scales."""
+    st = load().fp4_requant_nvfp4_to_mxfp4_grouped(_ptr(w_packed), _ptr(w_scale_e4m3), _ptr(w_global),
+                                                   _ptr(out_packed), _ptr(out_scale), E, N, K,
+                                                   _opts(scale_alg, sf_layout), _stream(stream))
+    _check(st, "fp4_requant_nvfp4_to_mxfp4_grouped")
 
 
 def fp4_quant_act_mxfp4(x_bf16, out_packed, out_scale, M, K, stream=None, scale_alg=None, sf_layout=None):

@@ -62,12 +62,17 @@ def test_argument_checks_precede_device_use(L):
     assert raw.fp4_gemm_mxfp4(16, 16, 16, 16, None, 16, 1, 12, 128, None) == 2     # N % 8
     assert raw.fp4_quant_act_mxfp4(16, 16, 16, 4, 48, None, None) == 2             # K % 32
     assert raw.fp4_requant_nvfp4_to_mxfp4(16, 16, 1.0, 16, 16, 0, 32, None) == 2   # N = 0
+    assert raw.fp4_requant_nvfp4_to_mxfp4_grouped(32, 32, 32, 32, 32, 2, 4, 96, None, None) == 2   # K % 128
+    assert raw.fp4_requant_nvfp4_to_mxfp4_grouped(32, 32, 32, 32, 32, 0, 4, 128, None, None) == 2  # E = 0
+    assert raw.fp4_gemm_mxfp4_grouped(16, 16, 16, 16, None, 16, 16, 1025, 4, 8, 128, None) == 2    # E > 1024
     # null pointers
     assert raw.fp4_gemm_mxfp4(None, 16, 16, 16, None, 16, 1, 8, 128, None) == 1
     assert raw.fp4_requant_nvfp4_to_mxfp4(None, 16, 1.0, 16, 16, 4, 32, None) == 1
+    assert raw.fp4_requant_nvfp4_to_mxfp4_grouped(32, 32, None, 32, 32, 2, 4, 128, None, None) == 1  # no scales
     # alignment
     assert raw.fp4_gemm_mxfp4(17, 16, 16, 16, None, 16, 1, 8, 128, None) == 3
     assert raw.fp4_quant_act_mxfp4(24, 16, 16, 4, 32, None, None) == 3
+    assert raw.fp4_requant_nvfp4_to_mxfp4_grouped(16, 32, 32, 32, 32, 2, 4, 128, None, None) == 3  # codes 32 B
     # bad option values
     from nvfp4_mxfp4_w4a4_gb300.fp4lin import fp4_quant_opts
 

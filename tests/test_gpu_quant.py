@@ -69,6 +69,77 @@ def test_requant_tiny_workload_recipe(orc, L):
             _check_requant(orc, L, packed, scale, g, alg, layout)
 
 
+@pytest.mark.parametrize("N,K", [(1, 128), (5, 256), (130, 1024), (257, 384), (64, 4096)])
+@pytest.mark.parametrize("alg", [OCP, UOS])
+@pytest.mark.parametrize("layout", [SWZ, ROW])
+def test_requant_flat_shapes(orc, L, N, K, alg, layout):
+    # K % 128 == 0 with aligned buffers: the flattened-block kernel
+    rng = np.random.default_rng(N * 131 + K)
+    packed, scale = _random_nvfp4(rng, N, K)
+    for g in (1.0, 0.0037, -0.25):
+        _check_requant(orc, L, packed, scale, float(np.float32(g)), alg, layout)
+
+
+def test_requant_16_byte_aligned_buffers(orc, L):
+    # codes only 16-byte aligned: the row kernel takes the K % 128 == 0 shape
+    import torch
+
+    N, K = 131, 512
+    rng = np.random.default_rng(77)
+    packed, scale = _random_nvfp4(rng, N, K)
+    src = torch.zeros(N * K // 2 + 16, dtype=torch.uint8, device="cuda")
+    src[16:] = dev(packed.reshape(-1))
+    dst = torch.full((N * K // 2 + 16,), 0xA5, dtype=torch.uint8, device="cuda")
+    osf = empty_u8(L.fp4_sf_bytes(N, K, SWZ))
+    g = float(np.float32(0.0123))
+    L.fp4_requant_nvfp4_to_mxfp4(src[16:], dev(scale), g, dst[16:], osf, N, K)
+    assert L.fp4_get_device_status() == 0
+    rp, rs = orc.requant(packed, scale, g, OCP, threads=THREADS)
+    assert np.array_equal(host(dst[16:]).reshape(N, K // 2), rp)
+    assert np.array_equal(host(osf), orc.sf_swizzle(rs))
+
+
+def _check_requant_grouped(orc, L, packed, scale, gs, alg, layout):
+    import torch
+
+    E, N, half = packed.shape
+    K = 2 * half
+    per = L.fp4_sf_bytes(N, K, layout)
+    op = empty_u8(E * N * K // 2)
+    osf = empty_u8(E * per)
+    gdev = torch.from_numpy(np.asarray(gs, np.float32)).cuda()
+    L.fp4_requant_nvfp4_to_mxfp4_grouped(dev(packed), dev(scale), gdev, op, osf, E, N, K, scale_alg=alg,
+                                         sf_layout=layout)
+    assert L.fp4_get_device_status() == 0
+    hp = host(op)[: E * N * K // 2].reshape(E, N, K // 2)
+    hs = host(osf)[: E * per].reshape(E, per)
+    for e in range(E):
+        rp, rs = orc.requant(packed[e], scale[e], float(gs[e]), alg, threads=THREADS)
+        assert np.array_equal(hp[e], rp), f"expert {e}: codes differ at {np.argwhere(hp[e] != rp)[:5]}"
+        expect = orc.sf_swizzle(rs) if layout == SWZ else rs.reshape(-1)
+        assert np.array_equal(hs[e], expect), f"expert {e}: scales differ at {np.argwhere(hs[e] != expect)[:5]}"
+
+
+@pytest.mark.parametrize("E,N,K", [(3, 130, 1024), (5, 64, 256), (2, 1, 128), (7, 200, 512)])
+@pytest.mark.parametrize("alg", [OCP, UOS])
+@pytest.mark.parametrize("layout", [SWZ, ROW])
+def test_requant_grouped(orc, L, E, N, K, alg, layout):
+    rng = np.random.default_rng(E * 1000 + N + K)
+    packed = rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
+    scale = rng.integers(0, 256, (E, N, K // 16), dtype=np.uint8)
+    gs = np.float32([1.0, 0.0037, -0.25, 2.0 ** -20, 3.0, 1e-4, 7.5])[:E]
+    _check_requant_grouped(orc, L, packed, scale, gs, alg, layout)
+
+
+def test_requant_grouped_special_scales(orc, L):
+    rng = np.random.default_rng(9)
+    E, N, K = 6, 40, 256
+    packed = rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
+    scale = rng.integers(0, 0x7F, (E, N, K // 16), dtype=np.uint8)
+    gs = np.float32([0.0, -0.0, np.inf, np.nan, 3.0e38, 1.0e-45])
+    _check_requant_grouped(orc, L, packed, scale, gs, OCP, SWZ)
+
+
 # ---------------------------------------------------------------- activations
 def _kernel_act(L, x_bits, alg, layout):
     M, K = x_bits.shape
