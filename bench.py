@@ -204,6 +204,22 @@ class Weight:
                                               stream=s)
 
 
+_WORKSPACE = {}
+
+
+def gemm_workspace(L, torch, M, N, K):
+    """One zero-initialised split-K workspace shared by the GEMMs of a run
+    (they run one after another on one stream), grown to the largest need."""
+    need = L.fp4_gemm_workspace_size(M, N, K)
+    if need == 0:
+        return None
+    ws = _WORKSPACE.get("ws")
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+        _WORKSPACE["ws"] = ws
+    return ws
+
+
 class Act:
     """bf16 activations of one GEMM (dense, or grouped by `offsets`)."""
 
@@ -219,6 +235,7 @@ class Act:
                else L.fp4_sf_bytes_grouped(self.M, self.E, self.K))
         self.a_scale = torch.empty(sfb, dtype=torch.uint8, device=dev)
         self.out = torch.empty((self.M, weight.N), dtype=torch.bfloat16, device=dev)
+        self.torch = torch
 
     def clone(self, weight):
         c = object.__new__(Act)
@@ -252,8 +269,9 @@ class Act:
     def gemm(self, s):
         w = self.w
         if self.offsets is None:
-            self.L.fp4_gemm_mxfp4(self.a_packed, self.a_scale, w.b_packed, w.b_scale, w.bias, self.out, self.M,
-                                  w.N, self.K, stream=s)
+            ws = gemm_workspace(self.L, self.torch, self.M, w.N, self.K)
+            self.L.fp4_gemm_mxfp4_ws(self.a_packed, self.a_scale, w.b_packed, w.b_scale, w.bias, self.out, self.M,
+                                     w.N, self.K, ws, stream=s)
         else:
             self.L.fp4_gemm_mxfp4_grouped(self.a_packed, self.a_scale, w.b_packed, w.b_scale, w.bias, self.out,
                                           self.offsets, self.E, self.M, w.N, self.K, stream=s)

@@ -202,6 +202,35 @@ FP4LIN_API fp4_status fp4_gemm_mxfp4(const uint8_t* a, const uint8_t* sa, const 
                           const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K,
                           void* stream);
 
+/* Bytes of workspace fp4_gemm_mxfp4_ws can use for an M x N x K problem on
+ * the current device (0: the problem never needs any; also 0 when the
+ * device is unusable).  Decode-sized M (1..64): one 32-bit counter per SM
+ * (256-byte padded) and one 64 x 128 fp32 partial tile per SM.             */
+FP4LIN_API size_t fp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/* fp4_gemm_mxfp4 with caller workspace for split-K (the tile scheduling
+ * for decode-sized M that the library's design adds to the pages' GEMM).
+ * When M <= 64, K % 256 == 0, the 128-row weight tiles number at most half
+ * the SMs, the split saves enough work (with n = K / 512 stages per tile,
+ * n (S - 1) / S >= 10) and workspace_bytes >= fp4_gemm_workspace_size(M, N,
+ * K), the K stages of every tile are split evenly between S = min(8,
+ * SMs / tiles, n) CTAs; the CTA holding a tile's first stages adds the others' fp32
+ * partial sums in K order (fixed order: the same result on every run on
+ * the same device; results can differ in the last bits from
+ * fp4_gemm_mxfp4, within the same tolerance).  Otherwise it runs exactly as
+ * fp4_gemm_mxfp4.
+ *   workspace  device memory, 256-byte aligned, or NULL; the counter area
+ *              (the first 256-byte padded 4 * SM-count bytes) must be zero
+ *              before the first call; every call that returns without a
+ *              device timeout leaves it zero again.  Calls that use the
+ *              same workspace must not overlap in time (same stream, or
+ *              ordered by events).  Owned by the caller.
+ * Same shape and alignment rules as fp4_gemm_mxfp4.                        */
+FP4LIN_API fp4_status fp4_gemm_mxfp4_ws(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
+                             const uint8_t* sb, const void* bias_bf16, void* out_bf16,
+                             int64_t M, int64_t N, int64_t K, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
 /* Grouped (MoE) W4A4 GEMM ([AMD] "Native FP4 matmul": MoE experts on
  * MXFP4): for every expert e and every row m in [row_offsets[e],
  * row_offsets[e+1]):  out[m, :] = A[m, :] . B_e^T (+ bias_e).

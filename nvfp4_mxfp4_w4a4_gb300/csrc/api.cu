@@ -247,7 +247,7 @@ fp4_status fp4_quant_nvfp4(const void* x_bf16, float g, uint8_t* out_packed, uin
 
 static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                               const void* bias, void* out, const int32_t* offsets, int32_t E, int64_t M, int64_t N,
-                              int64_t K, void* stream)
+                              int64_t K, void* workspace, size_t workspace_bytes, void* stream)
 {
     if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 8 != 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
         return FP4_ERR_SHAPE;
@@ -277,13 +277,31 @@ static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t
     args.N = N;
     args.K = K;
     args.status = status;
+    args.workspace = workspace;
+    args.workspace_bytes = workspace ? workspace_bytes : 0;
     return from_cuda(fp4lin::launch_gemm(args, static_cast<cudaStream_t>(stream)));
 }
 
 fp4_status fp4_gemm_mxfp4(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                           const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, void* stream)
 {
-    return gemm_common(a, sa, b, sb, bias_bf16, out_bf16, nullptr, 1, M, N, K, stream);
+    return gemm_common(a, sa, b, sb, bias_bf16, out_bf16, nullptr, 1, M, N, K, nullptr, 0, stream);
+}
+
+size_t fp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K)
+{
+    if (current_device(nullptr) != FP4_OK)
+        return 0;
+    return fp4lin::gemm_workspace_bytes(M, N, K);
+}
+
+fp4_status fp4_gemm_mxfp4_ws(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                             const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
+                             size_t workspace_bytes, void* stream)
+{
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FP4_ERR_ALIGNMENT;
+    return gemm_common(a, sa, b, sb, bias_bf16, out_bf16, nullptr, 1, M, N, K, workspace, workspace_bytes, stream);
 }
 
 fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
@@ -296,7 +314,7 @@ fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uin
         return FP4_ERR_INVALID_ARG;
     if (row_offsets && (reinterpret_cast<uintptr_t>(row_offsets) & 3u))
         return FP4_ERR_ALIGNMENT;
-    return gemm_common(a, sa, b, sb, bias_bf16, out_bf16, row_offsets, E, total_M, N, K, stream);
+    return gemm_common(a, sa, b, sb, bias_bf16, out_bf16, row_offsets, E, total_M, N, K, nullptr, 0, stream);
 }
 
 }  // extern "C"

@@ -37,6 +37,13 @@
 // Orientation: the MMA-M operand is A (activations) in the normal mode and
 // the weights in the swapped mode used for small M (decode); there the
 // tokens are the MMA N dimension and the staged tile is the transpose.
+// Split-K (swapped mode, at most half the SMs busy otherwise, caller
+// workspace): the tiles' K stages form one sequence of units cut into equal
+// contiguous ranges, one per CTA, with S CTAs per tile so that a range never
+// leaves its tile.  The CTA holding a tile's first K stages finishes it: it
+// adds the fp32 partial sums the other S - 1 CTAs left in the workspace, in
+// K order (a fixed reduction order, so results do not vary from run to run),
+// then runs the epilogue.
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the status word and winds down.
 #include <cuda_bf16.h>
@@ -57,6 +64,9 @@ constexpr int kEpiWarps = 8;
 constexpr int kChunk = 32;      // normal-mode store chunk: 32 rows x 32 columns per warp
 
 struct GemmParams {
+    int64_t units;              // split-K: total K-stage units (0: one CTA per whole tile)
+    uint32_t* flags;            // split-K: per-CTA partial-ready counters (zero between calls)
+    float* partials;            // split-K: per-CTA partial tile [BN][128] fp32
     const uint8_t* sfa;         // swizzled scales of the MMA-M operand
     const uint8_t* sfb;         // swizzled scales of the MMA-N operand (per expert when grouped)
     const __nv_bfloat16* bias;  // per output channel (per expert when grouped)
@@ -172,6 +182,76 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* v)
     }
 }
 
+// A CTA's work: whole tiles t = blockIdx.x, + gridDim.x, ... or, in split-K
+// mode, the segments of its unit range [u0, u1) (unit = tile * nkb + stage).
+enum WorkMode { kWhole = 0, kHead = 1, kPartial = 2 };
+
+struct Work {
+    int t;
+    int kb0, kb1;  // stages [kb0, kb1) of tile t
+    int mode;      // kWhole; kHead: first stages, adds the others' partials; kPartial: later stages
+};
+
+struct WorkIter {
+    int64_t cur, end;
+    bool split;
+};
+
+__device__ __forceinline__ WorkIter work_begin(const GemmParams& p, int total_tiles)
+{
+    WorkIter w;
+    w.split = p.units > 0;
+    if (w.split) {
+        w.cur = static_cast<int64_t>(blockIdx.x) * p.units / gridDim.x;
+        w.end = static_cast<int64_t>(blockIdx.x + 1) * p.units / gridDim.x;
+    } else {
+        w.cur = blockIdx.x;
+        w.end = total_tiles;
+    }
+    return w;
+}
+
+__device__ __forceinline__ bool work_next(WorkIter& it, int nkb, Work& w)
+{
+    if (it.cur >= it.end)
+        return false;
+    if (it.split) {
+        w.t = static_cast<int>(it.cur / nkb);
+        const int64_t base = static_cast<int64_t>(w.t) * nkb;
+        w.kb0 = static_cast<int>(it.cur - base);
+        w.kb1 = static_cast<int>(min(it.end - base, static_cast<int64_t>(nkb)));
+        w.mode = w.kb0 > 0 ? kPartial : (w.kb1 < nkb ? kHead : kWhole);
+        it.cur = base + w.kb1;
+    } else {
+        w.t = static_cast<int>(it.cur);
+        w.kb0 = 0;
+        w.kb1 = nkb;
+        w.mode = kWhole;
+        it.cur += gridDim.x;
+    }
+    return true;
+}
+
+// Split-K: the CTA whose unit range holds unit u.
+__device__ __forceinline__ int unit_owner(int64_t u, int64_t units)
+{
+    return static_cast<int>(((u + 1) * gridDim.x - 1) / units);
+}
+
+// Release add at GPU scope: the warp's earlier writes (ordered before it by a
+// __syncwarp) are visible to whoever acquires the counter afterwards.
+__device__ __forceinline__ void red_release_add_gpu(uint32_t* p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 template <int KC>
 __device__ __forceinline__ void load_operand(void* dst, const CUtensorMap* map, uint64_t* bar, int kb, int64_t row0)
 {
@@ -257,15 +337,17 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
             // ------------------------------------------------- TMA producer
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const Tile T = decode_tile<BN, kGrouped>(t, p, tiles_before);
+            WorkIter wi = work_begin(p, total_tiles);
+            Work w;
+            while (ok && work_next(wi, nkb, w)) {
+                const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
                 if (!T.valid)
                     continue;
                 const int64_t b_row0 = static_cast<int64_t>(T.expert) * p.rows_b + T.n0;
                 const uint8_t* sfb = p.sfb + static_cast<int64_t>(T.expert) * p.sfb_expert_stride;
                 int nsfb = (p.rows_b + 127) / 128 - T.n0 / 128;
                 nsfb = nsfb < C::SFB_TILES ? nsfb : C::SFB_TILES;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const int s = static_cast<int>(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kStatusTimeout, kWaitLimitNs)) {
@@ -294,8 +376,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
             constexpr uint32_t idesc = idesc_mxf4(BM, BN);
             uint32_t it = 0, tcount = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const Tile T = decode_tile<BN, kGrouped>(t, p, tiles_before);
+            WorkIter wi = work_begin(p, total_tiles);
+            Work w;
+            while (ok && work_next(wi, nkb, w)) {
+                const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
                 if (!T.valid)
                     continue;
                 // the epilogue must have drained the accumulator of the previous tile
@@ -304,7 +388,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const int s = static_cast<int>(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, kWaitLimitNs) ||
@@ -326,7 +410,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
                         tc_mma_mxf4(tmem_base, smem_desc(a_s + slab * (BM * kSlabBytes) + 32 * (k & 3), 16, 1024, 2),
                                     smem_desc(b_s + slab * (BN * kSlabBytes) + 32 * (k & 3), 16, 1024, 2),
                                     idesc_with_sf_id(idesc, sf_id), sfa_t + 4 * g, sfb_t + g * C::SF_COLS_B_GROUP,
-                                    (kb | k) != 0 ? 1u : 0u);
+                                    (kb != w.kb0 || k != 0) ? 1u : 0u);
                     }
                     tc_commit(&empty[s]);
                 }
@@ -343,11 +427,13 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
             const int me = warp - 2;
             uint32_t it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-                const Tile T = decode_tile<BN, kGrouped>(t, p, tiles_before);
+            WorkIter wi = work_begin(p, total_tiles);
+            Work w;
+            while (ok && work_next(wi, nkb, w)) {
+                const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
                 if (!T.valid)
                     continue;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const int s = static_cast<int>(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, kWaitLimitNs)) {
@@ -385,8 +471,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
         uint8_t* epi = smem + C::OFF_EPI;
         uint32_t tcount = 0;
         bool stored = false;  // this thread has bulk stores in flight
-        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-            const Tile T = decode_tile<BN, kGrouped>(t, p, tiles_before);
+        WorkIter wi = work_begin(p, total_tiles);
+        Work w;
+        while (work_next(wi, nkb, w)) {
+            const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
             if (!T.valid)
                 continue;
             const bool ok = mbar_wait_bounded(accum_full, tcount & 1u, p.status, kStatusTimeout, kWaitLimitNs);
@@ -408,6 +496,61 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
                 bulk_wait_group_read0();  // the previous store has left the staging area
             __syncwarp();
             if constexpr (kSwap) {
+                if (w.mode == kPartial) {
+                    // later stages of a split tile: leave the fp32 sums for the
+                    // finishing CTA ([BN tokens][128 rows], coalesced per column)
+                    float* slot = p.partials + static_cast<int64_t>(blockIdx.x) * (BN * BM);
+#pragma unroll
+                    for (int j = 0; j < CW; ++j)
+                        __stcg(slot + (half * CW + j) * BM + r, __uint_as_float(v[j]));
+                    __syncwarp();
+                    if (lane == 0)
+                        red_release_add_gpu(p.flags + blockIdx.x, 1u);  // ready once all 8 warps have added
+                    continue;
+                }
+                if (w.mode == kHead) {
+                    // add the partials of the CTAs holding the rest of the tile, in K order
+                    const int64_t last_unit = static_cast<int64_t>(w.t + 1) * nkb - 1;
+                    const int nparts = unit_owner(last_unit, p.units) - static_cast<int>(blockIdx.x);
+                    uint32_t* flags = p.flags + blockIdx.x + 1;
+                    // lane j waits for partial j (all in parallel), bounded
+                    for (int j = lane; j < nparts; j += 32) {
+                        const uint64_t t0 = global_timer_ns();
+                        while (ld_acquire_gpu(flags + j) < kEpiWarps) {
+                            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                                atomicOr(p.status, kStatusTimeout);
+                                break;
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    // the loads of partial c + 1 are in flight while partial c is added
+                    const float* slot = p.partials + static_cast<int64_t>(blockIdx.x + 1) * (BN * BM) + half * CW * BM + r;
+                    float nxt[CW];
+#pragma unroll
+                    for (int j = 0; j < CW; ++j)
+                        nxt[j] = nparts > 0 ? __ldcg(slot + j * BM) : 0.0f;
+                    for (int c = 0; c < nparts; ++c) {
+                        float cur[CW];
+#pragma unroll
+                        for (int j = 0; j < CW; ++j)
+                            cur[j] = nxt[j];
+                        if (c + 1 < nparts) {
+                            const float* ns = slot + static_cast<int64_t>(c + 1) * (BN * BM);
+#pragma unroll
+                            for (int j = 0; j < CW; ++j)
+                                nxt[j] = __ldcg(ns + j * BM);
+                        }
+#pragma unroll
+                        for (int j = 0; j < CW; ++j)
+                            v[j] = __float_as_uint(__uint_as_float(v[j]) + cur[j]);
+                    }
+                    __syncwarp();
+                    // the last of the 8 reading warps puts each counter back to zero
+                    for (int j = lane; j < nparts; j += 32)
+                        if (atomicAdd(flags + j, 1u) == 2 * kEpiWarps - 1)
+                            atomicExch(flags + j, 0u);
+                }
                 // lane = output column n (weight row); tile columns = tokens.
                 // This warp's 32 columns x CW tokens go out as one box,
                 // staged as [CW tokens][32 n].
@@ -586,6 +729,9 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
                 : make_output_map(&tmO, a.out, a.M, a.N, kChunk, kChunk, CU_TENSOR_MAP_SWIZZLE_64B)))
         return cudaErrorInvalidValue;
     GemmParams p;
+    p.units = 0;
+    p.flags = nullptr;
+    p.partials = nullptr;
     p.sfa = kSwap ? a.sb : a.sa;
     p.sfb = kSwap ? a.sa : a.sb;
     p.bias = static_cast<const __nv_bfloat16*>(a.bias);
@@ -605,7 +751,25 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (tiles == 0)
         return cudaSuccess;
-    const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count()));
+    const int sms = sm_count();
+    int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
+    if constexpr (kSwap && !kGrouped) {
+        // Split-K when at least half the SMs would sit idle: S CTAs per tile
+        // (S <= 8 keeps the finishing CTA's reduction short), each holding an
+        // equal run of the tile's K stages.  Handing the partial sums over
+        // through L2 (write, publish, wait, read) costs about as much as ten
+        // stages, so it is used only where it saves more stages than that.
+        const int64_t nkb = (p.kb4 + C::GROUPS - 1) / C::GROUPS;
+        const int64_t S = std::min<int64_t>(std::min<int64_t>(8, sms / tiles), nkb);
+        const size_t flag_bytes = (static_cast<size_t>(sms) * 4 + 255) / 256 * 256;
+        const size_t need = flag_bytes + static_cast<size_t>(tiles * S) * BN * BM * 4;
+        if (a.workspace && a.workspace_bytes >= need && S >= 2 && nkb * (S - 1) >= 10 * S) {
+            p.units = tiles * nkb;
+            p.flags = static_cast<uint32_t*>(a.workspace);
+            p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + flag_bytes);
+            grid = static_cast<int>(tiles * S);
+        }
+    }
     const size_t smem = C::SMEM_FIXED + (kGrouped ? sizeof(int32_t) * (a.E + 1) : 0);
     auto kern = gemm_mxfp4_kernel<BN, STAGES, KC, CPW, kSwap, kGrouped>;
     // The shared-memory opt-in is a per-device function attribute: set it
@@ -629,6 +793,16 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
 }
 
 }  // namespace
+
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K)
+{
+    (void)N;
+    (void)K;
+    if (M < 1 || M > 64)
+        return 0;
+    const size_t sms = static_cast<size_t>(sm_count());
+    return (sms * 4 + 255) / 256 * 256 + sms * 64 * BM * 4;  // sized for the widest swapped tile (64 tokens)
+}
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream)
 {

@@ -74,8 +74,15 @@ struct GemmArgs {
     int64_t N;
     int64_t K;
     unsigned int* status;
+    void* workspace;             // split-K scratch (nullptr: none)
+    size_t workspace_bytes;
 };
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
+
+// Workspace the decode-sized (M <= 64) GEMM uses for split-K on the current
+// device: a zero-initialised counter per SM, then one fp32 partial tile per
+// SM.  0 for other M.
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 }  // namespace fp4lin

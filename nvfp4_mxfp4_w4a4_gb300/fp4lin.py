@@ -26,7 +26,8 @@ SYMBOLS = (
     "fp4_sf_bytes", "fp4_sf_bytes_grouped", "fp4_status_string", "fp4_get_device_status",
     "fp4_requant_nvfp4_to_mxfp4", "fp4_requant_nvfp4_to_mxfp4_ex", "fp4_requant_nvfp4_to_mxfp4_grouped",
     "fp4_quant_act_mxfp4",
-    "fp4_quant_act_mxfp4_grouped", "fp4_quant_nvfp4", "fp4_gemm_mxfp4", "fp4_gemm_mxfp4_grouped",
+    "fp4_quant_act_mxfp4_grouped", "fp4_quant_nvfp4", "fp4_gemm_mxfp4", "fp4_gemm_workspace_size",
+    "fp4_gemm_mxfp4_ws", "fp4_gemm_mxfp4_grouped",
 )
 
 
@@ -68,6 +69,8 @@ def load(path: str = LIB_PATH):
                                                            ctypes.POINTER(fp4_quant_opts), _p]),
             "fp4_quant_nvfp4": (ctypes.c_int, [_p, ctypes.c_float, _p, _p, _i64, _i64, _p]),
             "fp4_gemm_mxfp4": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p]),
+            "fp4_gemm_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64]),
+            "fp4_gemm_mxfp4_ws": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, ctypes.c_size_t, _p]),
             "fp4_gemm_mxfp4_grouped": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p]),
         }
         for name, (res, args) in sig.items():
@@ -170,6 +173,19 @@ def fp4_gemm_mxfp4(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, stream=None):
     st = load().fp4_gemm_mxfp4(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias_bf16), _ptr(out_bf16), M, N, K,
                                _stream(stream))
     _check(st, "fp4_gemm_mxfp4")
+
+
+def fp4_gemm_workspace_size(M, N, K) -> int:
+    return load().fp4_gemm_workspace_size(M, N, K)
+
+
+def fp4_gemm_mxfp4_ws(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, workspace, workspace_bytes=None, stream=None):
+    """workspace: device buffer (e.g. a zero-initialised uint8 tensor) or None."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().fp4_gemm_mxfp4_ws(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias_bf16), _ptr(out_bf16), M, N, K,
+                                  _ptr(workspace), workspace_bytes, _stream(stream))
+    _check(st, "fp4_gemm_mxfp4_ws")
 
 
 def fp4_gemm_mxfp4_grouped(a, sa, b, sb, bias_bf16, out_bf16, row_offsets, E, total_M, N, K, stream=None):

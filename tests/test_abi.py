@@ -72,6 +72,7 @@ def test_argument_checks_precede_device_use(L):
     # alignment
     assert raw.fp4_gemm_mxfp4(17, 16, 16, 16, None, 16, 1, 8, 128, None) == 3
     assert raw.fp4_quant_act_mxfp4(24, 16, 16, 4, 32, None, None) == 3
+    assert raw.fp4_gemm_mxfp4_ws(16, 16, 16, 16, None, 16, 1, 8, 128, 16, 1 << 20, None) == 3   # workspace 256 B
     assert raw.fp4_requant_nvfp4_to_mxfp4_grouped(16, 32, 32, 32, 32, 2, 4, 128, None, None) == 3  # codes 32 B
     # bad option values
     from nvfp4_mxfp4_w4a4_gb300.fp4lin import fp4_quant_opts
