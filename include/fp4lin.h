@@ -202,10 +202,10 @@ FP4LIN_API fp4_status fp4_gemm_mxfp4(const uint8_t* a, const uint8_t* sa, const 
                           const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K,
                           void* stream);
 
-/* Bytes of workspace fp4_gemm_mxfp4_ws can use for an M x N x K problem on
- * the current device (0: the problem never needs any; also 0 when the
- * device is unusable).  Decode-sized M (1..64): one 32-bit counter per SM
- * (256-byte padded) and one 64 x 128 fp32 partial tile per SM.             */
+/* Bytes of workspace fp4_gemm_mxfp4_ws uses for an M x N x K problem on
+ * the current device: 0 when the problem is not split (see below; also 0
+ * when the device is unusable), else one 32-bit counter per SM (256-byte
+ * padded) followed by one fp32 partial tile (tile width x 128) per CTA.     */
 FP4LIN_API size_t fp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /* fp4_gemm_mxfp4 with caller workspace for split-K (the tile scheduling

@@ -711,6 +711,37 @@ int sm_count()
     return cached[dev];
 }
 
+// Split-K plan of a swapped (M <= 64) problem: S CTAs per tile (S < 2: no
+// split) and the workspace that takes.  Split only when at least half the
+// SMs would sit idle; S <= 8 keeps the finishing CTA's reduction short, and
+// handing the partial sums over through L2 (write, publish, wait, read)
+// costs about as much as ten stages, so the split must save more than that.
+struct SplitPlan {
+    int64_t S;
+    size_t bytes;
+};
+
+SplitPlan split_plan(int64_t tiles, int64_t nkb, int bn, int sms)
+{
+    SplitPlan sp{1, 0};
+    if (tiles <= 0)
+        return sp;
+    const int64_t S = std::min<int64_t>(std::min<int64_t>(8, sms / tiles), nkb);
+    if (S >= 2 && nkb * (S - 1) >= 10 * S) {
+        sp.S = S;
+        sp.bytes = (static_cast<size_t>(sms) * 4 + 255) / 256 * 256 + static_cast<size_t>(tiles * S) * bn * BM * 4;
+    }
+    return sp;
+}
+
+// The swapped configuration launch_gemm picks for M <= 64: tile width and
+// 256-element slabs per stage.
+void swap_config(int64_t M, int64_t K, int* bn, int* kc)
+{
+    *kc = K % 256 == 0 ? 2 : 1;
+    *bn = (*kc == 2 && M <= 32) ? 32 : 64;
+}
+
 template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped>
 cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
 {
@@ -754,20 +785,15 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
     const int sms = sm_count();
     int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
     if constexpr (kSwap && !kGrouped) {
-        // Split-K when at least half the SMs would sit idle: S CTAs per tile
-        // (S <= 8 keeps the finishing CTA's reduction short), each holding an
-        // equal run of the tile's K stages.  Handing the partial sums over
-        // through L2 (write, publish, wait, read) costs about as much as ten
-        // stages, so it is used only where it saves more stages than that.
+        // split-K: S CTAs per tile, each an equal run of the tile's K stages
         const int64_t nkb = (p.kb4 + C::GROUPS - 1) / C::GROUPS;
-        const int64_t S = std::min<int64_t>(std::min<int64_t>(8, sms / tiles), nkb);
-        const size_t flag_bytes = (static_cast<size_t>(sms) * 4 + 255) / 256 * 256;
-        const size_t need = flag_bytes + static_cast<size_t>(tiles * S) * BN * BM * 4;
-        if (a.workspace && a.workspace_bytes >= need && S >= 2 && nkb * (S - 1) >= 10 * S) {
+        const SplitPlan sp = split_plan(tiles, nkb, BN, sms);
+        if (sp.S >= 2 && a.workspace && a.workspace_bytes >= sp.bytes) {
+            const size_t flag_bytes = (static_cast<size_t>(sms) * 4 + 255) / 256 * 256;
             p.units = tiles * nkb;
             p.flags = static_cast<uint32_t*>(a.workspace);
             p.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + flag_bytes);
-            grid = static_cast<int>(tiles * S);
+            grid = static_cast<int>(tiles * sp.S);
         }
     }
     const size_t smem = C::SMEM_FIXED + (kGrouped ? sizeof(int32_t) * (a.E + 1) : 0);
@@ -796,12 +822,12 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K)
 {
-    (void)N;
-    (void)K;
-    if (M < 1 || M > 64)
+    if (M < 1 || M > 64 || N <= 0 || K <= 0 || K % 128 != 0)
         return 0;
-    const size_t sms = static_cast<size_t>(sm_count());
-    return (sms * 4 + 255) / 256 * 256 + sms * 64 * BM * 4;  // sized for the widest swapped tile (64 tokens)
+    int bn = 0, kc = 0;
+    swap_config(M, K, &bn, &kc);
+    const int64_t nkb = (K / 128 + 2 * kc - 1) / (2 * kc);
+    return split_plan((N + BM - 1) / BM, nkb, bn, sm_count()).bytes;
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream)
@@ -819,6 +845,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream)
                     : launch_kernel<128, 6, 1, 4, false, true>(a, stream);
     }
     // decode-sized batches: weights on the 128-row MMA side, tokens as N
+    // (the choice swap_config describes)
     if (a.M <= 64) {
         if (!k256)
             return launch_kernel<64, 8, 1, 4, true, false>(a, stream);

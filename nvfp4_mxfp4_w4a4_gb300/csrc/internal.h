@@ -80,9 +80,9 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
 
-// Workspace the decode-sized (M <= 64) GEMM uses for split-K on the current
-// device: a zero-initialised counter per SM, then one fp32 partial tile per
-// SM.  0 for other M.
+// Workspace the GEMM uses for split-K on this problem on the current device
+// (0: the problem is not split): a zero-initialised counter per SM (256-byte
+// padded), then one fp32 partial tile per CTA.
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 }  // namespace fp4lin

@@ -28,12 +28,12 @@ def _operands(orc, M, N, K, seed):
     return a, sa, b, sb
 
 
-def _workspace(L, M, N, K):
+def _workspace(L, M, N, K, split=True):
     import torch
 
     n = L.fp4_gemm_workspace_size(M, N, K)
-    assert n > 0
-    return torch.zeros(n, dtype=torch.uint8, device="cuda")
+    assert (n > 0) == split
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device="cuda")
 
 
 def _run(L, orc, a, sa, b, sb, bias, M, N, K, ws):
@@ -86,7 +86,7 @@ def test_workspace_entry_without_split_k(orc, L):
     workspace) run the plain path through the same entry point."""
     for (M, N, K, use_ws) in ((100, 256, 1024, True), (16, 12288, 512, True), (8, 1024, 4096, False), (64, 4096, 4096, True)):
         a, sa, b, sb = _operands(orc, M, N, K, M + N)
-        ws = _workspace(L, min(M, 64), N, K) if use_ws else None
+        ws = _workspace(L, M, N, K, split=False) if use_ws else None
         out = _run(L, orc, a, sa, b, sb, None, M, N, K, ws)
         ref, absum = orc.gemm(a, sa, b, sb, threads=THREADS)
         ok, ratio = gemm_check(out, ref, absum)
