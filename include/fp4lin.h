@@ -231,6 +231,28 @@ FP4LIN_API fp4_status fp4_gemm_mxfp4_ws(const uint8_t* a, const uint8_t* sa, con
                              int64_t M, int64_t N, int64_t K, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/* fp4_gemm_mxfp4_ws for callers that cannot provide device memory (a host
+ * program holding no device allocator of its own, or a runtime that must
+ * not allocate on its request path).  The pages have no counterpart: it
+ * exists because of this library's split-K workspace.  The scratch is a
+ * fixed 2 MiB array inside the library's device image (one per device,
+ * zero when the library loads); nothing is allocated by this call or by
+ * the library for it.
+ *   Same arguments, results and rules as fp4_gemm_mxfp4_ws with the
+ *   array as workspace (bit-identical outputs).
+ *   FP4_ERR_SHAPE also when the problem's split-K plan needs more than
+ *   2 MiB (fp4_gemm_workspace_size(M, N, K) > 2 MiB): use
+ *   fp4_gemm_mxfp4_ws with a workspace of that size instead.
+ *   The first call on a device looks up the array's device address; make
+ *   that first call before starting a stream capture.
+ *   Calls on one device must not overlap in time (the array is shared by
+ *   every caller in the process).  Each call needs the array's counters
+ *   at zero and leaves them zero; after FP4_ERR_TIMEOUT their state is
+ *   unknown.                                                                */
+FP4LIN_API fp4_status fp4_gemm_mxfp4_noalloc(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
+                                  const uint8_t* sb, const void* bias_bf16, void* out_bf16,
+                                  int64_t M, int64_t N, int64_t K, void* stream);
+
 /* Grouped (MoE) W4A4 GEMM ([AMD] "Native FP4 matmul": MoE experts on
  * MXFP4): for every expert e and every row m in [row_offsets[e],
  * row_offsets[e+1]):  out[m, :] = A[m, :] . B_e^T (+ bias_e).

@@ -17,7 +17,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfp4lin.so")
 LIB_PEAK = os.path.join(HERE, "libfp4peak.so")
 ROOT = os.path.dirname(HERE)
-SOURCES = ["api.cu", "quant.cu", "gemm.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm_noalloc.cu"]
 PEAK_SOURCES = ["mma_peak.cu"]
 HEADERS = ["ptx.cuh", "formats.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

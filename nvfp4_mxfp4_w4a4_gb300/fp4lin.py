@@ -16,6 +16,12 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp4lin.so")
 
 FP4_OK = 0
+FP4_ERR_INVALID_ARG = 1
+FP4_ERR_SHAPE = 2
+FP4_ERR_ALIGNMENT = 3
+FP4_ERR_UNSUPPORTED = 4
+FP4_ERR_CUDA = 5
+FP4_ERR_TIMEOUT = 6
 FP4_SCALE_OCP = 0
 FP4_SCALE_UOS = 2
 FP4_SF_SWIZZLED = 0
@@ -27,7 +33,7 @@ SYMBOLS = (
     "fp4_requant_nvfp4_to_mxfp4", "fp4_requant_nvfp4_to_mxfp4_ex", "fp4_requant_nvfp4_to_mxfp4_grouped",
     "fp4_quant_act_mxfp4",
     "fp4_quant_act_mxfp4_grouped", "fp4_quant_nvfp4", "fp4_gemm_mxfp4", "fp4_gemm_workspace_size",
-    "fp4_gemm_mxfp4_ws", "fp4_gemm_mxfp4_grouped",
+    "fp4_gemm_mxfp4_ws", "fp4_gemm_mxfp4_noalloc", "fp4_gemm_mxfp4_grouped",
 )
 
 
@@ -71,6 +77,7 @@ def load(path: str = LIB_PATH):
             "fp4_gemm_mxfp4": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p]),
             "fp4_gemm_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64]),
             "fp4_gemm_mxfp4_ws": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, ctypes.c_size_t, _p]),
+            "fp4_gemm_mxfp4_noalloc": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p]),
             "fp4_gemm_mxfp4_grouped": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p]),
         }
         for name, (res, args) in sig.items():
@@ -186,6 +193,13 @@ def fp4_gemm_mxfp4_ws(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, workspace, wor
     st = load().fp4_gemm_mxfp4_ws(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias_bf16), _ptr(out_bf16), M, N, K,
                                   _ptr(workspace), workspace_bytes, _stream(stream))
     _check(st, "fp4_gemm_mxfp4_ws")
+
+
+def fp4_gemm_mxfp4_noalloc(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, stream=None):
+    """The GEMM with the library's fixed device scratch (allocates nothing)."""
+    st = load().fp4_gemm_mxfp4_noalloc(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias_bf16), _ptr(out_bf16), M, N,
+                                       K, _stream(stream))
+    _check(st, "fp4_gemm_mxfp4_noalloc")
 
 
 def fp4_gemm_mxfp4_grouped(a, sa, b, sb, bias_bf16, out_bf16, row_offsets, E, total_M, N, K, stream=None):
