@@ -511,7 +511,8 @@ def _committed_traffic(workload, kernel):
     import hashlib
 
     p = os.path.join(ROOT, "profiles", "traffic.md")
-    src = {"gemm_mxfp4_kernel": "gemm.cu", "requant_kernel": "quant.cu", "act_quant_kernel": "quant.cu"}.get(kernel)
+    src = {"gemm_mxfp4_kernel": "gemm.cu", "requant_kernel": "quant.cu", "requant_flat_kernel": "quant.cu",
+           "act_quant_kernel": "quant.cu"}.get(kernel)
     if not os.path.exists(p) or src is None:
         return None
     sha = hashlib.sha256(open(os.path.join(ROOT, "nvfp4_mxfp4_w4a4_gb300", "csrc", src), "rb").read()).hexdigest()
