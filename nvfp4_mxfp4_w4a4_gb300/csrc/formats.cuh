@@ -43,46 +43,23 @@ __device__ __forceinline__ uint32_t e2m1_code(float z)
     return __float_as_uint(e2m1_code_scaled<0>(z)) & 0xFFu;
 }
 
-// Packed bf16 pairs (two values per 32-bit word, low half first), with
-// round-to-nearest-even and subnormals kept.
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
+// Eight values to eight E2M1 codes in one word (value 2k in bits 8k..8k+3,
+// value 2k+1 in bits 8k+4..8k+7): the hardware pair conversion, which rounds
+// to the nearest grid value with ties to the even code, saturates at +-6 and
+// keeps the sign of zero, as the MX encoding wants.
+__device__ __forceinline__ uint32_t e2m1x8_pack(float q0, float q1, float q2, float q3, float q4, float q5, float q6,
+                                                float q7)
 {
-    uint32_t d;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-__device__ __forceinline__ uint32_t bf16x2_add(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c)
-{
-    uint32_t d;
-    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-// E2M1 magnitude codes of two non-negative bf16 values q < 8 in one word:
-// the same lower-envelope rounding as e2m1_code_scaled, in bf16 pairs.  The
-// magic constant is 192 = 1.5 * 2^7, whose bf16 ulp is 1, so 192 + y rounds
-// y to an integer (nearest even) for 0 <= y < 64; each half of the result
-// holds 192 + code, i.e. the code in its 3 low mantissa bits.
-__device__ __forceinline__ uint32_t e2m1_codes_bf16x2(uint32_t q)
-{
-    constexpr uint32_t kTwo = 0x40004000u, kHalf = 0x3F003F00u;
-    constexpr uint32_t kM0 = 0x43404340u, kM2 = 0x43424342u, kM4 = 0x43444344u, kM7 = 0x43474347u;
-    const uint32_t a = bf16x2_fma(q, kTwo, kM0);   // 192 + rint(2q)
-    const uint32_t b = bf16x2_add(q, kM2);         // 194 + rint(q)
-    const uint32_t c = bf16x2_fma(q, kHalf, kM4);  // 196 + rint(q/2)
-    return bf16x2_min(bf16x2_min(a, b), bf16x2_min(c, kM7));
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(q0), "f"(q1), "f"(q2), "f"(q3), "f"(q4), "f"(q5), "f"(q6), "f"(q7));
+    return r;
 }
 
 // Shared exponent from the fp32 bit pattern of a finite, non-negative amax.

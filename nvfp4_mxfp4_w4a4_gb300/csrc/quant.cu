@@ -452,9 +452,10 @@ __global__ void __launch_bounds__(kThreads) requant_flat_kernel(const uint8_t* _
 // ------------------------------------------------------- activation quant
 // One lane holds 8 consecutive bf16 of a 32-element block (4 lanes per
 // block).  Returns the packed codes (4 bytes) and, through `sf`, the block's
-// scale byte (the same on all 4 lanes).  q = |x| * 2^-e is exact in bf16
-// (a power-of-two scaling; results too small for bf16's normal range round
-// to codes of 0 whatever they are), so the rounding runs on bf16 pairs.
+// scale byte (the same on all 4 lanes).  q = x * 2^-e is exact in fp32 (a
+// bf16 value times a power of two; e <= 125 for a finite bf16 amax and
+// e >= -127 after the clamp, so 2^-e is a normal fp32), and the hardware
+// pair conversion rounds it to E2M1.
 __device__ __forceinline__ uint32_t act_quant_lane(uint4 v, int uos, uint32_t& sf)
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -471,17 +472,14 @@ __device__ __forceinline__ uint32_t act_quant_lane(uint4 v, int uos, uint32_t& s
     }
     const int e = mx_shared_exp(ab, uos);
     sf = static_cast<uint32_t>(e + 127);
-    const uint32_t se = static_cast<uint32_t>(127 - e) << 7;  // bf16 2^-e
-    const uint32_t se2 = se | (se << 16);
-    uint32_t t[4];
+    const float se = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
+    float q[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const uint32_t r = e2m1_codes_bf16x2(bf16x2_mul(w[j] & 0x7FFF7FFFu, se2));
-        // code + sign of the low element in bits 0-3, of the high one in 16-19
-        const uint32_t c = (r & 0x00070007u) | ((w[j] >> 12) & 0x00080008u);
-        t[j] = c | (c >> 12);  // byte 0 = low | high << 4
+        q[2 * j] = __fmul_rn(__uint_as_float(w[j] << 16), se);
+        q[2 * j + 1] = __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), se);
     }
-    return __byte_perm(__byte_perm(t[0], t[1], 0x0040u), __byte_perm(t[2], t[3], 0x4000u), 0x7610u);
+    return e2m1x8_pack(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
 }
 
 // Tile-prefix of a grouped activation tensor: group e starts at scale row
