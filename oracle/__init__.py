@@ -65,6 +65,8 @@ def lib():
                 ("orc_requant", None, [_p, _p, ctypes.c_float, _i64, _i64, _i64, ctypes.c_int, _p, _p]),
                 ("orc_act_quant", None, [_p, _i64, _i64, _i64, ctypes.c_int, _p, _p]),
                 ("orc_gemm", None, [_p, _p, _p, _p, _p, _i64, _p, _i64, _p, _i64, _p, _p]),
+                ("orc_gemm_nvfp4", None,
+                 [_p, _p, _p, _p, ctypes.c_double, _p, _i64, _p, _i64, _p, _i64, _p, _p]),
                 ("orc_nvfp4_global_scale", ctypes.c_float, [_p, _i64]),
                 ("orc_nvfp4_quantize", None, [_p, ctypes.c_float, _i64, _i64, _i64, _p, _p]),
                 ("orc_sf_swizzled_bytes", _i64, [_i64, _i64]),
@@ -199,6 +201,39 @@ def gemm(a, sa, b, sb, bias_bf16_bits=None, rows=None, cols=None, threads=1):
         s = np.empty_like(r)
         L.orc_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias), K, _ptr(sub_rows), r1 - r0,
                    _ptr(cols), len(cols), _ptr(r), _ptr(s))
+        ref[r0:r1] = r
+        absum[r0:r1] = s
+
+    _parallel(run, len(rows), threads)
+    return ref, absum
+
+
+def gemm_nvfp4(a, sa, b, sb, alpha, bias_bf16_bits=None, rows=None, cols=None, threads=1):
+    """float64 reference of the NVFP4 x NVFP4 GEMM (codes times E4M3 scales, times alpha).
+
+    a [M, K/2], sa row-major E4M3 [M, K/16]; b [N, K/2], sb row-major [N, K/16].
+    Returns (ref, absum) of shape [len(rows), len(cols)].
+    """
+    a = np.ascontiguousarray(a)
+    b = np.ascontiguousarray(b)
+    sa = np.ascontiguousarray(sa)
+    sb = np.ascontiguousarray(sb)
+    M, half = a.shape
+    N = b.shape[0]
+    K = 2 * half
+    rows = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    cols = np.arange(N, dtype=np.int64) if cols is None else np.ascontiguousarray(cols, np.int64)
+    bias = None if bias_bf16_bits is None else np.ascontiguousarray(bias_bf16_bits, np.uint16)
+    ref = np.empty((len(rows), len(cols)), np.float64)
+    absum = np.empty_like(ref)
+    L = lib()
+
+    def run(r0, r1):
+        sub_rows = np.ascontiguousarray(rows[r0:r1])
+        r = np.empty((r1 - r0, len(cols)), np.float64)
+        s = np.empty_like(r)
+        L.orc_gemm_nvfp4(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), float(alpha), _ptr(bias), K, _ptr(sub_rows),
+                         r1 - r0, _ptr(cols), len(cols), _ptr(r), _ptr(s))
         ref[r0:r1] = r
         absum[r0:r1] = s
 

@@ -276,6 +276,56 @@ void orc_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8
 }
 
 /* ------------------------------------------------------------------------
+ * NVFP4 x NVFP4 GEMM: the FP4 inference path of [SGL] sections 5-6, which
+ * runs the GEMM on NVFP4 operands directly (hardware with native NVFP4).
+ * Both operands are E2M1 codes with one E4M3 scale per 16 elements; the
+ * GEMM works on the scaled codes and one per-tensor factor alpha restores
+ * the two global scales (section 5 forms alpha as 1 / (input_global_scale *
+ * weight_global_scale) from divisor-form scales; with the multiplicative
+ * global scales used here alpha = g_a * g_b); section 6 adds the bias to the
+ * GEMM output.  The definition, in double:
+ *   out[m][n] = alpha * sum_k (E2M1(a) E4M3(sa))[m][k] * (E2M1(b) E4M3(sb))[n][k]
+ *               + bias[n]
+ * Every code-times-scale value is exact in double.                       */
+static void scaled_nv_row(const uint8_t* packed, const uint8_t* s, int64_t K, double* out)
+{
+    for (int64_t k = 0; k < K; ++k) {
+        uint8_t byte = packed[k / 2];
+        unsigned c = (k % 2 == 0) ? (byte & 0xFu) : (byte >> 4);
+        out[k] = orc_e2m1_value(c) * orc_e4m3_value(s[k / 16]);
+    }
+}
+
+void orc_gemm_nvfp4(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                    double alpha, const uint16_t* bias_bf16, int64_t K,
+                    const int64_t* rows, int64_t n_rows, const int64_t* cols, int64_t n_cols,
+                    double* ref, double* absum)
+{
+    double* arows = (double*)malloc(sizeof(double) * (size_t)(n_rows * K));
+    double* brow = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int64_t i = 0; i < n_rows; ++i)
+        scaled_nv_row(a + rows[i] * (K / 2), sa + rows[i] * (K / 16), K, arows + i * K);
+    for (int64_t j = 0; j < n_cols; ++j) {
+        int64_t n = cols[j];
+        scaled_nv_row(b + n * (K / 2), sb + n * (K / 16), K, brow);
+        double bias = bias_bf16 ? orc_bf16_value(bias_bf16[n]) : 0.0;
+        for (int64_t i = 0; i < n_rows; ++i) {
+            const double* arow = arows + i * K;
+            double s = 0.0, sabs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = arow[k] * brow[k];
+                s += p;
+                sabs += fabs(p);
+            }
+            ref[i * n_cols + j] = alpha * s + bias;
+            absum[i * n_cols + j] = fabs(alpha) * sabs;
+        }
+    }
+    free(brow);
+    free(arows);
+}
+
+/* ------------------------------------------------------------------------
  * NVFP4 producer, used only to build NVFP4 test inputs from bf16 tensors.
  * The recipe: g = amax / (6 * 448); per 16-element block the E4M3 scale is
  * the nearest E4M3 to block_amax / (6 g); each element is x / (scale * g)

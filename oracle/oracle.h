@@ -67,6 +67,16 @@ void orc_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8
               const int64_t* rows, int64_t n_rows, const int64_t* cols, int64_t n_cols,
               double* ref, double* absum);
 
+/* NVFP4 x NVFP4 GEMM ([SGL] sections 5-6): E2M1 codes with row-major E4M3
+ * scales per 16 elements (sa [rows][K/16], sb [cols][K/16]), one per-tensor
+ * factor alpha (= g_a * g_b), float64 accumulation:
+ *   ref[i][j] = alpha * sum_k (c s)_A[rows[i]][k] * (c s)_B[cols[j]][k] + bias
+ *   absum[i][j] = |alpha| * sum_k |(c s)_A * (c s)_B|.  bias may be NULL.   */
+void orc_gemm_nvfp4(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                    double alpha, const uint16_t* bias_bf16, int64_t K,
+                    const int64_t* rows, int64_t n_rows, const int64_t* cols, int64_t n_cols,
+                    double* ref, double* absum);
+
 /* ---- input preparation (NVFP4 producer used to build test inputs) ----- */
 float orc_nvfp4_global_scale(const uint16_t* x_bf16, int64_t n);   /* amax/(6*448) */
 void orc_nvfp4_quantize(const uint16_t* x_bf16, float g, int64_t row0, int64_t row1,

@@ -332,6 +332,78 @@ def test_gemm_one_hot_selects_columns(orc):
     assert np.array_equal(ref, A[:, sel])
 
 
+# ------------------------------------------------------ NVFP4 x NVFP4 GEMM
+
+
+def _nv_scaled_indep(packed, s_rowmajor):
+    """codes x E4M3 scales per 16 elements, decoded by the E2M1 fixture and torch."""
+    table = _e2m1_table()
+    vals = np.vectorize(lambda c: table[int(c)])(_unpack(packed))
+    return vals * np.repeat(_torch_e4m3(s_rowmajor).astype(np.float64), 16, axis=1)
+
+
+def test_gemm_nvfp4_matches_numpy_matmul(orc):
+    """Random codes and every finite E4M3 scale byte (both signs): the oracle is
+    alpha * (scaled A) @ (scaled B)^T + bias, decoded independently."""
+    rng = np.random.default_rng(23)
+    M, N, K = 5, 11, 192
+    finite = np.array([x for x in range(256) if (x & 0x7F) != 0x7F], np.uint8)
+    a = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = rng.choice(finite, (M, K // 16))
+    sb = rng.choice(finite, (N, K // 16))
+    bias = torch.randn(N).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    bias_f = torch.from_numpy(bias.view(np.int16)).view(torch.bfloat16).double().numpy()
+    alpha = 0.3711
+    A = _nv_scaled_indep(a, sa)
+    B = _nv_scaled_indep(b, sb)
+    prod_abs = np.abs(A) @ np.abs(B).T
+    ref, absum = orc.gemm_nvfp4(a, sa, b, sb, alpha, bias)
+    assert np.allclose(ref, alpha * (A @ B.T) + bias_f, rtol=1e-12, atol=1e-12 * alpha * prod_abs + 1e-300)
+    assert np.allclose(absum, alpha * prod_abs, rtol=1e-12)
+    rows, cols = np.array([4, 1]), np.array([0, 10, 7])
+    r2, _ = orc.gemm_nvfp4(a, sa, b, sb, alpha, bias, rows=rows, cols=cols)
+    assert np.array_equal(r2, ref[np.ix_(rows, cols)])
+
+
+def test_gemm_nvfp4_power_of_two_scales_equal_mx_gemm(orc):
+    """When both 16-element scales of every 32-block are the same power of two
+    2^j, an NVFP4 operand is the MXFP4 operand with E8M0 byte j + 127 and the
+    same codes: with alpha = 1 the two GEMMs agree bit for bit."""
+    rng = np.random.default_rng(29)
+    M, N, K = 6, 9, 256
+    a = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    ja = rng.integers(-6, 9, (M, K // 32))
+    jb = rng.integers(-6, 9, (N, K // 32))
+    # E4M3 of 2^j (normal range): exponent field j + 7, mantissa 0
+    nva = np.repeat(((ja + 7) << 3).astype(np.uint8), 2, axis=1)
+    nvb = np.repeat(((jb + 7) << 3).astype(np.uint8), 2, axis=1)
+    assert np.array_equal(_torch_e4m3(nva[:, ::2]), 2.0 ** ja)
+    ref_nv, abs_nv = orc.gemm_nvfp4(a, nva, b, nvb, 1.0)
+    ref_mx, abs_mx = orc.gemm(a, (ja + 127).astype(np.uint8), b, (jb + 127).astype(np.uint8))
+    assert np.array_equal(ref_nv, ref_mx)
+    assert np.array_equal(abs_nv, abs_mx)
+
+
+def test_gemm_nvfp4_one_hot_selects_columns(orc):
+    """B rows one-hot with code 1.0 under scale 1.0: out[:, n] = alpha * scaled A[:, sel[n]] exactly."""
+    rng = np.random.default_rng(31)
+    M, N, K = 4, 12, 128
+    a = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    sa = rng.integers(0x20, 0x60, (M, K // 16), dtype=np.uint8)
+    sel = rng.integers(0, K, N)
+    codes = np.zeros((N, K), np.uint8)
+    codes[np.arange(N), sel] = 0x2
+    b = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    sb = np.full((N, K // 16), 0x38, np.uint8)   # E4M3 1.0
+    ref, _ = orc.gemm_nvfp4(a, sa, b, sb, 0.5)
+    assert np.array_equal(ref, 0.5 * _nv_scaled_indep(a, sa)[:, sel])
+    # the same through the (separately pinned) NVFP4 decode with g = 1
+    dq = orc.nvfp4_dequant(a, sa, 1.0).astype(np.float64)
+    assert np.array_equal(ref, 0.5 * dq[:, sel])
+
+
 # ------------------------------------------------------ SF layout
 
 
