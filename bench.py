@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--breakdown-reps", type=int, default=200)
+    ap.add_argument("--no-nvfp4", action="store_true",
+                    help="skip the NVFP4 x NVFP4 comparison (dense workloads)")
     return ap.parse_args()
 
 
@@ -168,6 +170,7 @@ class Weight:
 
         dev = torch.device("cuda")
         self.L, self.N, self.K, self.E = L, N, K, len(bf16_list)
+        self.bf16_host = bf16_list[0] if self.E == 1 else None  # for the accuracy comparison
         self.packed = torch.empty((self.E * N, K // 2), dtype=torch.uint8, device=dev)
         self.scale = torch.empty((self.E * N, K // 16), dtype=torch.uint8, device=dev)
         self.g = []
@@ -389,7 +392,7 @@ class Bench:
         return out
 
 
-KERNEL_NAMES = {"gemm": "gemm_mxfp4_kernel", "requant": "requant_kernel", "act_quant": "act_quant_kernel"}
+KERNEL_NAMES = {"gemm": "gemm_fp4_kernel", "requant": "requant_flat_kernel", "act_quant": "act_quant_kernel"}
 
 
 def run_ours(args):
@@ -477,6 +480,9 @@ def run_ours(args):
         fp4_probe = {"error": str(exc)}
 
     e2e = _e2e(b, torch, L, min(args.steps, 50))
+    nvfp4 = None
+    if not args.no_nvfp4 and all(a.offsets is None for a in b.acts):
+        nvfp4 = nvfp4_comparison(b, L, torch, args.breakdown_reps, breakdown)
 
     req = [breakdown[k] for k in breakdown if k.startswith("requant")]
     result = {
@@ -493,7 +499,7 @@ def run_ours(args):
                               "of_probe": (round(100 * value / world / fp4_probe["tflops"], 3)
                                            if "tflops" in fp4_probe else None)},
         "fp4_probe_peak": fp4_probe,
-        "breakdown": breakdown, "shares": shares, "roofline": roofline, "e2e": e2e,
+        "breakdown": breakdown, "shares": shares, "roofline": roofline, "e2e": e2e, "nvfp4_path": nvfp4,
         "gpu_launches": b.launches_per_step * steps, "clocks": clk, "wall_s_timed_region": round(t_wall, 3),
     }
     if rank == 0 and not args.no_cpu_baseline and args.workload == "decode":
@@ -504,6 +510,94 @@ def run_ours(args):
         pg.destroy_process_group()
 
 
+class NvAct:
+    """The NVFP4 x NVFP4 path of "[SGLang] FP4 ..." sections 5-6 on the same
+    bf16 activations and NVFP4 weight: NVFP4 act-quant with swizzled scales,
+    then the NVFP4 GEMM with alpha = g_x * g_w (no requantization)."""
+
+    def __init__(self, L, torch, act):
+        dev = torch.device("cuda")
+        w = act.w
+        self.L, self.act, self.w = L, act, w
+        M, K = act.M, act.K
+        amax = float(act.x.float().abs().max())           # setup: the activations' global scale
+        self.g = float(np.float32(amax) / np.float32(6.0 * 448.0))
+        self.alpha = float(np.float32(self.g) * np.float32(w.g[0]))
+        self.packed = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+        self.scale = torch.empty(L.fp4_sf_bytes_nvfp4(M, K), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((M, w.N), dtype=torch.bfloat16, device=dev)
+        if not hasattr(w, "nv_scale"):                     # setup: the weight's scales in the MMA layout
+            w.nv_scale = torch.empty(L.fp4_sf_bytes_nvfp4(w.N, w.K), dtype=torch.uint8, device=dev)
+            L.fp4_sf_swizzle(w.scale, w.nv_scale, w.N, w.K // 16)
+        self.torch = torch
+
+    def quant(self, s):
+        a = self.act
+        self.L.fp4_quant_nvfp4_ex(a.x, self.g, self.packed, self.scale, a.M, a.K, stream=s)
+
+    def gemm(self, s):
+        a, w = self.act, self.w
+        ws = gemm_workspace(self.L, self.torch, a.M, w.N, a.K)
+        self.L.fp4_gemm_nvfp4(self.packed, self.scale, w.packed, w.nv_scale, self.alpha, w.bias, self.out, a.M,
+                              w.N, a.K, ws, stream=s)
+
+
+def _rel_err(out, X_bits, W_bits, bias, rows, cols):
+    """||out - X W^T (+ bias)|| / ||X W^T (+ bias)|| over a row/column sample,
+    the exact product of the unquantized bf16 tensors in float64."""
+    import synth
+
+    X = synth.bf16_bits_to_f32(X_bits[rows]).astype(np.float64)
+    W = synth.bf16_bits_to_f32(W_bits[cols]).astype(np.float64)
+    ref = X @ W.T
+    if bias is not None:
+        ref = ref + bias.float().cpu().numpy().astype(np.float64)[cols]
+    got = out.float().cpu().numpy().astype(np.float64)[np.ix_(rows, cols)]
+    return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+
+
+def nvfp4_comparison(b, L, torch, reps, breakdown):
+    """What the requant trades against a GPU with native NVFP4: per dense
+    GEMM of the workload, the NVFP4 act-quant and NVFP4 x NVFP4 GEMM times
+    (rotated over the same buffer sets as the breakdown) beside the MXFP4
+    ones, and both paths' output error against the unquantized bf16 product
+    on a sample."""
+    nv_sets = [[NvAct(L, torch, a) for a in acts] for _, acts in b.sets]
+    res = {"what": "NVFP4 act-quant + NVFP4 x NVFP4 GEMM (alpha = g_x g_w, no requant) vs the MXFP4 path",
+           "per_gemm": {}}
+    rng = np.random.default_rng(0)
+    for ai, a in enumerate(b.acts):
+        tag = f"M{a.M}_N{a.w.N}_K{a.K}"
+        entry = {}
+        for kind in ("quant", "gemm"):
+            g = b.graph(lambda s, i, ai=ai, kind=kind: getattr(nv_sets[i][ai], kind)(s))
+            r = max(1, -(-reps // b.n_sets))
+            b.time_graph(g, 1)
+            t = b.time_graph(g, r) / (r * b.n_sets) * 1e-3
+            entry[f"nv_{kind}_us"] = round(t * 1e6, 2)
+            if kind == "gemm":
+                entry["nv_gemm_TFLOPS"] = round(a.flops / t / 1e12, 2)
+        entry["mx_quant_us"] = breakdown[f"act_quant_{tag}"]["us"]
+        entry["mx_gemm_us"] = breakdown[f"gemm_{tag}"]["us"]
+        # accuracy on one set: both paths from the same bf16 tensors
+        nv = nv_sets[0][ai]
+        with torch.cuda.stream(b.stream):
+            a.quant(b.stream)
+            a.gemm(b.stream)
+            nv.quant(b.stream)
+            nv.gemm(b.stream)
+        torch.cuda.synchronize()
+        X_bits = a.x.view(torch.int16).cpu().numpy().view(np.uint16)
+        rows = np.sort(rng.choice(a.M, min(a.M, 128), replace=False))
+        cols = np.sort(rng.choice(a.w.N, min(a.w.N, 512), replace=False))
+        entry["mx_rel_err"] = round(_rel_err(a.out, X_bits, a.w.bf16_host, a.w.bias, rows, cols), 5)
+        entry["nv_rel_err"] = round(_rel_err(nv.out, X_bits, a.w.bf16_host, a.w.bias, rows, cols), 5)
+        res["per_gemm"][tag] = entry
+    res["requant_once_per_load_us"] = round(sum(v["us"] for k, v in breakdown.items() if k.startswith("requant")), 2)
+    res["sample"] = "rel. Frobenius error over <=128 rows x 512 columns, reference = bf16 X W^T in float64"
+    return res
+
+
 def _committed_traffic(workload, kernel):
     """DRAM bytes per launch of `kernel` on `workload` from profiles/traffic.md
     (table rows `| workload | kernel | source sha256 prefix | bytes |`), if
@@ -511,7 +605,7 @@ def _committed_traffic(workload, kernel):
     import hashlib
 
     p = os.path.join(ROOT, "profiles", "traffic.md")
-    src = {"gemm_mxfp4_kernel": "gemm.cu", "requant_kernel": "quant.cu", "requant_flat_kernel": "quant.cu",
+    src = {"gemm_fp4_kernel": "gemm.cu", "requant_kernel": "quant.cu", "requant_flat_kernel": "quant.cu",
            "act_quant_kernel": "quant.cu"}.get(kernel)
     if not os.path.exists(p) or src is None:
         return None

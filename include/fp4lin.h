@@ -185,6 +185,34 @@ FP4LIN_API fp4_status fp4_quant_act_mxfp4_grouped(const void* x_bf16, const int3
 FP4LIN_API fp4_status fp4_quant_nvfp4(const void* x_bf16, float g, uint8_t* out_packed,
                            uint8_t* out_scale_e4m3, int64_t M, int64_t K, void* stream);
 
+/* fp4_quant_nvfp4 with a choice of scale layout: FP4_SF_ROWMAJOR writes
+ * [M, K/16] (as fp4_quant_nvfp4), FP4_SF_SWIZZLED writes the layout
+ * fp4_gemm_nvfp4 reads (the swizzled layout of this header with 16-element
+ * blocks, fp4_sf_bytes_nvfp4(M, K, FP4_SF_SWIZZLED) bytes, pad bytes 0).
+ * FP4_ERR_INVALID_ARG for another sf_layout value; otherwise the rules of
+ * fp4_quant_nvfp4.                                                         */
+FP4LIN_API fp4_status fp4_quant_nvfp4_ex(const void* x_bf16, float g, uint8_t* out_packed,
+                              uint8_t* out_scale_e4m3, int64_t M, int64_t K, int32_t sf_layout,
+                              void* stream);
+
+/* Bytes of the E4M3 scales of an NVFP4 [rows, K] tensor (one per 16
+ * elements): row-major rows * K/16; swizzled ceil(rows/128)*128 *
+ * ceil(K/64)*4.  0 for K not a positive multiple of 16 or rows < 0.         */
+FP4LIN_API size_t fp4_sf_bytes_nvfp4(int64_t rows, int64_t K, int32_t sf_layout);
+
+/* Scale bytes row-major [rows][kblocks] -> the swizzled layout above, for
+ * either format (kblocks = K/32 for MXFP4 E8M0 scales, K/16 for NVFP4 E4M3
+ * scales).  The step [SGL] section 5 calls swizzle_blockscale, and what a
+ * pre-quantized MXFP4 checkpoint ([OMNI] "Pre-Quantized Single-Scale
+ * Weights": row-major (N, K/32) bytes) needs before fp4_gemm_mxfp4.
+ *   in_rowmajor  rows * kblocks bytes (device)
+ *   out          ceil(rows/128) * ceil(kblocks/4) * 512 bytes (device,
+ *                4-byte aligned); every byte is written, pad bytes as 0
+ * Requires rows >= 0 (0 is a no-op), kblocks >= 1; in and out must not
+ * overlap.                                                                  */
+FP4LIN_API fp4_status fp4_sf_swizzle(const uint8_t* in_rowmajor, uint8_t* out, int64_t rows,
+                          int64_t kblocks, void* stream);
+
 /* ------------------------------------------------------------------ GEMM */
 
 /* W4A4 GEMM on block-scaled FP4 tensor cores ([AMD] "Native FP4 matmul":
@@ -252,6 +280,28 @@ FP4LIN_API fp4_status fp4_gemm_mxfp4_ws(const uint8_t* a, const uint8_t* sa, con
 FP4LIN_API fp4_status fp4_gemm_mxfp4_noalloc(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
                                   const uint8_t* sb, const void* bias_bf16, void* out_bf16,
                                   int64_t M, int64_t N, int64_t K, void* stream);
+
+/* NVFP4 x NVFP4 GEMM on block-scaled FP4 tensor cores, the path [SGL]
+ * sections 5-6 take on hardware with native NVFP4 (the comparison point for
+ * the MXFP4 path: no requantization, twice the scale bytes):
+ *   out[m, n] = bf16_rne( alpha * sum_k (c s)_A[m,k] * (c s)_B[n,k] + bias[n] )
+ * with (c s) = E2M1 code times its 16-element block's E4M3 scale and fp32
+ * accumulation.  alpha restores the per-tensor global scales: g_a * g_b for
+ * multiplicative scales (section 5 forms 1 / (input_global_scale *
+ * weight_global_scale) from divisor-form ones).
+ *   a, b   [M, K/2], [N, K/2] u8 E2M1 codes
+ *   sa, sb SWIZZLED E4M3 scales (fp4_sf_bytes_nvfp4(rows, K, 0)); the tensor
+ *          cores read them as unsigned E4M3: every scale byte must be a
+ *          finite, non-negative E4M3 value (sign bit clear, not 0x7F), as
+ *          fp4_quant_nvfp4_ex writes for finite inputs and g > 0
+ *   bias   [N] bf16 or NULL;  out [M, N] bf16, row-major
+ *   workspace, workspace_bytes: split-K scratch as in fp4_gemm_mxfp4_ws
+ *          (same plan, same size: fp4_gemm_workspace_size(M, N, K)), or NULL
+ * Same shape and alignment rules as fp4_gemm_mxfp4.                        */
+FP4LIN_API fp4_status fp4_gemm_nvfp4(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
+                          const uint8_t* sb, float alpha, const void* bias_bf16, void* out_bf16,
+                          int64_t M, int64_t N, int64_t K, void* workspace,
+                          size_t workspace_bytes, void* stream);
 
 /* Grouped (MoE) W4A4 GEMM ([AMD] "Native FP4 matmul": MoE experts on
  * MXFP4): for every expert e and every row m in [row_offsets[e],

@@ -91,6 +91,16 @@ size_t fp4_sf_bytes(int64_t rows, int64_t K, int32_t sf_layout)
     return static_cast<size_t>(((rows + 127) / 128) * 128 * ((kb + 3) / 4) * 4);
 }
 
+size_t fp4_sf_bytes_nvfp4(int64_t rows, int64_t K, int32_t sf_layout)
+{
+    if (rows < 0 || K <= 0 || K % 16 != 0)
+        return 0;
+    const int64_t kb = K / 16;
+    if (sf_layout == FP4_SF_ROWMAJOR)
+        return static_cast<size_t>(rows * kb);
+    return static_cast<size_t>(((rows + 127) / 128) * 128 * ((kb + 3) / 4) * 4);
+}
+
 size_t fp4_sf_bytes_grouped(int64_t total_M, int32_t E, int64_t K)
 {
     if (total_M < 0 || E <= 0 || K <= 0 || K % 32 != 0)
@@ -227,11 +237,13 @@ fp4_status fp4_quant_act_mxfp4_grouped(const void* x_bf16, const int32_t* row_of
                                                       static_cast<cudaStream_t>(stream)));
 }
 
-fp4_status fp4_quant_nvfp4(const void* x_bf16, float g, uint8_t* out_packed, uint8_t* out_scale_e4m3, int64_t M,
-                           int64_t K, void* stream)
+fp4_status fp4_quant_nvfp4_ex(const void* x_bf16, float g, uint8_t* out_packed, uint8_t* out_scale_e4m3, int64_t M,
+                              int64_t K, int32_t sf_layout, void* stream)
 {
     if (M < 0 || K <= 0 || K % 16 != 0 || M >= kMaxDim || K >= kMaxDim)
         return FP4_ERR_SHAPE;
+    if (sf_layout != FP4_SF_SWIZZLED && sf_layout != FP4_SF_ROWMAJOR)
+        return FP4_ERR_INVALID_ARG;
     if (M == 0)
         return FP4_OK;
     if (!x_bf16 || !out_packed || !out_scale_e4m3)
@@ -241,13 +253,37 @@ fp4_status fp4_quant_nvfp4(const void* x_bf16, float g, uint8_t* out_packed, uin
     fp4_status st;
     if ((st = current_device(nullptr)) != FP4_OK)
         return st;
-    return from_cuda(
-        fp4lin::launch_quant_nvfp4(x_bf16, g, out_packed, out_scale_e4m3, M, K, static_cast<cudaStream_t>(stream)));
+    return from_cuda(fp4lin::launch_quant_nvfp4(x_bf16, g, out_packed, out_scale_e4m3, M, K,
+                                                sf_layout == FP4_SF_SWIZZLED ? 1 : 0,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status fp4_quant_nvfp4(const void* x_bf16, float g, uint8_t* out_packed, uint8_t* out_scale_e4m3, int64_t M,
+                           int64_t K, void* stream)
+{
+    return fp4_quant_nvfp4_ex(x_bf16, g, out_packed, out_scale_e4m3, M, K, FP4_SF_ROWMAJOR, stream);
+}
+
+fp4_status fp4_sf_swizzle(const uint8_t* in_rowmajor, uint8_t* out, int64_t rows, int64_t kblocks, void* stream)
+{
+    if (rows < 0 || kblocks <= 0 || rows >= kMaxDim || kblocks >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    if (rows == 0)
+        return FP4_OK;
+    if (!in_rowmajor || !out)
+        return FP4_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(out) & 3u)
+        return FP4_ERR_ALIGNMENT;
+    fp4_status st;
+    if ((st = current_device(nullptr)) != FP4_OK)
+        return st;
+    return from_cuda(fp4lin::launch_sf_swizzle(in_rowmajor, out, rows, kblocks, static_cast<cudaStream_t>(stream)));
 }
 
 static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                               const void* bias, void* out, const int32_t* offsets, int32_t E, int64_t M, int64_t N,
-                              int64_t K, void* workspace, size_t workspace_bytes, void* stream)
+                              int64_t K, void* workspace, size_t workspace_bytes, void* stream, bool nvfp4 = false,
+                              float alpha = 1.0f)
 {
     if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 8 != 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
         return FP4_ERR_SHAPE;
@@ -279,6 +315,8 @@ static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t
     args.status = status;
     args.workspace = workspace;
     args.workspace_bytes = workspace ? workspace_bytes : 0;
+    args.nvfp4 = nvfp4;
+    args.alpha = alpha;
     return from_cuda(fp4lin::launch_gemm(args, static_cast<cudaStream_t>(stream)));
 }
 
@@ -302,6 +340,16 @@ fp4_status fp4_gemm_mxfp4_ws(const uint8_t* a, const uint8_t* sa, const uint8_t*
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FP4_ERR_ALIGNMENT;
     return gemm_common(a, sa, b, sb, bias_bf16, out_bf16, nullptr, 1, M, N, K, workspace, workspace_bytes, stream);
+}
+
+fp4_status fp4_gemm_nvfp4(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb, float alpha,
+                          const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
+                          size_t workspace_bytes, void* stream)
+{
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FP4_ERR_ALIGNMENT;
+    return gemm_common(a, sa, b, sb, bias_bf16, out_bf16, nullptr, 1, M, N, K, workspace, workspace_bytes, stream,
+                       true, alpha);
 }
 
 fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,

@@ -44,6 +44,12 @@
 // adds the fp32 partial sums the other S - 1 CTAs left in the workspace, in
 // K order (a fixed reduction order, so results do not vary from run to run),
 // then runs the epilogue.
+// NVFP4 mode (kNv): both operands NVFP4 as "[SGLang] FP4 ..." sections 5-6
+// run them on hardware with native NVFP4: one E4M3 scale per 16 elements
+// (two 512-byte scale chunks per 128 elements of K instead of one, four
+// scales per row per K = 64 step, tcgen05.mma kind::mxf4nvf4 with
+// scale_vec::4X) and a per-tensor alpha applied to the accumulator in the
+// epilogue before the bias.
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the status word and winds down.
 #include <cuda_bf16.h>
@@ -81,19 +87,22 @@ struct GemmParams {
     int n_tiles;
     int ldo;                    // output row stride (elements) = the problem's N
     int64_t sfb_expert_stride;
+    float alpha;                // NVFP4 mode: factor on the accumulator before the bias
     unsigned int* status;
 };
 
-template <int BN, int STAGES, int KC, int CPW, bool kSwap>
+template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kNv>
 struct Cfg {
     static constexpr int FIRST_EPI_WARP = 2 + CPW;
     static constexpr int THREADS = 32 * (FIRST_EPI_WARP + kEpiWarps);
-    static constexpr int GROUPS = 2 * KC;  // 128-element scale groups per stage
+    static constexpr int GROUPS = 2 * KC;  // 128-element groups of K per stage
+    static constexpr int APG = kNv ? 2 : 1;  // 512-byte scale chunks per group and 128-row tile
+    static constexpr int ATOMS = GROUPS * APG;  // scale chunks per stage and 128-row tile
     static constexpr int A_BYTES = BM * kSlabBytes * KC;
     static constexpr int B_BYTES = BN * kSlabBytes * KC;
     static constexpr int SFB_TILES = (BN + 127) / 128;
-    static constexpr int SFA_BYTES = GROUPS * 512;
-    static constexpr int SFB_BYTES = SFB_TILES * GROUPS * 512;
+    static constexpr int SFA_BYTES = ATOMS * 512;
+    static constexpr int SFB_BYTES = SFB_TILES * ATOMS * 512;
     static constexpr int EPI_WARP_BYTES = kSwap ? 32 * (BN / 2) * 2 : kChunk * kChunk * 2;
     static constexpr int EPI_BYTES = kEpiWarps * EPI_WARP_BYTES;
     static constexpr int OFF_A = 0;
@@ -106,9 +115,9 @@ struct Cfg {
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_PREFIX = OFF_TMEM_SLOT + 16;
     static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;  // + 1 KB alignment slack
-    static constexpr int SF_COLS_A = 4 * GROUPS;
-    static constexpr int SF_COLS_B_GROUP = 4 * SFB_TILES;
-    static constexpr int SF_COLS = SF_COLS_A + GROUPS * SF_COLS_B_GROUP;
+    static constexpr int SF_COLS_A = 4 * ATOMS;
+    static constexpr int SF_COLS_B_ATOM = 4 * SFB_TILES;
+    static constexpr int SF_COLS = SF_COLS_A + ATOMS * SF_COLS_B_ATOM;
     static constexpr int TMEM_USED = BN + STAGES * SF_COLS;  // one scale buffer per smem stage
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                      : TMEM_USED <= 256 ? 256 : 512;
@@ -261,12 +270,12 @@ __device__ __forceinline__ void load_operand(void* dst, const CUtensorMap* map, 
         tma_load_3d(dst, map, bar, 0, static_cast<int32_t>(row0), kb * KC);
 }
 
-template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped>
-__global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
-    gemm_mxfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const __grid_constant__ CUtensorMap tmO, const GemmParams p)
+template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped, bool kNv>
+__global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kNv>::THREADS, 1)
+    gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmO, const GemmParams p)
 {
-    using C = Cfg<BN, STAGES, KC, CPW, kSwap>;
+    using C = Cfg<BN, STAGES, KC, CPW, kSwap, kNv>;
     constexpr int kFirstEpiWarp = C::FIRST_EPI_WARP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -355,25 +364,24 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
                         break;
                     }
                     const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
-                    const uint32_t sf_bytes = static_cast<uint32_t>(groups) * 512u;
+                    const uint32_t sf_bytes = static_cast<uint32_t>(groups * C::APG) * 512u;
+                    const int64_t atoms_per_rt = static_cast<int64_t>(p.kb4) * C::APG;  // chunks per 128-row tile
                     // boxes past the end of K or of the rows are zero-filled and still counted
                     mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES + sf_bytes * (1u + nsfb));
                     load_operand<KC>(smem + C::OFF_A + s * C::A_BYTES, &tmA, &full[s], kb, T.a_row0);
                     load_operand<KC>(smem + C::OFF_B + s * C::B_BYTES, &tmB, &full[s], kb, b_row0);
                     bulk_load(smem + C::OFF_SFA + s * C::SFA_BYTES,
-                              p.sfa + (static_cast<int64_t>(T.sfa_rt) * p.kb4 + C::GROUPS * kb) * 512, sf_bytes,
-                              &full[s]);
+                              p.sfa + (T.sfa_rt * atoms_per_rt + C::ATOMS * kb) * 512, sf_bytes, &full[s]);
                     for (int j = 0; j < nsfb; ++j)
-                        bulk_load(smem + C::OFF_SFB + s * C::SFB_BYTES + j * C::GROUPS * 512,
-                                  sfb + (static_cast<int64_t>(T.n0 / 128 + j) * p.kb4 + C::GROUPS * kb) * 512,
-                                  sf_bytes, &full[s]);
+                        bulk_load(smem + C::OFF_SFB + s * C::SFB_BYTES + j * C::ATOMS * 512,
+                                  sfb + ((T.n0 / 128 + j) * atoms_per_rt + C::ATOMS * kb) * 512, sf_bytes, &full[s]);
                 }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // --------------------------------------------------- MMA issuer
-            constexpr uint32_t idesc = idesc_mxf4(BM, BN);
+            constexpr uint32_t idesc = kNv ? idesc_nvf4(BM, BN) : idesc_mxf4(BM, BN);
             uint32_t it = 0, tcount = 0;
             bool ok = true;
             WorkIter wi = work_begin(p, total_tiles);
@@ -403,14 +411,20 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
                     const uint32_t a_s = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
                     const uint32_t b_s = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
                     for (int k = 0; k < 2 * groups; ++k) {
-                        // k-th 64-element step: slab k / 4, 32-byte column k % 4, scale group k / 2
+                        // k-th 64-element step: slab k / 4, 32-byte column k % 4, scale chunk k / 2
+                        // (MXFP4: bytes 2 (k % 2), +1 of it) or k (NVFP4: all four bytes)
                         const int slab = k >> 2;
-                        const int g = k >> 1;
-                        const uint32_t sf_id = static_cast<uint32_t>(k & 1) * 2u;
-                        tc_mma_mxf4(tmem_base, smem_desc(a_s + slab * (BM * kSlabBytes) + 32 * (k & 3), 16, 1024, 2),
-                                    smem_desc(b_s + slab * (BN * kSlabBytes) + 32 * (k & 3), 16, 1024, 2),
-                                    idesc_with_sf_id(idesc, sf_id), sfa_t + 4 * g, sfb_t + g * C::SF_COLS_B_GROUP,
-                                    (kb != w.kb0 || k != 0) ? 1u : 0u);
+                        const uint64_t ad = smem_desc(a_s + slab * (BM * kSlabBytes) + 32 * (k & 3), 16, 1024, 2);
+                        const uint64_t bd = smem_desc(b_s + slab * (BN * kSlabBytes) + 32 * (k & 3), 16, 1024, 2);
+                        const uint32_t acc = (kb != w.kb0 || k != 0) ? 1u : 0u;
+                        if constexpr (kNv) {
+                            tc_mma_nvf4(tmem_base, ad, bd, idesc, sfa_t + 4 * k, sfb_t + k * C::SF_COLS_B_ATOM, acc);
+                        } else {
+                            const int g = k >> 1;
+                            const uint32_t sf_id = static_cast<uint32_t>(k & 1) * 2u;
+                            tc_mma_mxf4(tmem_base, ad, bd, idesc_with_sf_id(idesc, sf_id), sfa_t + 4 * g,
+                                        sfb_t + g * C::SF_COLS_B_ATOM, acc);
+                        }
                     }
                     tc_commit(&empty[s]);
                 }
@@ -422,8 +436,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
         if (lane == 0) {
             // ------------------------------------------------ scale movers
             // Copy q of a stage (q = g * (1 + SFB_TILES) + i: i = 0 the
-            // MMA-M operand's chunk of group g, i = 1 + j the MMA-N
-            // operand's row tile j) belongs to warp 2 + q % CPW.
+            // MMA-M operand's scale chunk g, i = 1 + j the MMA-N operand's
+            // chunk g of row tile j) belongs to warp 2 + q % CPW.
             const int me = warp - 2;
             uint32_t it = 0;
             bool ok = true;
@@ -441,22 +455,22 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
+                    const int atoms = min(C::GROUPS, p.kb4 - C::GROUPS * kb) * C::APG;
                     const uint32_t sfa_t = tmem_base + BN + s * C::SF_COLS;
                     const uint32_t sfb_t = sfa_t + C::SF_COLS_A;
                     const uint32_t sfa_s = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
                     const uint32_t sfb_s = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
 #pragma unroll
-                    for (int q = me; q < C::GROUPS * (1 + C::SFB_TILES); q += CPW) {
+                    for (int q = me; q < C::ATOMS * (1 + C::SFB_TILES); q += CPW) {
                         const int g = q / (1 + C::SFB_TILES);
                         const int i = q % (1 + C::SFB_TILES);
-                        if (g >= groups)
+                        if (g >= atoms)
                             break;
                         if (i == 0)
                             tc_cp_32x128b_warpx4(sfa_t + 4 * g, smem_desc(sfa_s + 512 * g, 0, 128, 0));
                         else
-                            tc_cp_32x128b_warpx4(sfb_t + g * C::SF_COLS_B_GROUP + 4 * (i - 1),
-                                                 smem_desc(sfb_s + (i - 1) * C::GROUPS * 512 + 512 * g, 0, 128, 0));
+                            tc_cp_32x128b_warpx4(sfb_t + g * C::SF_COLS_B_ATOM + 4 * (i - 1),
+                                                 smem_desc(sfb_s + (i - 1) * C::ATOMS * 512 + 512 * g, 0, 128, 0));
                     }
                     tc_commit(&sf_full[s]);  // arrives once this thread's copies have landed
                 }
@@ -558,8 +572,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
                 const float bn = (bias && r < T.rows_valid) ? __bfloat162float(bias[n]) : 0.0f;
                 __nv_bfloat16* srow = reinterpret_cast<__nv_bfloat16*>(stg) + lane;
 #pragma unroll
-                for (int j = 0; j < CW; ++j)
-                    srow[j * 32] = __float2bfloat16_rn(__uint_as_float(v[j]) + bn);
+                for (int j = 0; j < CW; ++j) {
+                    float x = __uint_as_float(v[j]);
+                    if constexpr (kNv)
+                        x *= p.alpha;
+                    srow[j * 32] = __float2bfloat16_rn(x + bn);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -590,8 +608,11 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap>::THREADS, 1)
                     for (int j = 0; j < kChunk; j += 8) {
                         float f[8];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
+                        for (int i = 0; i < 8; ++i) {
                             f[i] = __uint_as_float(v[c + j + i]);
+                            if constexpr (kNv)
+                                f[i] *= p.alpha;
+                        }
                         if (bias && col0 + j < p.ldo) {
                             const uint4 bb = *reinterpret_cast<const uint4*>(bias + col0 + j);
                             const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
@@ -742,10 +763,10 @@ void swap_config(int64_t M, int64_t K, int* bn, int* kc)
     *bn = (*kc == 2 && M <= 32) ? 32 : 64;
 }
 
-template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped>
+template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped, bool kNv = false>
 cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
 {
-    using C = Cfg<BN, STAGES, KC, CPW, kSwap>;
+    using C = Cfg<BN, STAGES, KC, CPW, kSwap, kNv>;
     // MMA-M operand / MMA-N operand
     const uint8_t* opA = kSwap ? a.b : a.a;
     const uint8_t* opB = kSwap ? a.a : a.b;
@@ -777,7 +798,8 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
                          : static_cast<int>((rows_a + 127) / 128);
     p.n_tiles = static_cast<int>((rows_b + BN - 1) / BN);
     p.ldo = static_cast<int>(a.N);
-    p.sfb_expert_stride = ((a.N + 127) / 128) * 128 * (a.K / 32);
+    p.sfb_expert_stride = ((a.N + 127) / 128) * 128 * (a.K / (kNv ? 16 : 32));
+    p.alpha = a.alpha;
     p.status = a.status;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (tiles == 0)
@@ -797,7 +819,7 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
         }
     }
     const size_t smem = C::SMEM_FIXED + (kGrouped ? sizeof(int32_t) * (a.E + 1) : 0);
-    auto kern = gemm_mxfp4_kernel<BN, STAGES, KC, CPW, kSwap, kGrouped>;
+    auto kern = gemm_fp4_kernel<BN, STAGES, KC, CPW, kSwap, kGrouped, kNv>;
     // The shared-memory opt-in is a per-device function attribute: set it
     // once per device (and grow it if a larger grouped prefix needs more).
     static std::mutex mu;
@@ -830,8 +852,27 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K)
     return split_plan((N + BM - 1) / BM, nkb, bn, sm_count()).bytes;
 }
 
+// NVFP4 operands (dense only): the tile shapes of the MXFP4 path with one
+// stage fewer where the doubled scale chunks would overflow shared memory.
+cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t stream)
+{
+    const bool k256 = a.K % 256 == 0;
+    if (a.M <= 64) {
+        if (!k256)
+            return launch_kernel<64, 7, 1, 4, true, false, true>(a, stream);
+        return a.M <= 32 ? launch_kernel<32, 4, 2, 4, true, false, true>(a, stream)
+                         : launch_kernel<64, 3, 2, 4, true, false, true>(a, stream);
+    }
+    const bool wide = a.N >= 256 && ((a.M + 127) / 128) * ((a.N + 255) / 256) >= 148;
+    if (wide)
+        return launch_kernel<256, 3, 1, 2, false, false, true>(a, stream);
+    return launch_kernel<128, 5, 1, 4, false, false, true>(a, stream);
+}
+
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream)
 {
+    if (a.nvfp4)
+        return launch_gemm_nvfp4(a, stream);
     // Stages of two slabs need the 3-D operand view, which needs
     // K % 256 == 0; otherwise the one-slab configurations run.
     const bool k256 = a.K % 256 == 0;

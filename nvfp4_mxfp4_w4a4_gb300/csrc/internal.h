@@ -58,7 +58,10 @@ cudaError_t launch_act_quant_grouped(const void* x, const int32_t* offsets, int 
                                      int64_t K, uint8_t* op, uint8_t* osf, int alg, cudaStream_t stream);
 
 cudaError_t launch_quant_nvfp4(const void* x, float g, uint8_t* op, uint8_t* osf, int64_t M, int64_t K,
-                               cudaStream_t stream);
+                               int swizzled, cudaStream_t stream);
+
+// Row-major [rows][kb] scale bytes -> swizzled layout (any block size).
+cudaError_t launch_sf_swizzle(const uint8_t* in, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t stream);
 
 // Dense (offsets == nullptr) or grouped GEMM.
 struct GemmArgs {
@@ -76,6 +79,8 @@ struct GemmArgs {
     unsigned int* status;
     void* workspace;             // split-K scratch (nullptr: none)
     size_t workspace_bytes;
+    bool nvfp4 = false;          // NVFP4 operands (E4M3 scales per 16 elements)
+    float alpha = 1.0f;          // NVFP4: factor on the accumulator before the bias
 };
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);

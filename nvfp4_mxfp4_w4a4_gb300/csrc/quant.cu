@@ -587,20 +587,27 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
 
 // ------------------------------------------------------- NVFP4 producer
 // One thread per 8 consecutive bf16 (two threads per 16-element block).
+// Threads walk the blocks of the scale layout: rows_pad x kbp blocks
+// (swizzled: rows padded to 128 and blocks to 4, whose scale bytes are
+// written as 0) or M x kb (row-major).
 __global__ void __launch_bounds__(kThreads) quant_nvfp4_kernel(const uint16_t* __restrict__ x, float g,
                                                                uint8_t* __restrict__ op,
-                                                               uint8_t* __restrict__ osf, int64_t groups,
-                                                               int64_t K)
+                                                               uint8_t* __restrict__ osf, int64_t halves,
+                                                               int64_t M, int64_t K, int kb, int kbp, int swizzled)
 {
     grid_dependency_wait();
     launch_dependents();
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-    // both threads of a block stay active for the shuffle; t / 2 indexes blocks
-    const bool active = t < groups;
+    const int64_t bi = t >> 1;
+    const int64_t row = bi / kbp;
+    const int c = static_cast<int>(bi - row * kbp);
+    // both threads of a block stay active for the shuffle
+    const bool inside = t < halves;
+    const bool real = inside && row < M && c < kb;
+    const int64_t xoff = row * K + static_cast<int64_t>(c) * 16 + (t & 1) * 8;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    const int64_t tt = active ? t : 0;
-    if (active)
-        v = ld_stream_u4(x + tt * 8);
+    if (real)
+        v = ld_stream_u4(x + xoff);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     const uint32_t a = __vmaxu2(__vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
                                 __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
@@ -626,12 +633,41 @@ __global__ void __launch_bounds__(kThreads) quant_nvfp4_kernel(const uint16_t* _
         }
         packed |= code << (4 * j);
     }
-    if (active) {
-        *reinterpret_cast<uint32_t*>(op + tt * 4) = packed;
-        if ((tt & 1) == 0)
-            osf[tt >> 1] = static_cast<uint8_t>(sb);
+    if (real)
+        *reinterpret_cast<uint32_t*>(op + xoff / 2) = packed;
+    if (inside && (t & 1) == 0) {
+        const uint8_t sv = real ? static_cast<uint8_t>(sb) : uint8_t(0);
+        osf[swizzled ? sf_swizzled_offset(row, c, kbp >> 2) : bi] = sv;
     }
-    (void)K;
+}
+
+// ------------------------------------------------------- scale layout
+// Row-major [rows][kb] scale bytes -> the swizzled layout the MMA reads,
+// for either block size.  One thread per 4-byte word of the output: word w
+// of 512-byte chunk (row tile rt, column group cg) holds blocks 4 cg .. +3
+// of row 128 rt + 32 (w % 4) + w / 4 (pad rows and blocks as 0).
+__global__ void __launch_bounds__(kThreads) sf_swizzle_kernel(const uint8_t* __restrict__ in,
+                                                              uint32_t* __restrict__ out, int64_t rows, int64_t kb,
+                                                              int64_t kb4, int64_t words)
+{
+    grid_dependency_wait();
+    launch_dependents();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t wi = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; wi < words; wi += stride) {
+        const int64_t chunk = wi >> 7;
+        const int within = static_cast<int>(wi & 127);
+        const int64_t rt = chunk / kb4;
+        const int64_t c0 = (chunk - rt * kb4) * 4;
+        const int64_t r = rt * 128 + (within & 3) * 32 + (within >> 2);
+        uint32_t v = 0u;
+        if (r < rows) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (c0 + j < kb)
+                    v |= static_cast<uint32_t>(__ldg(in + r * kb + c0 + j)) << (8 * j);
+        }
+        out[wi] = v;
+    }
 }
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -748,14 +784,28 @@ cudaError_t launch_act_quant_grouped(const void* x, const int32_t* offsets, int 
 }
 
 cudaError_t launch_quant_nvfp4(const void* x, float g, uint8_t* op, uint8_t* osf, int64_t M, int64_t K,
-                               cudaStream_t stream)
+                               int swizzled, cudaStream_t stream)
 {
-    const int64_t groups = M * K / 8;
-    const int64_t blocks = ceil_div(groups, kThreads);
+    const int kb = static_cast<int>(K / 16);
+    const int kbp = swizzled ? static_cast<int>(ceil_div(kb, 4) * 4) : kb;
+    const int64_t rows = swizzled ? ceil_div(M, 128) * 128 : M;
+    const int64_t halves = rows * kbp * 2;
+    const int64_t blocks = ceil_div(halves, kThreads);
     if (blocks == 0)
         return cudaSuccess;
     return launch_pdl(quant_nvfp4_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream,
-                      static_cast<const uint16_t*>(x), g, op, osf, groups, K);
+                      static_cast<const uint16_t*>(x), g, op, osf, halves, M, K, kb, kbp, swizzled);
+}
+
+cudaError_t launch_sf_swizzle(const uint8_t* in, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t stream)
+{
+    const int64_t kb4 = ceil_div(kb, 4);
+    const int64_t words = ceil_div(rows, 128) * kb4 * 128;
+    const int64_t blocks = std::min<int64_t>(ceil_div(words, kThreads), resident_ctas(sf_swizzle_kernel));
+    if (blocks == 0)
+        return cudaSuccess;
+    return launch_pdl(sf_swizzle_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, in,
+                      reinterpret_cast<uint32_t*>(out), rows, kb, kb4, words);
 }
 
 }  // namespace fp4lin

@@ -34,6 +34,7 @@ SYMBOLS = (
     "fp4_quant_act_mxfp4",
     "fp4_quant_act_mxfp4_grouped", "fp4_quant_nvfp4", "fp4_gemm_mxfp4", "fp4_gemm_workspace_size",
     "fp4_gemm_mxfp4_ws", "fp4_gemm_mxfp4_noalloc", "fp4_gemm_mxfp4_grouped",
+    "fp4_quant_nvfp4_ex", "fp4_sf_bytes_nvfp4", "fp4_sf_swizzle", "fp4_gemm_nvfp4",
 )
 
 
@@ -79,6 +80,11 @@ def load(path: str = LIB_PATH):
             "fp4_gemm_mxfp4_ws": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, ctypes.c_size_t, _p]),
             "fp4_gemm_mxfp4_noalloc": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p]),
             "fp4_gemm_mxfp4_grouped": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _i32, _i64, _i64, _i64, _p]),
+            "fp4_quant_nvfp4_ex": (ctypes.c_int, [_p, ctypes.c_float, _p, _p, _i64, _i64, _i32, _p]),
+            "fp4_sf_bytes_nvfp4": (ctypes.c_size_t, [_i64, _i64, _i32]),
+            "fp4_sf_swizzle": (ctypes.c_int, [_p, _p, _i64, _i64, _p]),
+            "fp4_gemm_nvfp4": (ctypes.c_int, [_p, _p, _p, _p, ctypes.c_float, _p, _p, _i64, _i64, _i64, _p,
+                                              ctypes.c_size_t, _p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -174,6 +180,30 @@ def fp4_quant_nvfp4(x_bf16, g, out_packed, out_scale_e4m3, M, K, stream=None):
     st = load().fp4_quant_nvfp4(_ptr(x_bf16), float(g), _ptr(out_packed), _ptr(out_scale_e4m3), M, K,
                                 _stream(stream))
     _check(st, "fp4_quant_nvfp4")
+
+
+def fp4_quant_nvfp4_ex(x_bf16, g, out_packed, out_scale_e4m3, M, K, sf_layout=FP4_SF_SWIZZLED, stream=None):
+    st = load().fp4_quant_nvfp4_ex(_ptr(x_bf16), float(g), _ptr(out_packed), _ptr(out_scale_e4m3), M, K, sf_layout,
+                                   _stream(stream))
+    _check(st, "fp4_quant_nvfp4_ex")
+
+
+def fp4_sf_bytes_nvfp4(rows: int, K: int, sf_layout: int = FP4_SF_SWIZZLED) -> int:
+    return load().fp4_sf_bytes_nvfp4(rows, K, sf_layout)
+
+
+def fp4_sf_swizzle(in_rowmajor, out, rows, kblocks, stream=None):
+    st = load().fp4_sf_swizzle(_ptr(in_rowmajor), _ptr(out), rows, kblocks, _stream(stream))
+    _check(st, "fp4_sf_swizzle")
+
+
+def fp4_gemm_nvfp4(a, sa, b, sb, alpha, bias_bf16, out_bf16, M, N, K, workspace=None, workspace_bytes=None,
+                   stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().fp4_gemm_nvfp4(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), float(alpha), _ptr(bias_bf16), _ptr(out_bf16),
+                               M, N, K, _ptr(workspace), workspace_bytes, _stream(stream))
+    _check(st, "fp4_gemm_nvfp4")
 
 
 def fp4_gemm_mxfp4(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, stream=None):

@@ -47,6 +47,11 @@ def test_sf_sizes(L):
     assert L.fp4_sf_bytes(5, 48, L.FP4_SF_SWIZZLED) == 0                   # K not a multiple of 32
     # grouped bound: sum over groups of ceil(rows/128) <= (total + E*127) / 128
     assert L.fp4_sf_bytes_grouped(32768, 64, 4096) == ((32768 + 64 * 127) // 128) * 128 * 128
+    # NVFP4: one E4M3 byte per 16 elements
+    assert L.fp4_sf_bytes_nvfp4(256, 512, L.FP4_SF_ROWMAJOR) == 256 * 32
+    assert L.fp4_sf_bytes_nvfp4(200, 208, L.FP4_SF_SWIZZLED) == 256 * 16   # 13 blocks -> 16
+    assert L.fp4_sf_bytes_nvfp4(1, 16, L.FP4_SF_SWIZZLED) == 128 * 4
+    assert L.fp4_sf_bytes_nvfp4(5, 24, L.FP4_SF_SWIZZLED) == 0             # K not a multiple of 16
 
 
 def test_status_strings(L):
@@ -79,6 +84,17 @@ def test_argument_checks_precede_device_use(L):
 
     bad = fp4_quant_opts(1, 0)
     assert raw.fp4_quant_act_mxfp4(16, 16, 16, 4, 32, ctypes.byref(bad), None) == 1
+    # NVFP4 side path
+    assert raw.fp4_gemm_nvfp4(16, 16, 16, 16, 1.0, None, 16, 1, 8, 192, None, 0, None) == 2     # K % 128
+    assert raw.fp4_gemm_nvfp4(16, None, 16, 16, 1.0, None, 16, 1, 8, 128, None, 0, None) == 1    # no scales
+    assert raw.fp4_gemm_nvfp4(16, 16, 16, 24, 1.0, None, 16, 1, 8, 128, None, 0, None) == 3      # sb 16 B
+    assert raw.fp4_gemm_nvfp4(16, 16, 16, 16, 1.0, None, 16, 1, 8, 128, 16, 1 << 20, None) == 3  # workspace
+    assert raw.fp4_quant_nvfp4_ex(16, 1.0, 16, 16, 4, 24, 0, None) == 2                          # K % 16
+    assert raw.fp4_quant_nvfp4_ex(16, 1.0, 16, 16, 4, 32, 5, None) == 1                          # layout
+    assert raw.fp4_sf_swizzle(16, 16, 4, 0, None) == 2                                           # kblocks
+    assert raw.fp4_sf_swizzle(None, 16, 4, 4, None) == 1
+    assert raw.fp4_sf_swizzle(16, 18, 4, 4, None) == 3                                           # out 4 B
+    assert raw.fp4_sf_swizzle(None, None, 0, 4, None) == 0
     # empty problems are no-ops that need no device
     assert raw.fp4_quant_act_mxfp4(None, None, None, 0, 32, None, None) == 0
     assert raw.fp4_gemm_mxfp4(None, None, None, None, None, None, 0, 8, 128, None) == 0
