@@ -67,7 +67,6 @@ namespace {
 constexpr int BM = 128;
 constexpr int kSlabBytes = 128;  // packed bytes of K per row per slab (256 elements)
 constexpr int kEpiWarps = 8;
-constexpr int kChunk = 32;      // normal-mode store chunk: 32 rows x 32 columns per warp
 
 struct GemmParams {
     int64_t units;              // split-K: total K-stage units (0: one CTA per whole tile)
@@ -93,7 +92,13 @@ struct GemmParams {
 
 template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kNv>
 struct Cfg {
-    static constexpr int FIRST_EPI_WARP = 2 + CPW;
+    // Four scale warps beside a 256-wide epilogue do not fit the register
+    // file at 14 warps: 16 warps then, warps 6-7 idle, and the two non-
+    // epilogue warpgroups hand registers to the epilogue ones (setmaxnreg).
+    static constexpr bool SPLIT = BN == 256 && CPW > 2;
+    static constexpr int REGS_LOW = 80;    // warps 0-7 after the split
+    static constexpr int REGS_HIGH = 176;  // epilogue warps after the split
+    static constexpr int FIRST_EPI_WARP = SPLIT ? 8 : 2 + CPW;
     static constexpr int THREADS = 32 * (FIRST_EPI_WARP + kEpiWarps);
     static constexpr int GROUPS = 2 * KC;  // 128-element groups of K per stage
     static constexpr int APG = kNv ? 2 : 1;  // 512-byte scale chunks per group and 128-row tile
@@ -103,7 +108,10 @@ struct Cfg {
     static constexpr int SFB_TILES = (BN + 127) / 128;
     static constexpr int SFA_BYTES = ATOMS * 512;
     static constexpr int SFB_BYTES = SFB_TILES * ATOMS * 512;
-    static constexpr int EPI_WARP_BYTES = kSwap ? 32 * (BN / 2) * 2 : kChunk * kChunk * 2;
+    // normal-mode store chunk: 32 rows x CHUNK columns per warp (16 where the
+    // NVFP4 scale chunks need the shared memory for a fourth stage)
+    static constexpr int CHUNK = (kNv && BN == 256) ? 16 : 32;
+    static constexpr int EPI_WARP_BYTES = kSwap ? 32 * (BN / 2) * 2 : 32 * CHUNK * 2;
     static constexpr int EPI_BYTES = kEpiWarps * EPI_WARP_BYTES;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -125,7 +133,7 @@ struct Cfg {
     static_assert(OFF_EPI % 1024 == 0, "staging alignment (swizzled store boxes)");
     static_assert(SMEM_FIXED <= 232448, "shared memory budget");
     static constexpr int CW = BN / 2;  // accumulator columns per epilogue warp
-    static_assert(kSwap || CW % kChunk == 0, "normal-mode columns per warp must be whole store chunks");
+    static_assert(kSwap || CW % CHUNK == 0, "normal-mode columns per warp must be whole store chunks");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
@@ -341,142 +349,150 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kNv>::THREADS,
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------- TMA producer
-            uint32_t it = 0;
-            bool ok = true;
-            WorkIter wi = work_begin(p, total_tiles);
-            Work w;
-            while (ok && work_next(wi, nkb, w)) {
-                const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
-                if (!T.valid)
-                    continue;
-                const int64_t b_row0 = static_cast<int64_t>(T.expert) * p.rows_b + T.n0;
-                const uint8_t* sfb = p.sfb + static_cast<int64_t>(T.expert) * p.sfb_expert_stride;
-                int nsfb = (p.rows_b + 127) / 128 - T.n0 / 128;
-                nsfb = nsfb < C::SFB_TILES ? nsfb : C::SFB_TILES;
-                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-                    const int s = static_cast<int>(it % STAGES);
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kStatusTimeout, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
-                    const uint32_t sf_bytes = static_cast<uint32_t>(groups * C::APG) * 512u;
-                    const int64_t atoms_per_rt = static_cast<int64_t>(p.kb4) * C::APG;  // chunks per 128-row tile
-                    // boxes past the end of K or of the rows are zero-filled and still counted
-                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES + sf_bytes * (1u + nsfb));
-                    load_operand<KC>(smem + C::OFF_A + s * C::A_BYTES, &tmA, &full[s], kb, T.a_row0);
-                    load_operand<KC>(smem + C::OFF_B + s * C::B_BYTES, &tmB, &full[s], kb, b_row0);
-                    bulk_load(smem + C::OFF_SFA + s * C::SFA_BYTES,
-                              p.sfa + (T.sfa_rt * atoms_per_rt + C::ATOMS * kb) * 512, sf_bytes, &full[s]);
-                    for (int j = 0; j < nsfb; ++j)
-                        bulk_load(smem + C::OFF_SFB + s * C::SFB_BYTES + j * C::ATOMS * 512,
-                                  sfb + ((T.n0 / 128 + j) * atoms_per_rt + C::ATOMS * kb) * 512, sf_bytes, &full[s]);
-                }
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // --------------------------------------------------- MMA issuer
-            constexpr uint32_t idesc = kNv ? idesc_nvf4(BM, BN) : idesc_mxf4(BM, BN);
-            uint32_t it = 0, tcount = 0;
-            bool ok = true;
-            WorkIter wi = work_begin(p, total_tiles);
-            Work w;
-            while (ok && work_next(wi, nkb, w)) {
-                const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
-                if (!T.valid)
-                    continue;
-                // the epilogue must have drained the accumulator of the previous tile
-                if (!mbar_wait_bounded(accum_empty, (tcount & 1u) ^ 1u, p.status, kStatusTimeout, kWaitLimitNs)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-                    const int s = static_cast<int>(it % STAGES);
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, kWaitLimitNs) ||
-                        !mbar_wait_bounded(&sf_full[s], ph, p.status, kStatusTimeout, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
-                    const uint32_t sfa_t = tmem_base + BN + s * C::SF_COLS;
-                    const uint32_t sfb_t = sfa_t + C::SF_COLS_A;
-                    const uint32_t a_s = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
-                    const uint32_t b_s = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
-                    for (int k = 0; k < 2 * groups; ++k) {
-                        // k-th 64-element step: slab k / 4, 32-byte column k % 4, scale chunk k / 2
-                        // (MXFP4: bytes 2 (k % 2), +1 of it) or k (NVFP4: all four bytes)
-                        const int slab = k >> 2;
-                        const uint64_t ad = smem_desc(a_s + slab * (BM * kSlabBytes) + 32 * (k & 3), 16, 1024, 2);
-                        const uint64_t bd = smem_desc(b_s + slab * (BN * kSlabBytes) + 32 * (k & 3), 16, 1024, 2);
-                        const uint32_t acc = (kb != w.kb0 || k != 0) ? 1u : 0u;
-                        if constexpr (kNv) {
-                            tc_mma_nvf4(tmem_base, ad, bd, idesc, sfa_t + 4 * k, sfb_t + k * C::SF_COLS_B_ATOM, acc);
-                        } else {
-                            const int g = k >> 1;
-                            const uint32_t sf_id = static_cast<uint32_t>(k & 1) * 2u;
-                            tc_mma_mxf4(tmem_base, ad, bd, idesc_with_sf_id(idesc, sf_id), sfa_t + 4 * g,
-                                        sfb_t + g * C::SF_COLS_B_ATOM, acc);
-                        }
-                    }
-                    tc_commit(&empty[s]);
-                }
-                tc_commit(accum_full);  // also on the abort path: the epilogue never waits on missing MMAs
-                ++tcount;
-            }
-        }
-    } else if (warp < kFirstEpiWarp) {
-        if (lane == 0) {
-            // ------------------------------------------------ scale movers
-            // Copy q of a stage (q = g * (1 + SFB_TILES) + i: i = 0 the
-            // MMA-M operand's scale chunk g, i = 1 + j the MMA-N operand's
-            // chunk g of row tile j) belongs to warp 2 + q % CPW.
-            const int me = warp - 2;
-            uint32_t it = 0;
-            bool ok = true;
-            WorkIter wi = work_begin(p, total_tiles);
-            Work w;
-            while (ok && work_next(wi, nkb, w)) {
-                const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
-                if (!T.valid)
-                    continue;
-                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-                    const int s = static_cast<int>(it % STAGES);
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const int atoms = min(C::GROUPS, p.kb4 - C::GROUPS * kb) * C::APG;
-                    const uint32_t sfa_t = tmem_base + BN + s * C::SF_COLS;
-                    const uint32_t sfb_t = sfa_t + C::SF_COLS_A;
-                    const uint32_t sfa_s = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
-                    const uint32_t sfb_s = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
-#pragma unroll
-                    for (int q = me; q < C::ATOMS * (1 + C::SFB_TILES); q += CPW) {
-                        const int g = q / (1 + C::SFB_TILES);
-                        const int i = q % (1 + C::SFB_TILES);
-                        if (g >= atoms)
+    // Each role sits inside its register branch: with the register split
+    // (SPLIT) ptxas then sizes each branch for its own budget.
+    if (warp < kFirstEpiWarp) {
+        if constexpr (C::SPLIT)
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REGS_LOW));
+        if (warp == 0) {
+            if (lane == 0) {
+                // ------------------------------------------------- TMA producer
+                uint32_t it = 0;
+                bool ok = true;
+                WorkIter wi = work_begin(p, total_tiles);
+                Work w;
+                while (ok && work_next(wi, nkb, w)) {
+                    const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
+                    if (!T.valid)
+                        continue;
+                    const int64_t b_row0 = static_cast<int64_t>(T.expert) * p.rows_b + T.n0;
+                    const uint8_t* sfb = p.sfb + static_cast<int64_t>(T.expert) * p.sfb_expert_stride;
+                    int nsfb = (p.rows_b + 127) / 128 - T.n0 / 128;
+                    nsfb = nsfb < C::SFB_TILES ? nsfb : C::SFB_TILES;
+                    for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+                        const int s = static_cast<int>(it % STAGES);
+                        const uint32_t ph = (it / STAGES) & 1u;
+                        if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kStatusTimeout, kWaitLimitNs)) {
+                            ok = false;
                             break;
-                        if (i == 0)
-                            tc_cp_32x128b_warpx4(sfa_t + 4 * g, smem_desc(sfa_s + 512 * g, 0, 128, 0));
-                        else
-                            tc_cp_32x128b_warpx4(sfb_t + g * C::SF_COLS_B_ATOM + 4 * (i - 1),
-                                                 smem_desc(sfb_s + (i - 1) * C::ATOMS * 512 + 512 * g, 0, 128, 0));
+                        }
+                        const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
+                        const uint32_t sf_bytes = static_cast<uint32_t>(groups * C::APG) * 512u;
+                        const int64_t atoms_per_rt = static_cast<int64_t>(p.kb4) * C::APG;  // chunks per 128-row tile
+                        // boxes past the end of K or of the rows are zero-filled and still counted
+                        mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES + sf_bytes * (1u + nsfb));
+                        load_operand<KC>(smem + C::OFF_A + s * C::A_BYTES, &tmA, &full[s], kb, T.a_row0);
+                        load_operand<KC>(smem + C::OFF_B + s * C::B_BYTES, &tmB, &full[s], kb, b_row0);
+                        bulk_load(smem + C::OFF_SFA + s * C::SFA_BYTES,
+                                  p.sfa + (T.sfa_rt * atoms_per_rt + C::ATOMS * kb) * 512, sf_bytes, &full[s]);
+                        for (int j = 0; j < nsfb; ++j)
+                            bulk_load(smem + C::OFF_SFB + s * C::SFB_BYTES + j * C::ATOMS * 512,
+                                      sfb + ((T.n0 / 128 + j) * atoms_per_rt + C::ATOMS * kb) * 512, sf_bytes, &full[s]);
                     }
-                    tc_commit(&sf_full[s]);  // arrives once this thread's copies have landed
+                }
+            }
+        } else if (warp == 1) {
+            if (lane == 0) {
+                // --------------------------------------------------- MMA issuer
+                constexpr uint32_t idesc = kNv ? idesc_nvf4(BM, BN) : idesc_mxf4(BM, BN);
+                uint32_t it = 0, tcount = 0;
+                bool ok = true;
+                WorkIter wi = work_begin(p, total_tiles);
+                Work w;
+                while (ok && work_next(wi, nkb, w)) {
+                    const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
+                    if (!T.valid)
+                        continue;
+                    // the epilogue must have drained the accumulator of the previous tile
+                    if (!mbar_wait_bounded(accum_empty, (tcount & 1u) ^ 1u, p.status, kStatusTimeout, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+                        const int s = static_cast<int>(it % STAGES);
+                        const uint32_t ph = (it / STAGES) & 1u;
+                        if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, kWaitLimitNs) ||
+                            !mbar_wait_bounded(&sf_full[s], ph, p.status, kStatusTimeout, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
+                        const uint32_t sfa_t = tmem_base + BN + s * C::SF_COLS;
+                        const uint32_t sfb_t = sfa_t + C::SF_COLS_A;
+                        const uint32_t a_s = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
+                        const uint32_t b_s = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
+                        for (int k = 0; k < 2 * groups; ++k) {
+                            // k-th 64-element step: slab k / 4, 32-byte column k % 4, scale chunk k / 2
+                            // (MXFP4: bytes 2 (k % 2), +1 of it) or k (NVFP4: all four bytes)
+                            const int slab = k >> 2;
+                            const uint64_t ad = smem_desc(a_s + slab * (BM * kSlabBytes) + 32 * (k & 3), 16, 1024, 2);
+                            const uint64_t bd = smem_desc(b_s + slab * (BN * kSlabBytes) + 32 * (k & 3), 16, 1024, 2);
+                            const uint32_t acc = (kb != w.kb0 || k != 0) ? 1u : 0u;
+                            if constexpr (kNv) {
+                                tc_mma_nvf4(tmem_base, ad, bd, idesc, sfa_t + 4 * k, sfb_t + k * C::SF_COLS_B_ATOM, acc);
+                            } else {
+                                const int g = k >> 1;
+                                const uint32_t sf_id = static_cast<uint32_t>(k & 1) * 2u;
+                                tc_mma_mxf4(tmem_base, ad, bd, idesc_with_sf_id(idesc, sf_id), sfa_t + 4 * g,
+                                            sfb_t + g * C::SF_COLS_B_ATOM, acc);
+                            }
+                        }
+                        tc_commit(&empty[s]);
+                    }
+                    tc_commit(accum_full);  // also on the abort path: the epilogue never waits on missing MMAs
+                    ++tcount;
+                }
+            }
+        } else if (warp < 2 + CPW) {
+            if (lane == 0) {
+                // ------------------------------------------------ scale movers
+                // Copy q of a stage (q = g * (1 + SFB_TILES) + i: i = 0 the
+                // MMA-M operand's scale chunk g, i = 1 + j the MMA-N operand's
+                // chunk g of row tile j) belongs to warp 2 + q % CPW.
+                const int me = warp - 2;
+                uint32_t it = 0;
+                bool ok = true;
+                WorkIter wi = work_begin(p, total_tiles);
+                Work w;
+                while (ok && work_next(wi, nkb, w)) {
+                    const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
+                    if (!T.valid)
+                        continue;
+                    for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+                        const int s = static_cast<int>(it % STAGES);
+                        const uint32_t ph = (it / STAGES) & 1u;
+                        if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const int atoms = min(C::GROUPS, p.kb4 - C::GROUPS * kb) * C::APG;
+                        const uint32_t sfa_t = tmem_base + BN + s * C::SF_COLS;
+                        const uint32_t sfb_t = sfa_t + C::SF_COLS_A;
+                        const uint32_t sfa_s = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
+                        const uint32_t sfb_s = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
+    #pragma unroll
+                        for (int q = me; q < C::ATOMS * (1 + C::SFB_TILES); q += CPW) {
+                            const int g = q / (1 + C::SFB_TILES);
+                            const int i = q % (1 + C::SFB_TILES);
+                            if (g >= atoms)
+                                break;
+                            if (i == 0)
+                                tc_cp_32x128b_warpx4(sfa_t + 4 * g, smem_desc(sfa_s + 512 * g, 0, 128, 0));
+                            else
+                                tc_cp_32x128b_warpx4(sfb_t + g * C::SF_COLS_B_ATOM + 4 * (i - 1),
+                                                     smem_desc(sfb_s + (i - 1) * C::ATOMS * 512 + 512 * g, 0, 128, 0));
+                        }
+                        tc_commit(&sf_full[s]);  // arrives once this thread's copies have landed
+                    }
                 }
             }
         }
     } else {
+        if constexpr (C::SPLIT)
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REGS_HIGH));
         // ------------------------------------------------------ epilogue
         const int ew = warp - kFirstEpiWarp;
         const int quad = warp & 3;  // TMEM lanes 32 * quad ... (a warp reaches only its own quarter)
@@ -587,12 +603,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kNv>::THREADS,
                 }
             } else {
                 // lane = output row; this warp's columns n0 + half*CW + [0, CW)
-                // go out in 32 x 32 chunks through its staging area, in the
-                // 64-byte swizzled layout of the output map (16-byte piece q of
-                // row i sits at piece position q ^ ((i / 2) % 4)), which keeps
-                // the rows of one store phase on different banks.
+                // go out in 32 x CHUNK chunks through its staging area, in the
+                // swizzled layout of the output map (64-byte rows: 16-byte
+                // piece q of row i sits at piece position q ^ ((i / 2) % 4);
+                // 32-byte rows: q ^ ((i / 4) % 2)), which keeps the rows of
+                // one store phase on different banks.
+                constexpr int kChunk = C::CHUNK;
                 uint8_t* my_row = stg + lane * (kChunk * 2);
-                const int rot = (lane >> 1) & 3;
+                const int rot = kChunk == 32 ? (lane >> 1) & 3 : (lane >> 2) & 1;
                 // rows past the end of this expert belong to the next one:
                 // there a chunk is stored row by row instead
                 const bool whole = !kGrouped || quad * 32 + 31 < T.rows_valid;
@@ -778,7 +796,8 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
     if (!make_operand_map(&tmB, opB, static_cast<int64_t>(a.E) * rows_b, a.K, BN, KC))
         return cudaErrorInvalidValue;
     if (!(kSwap ? make_output_map(&tmO, a.out, a.M, a.N, 32, BN / 2, CU_TENSOR_MAP_SWIZZLE_NONE)
-                : make_output_map(&tmO, a.out, a.M, a.N, kChunk, kChunk, CU_TENSOR_MAP_SWIZZLE_64B)))
+                : make_output_map(&tmO, a.out, a.M, a.N, C::CHUNK, 32,
+                                  C::CHUNK == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B)))
         return cudaErrorInvalidValue;
     GemmParams p;
     p.units = 0;
@@ -836,6 +855,23 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
                 return err;
             configured[dev] = smem;
         }
+        if constexpr (C::SPLIT) {
+            // setmaxnreg.inc waits until the registers it asks for are free:
+            // never launch a split that the launch's allocation cannot cover
+            static int split_ok[64] = {};
+            if (split_ok[dev] == 0) {
+                cudaFuncAttributes fa;
+                err = cudaFuncGetAttributes(&fa, kern);
+                if (err != cudaSuccess)
+                    return err;
+                split_ok[dev] = static_cast<int64_t>(fa.numRegs) * C::THREADS >=
+                                        static_cast<int64_t>(C::THREADS / 2) * (C::REGS_LOW + C::REGS_HIGH)
+                                    ? 1
+                                    : -1;
+            }
+            if (split_ok[dev] < 0)
+                return cudaErrorInvalidConfiguration;
+        }
     }
     return launch_pdl(kern, dim3(grid), dim3(C::THREADS), smem, stream, tmA, tmB, tmO, p);
 }
@@ -864,8 +900,12 @@ cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t stream)
                          : launch_kernel<64, 3, 2, 4, true, false, true>(a, stream);
     }
     const bool wide = a.N >= 256 && ((a.M + 127) / 128) * ((a.N + 255) / 256) >= 148;
-    if (wide)
-        return launch_kernel<256, 3, 1, 2, false, false, true>(a, stream);
+    if (wide) {
+        // twelve scale copies per stage: four scale warps (register split),
+        // or two where the split cannot be launched
+        const cudaError_t e = launch_kernel<256, 4, 1, 4, false, false, true>(a, stream);
+        return e == cudaErrorInvalidConfiguration ? launch_kernel<256, 4, 1, 2, false, false, true>(a, stream) : e;
+    }
     return launch_kernel<128, 5, 1, 4, false, false, true>(a, stream);
 }
 
