@@ -333,14 +333,18 @@ void orc_gemm_nvfp4(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const
  * time, in this order:
  *   d6 = 6 * g;  t = bamax / d6;  s = E4M3(t);  den = value(s) * g;
  *   q = x / den;  code = E2M1(q).
- * A zero or NaN den gives signed-zero codes.                              */
+ * A zero or NaN den gives signed-zero codes.  Both maxima propagate NaN
+ * (as the MX block amax does): a NaN element makes its block's scale NaN
+ * (byte 0x7F) and the tensor's global scale NaN.                          */
 float orc_nvfp4_global_scale(const uint16_t* x_bf16, int64_t n)
 {
     double amax = 0.0;
     for (int64_t i = 0; i < n; ++i) {
         double a = fabs(orc_bf16_value(x_bf16[i]));
-        if (a > amax)
+        if (a > amax || isnan(a))
             amax = a;
+        if (isnan(amax))
+            break;
     }
     float six_e4m3max = 6.0f * 448.0f;
     return (float)amax / six_e4m3max;
@@ -355,8 +359,10 @@ void orc_nvfp4_quantize(const uint16_t* x_bf16, float g, int64_t row0, int64_t r
             float bamax = 0.0f;
             for (int i = 0; i < 16; ++i) {
                 float a = (float)fabs(orc_bf16_value(x[i]));
-                if (a > bamax)
+                if (a > bamax || isnan(a))
                     bamax = a;
+                if (isnan(bamax))
+                    break;
             }
             float d6 = 6.0f * g;
             float t = bamax / d6;

@@ -428,6 +428,30 @@ def test_sf_swizzle_is_injective_and_pads_zero(orc):
 # ------------------------------------------------------ NVFP4 producer
 
 
+def test_nvfp4_quantize_nan_propagates(orc):
+    """A NaN element makes its block's scale NaN (0x7F) and the block's codes
+    signed zeros (the zero-or-NaN denominator rule); other blocks are
+    untouched; the global scale of a tensor holding a NaN is NaN."""
+    rng = np.random.default_rng(41)
+    x = torch.from_numpy(rng.standard_normal((2, 64)).astype(np.float32)).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16).copy()
+    g = orc.nvfp4_global_scale(bits)
+    p0, s0 = orc.nvfp4_quantize(bits, g)
+    bits[1, 37] = 0x7FC0                      # NaN in block 2 of row 1
+    assert math.isnan(orc.nvfp4_global_scale(bits))
+    p1, s1 = orc.nvfp4_quantize(bits, g)
+    assert s1[1, 2] == 0x7F
+    codes = _unpack(p1)[1, 32:48]
+    signs = (bits[1, 32:48] >> 15).astype(np.uint8) << 3
+    assert np.array_equal(codes, signs)
+    mask = np.ones_like(s0, bool)
+    mask[1, 2] = False
+    assert np.array_equal(s1[mask], s0[mask])
+    keep = np.ones((2, 64), bool)
+    keep[1, 32:48] = False
+    assert np.array_equal(_unpack(p1)[keep], _unpack(p0)[keep])
+
+
 def test_nvfp4_quantize_against_float32_recipe(orc):
     """Block scale = torch's E4M3 rounding of fp32(bamax / fp32(6 g)); codes
     are nearest E2M1 values of fp32(x / fp32(scale * g)); dequantization error
