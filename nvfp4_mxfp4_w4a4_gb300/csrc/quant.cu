@@ -620,18 +620,22 @@ __global__ void __launch_bounds__(kThreads) quant_nvfp4_kernel(const uint16_t* _
     const float den = __fmul_rn(e4m3x2_to_float2(sb).x, g);
     const bool zero_codes = (den == 0.0f) || (den != den);
     uint32_t packed = 0u;
+    if (zero_codes) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t bits = (j & 1) ? (w[j >> 1] & 0xFFFF0000u) : (w[j >> 1] << 16);
-        const float xv = __uint_as_float(bits);
-        uint32_t code;
-        if (zero_codes) {
-            code = (bits >> 28) & 0x8u;
-        } else {
-            const float qv = __fdiv_rn(xv, den);
-            code = e2m1_code(fabsf(qv)) | ((__float_as_uint(qv) >> 28) & 0x8u);
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t bits = (j & 1) ? (w[j >> 1] & 0xFFFF0000u) : (w[j >> 1] << 16);
+            packed |= ((bits >> 28) & 0x8u) << (4 * j);
         }
-        packed |= code << (4 * j);
+    } else {
+        // code = E2M1 nearest (ties to even, saturating, sign kept) of the
+        // correctly rounded quotient
+        float q[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t bits = (j & 1) ? (w[j >> 1] & 0xFFFF0000u) : (w[j >> 1] << 16);
+            q[j] = __fdiv_rn(__uint_as_float(bits), den);
+        }
+        packed = e2m1x8_pack(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
     }
     if (real)
         *reinterpret_cast<uint32_t*>(op + xoff / 2) = packed;

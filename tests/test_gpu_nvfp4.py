@@ -47,6 +47,34 @@ def test_quant_nvfp4_ex_matches_oracle(orc, L, M, K, layout):
     assert np.array_equal(host(osf)[: len(s_expect)], s_expect)
 
 
+@pytest.mark.parametrize("g", [None, 0.0, 1e-30, 3e30, -0.25])
+def test_quant_nvfp4_special_values(orc, L, g):
+    """Blocks of zeros and -0, infinities, NaN, bf16 subnormals, values near
+    the bf16 maximum and ordinary data, under several global scales
+    (including 0 and a negative one): byte-exact against the oracle."""
+    M, K = 6, 128
+    X = synth.bf16_normal(5, synth.S_ACT, (M, K), 1.0)
+    X[0, :16] = 0x0000
+    X[0, 16:32] = 0x8000                       # -0
+    X[1, 3] = 0x7F80                           # +inf
+    X[1, 20] = 0xFF80                          # -inf
+    X[2, 40] = 0x7FC0                          # NaN
+    X[3, :16] = np.arange(1, 17, dtype=np.uint16)          # positive subnormals
+    X[3, 16:32] = 0x8000 | np.arange(1, 17, dtype=np.uint16)
+    X[4, :16] = 0x7F7F                         # bf16 max
+    X[4, 16:32] = 0xFF00 | np.arange(0x60, 0x70, dtype=np.uint16)
+    gv = orc.nvfp4_global_scale(X) if g is None else g
+    p_ref, s_ref = orc.nvfp4_quantize(X, gv, threads=1)
+    for layout in (0, 1):
+        s_expect = orc.sf_swizzle(s_ref) if layout == 0 else s_ref.reshape(-1)
+        op = empty_u8(M * K // 2)
+        osf = empty_u8(len(s_expect))
+        L.fp4_quant_nvfp4_ex(dev_bf16(X), gv, op, osf, M, K, layout)
+        assert L.fp4_get_device_status() == 0
+        assert np.array_equal(host(op)[: M * K // 2].reshape(M, K // 2), p_ref)
+        assert np.array_equal(host(osf)[: len(s_expect)], s_expect)
+
+
 # ---------------------------------------------------------------- GEMM
 def _nv_operand(orc, x_bits):
     """bf16 -> NVFP4 by the oracle: (packed, row-major E4M3, swizzled E4M3, g)."""
