@@ -65,6 +65,9 @@ def lib():
                 ("orc_requant", None, [_p, _p, ctypes.c_float, _i64, _i64, _i64, ctypes.c_int, _p, _p]),
                 ("orc_act_quant", None, [_p, _i64, _i64, _i64, ctypes.c_int, _p, _p]),
                 ("orc_gemm", None, [_p, _p, _p, _p, _p, _i64, _p, _i64, _p, _i64, _p, _p]),
+                ("orc_mx8_shared_exp", ctypes.c_int, [ctypes.c_double]),
+                ("orc_act_quant_mxfp8", None, [_p, _i64, _i64, _i64, _p, _p]),
+                ("orc_gemm_w4a8", None, [_p, _p, _p, _p, _p, _i64, _p, _i64, _p, _i64, _p, _p]),
                 ("orc_gemm_nvfp4", None,
                  [_p, _p, _p, _p, ctypes.c_double, _p, _i64, _p, _i64, _p, _i64, _p, _p]),
                 ("orc_nvfp4_global_scale", ctypes.c_float, [_p, _i64]),
@@ -201,6 +204,53 @@ def gemm(a, sa, b, sb, bias_bf16_bits=None, rows=None, cols=None, threads=1):
         s = np.empty_like(r)
         L.orc_gemm(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias), K, _ptr(sub_rows), r1 - r0,
                    _ptr(cols), len(cols), _ptr(r), _ptr(s))
+        ref[r0:r1] = r
+        absum[r0:r1] = s
+
+    _parallel(run, len(rows), threads)
+    return ref, absum
+
+
+def mx8_shared_exp(amax: float) -> int:
+    return lib().orc_mx8_shared_exp(float(amax))
+
+
+def act_quant_mxfp8(x_bf16_bits, threads=1):
+    """bf16 (as uint16 bits) [M, K] -> (E4M3 codes [M, K], row-major E8M0 [M, K/32])."""
+    x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)
+    M, K = x.shape
+    out_c = np.empty((M, K), np.uint8)
+    out_s = np.empty((M, K // 32), np.uint8)
+    L = lib()
+    _parallel(lambda r0, r1: L.orc_act_quant_mxfp8(_ptr(x), r0, r1, K, _ptr(out_c), _ptr(out_s)), M, threads)
+    return out_c, out_s
+
+
+def gemm_w4a8(a8, sa, b, sb, bias_bf16_bits=None, rows=None, cols=None, threads=1):
+    """float64 reference of MXFP8 activations x MXFP4 weights.
+
+    a8 [M, K] E4M3 bytes, sa row-major [M, K/32]; b [N, K/2], sb row-major [N, K/32].
+    Returns (ref, absum) of shape [len(rows), len(cols)].
+    """
+    a8 = np.ascontiguousarray(a8)
+    b = np.ascontiguousarray(b)
+    sa = np.ascontiguousarray(sa)
+    sb = np.ascontiguousarray(sb)
+    M, K = a8.shape
+    N = b.shape[0]
+    rows = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    cols = np.arange(N, dtype=np.int64) if cols is None else np.ascontiguousarray(cols, np.int64)
+    bias = None if bias_bf16_bits is None else np.ascontiguousarray(bias_bf16_bits, np.uint16)
+    ref = np.empty((len(rows), len(cols)), np.float64)
+    absum = np.empty_like(ref)
+    L = lib()
+
+    def run(r0, r1):
+        sub_rows = np.ascontiguousarray(rows[r0:r1])
+        r = np.empty((r1 - r0, len(cols)), np.float64)
+        s = np.empty_like(r)
+        L.orc_gemm_w4a8(_ptr(a8), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias), K, _ptr(sub_rows), r1 - r0,
+                        _ptr(cols), len(cols), _ptr(r), _ptr(s))
         ref[r0:r1] = r
         absum[r0:r1] = s
 

@@ -232,6 +232,67 @@ void orc_act_quant(const uint16_t* x_bf16, int64_t row0, int64_t row1, int64_t K
 }
 
 /* ------------------------------------------------------------------------
+ * MXFP8 activations for the W4A8 fallback ([OMNI] "W4A8 fallback at
+ * selected layers and denoising steps": MXFP8 activations with the same
+ * MXFP4 weights; "Single-Scale Block Scaling (OCP / UOS)": the A8 path
+ * always quantizes to float8_e4m3fn with the OCP rule, 32-element blocks
+ * along K and "rint" rounding).  The OCP MX rule with E4M3 elements, whose
+ * largest value is 448 = 1.75 * 2^8:
+ *   e = floor(log2(amax)) - 8, clamped to [-127, 127] (all-zero: -127);
+ *   element = float8_e4m3fn nearest to v / 2^e, ties to the even code,
+ *   saturating at +-448 (reading: finite elements never become NaN), sign
+ *   kept (-0 is 0x80).
+ * A block holding NaN or Inf gets scale byte 0xFF and zero bytes, as in the
+ * MXFP4 rule (reading).                                                    */
+int orc_mx8_shared_exp(double amax)
+{
+    int ex;
+    if (amax == 0.0)
+        return -127;
+    (void)frexp(amax, &ex);           /* amax = f * 2^ex, f in [0.5, 1) */
+    int e = (ex - 1) - 8;
+    if (e < -127)
+        e = -127;
+    if (e > 127)
+        e = 127;
+    return e;
+}
+
+void orc_mx8_quantize_block(const float v[32], uint8_t codes[32], uint8_t* sf)
+{
+    double amax = 0.0;
+    int nonfinite = 0;
+    for (int i = 0; i < 32; ++i) {
+        if (!isfinite(v[i]))
+            nonfinite = 1;
+        else if (fabs((double)v[i]) > amax)
+            amax = fabs((double)v[i]);
+    }
+    if (nonfinite) {
+        *sf = 0xFFu;
+        memset(codes, 0, 32);
+        return;
+    }
+    int e = orc_mx8_shared_exp(amax);
+    *sf = (uint8_t)(e + 127);
+    double scale = ldexp(1.0, e);
+    for (int i = 0; i < 32; ++i)
+        codes[i] = (uint8_t)orc_e4m3_encode((float)((double)v[i] / scale));
+}
+
+void orc_act_quant_mxfp8(const uint16_t* x_bf16, int64_t row0, int64_t row1, int64_t K,
+                         uint8_t* out_codes, uint8_t* out_sf)
+{
+    float v[32];
+    for (int64_t r = row0; r < row1; ++r)
+        for (int64_t b = 0; b < K / 32; ++b) {
+            for (int i = 0; i < 32; ++i)
+                v[i] = (float)orc_bf16_value(x_bf16[r * K + 32 * b + i]);
+            orc_mx8_quantize_block(v, out_codes + r * K + 32 * b, out_sf + r * (K / 32) + b);
+        }
+}
+
+/* ------------------------------------------------------------------------
  * W4A4 GEMM ([AMD] "Native FP4 matmul": both operands MXFP4; [OMNI]
  * Configuration: bf16 output with a bf16 per-output-channel bias; [SGL]
  * section 6: the bias is added to the GEMM output).  The definition:
@@ -255,6 +316,46 @@ void orc_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8
     double* brow = (double*)malloc(sizeof(double) * (size_t)K);
     for (int64_t i = 0; i < n_rows; ++i)
         dequant_mx_row(a + rows[i] * (K / 2), sa + rows[i] * (K / 32), K, arows + i * K);
+    for (int64_t j = 0; j < n_cols; ++j) {
+        int64_t n = cols[j];
+        dequant_mx_row(b + n * (K / 2), sb + n * (K / 32), K, brow);
+        double bias = bias_bf16 ? orc_bf16_value(bias_bf16[n]) : 0.0;
+        for (int64_t i = 0; i < n_rows; ++i) {
+            const double* arow = arows + i * K;
+            double s = 0.0, sabs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = arow[k] * brow[k];
+                s += p;
+                sabs += fabs(p);
+            }
+            ref[i * n_cols + j] = s + bias;
+            absum[i * n_cols + j] = sabs;
+        }
+    }
+    free(brow);
+    free(arows);
+}
+
+/* ------------------------------------------------------------------------
+ * W4A8 GEMM ([OMNI] "Hardware Support": the mixed FP8/FP4 GEMM of the W4A8
+ * fallback, bf16 output with a bf16 row bias): MXFP8 activations (one E4M3
+ * byte per element, E8M0 per 32) times the MXFP4 weights, in double:
+ *   out[m][n] = sum_k dq8(A)[m][k] * dq4(B)[n][k] + bias[n]            */
+static void dequant_mx8_row(const uint8_t* codes, const uint8_t* sf, int64_t K, double* out)
+{
+    for (int64_t k = 0; k < K; ++k)
+        out[k] = orc_e4m3_value(codes[k]) * orc_e8m0_value(sf[k / 32]);
+}
+
+void orc_gemm_w4a8(const uint8_t* a8, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                   const uint16_t* bias_bf16, int64_t K,
+                   const int64_t* rows, int64_t n_rows, const int64_t* cols, int64_t n_cols,
+                   double* ref, double* absum)
+{
+    double* arows = (double*)malloc(sizeof(double) * (size_t)(n_rows * K));
+    double* brow = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int64_t i = 0; i < n_rows; ++i)
+        dequant_mx8_row(a8 + rows[i] * K, sa + rows[i] * (K / 32), K, arows + i * K);
     for (int64_t j = 0; j < n_cols; ++j) {
         int64_t n = cols[j];
         dequant_mx_row(b + n * (K / 2), sb + n * (K / 32), K, brow);

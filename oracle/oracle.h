@@ -67,6 +67,21 @@ void orc_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8
               const int64_t* rows, int64_t n_rows, const int64_t* cols, int64_t n_cols,
               double* ref, double* absum);
 
+/* ---- W4A8 fallback ([OMNI] W4A8 fallback, Single-Scale Block Scaling) --- */
+/* OCP MX exponent for float8_e4m3fn elements: floor(log2 amax) - 8, clamped. */
+int orc_mx8_shared_exp(double amax);
+/* One 32-element block -> 32 E4M3 bytes + one E8M0 byte. */
+void orc_mx8_quantize_block(const float v[32], uint8_t codes[32], uint8_t* sf);
+/* bf16 activations -> MXFP8: codes [rows][K] bytes, row-major E8M0 [rows][K/32]. */
+void orc_act_quant_mxfp8(const uint16_t* x_bf16, int64_t row0, int64_t row1, int64_t K,
+                         uint8_t* out_codes, uint8_t* out_sf);
+/* MXFP8 activations x MXFP4 weights, float64 accumulation; as orc_gemm with
+ * a8 [rows][K] E4M3 bytes and sa row-major [rows][K/32].                    */
+void orc_gemm_w4a8(const uint8_t* a8, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                   const uint16_t* bias_bf16, int64_t K,
+                   const int64_t* rows, int64_t n_rows, const int64_t* cols, int64_t n_cols,
+                   double* ref, double* absum);
+
 /* NVFP4 x NVFP4 GEMM ([SGL] sections 5-6): E2M1 codes with row-major E4M3
  * scales per 16 elements (sa [rows][K/16], sb [cols][K/16]), one per-tensor
  * factor alpha (= g_a * g_b), float64 accumulation:

@@ -332,6 +332,100 @@ def test_gemm_one_hot_selects_columns(orc):
     assert np.array_equal(ref, A[:, sel])
 
 
+# ------------------------------------------------------ W4A8: MXFP8 activations
+
+
+@pytest.mark.parametrize("row", _golden_lines("act_quant_mxfp8_examples.txt"), ids=lambda r: r[0])
+def test_act_quant_mxfp8_worked_examples(orc, row):
+    name, xs, sf, codes = row
+    x = np.array([int(h, 16) for h in xs.split(",")], np.uint16).reshape(1, 32)
+    c, s = orc.act_quant_mxfp8(x)
+    assert s[0, 0] == int(sf, 16), name
+    assert c.tobytes().hex() == codes, name
+
+
+def test_mx8_exponent_closed_form(orc):
+    """OCP rule with E4M3 elements: amax / 2^e in [256, 512) for every
+    unclamped amax; clamps at 2^-127 and 2^127; zero -> -127."""
+    rng = np.random.default_rng(43)
+    for amax in np.exp(rng.uniform(-80, 80, 2000)):
+        e = orc.mx8_shared_exp(float(amax))
+        assert 256.0 <= amax / 2.0 ** e < 512.0
+    assert orc.mx8_shared_exp(0.0) == -127
+    assert orc.mx8_shared_exp(2.0 ** -200) == -127
+    assert orc.mx8_shared_exp(2.0 ** 200) == 127
+
+
+def test_act_quant_mxfp8_against_torch_and_brute_force(orc):
+    """Elements in range match torch's float8_e4m3fn rounding of x / 2^e;
+    those beyond 448 saturate; every element is the nearest finite E4M3
+    value (ties to the even code) by brute force over all 254 codes."""
+    rng = np.random.default_rng(47)
+    M, K = 24, 256
+    x = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32) * np.exp(rng.uniform(-20, 20, (M, 1)))
+                         .astype(np.float32)).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    c, s = orc.act_quant_mxfp8(bits)
+    xv = x.double().numpy().reshape(M, K // 32, 32)
+    amax = np.abs(xv).max(-1)
+    e = np.floor(np.log2(amax)) - 8
+    assert np.array_equal(s.astype(np.int64) - 127, e.astype(np.int64))
+    q = (xv / 2.0 ** e[..., None]).reshape(M, K)
+    inrange = np.abs(q) <= 448
+    t = torch.from_numpy(q.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(c[inrange], t[inrange])
+    assert np.all((c[~inrange] & 0x7F) == 0x7E)
+    finite = np.array([b for b in range(256) if (b & 0x7F) != 0x7F], np.uint8)
+    vals = _torch_e4m3(finite).astype(np.float64)
+    got = _torch_e4m3(c).astype(np.float64)
+    for i in range(0, M * K, 97):
+        qi = float(q.flat[i])
+        d = np.abs(vals - qi)
+        best = d.min()
+        assert abs(got.flat[i] - qi) == best
+        ties = finite[d == best]
+        if len(ties) > 1:
+            assert c.flat[i] & 1 == 0            # the even code
+
+
+def test_gemm_w4a8_matches_numpy_matmul(orc):
+    rng = np.random.default_rng(53)
+    M, N, K = 6, 11, 160
+    finite = np.array([b for b in range(256) if (b & 0x7F) != 0x7F], np.uint8)
+    a8 = rng.choice(finite, (M, K))
+    b = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = rng.integers(110, 140, (M, K // 32), dtype=np.uint8)
+    sb = rng.integers(110, 140, (N, K // 32), dtype=np.uint8)
+    bias = torch.randn(N).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    bias_f = torch.from_numpy(bias.view(np.int16)).view(torch.bfloat16).double().numpy()
+    A = _torch_e4m3(a8).astype(np.float64) * np.repeat(2.0 ** (sa.astype(np.float64) - 127), 32, axis=1)
+    B = _dequant_indep(b, sb)
+    ref, absum = orc.gemm_w4a8(a8, sa, b, sb, bias)
+    prod_abs = np.abs(A) @ np.abs(B).T
+    assert np.allclose(ref, A @ B.T + bias_f, rtol=1e-12, atol=1e-12 * prod_abs + 1e-300)
+    assert np.allclose(absum, prod_abs, rtol=1e-12)
+    rows, cols = np.array([5, 2]), np.array([0, 9, 3])
+    r2, _ = orc.gemm_w4a8(a8, sa, b, sb, bias, rows=rows, cols=cols)
+    assert np.array_equal(r2, ref[np.ix_(rows, cols)])
+
+
+def test_gemm_w4a8_one_hot_selects_columns(orc):
+    """B rows one-hot with code 1.0 under scale 2^0: out[:, n] = A[:, sel[n]] exactly."""
+    rng = np.random.default_rng(59)
+    M, N, K = 5, 9, 128
+    finite = np.array([b for b in range(256) if (b & 0x7F) != 0x7F], np.uint8)
+    a8 = rng.choice(finite, (M, K))
+    sa = rng.integers(120, 135, (M, K // 32), dtype=np.uint8)
+    sel = rng.integers(0, K, N)
+    codes = np.zeros((N, K), np.uint8)
+    codes[np.arange(N), sel] = 0x2
+    b = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    sb = np.full((N, K // 32), 127, np.uint8)
+    ref, _ = orc.gemm_w4a8(a8, sa, b, sb)
+    A = _torch_e4m3(a8).astype(np.float64) * np.repeat(2.0 ** (sa.astype(np.float64) - 127), 32, axis=1)
+    assert np.array_equal(ref, A[:, sel])
+
+
 # ------------------------------------------------------ NVFP4 x NVFP4 GEMM
 
 
