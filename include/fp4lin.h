@@ -303,6 +303,43 @@ FP4LIN_API fp4_status fp4_gemm_nvfp4(const uint8_t* a, const uint8_t* sa, const 
                           int64_t M, int64_t N, int64_t K, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------- W4A8 fallback */
+
+/* bf16 -> MXFP8 activations for the W4A8 fallback ([OMNI] "W4A8 fallback at
+ * selected layers and denoising steps": MXFP8 activations with the same
+ * MXFP4 weights; "Single-Scale Block Scaling": float8_e4m3fn elements, the
+ * OCP rule, 32-element blocks along K, rint).  Per block: amax, e =
+ * floor(log2 amax) - 8 clamped to [-127, 127] (all-zero: -127), scale byte
+ * e + 127; each element the nearest E4M3 value of x / 2^e (ties to even,
+ * saturating at +-448, sign kept); a block holding NaN or Inf gets scale
+ * byte 0xFF and zero bytes.
+ *   out_e4m3   [M, K] bytes (device, 16-byte aligned)
+ *   out_scale  E8M0 bytes in sf_layout: fp4_sf_bytes(M, K, sf_layout)
+ * Requires M >= 0 (0 is a no-op), K a positive multiple of 32.             */
+FP4LIN_API fp4_status fp4_quant_act_mxfp8(const void* x_bf16, uint8_t* out_e4m3, uint8_t* out_scale,
+                               int64_t M, int64_t K, int32_t sf_layout, void* stream);
+
+/* W4A8 GEMM: MXFP8 activations x MXFP4 weights on block-scaled tensor cores
+ * (tcgen05.mma kind::mxf8f6f4), the mixed FP8/FP4 GEMM of [OMNI] "Hardware
+ * Support" (bf16 output, bf16 row bias):
+ *   out[m, n] = bf16_rne( sum_k A8[m,k] * B[n,k] + bias[n] )
+ * with fp32 accumulation.
+ *   a_e4m3  [M, K] E4M3 bytes, sa SWIZZLED E8M0 (fp4_sf_bytes(M, K, 0))
+ *   b       [N, K/2] MXFP4 codes (32-byte aligned: the tensor memory
+ *           accelerator reads them as 4-bit elements), sb SWIZZLED E8M0
+ *   workspace, workspace_bytes: split-K scratch as in fp4_gemm_mxfp4_ws,
+ *           sized by fp4_gemm_w4a8_workspace_size (this GEMM's stages cover
+ *           half as much K, so its split plan differs), or NULL
+ * Same shape rules as fp4_gemm_mxfp4.                                      */
+FP4LIN_API fp4_status fp4_gemm_w4a8(const uint8_t* a_e4m3, const uint8_t* sa, const uint8_t* b,
+                         const uint8_t* sb, const void* bias_bf16, void* out_bf16, int64_t M,
+                         int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* Workspace fp4_gemm_w4a8 uses for split-K on an M x N x K problem on the
+ * current device (0: not split, or no usable device).                      */
+FP4LIN_API size_t fp4_gemm_w4a8_workspace_size(int64_t M, int64_t N, int64_t K);
+
 /* Grouped (MoE) W4A4 GEMM ([AMD] "Native FP4 matmul": MoE experts on
  * MXFP4): for every expert e and every row m in [row_offsets[e],
  * row_offsets[e+1]):  out[m, :] = A[m, :] . B_e^T (+ bias_e).

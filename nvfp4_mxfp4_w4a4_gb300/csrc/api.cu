@@ -282,8 +282,8 @@ fp4_status fp4_sf_swizzle(const uint8_t* in_rowmajor, uint8_t* out, int64_t rows
 
 static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                               const void* bias, void* out, const int32_t* offsets, int32_t E, int64_t M, int64_t N,
-                              int64_t K, void* workspace, size_t workspace_bytes, void* stream, bool nvfp4 = false,
-                              float alpha = 1.0f)
+                              int64_t K, void* workspace, size_t workspace_bytes, void* stream,
+                              int fmt = fp4lin::kGemmMx, float alpha = 1.0f)
 {
     if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 8 != 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
         return FP4_ERR_SHAPE;
@@ -315,7 +315,7 @@ static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t
     args.status = status;
     args.workspace = workspace;
     args.workspace_bytes = workspace ? workspace_bytes : 0;
-    args.nvfp4 = nvfp4;
+    args.fmt = fmt;
     args.alpha = alpha;
     return from_cuda(fp4lin::launch_gemm(args, static_cast<cudaStream_t>(stream)));
 }
@@ -330,7 +330,7 @@ size_t fp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K)
 {
     if (current_device(nullptr) != FP4_OK)
         return 0;
-    return fp4lin::gemm_workspace_bytes(M, N, K);
+    return fp4lin::gemm_workspace_bytes(M, N, K, fp4lin::kGemmMx);
 }
 
 fp4_status fp4_gemm_mxfp4_ws(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
@@ -349,7 +349,47 @@ fp4_status fp4_gemm_nvfp4(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
     if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FP4_ERR_ALIGNMENT;
     return gemm_common(a, sa, b, sb, bias_bf16, out_bf16, nullptr, 1, M, N, K, workspace, workspace_bytes, stream,
-                       true, alpha);
+                       fp4lin::kGemmNv, alpha);
+}
+
+size_t fp4_gemm_w4a8_workspace_size(int64_t M, int64_t N, int64_t K)
+{
+    if (current_device(nullptr) != FP4_OK)
+        return 0;
+    return fp4lin::gemm_workspace_bytes(M, N, K, fp4lin::kGemmW4A8);
+}
+
+fp4_status fp4_gemm_w4a8(const uint8_t* a_e4m3, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                         const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
+                         size_t workspace_bytes, void* stream)
+{
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FP4_ERR_ALIGNMENT;
+    if (b && (reinterpret_cast<uintptr_t>(b) & 31u))
+        return FP4_ERR_ALIGNMENT;  // the TMA reads the weights as 4-bit elements: 32-byte aligned base
+    return gemm_common(a_e4m3, sa, b, sb, bias_bf16, out_bf16, nullptr, 1, M, N, K, workspace, workspace_bytes,
+                       stream, fp4lin::kGemmW4A8);
+}
+
+fp4_status fp4_quant_act_mxfp8(const void* x_bf16, uint8_t* out_e4m3, uint8_t* out_scale, int64_t M, int64_t K,
+                               int32_t sf_layout, void* stream)
+{
+    if (M < 0 || K <= 0 || K % 32 != 0 || M >= kMaxDim || K >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    if (sf_layout != FP4_SF_SWIZZLED && sf_layout != FP4_SF_ROWMAJOR)
+        return FP4_ERR_INVALID_ARG;
+    if (M == 0)
+        return FP4_OK;
+    if (!x_bf16 || !out_e4m3 || !out_scale)
+        return FP4_ERR_INVALID_ARG;
+    const bool swz = sf_layout == FP4_SF_SWIZZLED;
+    if (!aligned16(x_bf16) || !aligned16(out_e4m3) || (swz && (reinterpret_cast<uintptr_t>(out_scale) & 3u)))
+        return FP4_ERR_ALIGNMENT;
+    fp4_status st;
+    if ((st = current_device(nullptr)) != FP4_OK)
+        return st;
+    return from_cuda(fp4lin::launch_act_quant_mxfp8(x_bf16, out_e4m3, out_scale, M, K, swz ? 1 : 0,
+                                                    static_cast<cudaStream_t>(stream)));
 }
 
 fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,

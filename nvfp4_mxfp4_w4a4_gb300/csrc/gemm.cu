@@ -44,12 +44,21 @@
 // adds the fp32 partial sums the other S - 1 CTAs left in the workspace, in
 // K order (a fixed reduction order, so results do not vary from run to run),
 // then runs the epilogue.
-// NVFP4 mode (kNv): both operands NVFP4 as "[SGLang] FP4 ..." sections 5-6
+// Operand formats (kFmt):
+//   kFmtMx  both operands MXFP4 (the path above);
+//   kFmtNv  both operands NVFP4 as "[SGLang] FP4 ..." sections 5-6
 // run them on hardware with native NVFP4: one E4M3 scale per 16 elements
 // (two 512-byte scale chunks per 128 elements of K instead of one, four
 // scales per row per K = 64 step, tcgen05.mma kind::mxf4nvf4 with
 // scale_vec::4X) and a per-tensor alpha applied to the accumulator in the
-// epilogue before the bias.
+// epilogue before the bias;
+//   kFmtA8  the W4A8 fallback of "W4A4 MXFP4 Quantization" (MXFP8
+// activations with the same MXFP4 weights): E4M3 activations (one byte per
+// element) and the FP4 weights, which TMA expands to one element per byte
+// in shared memory (16 codes in the low half of every 16 bytes), so both
+// operands stage 128 elements of K per 128-byte row; tcgen05.mma
+// kind::mxf8f6f4 (K = 32, one E8M0 scale per row each, chosen by the
+// descriptor's byte selector).
 // Every mbarrier wait is bounded; on expiry the kernel records a timeout in
 // the status word and winds down.
 #include <cuda_bf16.h>
@@ -67,6 +76,8 @@ namespace {
 constexpr int BM = 128;
 constexpr int kSlabBytes = 128;  // packed bytes of K per row per slab (256 elements)
 constexpr int kEpiWarps = 8;
+
+enum : int { kFmtMx = kGemmMx, kFmtNv = kGemmNv, kFmtA8 = kGemmW4A8 };
 
 struct GemmParams {
     int64_t units;              // split-K: total K-stage units (0: one CTA per whole tile)
@@ -90,8 +101,10 @@ struct GemmParams {
     unsigned int* status;
 };
 
-template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kNv>
+template <int BN, int STAGES, int KC, int CPW, bool kSwap, int kFmt>
 struct Cfg {
+    static constexpr bool kNv = kFmt == kFmtNv;
+    static constexpr bool kA8 = kFmt == kFmtA8;
     // Four scale warps beside a 256-wide epilogue do not fit the register
     // file at 14 warps: 16 warps then, warps 6-7 idle, and the two non-
     // epilogue warpgroups hand registers to the epilogue ones (setmaxnreg).
@@ -100,11 +113,18 @@ struct Cfg {
     static constexpr int REGS_HIGH = 176;  // epilogue warps after the split
     static constexpr int FIRST_EPI_WARP = SPLIT ? 8 : 2 + CPW;
     static constexpr int THREADS = 32 * (FIRST_EPI_WARP + kEpiWarps);
-    static constexpr int GROUPS = 2 * KC;  // 128-element groups of K per stage
+    // a slab is one 128-byte row per operand row: 256 elements of K (packed
+    // FP4) or 128 (W4A8: E4M3, and FP4 expanded to a byte per element)
+    static constexpr int GROUPS = kA8 ? KC : 2 * KC;  // 128-element groups of K per stage
+    static constexpr int MMAS_PER_GROUP = kA8 ? 4 : 2;  // K = 32 (W4A8) or 64 per MMA
     static constexpr int APG = kNv ? 2 : 1;  // 512-byte scale chunks per group and 128-row tile
     static constexpr int ATOMS = GROUPS * APG;  // scale chunks per stage and 128-row tile
-    static constexpr int A_BYTES = BM * kSlabBytes * KC;
+    static constexpr int A_BYTES = BM * kSlabBytes * KC;  // shared memory per stage
     static constexpr int B_BYTES = BN * kSlabBytes * KC;
+    // bytes the TMA counts per stage: the expanded FP4 operand (the weights:
+    // MMA-M side when swapped) counts its global bytes, half its footprint
+    static constexpr int A_TX = (kA8 && kSwap) ? A_BYTES / 2 : A_BYTES;
+    static constexpr int B_TX = (kA8 && !kSwap) ? B_BYTES / 2 : B_BYTES;
     static constexpr int SFB_TILES = (BN + 127) / 128;
     static constexpr int SFA_BYTES = ATOMS * 512;
     static constexpr int SFB_BYTES = SFB_TILES * ATOMS * 512;
@@ -278,12 +298,13 @@ __device__ __forceinline__ void load_operand(void* dst, const CUtensorMap* map, 
         tma_load_3d(dst, map, bar, 0, static_cast<int32_t>(row0), kb * KC);
 }
 
-template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped, bool kNv>
-__global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kNv>::THREADS, 1)
+template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped, int kFmt>
+__global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmO, const GemmParams p)
 {
-    using C = Cfg<BN, STAGES, KC, CPW, kSwap, kNv>;
+    using C = Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>;
+    constexpr bool kNv = C::kNv, kA8 = C::kA8;
     constexpr int kFirstEpiWarp = C::FIRST_EPI_WARP;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -380,7 +401,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kNv>::THREADS,
                         const uint32_t sf_bytes = static_cast<uint32_t>(groups * C::APG) * 512u;
                         const int64_t atoms_per_rt = static_cast<int64_t>(p.kb4) * C::APG;  // chunks per 128-row tile
                         // boxes past the end of K or of the rows are zero-filled and still counted
-                        mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES + sf_bytes * (1u + nsfb));
+                        mbar_arrive_expect_tx(&full[s], C::A_TX + C::B_TX + sf_bytes * (1u + nsfb));
                         load_operand<KC>(smem + C::OFF_A + s * C::A_BYTES, &tmA, &full[s], kb, T.a_row0);
                         load_operand<KC>(smem + C::OFF_B + s * C::B_BYTES, &tmB, &full[s], kb, b_row0);
                         bulk_load(smem + C::OFF_SFA + s * C::SFA_BYTES,
@@ -394,7 +415,11 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kNv>::THREADS,
         } else if (warp == 1) {
             if (lane == 0) {
                 // --------------------------------------------------- MMA issuer
-                constexpr uint32_t idesc = kNv ? idesc_nvf4(BM, BN) : idesc_mxf4(BM, BN);
+                // W4A8: E4M3 activations, E2M1 weights (the MMA-M side when swapped)
+                constexpr uint32_t idesc = kNv   ? idesc_nvf4(BM, BN)
+                                           : kA8 ? idesc_mxf8f6f4(BM, BN, kSwap ? kTypeE2M1 : kTypeE4M3,
+                                                                  kSwap ? kTypeE4M3 : kTypeE2M1)
+                                                 : idesc_mxf4(BM, BN);
                 uint32_t it = 0, tcount = 0;
                 bool ok = true;
                 WorkIter wi = work_begin(p, total_tiles);
@@ -423,15 +448,20 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kNv>::THREADS,
                         const uint32_t sfb_t = sfa_t + C::SF_COLS_A;
                         const uint32_t a_s = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
                         const uint32_t b_s = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
-                        for (int k = 0; k < 2 * groups; ++k) {
-                            // k-th 64-element step: slab k / 4, 32-byte column k % 4, scale chunk k / 2
-                            // (MXFP4: bytes 2 (k % 2), +1 of it) or k (NVFP4: all four bytes)
+                        for (int k = 0; k < C::MMAS_PER_GROUP * groups; ++k) {
+                            // k-th MMA: slab k / 4, 32-byte column k % 4 (64 FP4 or 32 byte
+                            // elements); scale chunk k / 2 (MXFP4: bytes 2 (k % 2), +1 of it),
+                            // k (NVFP4: all four bytes) or k / 4 (W4A8: byte k % 4)
                             const int slab = k >> 2;
                             const uint64_t ad = smem_desc(a_s + slab * (BM * kSlabBytes) + 32 * (k & 3), 16, 1024, 2);
                             const uint64_t bd = smem_desc(b_s + slab * (BN * kSlabBytes) + 32 * (k & 3), 16, 1024, 2);
                             const uint32_t acc = (kb != w.kb0 || k != 0) ? 1u : 0u;
                             if constexpr (kNv) {
                                 tc_mma_nvf4(tmem_base, ad, bd, idesc, sfa_t + 4 * k, sfb_t + k * C::SF_COLS_B_ATOM, acc);
+                            } else if constexpr (kA8) {
+                                const int g = k >> 2;
+                                tc_mma_mxf8f6f4(tmem_base, ad, bd, idesc_with_sf_id(idesc, static_cast<uint32_t>(k & 3)),
+                                                sfa_t + 4 * g, sfb_t + g * C::SF_COLS_B_ATOM, acc);
                             } else {
                                 const int g = k >> 1;
                                 const uint32_t sf_id = static_cast<uint32_t>(k & 1) * 2u;
@@ -691,31 +721,45 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Packed operand [rows, K/2] bytes, 128-byte swizzle.  KC == 1: 2-D boxes of
-// 128 bytes x box_rows.  KC > 1 (needs K % 256 == 0): the rows viewed as
-// K/256 slabs of 128 bytes, 3-D boxes of 128 bytes x box_rows x KC slabs,
-// which land in shared memory as KC consecutive [box_rows][128 B] slabs.
-bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows, int kc)
+// Operand maps, 128-byte swizzle, one 128-byte shared-memory row per
+// operand row and slab:
+//   kOpFp4Packed    packed FP4 [rows, K/2] bytes, slab = 128 bytes (256 elements);
+//   kOpBytes        E4M3 [rows, K] bytes, slab = 128 bytes (128 elements);
+//   kOpFp4Expanded  packed FP4 [rows, K/2] read as 4-bit elements that the TMA
+//                   writes 16 to every 16 bytes (low half; 32-byte aligned
+//                   base, K % 128 == 0), slab = 128 elements (64 bytes read).
+// KC == 1: 2-D boxes of one slab x box_rows.  KC > 1: the rows viewed as
+// slabs (3-D), boxes of one slab x box_rows x KC slabs, which land as KC
+// consecutive [box_rows][128 B] slabs.
+enum : int { kOpFp4Packed = 0, kOpBytes = 1, kOpFp4Expanded = 2 };
+
+bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows, int kc, int kind)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return false;
     const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        kind == kOpFp4Expanded ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const int64_t row_bytes = kind == kOpBytes ? K : K / 2;
+    const int64_t slab_elems = kind == kOpFp4Packed ? kSlabBytes : 128;       // box width in map elements
+    const int64_t slab_step = kind == kOpFp4Expanded ? 64 : kSlabBytes;       // global bytes per slab
+    const int64_t row_elems = kind == kOpFp4Packed ? K / 2 : K;               // map elements per row
     if (kc == 1) {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(kSlabBytes), static_cast<cuuint32_t>(box_rows)};
-        return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_elems), static_cast<cuuint64_t>(rows)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(slab_elems), static_cast<cuuint32_t>(box_rows)};
+        return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kSlabBytes), static_cast<cuuint64_t>(rows),
-                                static_cast<cuuint64_t>(K / 256)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(kSlabBytes)};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kSlabBytes), static_cast<cuuint32_t>(box_rows),
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(slab_elems), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(row_elems / slab_elems)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(slab_step)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(slab_elems), static_cast<cuuint32_t>(box_rows),
                                static_cast<cuuint32_t>(kc)};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -781,19 +825,24 @@ void swap_config(int64_t M, int64_t K, int* bn, int* kc)
     *bn = (*kc == 2 && M <= 32) ? 32 : 64;
 }
 
-template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped, bool kNv = false>
+template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped, int kFmt = kFmtMx>
 cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
 {
-    using C = Cfg<BN, STAGES, KC, CPW, kSwap, kNv>;
+    using C = Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>;
+    constexpr bool kNv = C::kNv, kA8 = C::kA8;
     // MMA-M operand / MMA-N operand
     const uint8_t* opA = kSwap ? a.b : a.a;
     const uint8_t* opB = kSwap ? a.a : a.b;
     const int64_t rows_a = kSwap ? a.N : a.M;
     const int64_t rows_b = kSwap ? a.M : a.N;
     CUtensorMap tmA, tmB, tmO;
-    if (!make_operand_map(&tmA, opA, rows_a, a.K, BM, KC))
+    // operand kinds: packed FP4 bytes; W4A8: E4M3 bytes (activations) and
+    // FP4 expanded by the TMA (weights)
+    const int kind_a = kA8 ? (kSwap ? kOpFp4Expanded : kOpBytes) : kOpFp4Packed;
+    const int kind_b = kA8 ? (kSwap ? kOpBytes : kOpFp4Expanded) : kOpFp4Packed;
+    if (!make_operand_map(&tmA, opA, rows_a, a.K, BM, KC, kind_a))
         return cudaErrorInvalidValue;
-    if (!make_operand_map(&tmB, opB, static_cast<int64_t>(a.E) * rows_b, a.K, BN, KC))
+    if (!make_operand_map(&tmB, opB, static_cast<int64_t>(a.E) * rows_b, a.K, BN, KC, kind_b))
         return cudaErrorInvalidValue;
     if (!(kSwap ? make_output_map(&tmO, a.out, a.M, a.N, 32, BN / 2, CU_TENSOR_MAP_SWIZZLE_NONE)
                 : make_output_map(&tmO, a.out, a.M, a.N, C::CHUNK, 32,
@@ -838,7 +887,7 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
         }
     }
     const size_t smem = C::SMEM_FIXED + (kGrouped ? sizeof(int32_t) * (a.E + 1) : 0);
-    auto kern = gemm_fp4_kernel<BN, STAGES, KC, CPW, kSwap, kGrouped, kNv>;
+    auto kern = gemm_fp4_kernel<BN, STAGES, KC, CPW, kSwap, kGrouped, kFmt>;
     // The shared-memory opt-in is a per-device function attribute: set it
     // once per device (and grow it if a larger grouped prefix needs more).
     static std::mutex mu;
@@ -878,13 +927,19 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
 
 }  // namespace
 
-size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K)
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int fmt)
 {
     if (M < 1 || M > 64 || N <= 0 || K <= 0 || K % 128 != 0)
         return 0;
     int bn = 0, kc = 0;
     swap_config(M, K, &bn, &kc);
-    const int64_t nkb = (K / 128 + 2 * kc - 1) / (2 * kc);
+    int groups = 2 * kc;  // 128-element groups of K per stage
+    if (fmt == kGemmW4A8) {
+        // launch_gemm_w4a8: two 128-element slabs per stage at any K
+        bn = M <= 32 ? 32 : 64;
+        groups = 2;
+    }
+    const int64_t nkb = (K / 128 + groups - 1) / groups;
     return split_plan((N + BM - 1) / BM, nkb, bn, sm_count()).bytes;
 }
 
@@ -895,24 +950,39 @@ cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t stream)
     const bool k256 = a.K % 256 == 0;
     if (a.M <= 64) {
         if (!k256)
-            return launch_kernel<64, 7, 1, 4, true, false, true>(a, stream);
-        return a.M <= 32 ? launch_kernel<32, 4, 2, 4, true, false, true>(a, stream)
-                         : launch_kernel<64, 3, 2, 4, true, false, true>(a, stream);
+            return launch_kernel<64, 7, 1, 4, true, false, kFmtNv>(a, stream);
+        return a.M <= 32 ? launch_kernel<32, 4, 2, 4, true, false, kFmtNv>(a, stream)
+                         : launch_kernel<64, 3, 2, 4, true, false, kFmtNv>(a, stream);
     }
     const bool wide = a.N >= 256 && ((a.M + 127) / 128) * ((a.N + 255) / 256) >= 148;
     if (wide) {
         // twelve scale copies per stage: four scale warps (register split),
         // or two where the split cannot be launched
-        const cudaError_t e = launch_kernel<256, 4, 1, 4, false, false, true>(a, stream);
-        return e == cudaErrorInvalidConfiguration ? launch_kernel<256, 4, 1, 2, false, false, true>(a, stream) : e;
+        const cudaError_t e = launch_kernel<256, 4, 1, 4, false, false, kFmtNv>(a, stream);
+        return e == cudaErrorInvalidConfiguration ? launch_kernel<256, 4, 1, 2, false, false, kFmtNv>(a, stream) : e;
     }
-    return launch_kernel<128, 5, 1, 4, false, false, true>(a, stream);
+    return launch_kernel<128, 5, 1, 4, false, false, kFmtNv>(a, stream);
+}
+
+// W4A8: MXFP8 activations x the MXFP4 weights (dense only).  A stage of KC
+// slabs covers 128 KC elements of K; the 3-D view needs only K % 128 == 0.
+cudaError_t launch_gemm_w4a8(const GemmArgs& a, cudaStream_t stream)
+{
+    if (a.M <= 64)
+        return a.M <= 32 ? launch_kernel<32, 4, 2, 4, true, false, kFmtA8>(a, stream)
+                         : launch_kernel<64, 4, 2, 4, true, false, kFmtA8>(a, stream);
+    const bool wide = a.N >= 256 && ((a.M + 127) / 128) * ((a.N + 255) / 256) >= 148;
+    if (wide)
+        return launch_kernel<256, 4, 1, 2, false, false, kFmtA8>(a, stream);
+    return launch_kernel<128, 6, 1, 4, false, false, kFmtA8>(a, stream);
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream)
 {
-    if (a.nvfp4)
+    if (a.fmt == kGemmNv)
         return launch_gemm_nvfp4(a, stream);
+    if (a.fmt == kGemmW4A8)
+        return launch_gemm_w4a8(a, stream);
     // Stages of two slabs need the 3-D operand view, which needs
     // K % 256 == 0; otherwise the one-slab configurations run.
     const bool k256 = a.K % 256 == 0;

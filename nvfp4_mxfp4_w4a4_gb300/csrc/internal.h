@@ -54,6 +54,10 @@ bool requant_flat_ok(const uint8_t* wp, const uint8_t* ws, const uint8_t* op, co
 cudaError_t launch_act_quant(const void* x, uint8_t* op, uint8_t* osf, int64_t M, int64_t K, int alg,
                              int swizzled, cudaStream_t stream);
 
+// bf16 -> MXFP8 (E4M3 codes [M, K], E8M0 per 32, OCP rule) for the W4A8 path.
+cudaError_t launch_act_quant_mxfp8(const void* x, uint8_t* op, uint8_t* osf, int64_t M, int64_t K, int swizzled,
+                                   cudaStream_t stream);
+
 cudaError_t launch_act_quant_grouped(const void* x, const int32_t* offsets, int E, int64_t total_M,
                                      int64_t K, uint8_t* op, uint8_t* osf, int alg, cudaStream_t stream);
 
@@ -62,6 +66,10 @@ cudaError_t launch_quant_nvfp4(const void* x, float g, uint8_t* op, uint8_t* osf
 
 // Row-major [rows][kb] scale bytes -> swizzled layout (any block size).
 cudaError_t launch_sf_swizzle(const uint8_t* in, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t stream);
+
+// Operand formats of the GEMM: both MXFP4; both NVFP4 (E4M3 scales per 16
+// elements, alpha); MXFP8 activations (a: [M, K] E4M3 bytes) x MXFP4 weights.
+enum GemmFormat : int { kGemmMx = 0, kGemmNv = 1, kGemmW4A8 = 2 };
 
 // Dense (offsets == nullptr) or grouped GEMM.
 struct GemmArgs {
@@ -79,7 +87,7 @@ struct GemmArgs {
     unsigned int* status;
     void* workspace;             // split-K scratch (nullptr: none)
     size_t workspace_bytes;
-    bool nvfp4 = false;          // NVFP4 operands (E4M3 scales per 16 elements)
+    int fmt = 0;                 // GemmFormat
     float alpha = 1.0f;          // NVFP4: factor on the accumulator before the bias
 };
 
@@ -88,6 +96,6 @@ cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
 // Workspace the GEMM uses for split-K on this problem on the current device
 // (0: the problem is not split): a zero-initialised counter per SM (256-byte
 // padded), then one fp32 partial tile per CTA.
-size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int fmt);
 
 }  // namespace fp4lin

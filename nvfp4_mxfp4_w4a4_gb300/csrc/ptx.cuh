@@ -242,6 +242,20 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t adesc, uin
         : "memory");
 }
 
+// MXFP8 x MXFP4 block-scaled MMA (kind::mxf8f6f4, K = 32): one E8M0 scale
+// per row, the byte of the row's scale column the descriptor selects.
+__device__ __forceinline__ void tc_mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Each lane of the warp reads 32 consecutive 32-bit columns of its own
 // TMEM lane (lane = 32 * (warp % 4) + laneid).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r)
@@ -318,6 +332,14 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t m, uint32_t n)
 __host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t m, uint32_t n)
 {
     return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// kind::mxf8f6f4 element types (A in bits 7-9, B in bits 10-12), E8M0 scales.
+constexpr uint32_t kTypeE4M3 = 0;
+constexpr uint32_t kTypeE2M1 = 5;
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4(uint32_t m, uint32_t n, uint32_t a_type, uint32_t b_type)
+{
+    return (a_type << 7) | (b_type << 10) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24);
 }
 
 __device__ __forceinline__ uint32_t idesc_with_sf_id(uint32_t idesc, uint32_t sf_id)

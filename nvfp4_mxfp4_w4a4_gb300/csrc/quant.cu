@@ -482,6 +482,39 @@ __device__ __forceinline__ uint32_t act_quant_lane(uint4 v, int uos, uint32_t& s
     return e2m1x8_pack(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
 }
 
+// The same block to MXFP8 (float8_e4m3fn elements) for the W4A8 fallback:
+// OCP exponent e = floor(log2 amax) - 8 (8 = exponent of E4M3's largest
+// value 448); the lane's 8 bytes are the nearest E4M3 values of x * 2^-e
+// (ties to even, saturating at 448, sign kept), rounded two at a time by
+// the hardware conversion.  q is exact in fp32 wherever it can round to a
+// nonzero E4M3 value.
+__device__ __forceinline__ uint2 act_quant_lane8(uint4 v, uint32_t& sf)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t a = __vmaxu2(__vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
+                                __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
+    uint32_t am = max(a & 0xFFFFu, a >> 16);
+    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+    const uint32_t ab = am << 16;
+    if (ab >= 0x7F800000u) {
+        sf = 0xFFu;
+        return make_uint2(0u, 0u);
+    }
+    // subnormal and zero amax give <= -135, clamped to -127
+    const int e = max(-127, static_cast<int>(ab >> 23) - 135);
+    sf = static_cast<uint32_t>(e + 127);
+    const float se = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
+    uint32_t h[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float lo = __fmul_rn(__uint_as_float(w[j] << 16), se);
+        const float hi = __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), se);
+        h[j] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+    }
+    return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+}
+
 // Tile-prefix of a grouped activation tensor: group e starts at scale row
 // 128 * tiles_before[e].  Computed by one warp into shared memory.
 __device__ void group_tile_prefix(const int32_t* offsets, int E, int32_t* tiles_before)
@@ -510,7 +543,8 @@ __device__ void group_tile_prefix(const int32_t* offsets, int E, int32_t* tiles_
 // scale row is the activation row (rows >= M are pad rows).  For the grouped
 // tensor scale rows live in the padded per-group space; `grouped` selects
 // the mapping.  Lane owns quarter (lane & 3) of block chunk*8U + 8u + lane/4.
-template <int U, bool kGrouped>
+// kA8: MXFP8 output (one E4M3 byte per element, rows of K bytes).
+template <int U, bool kGrouped, bool kA8>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __restrict__ x,
                                                              uint8_t* __restrict__ op, uint8_t* __restrict__ osf,
                                                              int64_t M, int64_t K, int64_t sf_rows, int kb,
@@ -567,9 +601,15 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
         const int c = cbase + 8 * u;
         const bool real = row_real && c < kb;
         uint32_t sf;
-        const uint32_t packed = act_quant_lane(v[u], uos, sf);
-        if (real)
-            *reinterpret_cast<uint32_t*>(op + xrow * (K / 2) + static_cast<int64_t>(c) * 16 + q * 4) = packed;
+        if constexpr (kA8) {
+            const uint2 codes = act_quant_lane8(v[u], sf);
+            if (real)
+                *reinterpret_cast<uint2*>(op + xrow * K + static_cast<int64_t>(c) * 32 + q * 8) = codes;
+        } else {
+            const uint32_t packed = act_quant_lane(v[u], uos, sf);
+            if (real)
+                *reinterpret_cast<uint32_t*>(op + xrow * (K / 2) + static_cast<int64_t>(c) * 16 + q * 4) = packed;
+        }
         if (!real)
             sf = 0u;
         if (swizzled) {
@@ -765,8 +805,24 @@ cudaError_t launch_act_quant(const void* x, uint8_t* op, uint8_t* osf, int64_t M
     const int64_t blocks = ceil_div(rows * nch * 32, kThreads);
     if (blocks == 0)
         return cudaSuccess;
-    return launch_pdl(act_quant_kernel<U, false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream,
-                      static_cast<const uint16_t*>(x), op, osf, M, K, rows, kb, kbp, nch, alg == 2 ? 1 : 0, swizzled,
+    return launch_pdl(act_quant_kernel<U, false, false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
+                      stream, static_cast<const uint16_t*>(x), op, osf, M, K, rows, kb, kbp, nch, alg == 2 ? 1 : 0,
+                      swizzled, static_cast<const int32_t*>(nullptr), 0);
+}
+
+cudaError_t launch_act_quant_mxfp8(const void* x, uint8_t* op, uint8_t* osf, int64_t M, int64_t K, int swizzled,
+                                   cudaStream_t stream)
+{
+    constexpr int U = 4;
+    const int kb = static_cast<int>(K / 32);
+    const int kbp = swizzled ? static_cast<int>(ceil_div(kb, 4) * 4) : kb;
+    const int64_t rows = swizzled ? ceil_div(M, 128) * 128 : M;
+    const int nch = static_cast<int>(ceil_div(kbp, 8 * U));
+    const int64_t blocks = ceil_div(rows * nch * 32, kThreads);
+    if (blocks == 0)
+        return cudaSuccess;
+    return launch_pdl(act_quant_kernel<U, false, true>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
+                      stream, static_cast<const uint16_t*>(x), op, osf, M, K, rows, kb, kbp, nch, 0, swizzled,
                       static_cast<const int32_t*>(nullptr), 0);
 }
 
@@ -782,7 +838,7 @@ cudaError_t launch_act_quant_grouped(const void* x, const int32_t* offsets, int 
     if (blocks == 0)
         return cudaSuccess;
     const size_t smem = sizeof(int32_t) * static_cast<size_t>(E + 1);
-    return launch_pdl(act_quant_kernel<U, true>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), smem, stream,
+    return launch_pdl(act_quant_kernel<U, true, false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), smem, stream,
                       static_cast<const uint16_t*>(x), op, osf, total_M, K, rows, kb, kbp, nch, alg == 2 ? 1 : 0, 1,
                       offsets, E);
 }

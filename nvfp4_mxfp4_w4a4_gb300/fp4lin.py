@@ -35,6 +35,7 @@ SYMBOLS = (
     "fp4_quant_act_mxfp4_grouped", "fp4_quant_nvfp4", "fp4_gemm_mxfp4", "fp4_gemm_workspace_size",
     "fp4_gemm_mxfp4_ws", "fp4_gemm_mxfp4_noalloc", "fp4_gemm_mxfp4_grouped",
     "fp4_quant_nvfp4_ex", "fp4_sf_bytes_nvfp4", "fp4_sf_swizzle", "fp4_gemm_nvfp4",
+    "fp4_quant_act_mxfp8", "fp4_gemm_w4a8", "fp4_gemm_w4a8_workspace_size",
 )
 
 
@@ -85,6 +86,9 @@ def load(path: str = LIB_PATH):
             "fp4_sf_swizzle": (ctypes.c_int, [_p, _p, _i64, _i64, _p]),
             "fp4_gemm_nvfp4": (ctypes.c_int, [_p, _p, _p, _p, ctypes.c_float, _p, _p, _i64, _i64, _i64, _p,
                                               ctypes.c_size_t, _p]),
+            "fp4_quant_act_mxfp8": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i32, _p]),
+            "fp4_gemm_w4a8": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, ctypes.c_size_t, _p]),
+            "fp4_gemm_w4a8_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -204,6 +208,25 @@ def fp4_gemm_nvfp4(a, sa, b, sb, alpha, bias_bf16, out_bf16, M, N, K, workspace=
     st = load().fp4_gemm_nvfp4(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), float(alpha), _ptr(bias_bf16), _ptr(out_bf16),
                                M, N, K, _ptr(workspace), workspace_bytes, _stream(stream))
     _check(st, "fp4_gemm_nvfp4")
+
+
+def fp4_quant_act_mxfp8(x_bf16, out_e4m3, out_scale, M, K, sf_layout=FP4_SF_SWIZZLED, stream=None):
+    st = load().fp4_quant_act_mxfp8(_ptr(x_bf16), _ptr(out_e4m3), _ptr(out_scale), M, K, sf_layout,
+                                    _stream(stream))
+    _check(st, "fp4_quant_act_mxfp8")
+
+
+def fp4_gemm_w4a8_workspace_size(M, N, K) -> int:
+    return load().fp4_gemm_w4a8_workspace_size(M, N, K)
+
+
+def fp4_gemm_w4a8(a_e4m3, sa, b, sb, bias_bf16, out_bf16, M, N, K, workspace=None, workspace_bytes=None,
+                  stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().fp4_gemm_w4a8(_ptr(a_e4m3), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias_bf16), _ptr(out_bf16), M, N, K,
+                              _ptr(workspace), workspace_bytes, _stream(stream))
+    _check(st, "fp4_gemm_w4a8")
 
 
 def fp4_gemm_mxfp4(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, stream=None):

@@ -95,6 +95,13 @@ def test_argument_checks_precede_device_use(L):
     assert raw.fp4_sf_swizzle(None, 16, 4, 4, None) == 1
     assert raw.fp4_sf_swizzle(16, 18, 4, 4, None) == 3                                           # out 4 B
     assert raw.fp4_sf_swizzle(None, None, 0, 4, None) == 0
+    # W4A8 fallback
+    assert raw.fp4_gemm_w4a8(16, 16, 32, 16, None, 16, 1, 8, 192, None, 0, None) == 2           # K % 128
+    assert raw.fp4_gemm_w4a8(16, 16, 48, 16, None, 16, 1, 8, 128, None, 0, None) == 3           # b 32 B
+    assert raw.fp4_gemm_w4a8(16, 16, 32, 16, None, 16, 1, 8, 128, 16, 1 << 20, None) == 3       # workspace
+    assert raw.fp4_quant_act_mxfp8(16, 16, 16, 4, 48, 0, None) == 2                             # K % 32
+    assert raw.fp4_quant_act_mxfp8(16, 16, 16, 4, 32, 3, None) == 1                             # layout
+    assert raw.fp4_quant_act_mxfp8(16, 24, 16, 4, 32, 0, None) == 3                             # codes 16 B
     # empty problems are no-ops that need no device
     assert raw.fp4_quant_act_mxfp4(None, None, None, 0, 32, None, None) == 0
     assert raw.fp4_gemm_mxfp4(None, None, None, None, None, None, 0, 8, 128, None) == 0
