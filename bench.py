@@ -57,7 +57,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--breakdown-reps", type=int, default=200)
     ap.add_argument("--no-nvfp4", action="store_true",
-                    help="skip the NVFP4 x NVFP4 comparison (dense workloads)")
+                    help="skip the NVFP4 x NVFP4 and W4A8 comparisons (dense workloads)")
     return ap.parse_args()
 
 
@@ -268,6 +268,14 @@ class Act:
         else:
             self.L.fp4_quant_act_mxfp4_grouped(self.x, self.offsets, self.E, self.M, self.K, self.a_packed,
                                                self.a_scale, stream=s)
+
+    def gemm_static(self, s):
+        """The dense GEMM stating that the weights are not written by the
+        kernel before it (it streams its first weight stages early)."""
+        w = self.w
+        ws = gemm_workspace(self.L, self.torch, self.M, w.N, self.K)
+        self.L.fp4_gemm_mxfp4_ex(self.a_packed, self.a_scale, w.b_packed, w.b_scale, w.bias, self.out, self.M, w.N,
+                                 self.K, ws, flags=self.L.FP4_GEMM_WEIGHTS_STATIC, stream=s)
 
     def gemm(self, s):
         w = self.w
@@ -480,9 +488,14 @@ def run_ours(args):
         fp4_probe = {"error": str(exc)}
 
     e2e = _e2e(b, torch, L, min(args.steps, 50))
-    nvfp4 = None
+    nvfp4 = w4a8 = None
     if not args.no_nvfp4 and all(a.offsets is None for a in b.acts):
-        nvfp4 = nvfp4_comparison(b, L, torch, args.breakdown_reps, breakdown)
+        nvfp4 = side_path_comparison(b, L, torch, args.breakdown_reps, breakdown, NvAct, "nv",
+                                     "NVFP4 act-quant + NVFP4 x NVFP4 GEMM (alpha = g_x g_w, no requant) "
+                                     "vs the MXFP4 path")
+        w4a8 = side_path_comparison(b, L, torch, args.breakdown_reps, breakdown, A8Act, "a8",
+                                    "W4A8 fallback: MXFP8 act-quant + MXFP8 x MXFP4 GEMM (the same requantized "
+                                    "weight) vs the MXFP4 path")
 
     req = [breakdown[k] for k in breakdown if k.startswith("requant")]
     result = {
@@ -500,6 +513,7 @@ def run_ours(args):
                                            if "tflops" in fp4_probe else None)},
         "fp4_probe_peak": fp4_probe,
         "breakdown": breakdown, "shares": shares, "roofline": roofline, "e2e": e2e, "nvfp4_path": nvfp4,
+        "w4a8_path": w4a8,
         "gpu_launches": b.launches_per_step * steps, "clocks": clk, "wall_s_timed_region": round(t_wall, 3),
     }
     if rank == 0 and not args.no_cpu_baseline and args.workload == "decode":
@@ -542,6 +556,40 @@ class NvAct:
                               w.N, a.K, ws, stream=s)
 
 
+class A8Act:
+    """The W4A8 fallback of "W4A4 MXFP4 Quantization" on the same bf16
+    activations and the same requantized MXFP4 weight: MXFP8 act-quant,
+    then the MXFP8 x MXFP4 GEMM."""
+
+    def __init__(self, L, torch, act):
+        dev = torch.device("cuda")
+        w = act.w
+        self.L, self.act, self.w = L, act, w
+        M, K = act.M, act.K
+        self.codes = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        self.scale = torch.empty(L.fp4_sf_bytes(M, K), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((M, w.N), dtype=torch.bfloat16, device=dev)
+        need = L.fp4_gemm_w4a8_workspace_size(M, w.N, K)
+        self.ws = None if need == 0 else _w4a8_workspace(torch, need)
+
+    def quant(self, s):
+        a = self.act
+        self.L.fp4_quant_act_mxfp8(a.x, self.codes, self.scale, a.M, a.K, stream=s)
+
+    def gemm(self, s):
+        a, w = self.act, self.w
+        self.L.fp4_gemm_w4a8(self.codes, self.scale, w.b_packed, w.b_scale, w.bias, self.out, a.M, w.N, a.K,
+                             self.ws, stream=s)
+
+
+def _w4a8_workspace(torch, need):
+    ws = _WORKSPACE.get("w4a8")
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+        _WORKSPACE["w4a8"] = ws
+    return ws
+
+
 def _rel_err(out, X_bits, W_bits, bias, rows, cols):
     """||out - X W^T (+ bias)|| / ||X W^T (+ bias)|| over a row/column sample,
     the exact product of the unquantized bf16 tensors in float64."""
@@ -556,15 +604,14 @@ def _rel_err(out, X_bits, W_bits, bias, rows, cols):
     return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
 
 
-def nvfp4_comparison(b, L, torch, reps, breakdown):
-    """What the requant trades against a GPU with native NVFP4: per dense
-    GEMM of the workload, the NVFP4 act-quant and NVFP4 x NVFP4 GEMM times
-    (rotated over the same buffer sets as the breakdown) beside the MXFP4
-    ones, and both paths' output error against the unquantized bf16 product
-    on a sample."""
-    nv_sets = [[NvAct(L, torch, a) for a in acts] for _, acts in b.sets]
-    res = {"what": "NVFP4 act-quant + NVFP4 x NVFP4 GEMM (alpha = g_x g_w, no requant) vs the MXFP4 path",
-           "per_gemm": {}}
+def side_path_comparison(b, L, torch, reps, breakdown, cls, tag_prefix, what):
+    """A side path beside the MXFP4 one on the same tensors (the NVFP4 path
+    of a GPU with native NVFP4, or the W4A8 fallback): per dense GEMM of the
+    workload, its act-quant and GEMM times (rotated over the same buffer sets
+    as the breakdown) beside the MXFP4 ones, and both paths' output error
+    against the unquantized bf16 product on a sample."""
+    nv_sets = [[cls(L, torch, a) for a in acts] for _, acts in b.sets]
+    res = {"what": what, "per_gemm": {}}
     rng = np.random.default_rng(0)
     for ai, a in enumerate(b.acts):
         tag = f"M{a.M}_N{a.w.N}_K{a.K}"
@@ -574,9 +621,21 @@ def nvfp4_comparison(b, L, torch, reps, breakdown):
             r = max(1, -(-reps // b.n_sets))
             b.time_graph(g, 1)
             t = b.time_graph(g, r) / (r * b.n_sets) * 1e-3
-            entry[f"nv_{kind}_us"] = round(t * 1e6, 2)
+            entry[f"{tag_prefix}_{kind}_us"] = round(t * 1e6, 2)
             if kind == "gemm":
-                entry["nv_gemm_TFLOPS"] = round(a.flops / t / 1e12, 2)
+                entry[f"{tag_prefix}_gemm_TFLOPS"] = round(a.flops / t / 1e12, 2)
+        # the two launches back to back on one stream, as a serving step runs
+        # them (the GEMM's prologue overlaps the quantizer's tail)
+        g = b.graph(lambda s, i, ai=ai: (nv_sets[i][ai].quant(s), nv_sets[i][ai].gemm(s)))
+        r = max(1, -(-reps // b.n_sets))
+        b.time_graph(g, 1)
+        entry[f"{tag_prefix}_chain_us"] = round(b.time_graph(g, r) / (r * b.n_sets) * 1e3, 2)
+        g = b.graph(lambda s, i, ai=ai: (b.sets[i][1][ai].quant(s), b.sets[i][1][ai].gemm(s)))
+        b.time_graph(g, 1)
+        entry["mx_chain_us"] = round(b.time_graph(g, r) / (r * b.n_sets) * 1e3, 2)
+        g = b.graph(lambda s, i, ai=ai: (b.sets[i][1][ai].quant(s), b.sets[i][1][ai].gemm_static(s)))
+        b.time_graph(g, 1)
+        entry["mx_chain_static_w_us"] = round(b.time_graph(g, r) / (r * b.n_sets) * 1e3, 2)
         entry["mx_quant_us"] = breakdown[f"act_quant_{tag}"]["us"]
         entry["mx_gemm_us"] = breakdown[f"gemm_{tag}"]["us"]
         # accuracy on one set: both paths from the same bf16 tensors
@@ -591,7 +650,7 @@ def nvfp4_comparison(b, L, torch, reps, breakdown):
         rows = np.sort(rng.choice(a.M, min(a.M, 128), replace=False))
         cols = np.sort(rng.choice(a.w.N, min(a.w.N, 512), replace=False))
         entry["mx_rel_err"] = round(_rel_err(a.out, X_bits, a.w.bf16_host, a.w.bias, rows, cols), 5)
-        entry["nv_rel_err"] = round(_rel_err(nv.out, X_bits, a.w.bf16_host, a.w.bias, rows, cols), 5)
+        entry[f"{tag_prefix}_rel_err"] = round(_rel_err(nv.out, X_bits, a.w.bf16_host, a.w.bias, rows, cols), 5)
         res["per_gemm"][tag] = entry
     res["requant_once_per_load_us"] = round(sum(v["us"] for k, v in breakdown.items() if k.startswith("requant")), 2)
     res["sample"] = "rel. Frobenius error over <=128 rows x 512 columns, reference = bf16 X W^T in float64"

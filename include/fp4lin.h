@@ -259,6 +259,28 @@ FP4LIN_API fp4_status fp4_gemm_mxfp4_ws(const uint8_t* a, const uint8_t* sa, con
                              int64_t M, int64_t N, int64_t K, void* workspace,
                              size_t workspace_bytes, void* stream);
 
+/* Flags of fp4_gemm_mxfp4_ex. */
+#define FP4_GEMM_WEIGHTS_STATIC 1u
+
+/* fp4_gemm_mxfp4_ws with flags (0 gives fp4_gemm_mxfp4_ws exactly).
+ *   FP4_GEMM_WEIGHTS_STATIC  the caller states that b and sb are not written
+ *     by the kernel enqueued immediately before this call on `stream`
+ *     (typically the activation quantizer of a serving step; the weights
+ *     were written by work that has finished).  The library launches its
+ *     kernels with programmatic stream serialization, so a GEMM starts while
+ *     the previous kernel finishes; with this flag it streams the first
+ *     pipeline stages of its weights in that window and waits for the
+ *     previous kernel only before reading the activations.  Do not set it
+ *     when the previous kernel writes the weights (e.g. the requantization
+ *     of the same weights just before the GEMM): the GEMM could read them
+ *     before they are written.
+ * Other flag bits: FP4_ERR_INVALID_ARG.  Otherwise as fp4_gemm_mxfp4_ws
+ * (bit-identical results).                                                  */
+FP4LIN_API fp4_status fp4_gemm_mxfp4_ex(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
+                             const uint8_t* sb, const void* bias_bf16, void* out_bf16,
+                             int64_t M, int64_t N, int64_t K, void* workspace,
+                             size_t workspace_bytes, uint32_t flags, void* stream);
+
 /* fp4_gemm_mxfp4_ws for callers that cannot provide device memory (a host
  * program holding no device allocator of its own, or a runtime that must
  * not allocate on its request path).  The pages have no counterpart: it

@@ -283,7 +283,7 @@ fp4_status fp4_sf_swizzle(const uint8_t* in_rowmajor, uint8_t* out, int64_t rows
 static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                               const void* bias, void* out, const int32_t* offsets, int32_t E, int64_t M, int64_t N,
                               int64_t K, void* workspace, size_t workspace_bytes, void* stream,
-                              int fmt = fp4lin::kGemmMx, float alpha = 1.0f)
+                              int fmt = fp4lin::kGemmMx, float alpha = 1.0f, uint32_t flags = 0)
 {
     if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 8 != 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
         return FP4_ERR_SHAPE;
@@ -317,6 +317,7 @@ static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t
     args.workspace_bytes = workspace ? workspace_bytes : 0;
     args.fmt = fmt;
     args.alpha = alpha;
+    args.early_weights = (flags & FP4_GEMM_WEIGHTS_STATIC) != 0;
     return from_cuda(fp4lin::launch_gemm(args, static_cast<cudaStream_t>(stream)));
 }
 
@@ -390,6 +391,18 @@ fp4_status fp4_quant_act_mxfp8(const void* x_bf16, uint8_t* out_e4m3, uint8_t* o
         return st;
     return from_cuda(fp4lin::launch_act_quant_mxfp8(x_bf16, out_e4m3, out_scale, M, K, swz ? 1 : 0,
                                                     static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status fp4_gemm_mxfp4_ex(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                             const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
+                             size_t workspace_bytes, uint32_t flags, void* stream)
+{
+    if (flags & ~static_cast<uint32_t>(FP4_GEMM_WEIGHTS_STATIC))
+        return FP4_ERR_INVALID_ARG;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FP4_ERR_ALIGNMENT;
+    return gemm_common(a, sa, b, sb, bias_bf16, out_bf16, nullptr, 1, M, N, K, workspace, workspace_bytes, stream,
+                       fp4lin::kGemmMx, 1.0f, flags);
 }
 
 fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,

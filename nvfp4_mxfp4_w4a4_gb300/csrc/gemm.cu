@@ -98,6 +98,7 @@ struct GemmParams {
     int ldo;                    // output row stride (elements) = the problem's N
     int64_t sfb_expert_stride;
     float alpha;                // NVFP4 mode: factor on the accumulator before the bias
+    int early_w;                // weights not written by the kernel this one may overlap
     unsigned int* status;
 };
 
@@ -321,9 +322,41 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
     const int total_tiles = p.m_tiles * p.n_tiles;
     const int nkb = (p.kb4 + C::GROUPS - 1) / C::GROUPS;  // stages per tile
 
+    // Loads of one stage (producer thread): the weight half (the MMA-M
+    // operand when swapped, else the MMA-N one, with its scale chunks), the
+    // activation half, or both; `expect` posts the whole stage's bytes.
+    enum { kHalfW = 1, kHalfX = 2 };
+    auto stage_loads = [&](int s, int kb, const Tile& T, int halves, bool expect) {
+        const int64_t b_row0 = static_cast<int64_t>(T.expert) * p.rows_b + T.n0;
+        const uint8_t* sfb = p.sfb + static_cast<int64_t>(T.expert) * p.sfb_expert_stride;
+        int nsfb = (p.rows_b + 127) / 128 - T.n0 / 128;
+        nsfb = nsfb < C::SFB_TILES ? nsfb : C::SFB_TILES;
+        const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
+        const uint32_t sf_bytes = static_cast<uint32_t>(groups * C::APG) * 512u;
+        const int64_t atoms_per_rt = static_cast<int64_t>(p.kb4) * C::APG;  // chunks per 128-row tile
+        // boxes past the end of K or of the rows are zero-filled and still counted
+        if (expect)
+            mbar_arrive_expect_tx(&full[s], C::A_TX + C::B_TX + sf_bytes * (1u + nsfb));
+        const int a_half = kSwap ? kHalfW : kHalfX;
+        if (halves & a_half) {
+            load_operand<KC>(smem + C::OFF_A + s * C::A_BYTES, &tmA, &full[s], kb, T.a_row0);
+            bulk_load(smem + C::OFF_SFA + s * C::SFA_BYTES, p.sfa + (T.sfa_rt * atoms_per_rt + C::ATOMS * kb) * 512,
+                      sf_bytes, &full[s]);
+        }
+        if (halves & (kHalfW | kHalfX) & ~a_half) {
+            load_operand<KC>(smem + C::OFF_B + s * C::B_BYTES, &tmB, &full[s], kb, b_row0);
+            for (int j = 0; j < nsfb; ++j)
+                bulk_load(smem + C::OFF_SFB + s * C::SFB_BYTES + j * C::ATOMS * 512,
+                          sfb + ((T.n0 / 128 + j) * atoms_per_rt + C::ATOMS * kb) * 512, sf_bytes, &full[s]);
+        }
+    };
+
     // ------------------------------------------------------------ setup
     // (no global memory is touched before the dependency wait: this part
-    // overlaps the previous kernel in the stream)
+    // overlaps the previous kernel in the stream -- except, when the caller
+    // states that the weights are not written by that kernel, the weight
+    // half of the first stages of this CTA's first tile)
+    int npre = 0;  // producer thread: stages whose weight half is already in flight
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -336,6 +369,18 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
         tma_prefetch_map(&tmO);
+        if constexpr (!kGrouped) {
+            if (p.early_w) {
+                WorkIter wi = work_begin(p, total_tiles);
+                Work w;
+                if (work_next(wi, nkb, w)) {
+                    const Tile T = decode_tile<BN, false>(w.t, p, nullptr);
+                    npre = min(STAGES, w.kb1 - w.kb0);
+                    for (int i = 0; i < npre; ++i)
+                        stage_loads(i, w.kb0 + i, T, kHalfW, true);
+                }
+            }
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -386,29 +431,19 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                     const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
                     if (!T.valid)
                         continue;
-                    const int64_t b_row0 = static_cast<int64_t>(T.expert) * p.rows_b + T.n0;
-                    const uint8_t* sfb = p.sfb + static_cast<int64_t>(T.expert) * p.sfb_expert_stride;
-                    int nsfb = (p.rows_b + 127) / 128 - T.n0 / 128;
-                    nsfb = nsfb < C::SFB_TILES ? nsfb : C::SFB_TILES;
                     for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                         const int s = static_cast<int>(it % STAGES);
                         const uint32_t ph = (it / STAGES) & 1u;
+                        if (static_cast<int>(it) < npre) {
+                            // weight half issued before the dependency wait (first pass over the ring)
+                            stage_loads(s, kb, T, kHalfX, false);
+                            continue;
+                        }
                         if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kStatusTimeout, kWaitLimitNs)) {
                             ok = false;
                             break;
                         }
-                        const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
-                        const uint32_t sf_bytes = static_cast<uint32_t>(groups * C::APG) * 512u;
-                        const int64_t atoms_per_rt = static_cast<int64_t>(p.kb4) * C::APG;  // chunks per 128-row tile
-                        // boxes past the end of K or of the rows are zero-filled and still counted
-                        mbar_arrive_expect_tx(&full[s], C::A_TX + C::B_TX + sf_bytes * (1u + nsfb));
-                        load_operand<KC>(smem + C::OFF_A + s * C::A_BYTES, &tmA, &full[s], kb, T.a_row0);
-                        load_operand<KC>(smem + C::OFF_B + s * C::B_BYTES, &tmB, &full[s], kb, b_row0);
-                        bulk_load(smem + C::OFF_SFA + s * C::SFA_BYTES,
-                                  p.sfa + (T.sfa_rt * atoms_per_rt + C::ATOMS * kb) * 512, sf_bytes, &full[s]);
-                        for (int j = 0; j < nsfb; ++j)
-                            bulk_load(smem + C::OFF_SFB + s * C::SFB_BYTES + j * C::ATOMS * 512,
-                                      sfb + ((T.n0 / 128 + j) * atoms_per_rt + C::ATOMS * kb) * 512, sf_bytes, &full[s]);
+                        stage_loads(s, kb, T, kHalfW | kHalfX, true);
                     }
                 }
             }
@@ -868,6 +903,7 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
     p.ldo = static_cast<int>(a.N);
     p.sfb_expert_stride = ((a.N + 127) / 128) * 128 * (a.K / (kNv ? 16 : 32));
     p.alpha = a.alpha;
+    p.early_w = (a.early_weights && !kGrouped) ? 1 : 0;
     p.status = a.status;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (tiles == 0)
@@ -968,8 +1004,10 @@ cudaError_t launch_gemm_nvfp4(const GemmArgs& a, cudaStream_t stream)
 // slabs covers 128 KC elements of K; the 3-D view needs only K % 128 == 0.
 cudaError_t launch_gemm_w4a8(const GemmArgs& a, cudaStream_t stream)
 {
+    // the expanded FP4 weight tile takes twice its bytes in shared memory:
+    // as many stages as fit keep the weight stream in flight
     if (a.M <= 64)
-        return a.M <= 32 ? launch_kernel<32, 4, 2, 4, true, false, kFmtA8>(a, stream)
+        return a.M <= 32 ? launch_kernel<32, 5, 2, 4, true, false, kFmtA8>(a, stream)
                          : launch_kernel<64, 4, 2, 4, true, false, kFmtA8>(a, stream);
     const bool wide = a.N >= 256 && ((a.M + 127) / 128) * ((a.N + 255) / 256) >= 148;
     if (wide)

@@ -89,6 +89,7 @@ struct GemmArgs {
     size_t workspace_bytes;
     int fmt = 0;                 // GemmFormat
     float alpha = 1.0f;          // NVFP4: factor on the accumulator before the bias
+    bool early_weights = false;  // the weights are not written by the preceding kernel in the stream
 };
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);

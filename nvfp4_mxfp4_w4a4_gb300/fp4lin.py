@@ -35,7 +35,7 @@ SYMBOLS = (
     "fp4_quant_act_mxfp4_grouped", "fp4_quant_nvfp4", "fp4_gemm_mxfp4", "fp4_gemm_workspace_size",
     "fp4_gemm_mxfp4_ws", "fp4_gemm_mxfp4_noalloc", "fp4_gemm_mxfp4_grouped",
     "fp4_quant_nvfp4_ex", "fp4_sf_bytes_nvfp4", "fp4_sf_swizzle", "fp4_gemm_nvfp4",
-    "fp4_quant_act_mxfp8", "fp4_gemm_w4a8", "fp4_gemm_w4a8_workspace_size",
+    "fp4_quant_act_mxfp8", "fp4_gemm_w4a8", "fp4_gemm_w4a8_workspace_size", "fp4_gemm_mxfp4_ex",
 )
 
 
@@ -89,6 +89,8 @@ def load(path: str = LIB_PATH):
             "fp4_quant_act_mxfp8": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _i32, _p]),
             "fp4_gemm_w4a8": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, ctypes.c_size_t, _p]),
             "fp4_gemm_w4a8_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64]),
+            "fp4_gemm_mxfp4_ex": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, ctypes.c_size_t,
+                                                 ctypes.c_uint32, _p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -246,6 +248,21 @@ def fp4_gemm_mxfp4_ws(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, workspace, wor
     st = load().fp4_gemm_mxfp4_ws(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias_bf16), _ptr(out_bf16), M, N, K,
                                   _ptr(workspace), workspace_bytes, _stream(stream))
     _check(st, "fp4_gemm_mxfp4_ws")
+
+
+FP4_GEMM_WEIGHTS_STATIC = 1
+
+
+def fp4_gemm_mxfp4_ex(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, workspace=None, workspace_bytes=None, flags=0,
+                      stream=None):
+    """flags: FP4_GEMM_WEIGHTS_STATIC when b / sb are not written by the kernel
+    enqueued just before this call (the GEMM then streams its first weight
+    stages while that kernel finishes)."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().fp4_gemm_mxfp4_ex(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias_bf16), _ptr(out_bf16), M, N, K,
+                                  _ptr(workspace), workspace_bytes, flags, _stream(stream))
+    _check(st, "fp4_gemm_mxfp4_ex")
 
 
 def fp4_gemm_mxfp4_noalloc(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, stream=None):

@@ -95,6 +95,8 @@ def test_argument_checks_precede_device_use(L):
     assert raw.fp4_sf_swizzle(None, 16, 4, 4, None) == 1
     assert raw.fp4_sf_swizzle(16, 18, 4, 4, None) == 3                                           # out 4 B
     assert raw.fp4_sf_swizzle(None, None, 0, 4, None) == 0
+    assert raw.fp4_gemm_mxfp4_ex(16, 16, 16, 16, None, 16, 1, 8, 128, None, 0, 2, None) == 1     # unknown flag
+    assert raw.fp4_gemm_mxfp4_ex(16, 16, 16, 16, None, 16, 1, 8, 100, None, 0, 1, None) == 2     # K % 128
     # W4A8 fallback
     assert raw.fp4_gemm_w4a8(16, 16, 32, 16, None, 16, 1, 8, 192, None, 0, None) == 2           # K % 128
     assert raw.fp4_gemm_w4a8(16, 16, 48, 16, None, 16, 1, 8, 128, None, 0, None) == 3           # b 32 B
