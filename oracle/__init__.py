@@ -65,6 +65,9 @@ def lib():
                 ("orc_requant", None, [_p, _p, ctypes.c_float, _i64, _i64, _i64, ctypes.c_int, _p, _p]),
                 ("orc_act_quant", None, [_p, _i64, _i64, _i64, ctypes.c_int, _p, _p]),
                 ("orc_gemm", None, [_p, _p, _p, _p, _p, _i64, _p, _i64, _p, _i64, _p, _p]),
+                ("orc_bf16_encode", ctypes.c_uint16, [ctypes.c_float]),
+                ("orc_smooth_prepare", _i64, [_p, _i64, _p]),
+                ("orc_smooth_apply", None, [_p, _p, _i64, _i64, _p]),
                 ("orc_mx8_shared_exp", ctypes.c_int, [ctypes.c_double]),
                 ("orc_act_quant_mxfp8", None, [_p, _i64, _i64, _i64, _p, _p]),
                 ("orc_gemm_w4a8", None, [_p, _p, _p, _p, _p, _i64, _p, _i64, _p, _i64, _p, _p]),
@@ -209,6 +212,28 @@ def gemm(a, sa, b, sb, bias_bf16_bits=None, rows=None, cols=None, threads=1):
 
     _parallel(run, len(rows), threads)
     return ref, absum
+
+
+def bf16_encode(f: float) -> int:
+    return lib().orc_bf16_encode(float(f))
+
+
+def smooth_prepare(mul_scale_f32):
+    """float32 [K] -> (bf16 bits [K], count of rejected values)."""
+    m = np.ascontiguousarray(mul_scale_f32, np.float32)
+    out = np.empty(m.shape, np.uint16)
+    bad = lib().orc_smooth_prepare(_ptr(m), m.size, _ptr(out))
+    return out, int(bad)
+
+
+def smooth_apply(x_bf16_bits, m_bf16_bits):
+    """bf16(x * m) per element, m per input channel (bf16 bits)."""
+    x = np.ascontiguousarray(x_bf16_bits, np.uint16)
+    m = np.ascontiguousarray(m_bf16_bits, np.uint16)
+    rows, K = x.shape
+    out = np.empty_like(x)
+    lib().orc_smooth_apply(_ptr(x), _ptr(m), rows, K, _ptr(out))
+    return out
 
 
 def mx8_shared_exp(amax: float) -> int:

@@ -70,6 +70,22 @@ double orc_bf16_value(uint16_t bits)
     return (double)f;
 }
 
+/* float32 -> bf16, round to nearest, ties to even (the upper half of the
+ * float32 pattern after rounding); NaN stays NaN (quiet), overflow gives
+ * Inf.                                                                    */
+uint16_t orc_bf16_encode(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if (isnan(f))
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lower = u & 0xFFFFu;
+    uint32_t upper = u >> 16;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))
+        upper += 1u;                  /* carries into the exponent as it should */
+    return (uint16_t)upper;
+}
+
 /* Round to the nearest E2M1 value, ties to the even code, saturating at 6
  * ([OMNI] Single-Scale Block Scaling: round_mode "rint"; the largest finite
  * E2M1 value is 6).  Brute force over the eight magnitudes; the sign bit of
@@ -228,6 +244,38 @@ void orc_act_quant(const uint16_t* x_bf16, int64_t row0, int64_t row1, int64_t K
                 v[i] = (float)orc_bf16_value(x_bf16[r * K + 32 * b + i]);
             orc_mx_quantize_block(v, alg, out_packed + r * (K / 2) + 16 * b,
                                   out_sf + r * (K / 32) + b);
+        }
+}
+
+/* ------------------------------------------------------------------------
+ * Smooth pre-scale ([OMNI] "Pre-Quantized Single-Scale Weights"): both the
+ * W4A4 and the W4A8 path quantize x * mul_scale, a per-input-channel float32
+ * tensor converted to the activation dtype (bf16) after loading; NaN, Inf,
+ * non-positive values and values that overflow or underflow to zero in bf16
+ * are rejected.  The product is taken in the activation dtype: bf16(x * m)
+ * with m the bf16 scale (x * m of two bf16 values is exact in float32, then
+ * one rounding to bf16).                                                  */
+int64_t orc_smooth_prepare(const float* mul_scale, int64_t K, uint16_t* out_bf16)
+{
+    int64_t bad = 0;
+    for (int64_t k = 0; k < K; ++k) {
+        float m = mul_scale[k];
+        uint16_t b = orc_bf16_encode(m);
+        double v = orc_bf16_value(b);
+        out_bf16[k] = b;
+        if (!(m > 0.0f) || isinf(m) || isinf(v) || v == 0.0)
+            ++bad;
+    }
+    return bad;
+}
+
+void orc_smooth_apply(const uint16_t* x_bf16, const uint16_t* m_bf16, int64_t rows, int64_t K,
+                      uint16_t* out_bf16)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t k = 0; k < K; ++k) {
+            float p = (float)(orc_bf16_value(x_bf16[r * K + k]) * orc_bf16_value(m_bf16[k]));
+            out_bf16[r * K + k] = orc_bf16_encode(p);
         }
 }
 

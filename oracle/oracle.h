@@ -36,6 +36,7 @@ double orc_e4m3_value(unsigned byte);         /* float8_e4m3fn -> value   */
 double orc_e8m0_value(unsigned byte);         /* E8M0 -> 2^(b-127) or NaN */
 double orc_bf16_value(uint16_t bits);         /* bf16 -> value            */
 unsigned orc_e2m1_encode(double q);           /* nearest, ties to even code, saturating, sign copied */
+uint16_t orc_bf16_encode(float f);            /* float32 -> bf16, nearest, ties to even */
 unsigned orc_e4m3_encode(float t);            /* t >= 0: nearest finite, ties to even code, saturating at 448 */
 
 /* ---- MX shared exponent ([OMNI] Single-Scale Block Scaling) ----------- */
@@ -66,6 +67,14 @@ void orc_gemm(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8
               const uint16_t* bias_bf16, int64_t K,
               const int64_t* rows, int64_t n_rows, const int64_t* cols, int64_t n_cols,
               double* ref, double* absum);
+
+/* ---- Smooth pre-scale ([OMNI] Pre-Quantized Single-Scale Weights) ------ */
+/* mul_scale float32 [K] -> bf16 [K]; returns the count of rejected values
+ * (NaN, Inf, <= 0, or overflow / underflow to zero in bf16).               */
+int64_t orc_smooth_prepare(const float* mul_scale, int64_t K, uint16_t* out_bf16);
+/* out = bf16(x * m) per element (m per input channel, bf16).               */
+void orc_smooth_apply(const uint16_t* x_bf16, const uint16_t* m_bf16, int64_t rows, int64_t K,
+                      uint16_t* out_bf16);
 
 /* ---- W4A8 fallback ([OMNI] W4A8 fallback, Single-Scale Block Scaling) --- */
 /* OCP MX exponent for float8_e4m3fn elements: floor(log2 amax) - 8, clamped. */

@@ -332,6 +332,47 @@ def test_gemm_one_hot_selects_columns(orc):
     assert np.array_equal(ref, A[:, sel])
 
 
+# ------------------------------------------------------ smooth pre-scale
+
+
+def test_bf16_encode_matches_torch(orc):
+    rng = np.random.default_rng(61)
+    vals = np.concatenate([
+        rng.standard_normal(3000).astype(np.float32) * np.exp(rng.uniform(-40, 40, 3000)).astype(np.float32),
+        # exact ties: bf16 values plus half an ulp
+        (torch.randn(500).to(torch.bfloat16).float().numpy().view(np.uint32) | 0x8000).view(np.float32),
+        np.array([0.0, -0.0, 3.4e38, -3.4e38, 1e-45, np.inf, -np.inf, 3.3895314e38], np.float32),
+    ])
+    got = np.array([orc.bf16_encode(float(v)) for v in vals], np.uint16)
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+    assert orc.bf16_encode(float("nan")) & 0x7FC0 == 0x7FC0
+
+
+def test_smooth_prepare_rejects_what_the_page_rejects(orc):
+    """NaN, Inf, non-positive values and values that overflow or underflow to
+    zero in bf16 are rejected; the rest convert to bf16 as torch does."""
+    good = np.array([1.0, 0.5, 3.0, 1e-30, 2.5e38, 7.1234], np.float32)
+    out, bad = orc.smooth_prepare(good)
+    assert bad == 0
+    assert np.array_equal(out, torch.from_numpy(good).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    for v in (np.nan, np.inf, -np.inf, 0.0, -0.0, -1.0, 1e-45, 3.4e38):
+        _, bad = orc.smooth_prepare(np.array([1.0, v, 2.0], np.float32))
+        assert bad == 1, v
+
+
+def test_smooth_apply_matches_torch_bf16_multiply(orc):
+    rng = np.random.default_rng(67)
+    M, K = 7, 96
+    x = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32) * 3).to(torch.bfloat16)
+    m = torch.from_numpy(np.exp(rng.uniform(-3, 3, K)).astype(np.float32)).to(torch.bfloat16)
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    mb = m.view(torch.int16).numpy().view(np.uint16)
+    got = orc.smooth_apply(xb, mb)
+    ref = (x * m).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
 # ------------------------------------------------------ W4A8: MXFP8 activations
 
 
