@@ -171,6 +171,33 @@ FP4LIN_API fp4_status fp4_quant_act_mxfp4_grouped(const void* x_bf16, const int3
                                        uint8_t* out_scale, const fp4_quant_opts* opts,
                                        void* stream);
 
+/* ------------------------------------------------------ smooth pre-scale */
+
+/* The Smooth pre-scale of [OMNI] "Pre-Quantized Single-Scale Weights": both
+ * the W4A4 and the W4A8 path quantize x * mul_scale, a per-input-channel
+ * float32 tensor converted to the activation dtype (bf16) after loading.
+ * fp4_smooth_prepare converts it (round to nearest even) and counts the
+ * values loading must reject -- NaN, Inf, non-positive, or overflowing /
+ * underflowing to zero in bf16 -- into *bad_count (device int32, written
+ * by this call; read it after the stream reaches this point, and reject the
+ * tensor when it is not 0).
+ *   mul_scale  float32 [K] (device), out_bf16 bf16 [K] (device)
+ * Requires K >= 1.                                                         */
+FP4LIN_API fp4_status fp4_smooth_prepare(const float* mul_scale, void* out_bf16, int64_t K,
+                              int32_t* bad_count, void* stream);
+
+/* fp4_quant_act_mxfp4 / fp4_quant_act_mxfp8 of bf16(x * mul_scale): each
+ * element times its channel's bf16 scale, the exact float32 product rounded
+ * once to bf16, then the quantizer.  mul_scale_bf16: [K] bf16 (device,
+ * 16-byte aligned), as fp4_smooth_prepare writes it.  Otherwise the rules
+ * of the plain calls.                                                      */
+FP4LIN_API fp4_status fp4_quant_act_mxfp4_smooth(const void* x_bf16, const void* mul_scale_bf16,
+                                      uint8_t* out_packed, uint8_t* out_scale, int64_t M,
+                                      int64_t K, const fp4_quant_opts* opts, void* stream);
+FP4LIN_API fp4_status fp4_quant_act_mxfp8_smooth(const void* x_bf16, const void* mul_scale_bf16,
+                                      uint8_t* out_e4m3, uint8_t* out_scale, int64_t M, int64_t K,
+                                      int32_t sf_layout, void* stream);
+
 /* ----------------------------------------------------------- NVFP4 producer */
 
 /* bf16 -> NVFP4 with a caller-given global scale g (the NVFP4 quantize

@@ -191,8 +191,8 @@ fp4_status fp4_requant_nvfp4_to_mxfp4_grouped(const uint8_t* w_packed, const uin
                                                     alg, swz, static_cast<cudaStream_t>(stream)));
 }
 
-fp4_status fp4_quant_act_mxfp4(const void* x_bf16, uint8_t* out_packed, uint8_t* out_scale, int64_t M, int64_t K,
-                               const fp4_quant_opts* opts, void* stream)
+static fp4_status act_quant_common(const void* x_bf16, const void* mul, uint8_t* out_packed, uint8_t* out_scale,
+                                   int64_t M, int64_t K, const fp4_quant_opts* opts, void* stream)
 {
     int alg, swz;
     fp4_status st = check_opts(opts, &alg, &swz);
@@ -204,12 +204,28 @@ fp4_status fp4_quant_act_mxfp4(const void* x_bf16, uint8_t* out_packed, uint8_t*
         return FP4_OK;
     if (!x_bf16 || !out_packed || !out_scale)
         return FP4_ERR_INVALID_ARG;
-    if (!aligned16(x_bf16) || !aligned16(out_packed) || (swz && (reinterpret_cast<uintptr_t>(out_scale) & 3u)))
+    if (!aligned16(x_bf16) || !aligned16(out_packed) || (swz && (reinterpret_cast<uintptr_t>(out_scale) & 3u)) ||
+        (mul && !aligned16(mul)))
         return FP4_ERR_ALIGNMENT;
     if ((st = current_device(nullptr)) != FP4_OK)
         return st;
-    return from_cuda(
-        fp4lin::launch_act_quant(x_bf16, out_packed, out_scale, M, K, alg, swz, static_cast<cudaStream_t>(stream)));
+    return from_cuda(fp4lin::launch_act_quant(x_bf16, out_packed, out_scale, M, K, alg, swz,
+                                              static_cast<cudaStream_t>(stream), mul));
+}
+
+fp4_status fp4_quant_act_mxfp4(const void* x_bf16, uint8_t* out_packed, uint8_t* out_scale, int64_t M, int64_t K,
+                               const fp4_quant_opts* opts, void* stream)
+{
+    return act_quant_common(x_bf16, nullptr, out_packed, out_scale, M, K, opts, stream);
+}
+
+fp4_status fp4_quant_act_mxfp4_smooth(const void* x_bf16, const void* mul_scale_bf16, uint8_t* out_packed,
+                                      uint8_t* out_scale, int64_t M, int64_t K, const fp4_quant_opts* opts,
+                                      void* stream)
+{
+    if (!mul_scale_bf16 && M > 0)
+        return FP4_ERR_INVALID_ARG;
+    return act_quant_common(x_bf16, mul_scale_bf16, out_packed, out_scale, M, K, opts, stream);
 }
 
 fp4_status fp4_quant_act_mxfp4_grouped(const void* x_bf16, const int32_t* row_offsets, int32_t E, int64_t total_M,
@@ -372,8 +388,8 @@ fp4_status fp4_gemm_w4a8(const uint8_t* a_e4m3, const uint8_t* sa, const uint8_t
                        stream, fp4lin::kGemmW4A8);
 }
 
-fp4_status fp4_quant_act_mxfp8(const void* x_bf16, uint8_t* out_e4m3, uint8_t* out_scale, int64_t M, int64_t K,
-                               int32_t sf_layout, void* stream)
+static fp4_status act_quant8_common(const void* x_bf16, const void* mul, uint8_t* out_e4m3, uint8_t* out_scale,
+                                    int64_t M, int64_t K, int32_t sf_layout, void* stream)
 {
     if (M < 0 || K <= 0 || K % 32 != 0 || M >= kMaxDim || K >= kMaxDim)
         return FP4_ERR_SHAPE;
@@ -384,13 +400,44 @@ fp4_status fp4_quant_act_mxfp8(const void* x_bf16, uint8_t* out_e4m3, uint8_t* o
     if (!x_bf16 || !out_e4m3 || !out_scale)
         return FP4_ERR_INVALID_ARG;
     const bool swz = sf_layout == FP4_SF_SWIZZLED;
-    if (!aligned16(x_bf16) || !aligned16(out_e4m3) || (swz && (reinterpret_cast<uintptr_t>(out_scale) & 3u)))
+    if (!aligned16(x_bf16) || !aligned16(out_e4m3) || (swz && (reinterpret_cast<uintptr_t>(out_scale) & 3u)) ||
+        (mul && !aligned16(mul)))
         return FP4_ERR_ALIGNMENT;
     fp4_status st;
     if ((st = current_device(nullptr)) != FP4_OK)
         return st;
     return from_cuda(fp4lin::launch_act_quant_mxfp8(x_bf16, out_e4m3, out_scale, M, K, swz ? 1 : 0,
-                                                    static_cast<cudaStream_t>(stream)));
+                                                    static_cast<cudaStream_t>(stream), mul));
+}
+
+fp4_status fp4_quant_act_mxfp8(const void* x_bf16, uint8_t* out_e4m3, uint8_t* out_scale, int64_t M, int64_t K,
+                               int32_t sf_layout, void* stream)
+{
+    return act_quant8_common(x_bf16, nullptr, out_e4m3, out_scale, M, K, sf_layout, stream);
+}
+
+fp4_status fp4_quant_act_mxfp8_smooth(const void* x_bf16, const void* mul_scale_bf16, uint8_t* out_e4m3,
+                                      uint8_t* out_scale, int64_t M, int64_t K, int32_t sf_layout, void* stream)
+{
+    if (!mul_scale_bf16 && M > 0)
+        return FP4_ERR_INVALID_ARG;
+    return act_quant8_common(x_bf16, mul_scale_bf16, out_e4m3, out_scale, M, K, sf_layout, stream);
+}
+
+fp4_status fp4_smooth_prepare(const float* mul_scale, void* out_bf16, int64_t K, int32_t* bad_count, void* stream)
+{
+    if (K <= 0 || K >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    if (!mul_scale || !out_bf16 || !bad_count)
+        return FP4_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(mul_scale) & 3u) || (reinterpret_cast<uintptr_t>(out_bf16) & 1u) ||
+        (reinterpret_cast<uintptr_t>(bad_count) & 3u))
+        return FP4_ERR_ALIGNMENT;
+    fp4_status st;
+    if ((st = current_device(nullptr)) != FP4_OK)
+        return st;
+    return from_cuda(fp4lin::launch_smooth_prepare(mul_scale, out_bf16, K, bad_count,
+                                                   static_cast<cudaStream_t>(stream)));
 }
 
 fp4_status fp4_gemm_mxfp4_ex(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,

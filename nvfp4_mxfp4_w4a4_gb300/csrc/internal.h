@@ -51,12 +51,16 @@ cudaError_t launch_requant_grouped(const uint8_t* wp, const uint8_t* ws, const f
 bool requant_flat_ok(const uint8_t* wp, const uint8_t* ws, const uint8_t* op, const uint8_t* osf, int64_t K,
                      int swizzled);
 
+// mul: bf16 [K] smooth pre-scale or null.
 cudaError_t launch_act_quant(const void* x, uint8_t* op, uint8_t* osf, int64_t M, int64_t K, int alg,
-                             int swizzled, cudaStream_t stream);
+                             int swizzled, cudaStream_t stream, const void* mul = nullptr);
 
 // bf16 -> MXFP8 (E4M3 codes [M, K], E8M0 per 32, OCP rule) for the W4A8 path.
 cudaError_t launch_act_quant_mxfp8(const void* x, uint8_t* op, uint8_t* osf, int64_t M, int64_t K, int swizzled,
-                                   cudaStream_t stream);
+                                   cudaStream_t stream, const void* mul = nullptr);
+
+// Smooth pre-scale: float32 [K] -> bf16 [K], *bad = count of rejected values.
+cudaError_t launch_smooth_prepare(const float* m, void* out, int64_t K, int32_t* bad, cudaStream_t stream);
 
 cudaError_t launch_act_quant_grouped(const void* x, const int32_t* offsets, int E, int64_t total_M,
                                      int64_t K, uint8_t* op, uint8_t* osf, int alg, cudaStream_t stream);

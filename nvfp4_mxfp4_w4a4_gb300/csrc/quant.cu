@@ -515,6 +515,46 @@ __device__ __forceinline__ uint2 act_quant_lane8(uint4 v, uint32_t& sf)
     return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
 }
 
+// Eight bf16 times eight bf16, each product rounded once to bf16 (the exact
+// float32 product of two bf16 values, then round to nearest even).
+__device__ __forceinline__ uint4 smooth_bf16x8(uint4 x, uint4 m)
+{
+    const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+    const uint32_t mw[4] = {m.x, m.y, m.z, m.w};
+    uint32_t r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float lo = __fmul_rn(__uint_as_float(xw[j] << 16), __uint_as_float(mw[j] << 16));
+        const float hi = __fmul_rn(__uint_as_float(xw[j] & 0xFFFF0000u), __uint_as_float(mw[j] & 0xFFFF0000u));
+        const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+        r[j] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+// Smooth pre-scale preparation: float32 [K] -> bf16 [K] (nearest even) and
+// a count of the values the serving path must reject (NaN, Inf, <= 0, or
+// overflow / underflow to zero in bf16), added to *bad.
+__global__ void __launch_bounds__(kThreads) smooth_prepare_kernel(const float* __restrict__ m,
+                                                                  uint16_t* __restrict__ out, int64_t K,
+                                                                  int32_t* __restrict__ bad)
+{
+    grid_dependency_wait();
+    launch_dependents();
+    int n = 0;
+    for (int64_t k = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; k < K;
+         k += static_cast<int64_t>(gridDim.x) * kThreads) {
+        const float v = m[k];
+        const __nv_bfloat16 b = __float2bfloat16_rn(v);
+        const float bv = __bfloat162float(b);
+        out[k] = *reinterpret_cast<const uint16_t*>(&b);
+        n += (!(v > 0.0f) || isinf(v) || isinf(bv) || bv == 0.0f) ? 1 : 0;
+    }
+    n = __reduce_add_sync(0xFFFFFFFFu, n);
+    if ((threadIdx.x & 31) == 0 && n > 0)
+        atomicAdd(bad, n);
+}
+
 // Tile-prefix of a grouped activation tensor: group e starts at scale row
 // 128 * tiles_before[e].  Computed by one warp into shared memory.
 __device__ void group_tile_prefix(const int32_t* offsets, int E, int32_t* tiles_before)
@@ -544,12 +584,15 @@ __device__ void group_tile_prefix(const int32_t* offsets, int E, int32_t* tiles_
 // tensor scale rows live in the padded per-group space; `grouped` selects
 // the mapping.  Lane owns quarter (lane & 3) of block chunk*8U + 8u + lane/4.
 // kA8: MXFP8 output (one E4M3 byte per element, rows of K bytes).
+// mul (bf16 [K] or null): the smooth pre-scale; the block quantized is then
+// bf16(x * mul), rounded once from the exact float32 product.
 template <int U, bool kGrouped, bool kA8>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __restrict__ x,
                                                              uint8_t* __restrict__ op, uint8_t* __restrict__ osf,
                                                              int64_t M, int64_t K, int64_t sf_rows, int kb,
                                                              int kbp, int nch, int uos, int swizzled,
-                                                             const int32_t* __restrict__ offsets, int E)
+                                                             const int32_t* __restrict__ offsets, int E,
+                                                             const uint16_t* __restrict__ mul)
 {
     extern __shared__ int32_t tiles_before[];
     grid_dependency_wait();
@@ -594,6 +637,14 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
             v[u] = ld_stream_u4(x + xrow * K + static_cast<int64_t>(c) * 32 + q * 8);
         else
             v[u] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (mul != nullptr) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int c = cbase + 8 * u;
+            if (c < kb)
+                v[u] = smooth_bf16x8(v[u], __ldg(reinterpret_cast<const uint4*>(mul + static_cast<int64_t>(c) * 32 + q * 8)));
+        }
     }
     const int64_t kb4 = kbp >> 2;
 #pragma unroll
@@ -795,7 +846,7 @@ cudaError_t launch_requant_grouped(const uint8_t* wp, const uint8_t* ws, const f
 }
 
 cudaError_t launch_act_quant(const void* x, uint8_t* op, uint8_t* osf, int64_t M, int64_t K, int alg,
-                             int swizzled, cudaStream_t stream)
+                             int swizzled, cudaStream_t stream, const void* mul)
 {
     constexpr int U = 4;
     const int kb = static_cast<int>(K / 32);
@@ -807,11 +858,11 @@ cudaError_t launch_act_quant(const void* x, uint8_t* op, uint8_t* osf, int64_t M
         return cudaSuccess;
     return launch_pdl(act_quant_kernel<U, false, false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
                       stream, static_cast<const uint16_t*>(x), op, osf, M, K, rows, kb, kbp, nch, alg == 2 ? 1 : 0,
-                      swizzled, static_cast<const int32_t*>(nullptr), 0);
+                      swizzled, static_cast<const int32_t*>(nullptr), 0, static_cast<const uint16_t*>(mul));
 }
 
 cudaError_t launch_act_quant_mxfp8(const void* x, uint8_t* op, uint8_t* osf, int64_t M, int64_t K, int swizzled,
-                                   cudaStream_t stream)
+                                   cudaStream_t stream, const void* mul)
 {
     constexpr int U = 4;
     const int kb = static_cast<int>(K / 32);
@@ -823,7 +874,17 @@ cudaError_t launch_act_quant_mxfp8(const void* x, uint8_t* op, uint8_t* osf, int
         return cudaSuccess;
     return launch_pdl(act_quant_kernel<U, false, true>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
                       stream, static_cast<const uint16_t*>(x), op, osf, M, K, rows, kb, kbp, nch, 0, swizzled,
-                      static_cast<const int32_t*>(nullptr), 0);
+                      static_cast<const int32_t*>(nullptr), 0, static_cast<const uint16_t*>(mul));
+}
+
+cudaError_t launch_smooth_prepare(const float* m, void* out, int64_t K, int32_t* bad, cudaStream_t stream)
+{
+    cudaError_t err = cudaMemsetAsync(bad, 0, sizeof(int32_t), stream);
+    if (err != cudaSuccess)
+        return err;
+    const int64_t blocks = std::min<int64_t>(ceil_div(K, kThreads), resident_ctas(smooth_prepare_kernel));
+    return launch_pdl(smooth_prepare_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, m,
+                      static_cast<uint16_t*>(out), K, bad);
 }
 
 cudaError_t launch_act_quant_grouped(const void* x, const int32_t* offsets, int E, int64_t total_M, int64_t K,
@@ -840,7 +901,7 @@ cudaError_t launch_act_quant_grouped(const void* x, const int32_t* offsets, int 
     const size_t smem = sizeof(int32_t) * static_cast<size_t>(E + 1);
     return launch_pdl(act_quant_kernel<U, true, false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), smem, stream,
                       static_cast<const uint16_t*>(x), op, osf, total_M, K, rows, kb, kbp, nch, alg == 2 ? 1 : 0, 1,
-                      offsets, E);
+                      offsets, E, static_cast<const uint16_t*>(nullptr));
 }
 
 cudaError_t launch_quant_nvfp4(const void* x, float g, uint8_t* op, uint8_t* osf, int64_t M, int64_t K,

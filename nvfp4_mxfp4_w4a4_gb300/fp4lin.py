@@ -36,6 +36,7 @@ SYMBOLS = (
     "fp4_gemm_mxfp4_ws", "fp4_gemm_mxfp4_noalloc", "fp4_gemm_mxfp4_grouped",
     "fp4_quant_nvfp4_ex", "fp4_sf_bytes_nvfp4", "fp4_sf_swizzle", "fp4_gemm_nvfp4",
     "fp4_quant_act_mxfp8", "fp4_gemm_w4a8", "fp4_gemm_w4a8_workspace_size", "fp4_gemm_mxfp4_ex",
+    "fp4_smooth_prepare", "fp4_quant_act_mxfp4_smooth", "fp4_quant_act_mxfp8_smooth",
 )
 
 
@@ -91,6 +92,10 @@ def load(path: str = LIB_PATH):
             "fp4_gemm_w4a8_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64]),
             "fp4_gemm_mxfp4_ex": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p, ctypes.c_size_t,
                                                  ctypes.c_uint32, _p]),
+            "fp4_smooth_prepare": (ctypes.c_int, [_p, _p, _i64, _p, _p]),
+            "fp4_quant_act_mxfp4_smooth": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64,
+                                                          ctypes.POINTER(fp4_quant_opts), _p]),
+            "fp4_quant_act_mxfp8_smooth": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _i32, _p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -216,6 +221,27 @@ def fp4_quant_act_mxfp8(x_bf16, out_e4m3, out_scale, M, K, sf_layout=FP4_SF_SWIZ
     st = load().fp4_quant_act_mxfp8(_ptr(x_bf16), _ptr(out_e4m3), _ptr(out_scale), M, K, sf_layout,
                                     _stream(stream))
     _check(st, "fp4_quant_act_mxfp8")
+
+
+def fp4_smooth_prepare(mul_scale_f32, out_bf16, K, bad_count, stream=None):
+    """Converts the float32 smooth tensor to bf16; bad_count (device int32)
+    receives the number of values that loading must reject."""
+    st = load().fp4_smooth_prepare(_ptr(mul_scale_f32), _ptr(out_bf16), K, _ptr(bad_count), _stream(stream))
+    _check(st, "fp4_smooth_prepare")
+
+
+def fp4_quant_act_mxfp4_smooth(x_bf16, mul_scale_bf16, out_packed, out_scale, M, K, stream=None, scale_alg=None,
+                               sf_layout=None):
+    st = load().fp4_quant_act_mxfp4_smooth(_ptr(x_bf16), _ptr(mul_scale_bf16), _ptr(out_packed), _ptr(out_scale),
+                                           M, K, _opts(scale_alg, sf_layout), _stream(stream))
+    _check(st, "fp4_quant_act_mxfp4_smooth")
+
+
+def fp4_quant_act_mxfp8_smooth(x_bf16, mul_scale_bf16, out_e4m3, out_scale, M, K, sf_layout=FP4_SF_SWIZZLED,
+                               stream=None):
+    st = load().fp4_quant_act_mxfp8_smooth(_ptr(x_bf16), _ptr(mul_scale_bf16), _ptr(out_e4m3), _ptr(out_scale), M,
+                                           K, sf_layout, _stream(stream))
+    _check(st, "fp4_quant_act_mxfp8_smooth")
 
 
 def fp4_gemm_w4a8_workspace_size(M, N, K) -> int:

@@ -97,6 +97,13 @@ def test_argument_checks_precede_device_use(L):
     assert raw.fp4_sf_swizzle(None, None, 0, 4, None) == 0
     assert raw.fp4_gemm_mxfp4_ex(16, 16, 16, 16, None, 16, 1, 8, 128, None, 0, 2, None) == 1     # unknown flag
     assert raw.fp4_gemm_mxfp4_ex(16, 16, 16, 16, None, 16, 1, 8, 100, None, 0, 1, None) == 2     # K % 128
+    # smooth pre-scale
+    assert raw.fp4_smooth_prepare(16, 16, 0, 16, None) == 2                                     # K = 0
+    assert raw.fp4_smooth_prepare(None, 16, 8, 16, None) == 1
+    assert raw.fp4_smooth_prepare(16, 16, 8, 18, None) == 3                                     # counter 4 B
+    assert raw.fp4_quant_act_mxfp4_smooth(16, None, 16, 16, 4, 32, None, None) == 1             # no scale
+    assert raw.fp4_quant_act_mxfp8_smooth(16, None, 16, 16, 4, 32, 0, None) == 1
+    assert raw.fp4_quant_act_mxfp4_smooth(16, 24, 16, 16, 4, 32, None, None) == 3               # scale 16 B
     # W4A8 fallback
     assert raw.fp4_gemm_w4a8(16, 16, 32, 16, None, 16, 1, 8, 192, None, 0, None) == 2           # K % 128
     assert raw.fp4_gemm_w4a8(16, 16, 48, 16, None, 16, 1, 8, 128, None, 0, None) == 3           # b 32 B
