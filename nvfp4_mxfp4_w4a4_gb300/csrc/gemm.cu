@@ -958,6 +958,8 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
                 return cudaErrorInvalidConfiguration;
         }
     }
+    if (p.units > 0)  // split-K: a tile's first CTA waits for the others
+        return launch_coop(kern, dim3(grid), dim3(C::THREADS), smem, stream, tmA, tmB, tmO, p);
     return launch_pdl(kern, dim3(grid), dim3(C::THREADS), smem, stream, tmA, tmB, tmO, p);
 }
 

@@ -29,6 +29,35 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// The same for a kernel whose blocks wait on one another (the split-K GEMM:
+// a tile's first CTA waits for the others' partial sums): a cooperative
+// launch, which the runtime starts only when every block is resident at
+// once.  Programmatic serialization is kept where the runtime takes both
+// attributes together; otherwise the cooperative launch goes alone.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_coop(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                        Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    cudaError_t err = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (err == cudaSuccess)
+        return err;
+    (void)cudaGetLastError();  // a refused attribute combination leaves no error behind
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // Status word bits a kernel sets in the library-owned device status word.
 constexpr unsigned int kStatusTimeout = 1u;
 
