@@ -43,7 +43,8 @@
 // leaves its tile.  The CTA holding a tile's first K stages finishes it: it
 // adds the fp32 partial sums the other S - 1 CTAs left in the workspace, in
 // K order (a fixed reduction order, so results do not vary from run to run),
-// then runs the epilogue.
+// then runs the epilogue.  Such a launch is cooperative (its CTAs wait on
+// one another).
 // Operand formats (kFmt):
 //   kFmtMx  both operands MXFP4 (the path above);
 //   kFmtNv  both operands NVFP4 as "[SGLang] FP4 ..." sections 5-6
