@@ -177,31 +177,42 @@ template <int BN, bool kGrouped>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmParams& p, const int32_t* tiles_before)
 {
     Tile T;
-    const int g = t % p.m_tiles;
-    T.n0 = (t / p.m_tiles) * BN;
     T.expert = 0;
     T.valid = true;
-    T.sfa_rt = g;
-    T.a_row0 = static_cast<int64_t>(g) * BM;
-    int rows = p.rows_a - g * BM;
+    int rows;
     if constexpr (kGrouped) {
-        if (g >= tiles_before[p.E]) {
+        // expert-major walk: all tiles of expert e (its 128-row tiles fastest,
+        // then its weight tiles) before those of e + 1, so the CTAs running
+        // at once share a few experts' weights and activations in L2
+        const int nt = p.n_tiles;
+        if (t >= tiles_before[p.E] * nt) {
             T.valid = false;
             T.rows_valid = 0;
             return T;
         }
-        int lo = 0, hi = p.E;  // tiles_before[lo] <= g < tiles_before[hi]
+        int lo = 0, hi = p.E;  // tiles_before[lo] * nt <= t < tiles_before[hi] * nt
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (tiles_before[mid] <= g)
+            if (tiles_before[mid] * nt <= t)
                 lo = mid;
             else
                 hi = mid;
         }
+        const int mt = tiles_before[lo + 1] - tiles_before[lo];  // >= 1: expert lo holds tile t
+        const int local = t - tiles_before[lo] * nt;
+        const int gl = local % mt;
         T.expert = lo;
+        T.n0 = (local / mt) * BN;
+        T.sfa_rt = tiles_before[lo] + gl;
         const int start = __ldg(p.offsets + lo);
-        T.a_row0 = start + static_cast<int64_t>(g - tiles_before[lo]) * BM;
+        T.a_row0 = start + static_cast<int64_t>(gl) * BM;
         rows = __ldg(p.offsets + lo + 1) - static_cast<int>(T.a_row0);
+    } else {
+        const int g = t % p.m_tiles;
+        T.n0 = (t / p.m_tiles) * BN;
+        T.sfa_rt = g;
+        T.a_row0 = static_cast<int64_t>(g) * BM;
+        rows = p.rows_a - g * BM;
     }
     T.rows_valid = rows < BM ? rows : BM;
     return T;
