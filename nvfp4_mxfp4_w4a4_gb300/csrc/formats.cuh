@@ -103,6 +103,33 @@ __device__ __forceinline__ uint32_t float_to_e4m3_satfinite(float t)
     return static_cast<uint32_t>(v) & 0xFFu;
 }
 
+// Exact n / d for 0 <= n < 2^32 by a divisor d fixed for a launch, by one
+// multiply-high and shifts: the round-up method of Granlund and Montgomery,
+// "Division by invariant integers using multiplication" (PLDI 1994),
+// section 4.  With l = ceil(log2 d): m = floor(2^32 (2^l - d) / d) + 1,
+// s1 = min(l, 1), s2 = max(l - 1, 0).
+struct DivMagic {
+    uint32_t m, s1, s2;
+};
+
+__host__ __device__ inline DivMagic div_magic(uint32_t d)
+{
+    uint32_t l = 0;
+    while ((uint64_t(1) << l) < d)
+        ++l;
+    DivMagic g;
+    g.m = static_cast<uint32_t>(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
+    g.s1 = l < 1 ? l : 1;
+    g.s2 = l > 1 ? l - 1 : 0;
+    return g;
+}
+
+__device__ __forceinline__ uint32_t div_by_magic(uint32_t n, DivMagic g)
+{
+    const uint32_t t = __umulhi(g.m, n);
+    return (t + ((n - t) >> g.s1)) >> g.s2;
+}
+
 // Scale-factor byte offset of (row r, 32-block c) in the swizzled layout the
 // block-scaled MMA reads; kb4 = ceil(K/32 / 4).
 __device__ __forceinline__ int64_t sf_swizzled_offset(int64_t r, int64_t c, int64_t kb4)

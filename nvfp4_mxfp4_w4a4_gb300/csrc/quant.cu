@@ -112,13 +112,35 @@ __device__ __forceinline__ uint2 pack_code_map(uint32_t r1, uint32_t r2, uint32_
 constexpr int kMapD = 10;
 constexpr int kMapEntries = 128 * kMapD;
 
-__device__ void build_code_maps(float ag, uint2* __restrict__ map)
+// Per-tensor tables beside the code maps (all for the tensor's |g|):
+//   texp[s * 8 + m]  biased block exponent (e + 127) that a half with scale
+//                    byte s and largest magnitude code m asks for, from its
+//                    amax RN(E2M1(m) S |g|) by the scale rule; 255 when that
+//                    amax is NaN or Inf.  The rule is monotone in amax, so a
+//                    block's exponent is the larger of its halves' entries.
+//   ter[s]           biased exponent of RN(S |g|), which places the block
+//                    exponent among the scale's code maps.
+struct RequantTables {
+    uint2 map[kMapEntries];
+    uint8_t texp[128 * 8];
+    uint8_t ter[128];
+};
+
+__device__ void build_code_maps(float ag, int uos, RequantTables& tb)
 {
+    uint2* __restrict__ map = tb.map;
+    for (int i = threadIdx.x; i < 128 * 8; i += blockDim.x) {
+        const float S = fabsf(e4m3x2_to_float2(static_cast<uint32_t>(i >> 3)).x);
+        const float amax = __fmul_rn(__fmul_rn(e2m1_mag_value(static_cast<uint32_t>(i & 7)), S), ag);
+        const uint32_t ab = __float_as_uint(amax);
+        tb.texp[i] = ab >= 0x7F800000u ? uint8_t(255) : static_cast<uint8_t>(mx_shared_exp(ab, uos) + 127);
+    }
     for (int sb = threadIdx.x; sb < 128; sb += blockDim.x) {
         const float S = e4m3x2_to_float2(static_cast<uint32_t>(sb)).x;
         const float H = __fmul_rn(0.5f * S, ag);
         const float P = __fmul_rn(S, ag);
         const float Q = __fmul_rn(1.5f * S, ag);
+        tb.ter[sb] = static_cast<uint8_t>(__float_as_uint(P) >> 23);
         const int er = static_cast<int>(__float_as_uint(P) >> 23) - 127;
         uint32_t p2 = 0u, p3 = 0u, p4 = 0u, p5 = 0u;
         bool prev = false;
@@ -190,36 +212,33 @@ __device__ __forceinline__ uint32_t apply_map(uint32_t w, uint32_t m, uint32_t m
 
 // One block: codes in 4 words, its two E4M3 scale bytes in `sc` (low byte =
 // elements 0..15).  Returns the scale byte; writes the 4 output words.
-__device__ __forceinline__ uint32_t requant_block(const uint32_t* w, uint32_t sc, float ag, uint32_t gsign, int uos,
-                                                  const uint2* __restrict__ map, uint32_t* out)
+__device__ __forceinline__ uint32_t requant_block(const uint32_t* w, uint32_t sc, uint32_t gsign,
+                                                  const RequantTables& tb, uint32_t* out)
 {
-    const float2 s = e4m3x2_to_float2(sc);
-    const float S0 = fabsf(s.x), S1 = fabsf(s.y);
+    const uint32_t s0 = sc & 0x7Fu, s1 = (sc >> 8) & 0x7Fu;
     const uint32_t m0 = w[0] & 0x77777777u, m1 = w[1] & 0x77777777u;
     const uint32_t m2 = w[2] & 0x77777777u, m3 = w[3] & 0x77777777u;
     const uint32_t m0h = m0 >> 16, m1h = m1 >> 16, m2h = m2 >> 16, m3h = m3 >> 16;
     uint32_t mm0, mm1;
     max_codes(m0, m0h, m1, m1h, m2, m2h, m3, m3h, mm0, mm1);
-    const float amax0 = __fmul_rn(__fmul_rn(e2m1_mag_value(mm0), S0), ag);
-    const float amax1 = __fmul_rn(__fmul_rn(e2m1_mag_value(mm1), S1), ag);
-    const uint32_t ab = max(__float_as_uint(amax0), __float_as_uint(amax1));
-    if (ab >= 0x7F800000u) {  // NaN or Inf somewhere in the block
+    const int eb = max(tb.texp[s0 * 8 + mm0], tb.texp[s1 * 8 + mm1]);  // e + 127
+    if (eb == 255) {  // NaN or Inf somewhere in the block
         out[0] = out[1] = out[2] = out[3] = 0u;
         return 0xFFu;
     }
-    const int e = mx_shared_exp(ab, uos);
-    // d + 3 = e - er + 3 = e + 130 - biased exponent of RN(S |g|)
-    const int i0 = min(max(e + 130 - static_cast<int>(__float_as_uint(__fmul_rn(S0, ag)) >> 23), 0), kMapD - 1);
-    const int i1 = min(max(e + 130 - static_cast<int>(__float_as_uint(__fmul_rn(S1, ag)) >> 23), 0), kMapD - 1);
-    const uint2 t0 = map[(sc & 0x7Fu) * kMapD + i0];
-    const uint2 t1 = map[((sc >> 8) & 0x7Fu) * kMapD + i1];
-    const uint32_t f0 = ((__float_as_uint(s.x) >> 31) ^ gsign) ? 0x88888888u : 0u;
-    const uint32_t f1 = ((__float_as_uint(s.y) >> 31) ^ gsign) ? 0x88888888u : 0u;
+    // d + 3 = e - er + 3 = (e + 127) + 3 - biased exponent of RN(S |g|)
+    const int i0 = min(max(eb + 3 - static_cast<int>(tb.ter[s0]), 0), kMapD - 1);
+    const int i1 = min(max(eb + 3 - static_cast<int>(tb.ter[s1]), 0), kMapD - 1);
+    const uint2 t0 = tb.map[s0 * kMapD + i0];
+    const uint2 t1 = tb.map[s1 * kMapD + i1];
+    // element sign = code sign ^ scale sign ^ sign of g
+    const uint32_t f0 = (((sc >> 7) & 1u) ^ gsign) ? 0x88888888u : 0u;
+    const uint32_t f1 = (((sc >> 15) & 1u) ^ gsign) ? 0x88888888u : 0u;
     out[0] = apply_map(w[0], m0, m0h, t0, f0);
     out[1] = apply_map(w[1], m1, m1h, t0, f0);
     out[2] = apply_map(w[2], m2, m2h, t1, f1);
     out[3] = apply_map(w[3], m3, m3h, t1, f1);
-    return static_cast<uint32_t>(e + 127);
+    return static_cast<uint32_t>(eb);
 }
 
 struct RequantLane {
@@ -259,10 +278,10 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const uint8_t* __rest
                                                            int64_t N, int64_t K, int64_t rows, int kb, int kbp,
                                                            int nch, int uos, int swizzled)
 {
-    __shared__ uint2 map[kMapEntries];
+    __shared__ RequantTables tb;
     const float ag = fabsf(g);
     const uint32_t gsign = __float_as_uint(g) >> 31;
-    build_code_maps(ag, map);  // needs no global memory: overlaps the previous kernel
+    build_code_maps(ag, uos, tb);  // needs no global memory: overlaps the previous kernel
     __syncthreads();
     grid_dependency_wait();
     launch_dependents();
@@ -294,7 +313,7 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const uint8_t* __rest
         uint32_t sfw = 0u;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t sf = requant_block(cur.w + 4 * j, cur.sc[j], ag, gsign, uos, map, out + 4 * j);
+            const uint32_t sf = requant_block(cur.w + 4 * j, cur.sc[j], gsign, tb, out + 4 * j);
             if (j < nreal)
                 sfw |= sf << (8 * j);
         }
@@ -339,19 +358,19 @@ __global__ void __launch_bounds__(kThreads) requant_flat_kernel(const uint8_t* _
                                                                 uint8_t* __restrict__ op, uint8_t* __restrict__ osf,
                                                                 int64_t N, int64_t K, int64_t rows_pad, int kb,
                                                                 int64_t items, int ctas_per_e, int64_t sf_e_bytes,
-                                                                int uos, int swizzled)
+                                                                int uos, int swizzled, DivMagic kb_div, int idx32)
 {
-    __shared__ uint2 map[kMapEntries];
+    __shared__ RequantTables tb;
     const int e = kGrouped ? static_cast<int>(blockIdx.x) / ctas_per_e : 0;
     const int local = kGrouped ? static_cast<int>(blockIdx.x) - e * ctas_per_e : static_cast<int>(blockIdx.x);
     float g = g_dense;
     if (!kGrouped)
-        build_code_maps(fabsf(g), map);  // needs no global memory: overlaps the previous kernel
+        build_code_maps(fabsf(g), uos, tb);  // needs no global memory: overlaps the previous kernel
     grid_dependency_wait();
     launch_dependents();
     if (kGrouped) {
         g = __ldg(g_dev + e);
-        build_code_maps(fabsf(g), map);
+        build_code_maps(fabsf(g), uos, tb);
     }
     __syncthreads();
     const float ag = fabsf(g);
@@ -417,8 +436,10 @@ __global__ void __launch_bounds__(kThreads) requant_flat_kernel(const uint8_t* _
             uint32_t sfw = 0u;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                sfw |= requant_block(cur.w + 4 * j, cur.sc[j], ag, gsign, uos, map, out + 4 * j) << (8 * j);
-            const int64_t row = f / kb;
+                sfw |= requant_block(cur.w + 4 * j, cur.sc[j], gsign, tb, out + 4 * j) << (8 * j);
+            // block index -> (row, block column): a multiply-high while the
+            // tensor's block count fits 32 bits
+            const int64_t row = idx32 ? static_cast<int64_t>(div_by_magic(static_cast<uint32_t>(f), kb_div)) : f / kb;
             const int c0 = static_cast<int>(f - row * kb);
             if (real) {
                 uint32_t a[8], b[8];
@@ -806,16 +827,19 @@ cudaError_t launch_requant_flat(const uint8_t* wp, const uint8_t* ws, float g, c
     const int64_t sf_e_bytes = rows_pad * kb;            // swizzled bytes per tensor (kb % 4 == 0)
     const int uos = alg == 2 ? 1 : 0;
     const int64_t want = ceil_div(items * 32, kThreads);  // CTAs that give every warp one item
+    // a lane's first block index f < items * 128 (pad rows included)
+    const int idx32 = items * 128 <= int64_t(UINT32_MAX) ? 1 : 0;
+    const DivMagic kb_div = div_magic(static_cast<uint32_t>(kb));
     if (g_dev == nullptr) {
         const int64_t blocks = std::min<int64_t>(want, resident_ctas(requant_flat_kernel<false>));
         return launch_pdl(requant_flat_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream,
                           wp, ws, g, static_cast<const float*>(nullptr), op, osf, N, K, rows_pad, kb, items,
-                          static_cast<int>(blocks), sf_e_bytes, uos, swizzled);
+                          static_cast<int>(blocks), sf_e_bytes, uos, swizzled, kb_div, idx32);
     }
     const int64_t per_e = std::max<int64_t>(1, std::min<int64_t>(want, resident_ctas(requant_flat_kernel<true>) / E));
     return launch_pdl(requant_flat_kernel<true>, dim3(static_cast<unsigned>(per_e * E)), dim3(kThreads), 0, stream, wp,
                       ws, 0.0f, g_dev, op, osf, N, K, rows_pad, kb, items, static_cast<int>(per_e), sf_e_bytes, uos,
-                      swizzled);
+                      swizzled, kb_div, idx32);
 }
 
 cudaError_t launch_requant(const uint8_t* wp, const uint8_t* ws, float g, uint8_t* op, uint8_t* osf, int64_t N,
