@@ -202,3 +202,21 @@ def test_gemm_nvfp4_end_to_end_on_device(orc, L):
     ref, absum = orc.gemm_nvfp4(a, sa, b, sb, alpha, threads=THREADS)
     ok, ratio = gemm_check(bf16_bits_host(out), ref, absum)
     assert ok, f"max err/bound = {ratio}"
+
+
+# ---------------------------------------------------------------- full sizes
+@pytest.mark.slow
+def test_full_decode_and_prefill_nvfp4_gemm(orc, L):
+    """The benchmark's decode (14336 x 4096, M = 64, with bias) and prefill
+    (2048 x 18432 x 7168) shapes in the launch configurations the benchmark
+    times, on sampled rows (all columns)."""
+    rng = np.random.default_rng(7)
+    w1 = synth.workload1(Ms=(64,))
+    w2 = synth.workload2(Ms=(2048,))
+    for W, X, bias in ((w1["W"], w1["X"][64], w1["bias"]), (w2["W"], w2["X"][2048], None)):
+        M = X.shape[0]
+        a, sa, _, ga = _nv_operand(orc, X)
+        b, sb, _, gb = _nv_operand(orc, W)
+        rows = np.sort(rng.choice(M, min(M, 24), replace=False))
+        rows[-1] = M - 1
+        _check(orc, L, a, sa, b, sb, float(np.float32(ga) * np.float32(gb)), bias, rows=rows)

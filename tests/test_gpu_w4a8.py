@@ -159,3 +159,22 @@ def test_gemm_w4a8_split_k(orc, L, M, N, K):
     first = _check(orc, L, a8, sa, b, sb, None, workspace=ws)
     again = _run(L, a8, orc.sf_swizzle(sa), b, orc.sf_swizzle(sb), None, M, N, K, ws)
     assert np.array_equal(first, again)
+
+
+# ---------------------------------------------------------------- full sizes
+@pytest.mark.slow
+def test_full_decode_and_prefill_w4a8_gemm(orc, L):
+    """The benchmark's decode (14336 x 4096, M = 1 and 64, with bias) and
+    prefill (2048 x 18432 x 7168) shapes, on sampled rows (all columns)."""
+    rng = np.random.default_rng(8)
+    w1 = synth.workload1(Ms=(1, 64))
+    w2 = synth.workload2(Ms=(2048,))
+    b1, sb1 = _weight(orc, w1["W"])
+    for X in (w1["X"][1], w1["X"][64]):
+        a8, sa = orc.act_quant_mxfp8(X, threads=THREADS)
+        _check(orc, L, a8, sa, b1, sb1, w1["bias"])
+    b2, sb2 = _weight(orc, w2["W"])
+    a8, sa = orc.act_quant_mxfp8(w2["X"][2048], threads=THREADS)
+    rows = np.sort(rng.choice(2048, 24, replace=False))
+    rows[-1] = 2047
+    _check(orc, L, a8, sa, b2, sb2, None, rows=rows)
