@@ -113,6 +113,8 @@ struct Cfg {
     static constexpr bool SPLIT = BN == 256 && CPW > 2;
     static constexpr int REGS_LOW = 80;    // warps 0-7 after the split
     static constexpr int REGS_HIGH = 176;  // epilogue warps after the split
+    // the two halves of the split fill the 65536 registers of 16 warps x 32 x 128
+    static_assert(!SPLIT || (REGS_LOW + REGS_HIGH) * 256 == 65536, "register split must fill the register file");
     static constexpr int FIRST_EPI_WARP = SPLIT ? 8 : 2 + CPW;
     static constexpr int THREADS = 32 * (FIRST_EPI_WARP + kEpiWarps);
     // a slab is one 128-byte row per operand row: 256 elements of K (packed
