@@ -7,6 +7,10 @@
  *   2. dynamic per-batch MXFP4 quantization of bf16 activations,
  *   3. the block-scaled FP4 GEMM over two MXFP4 operands with a bf16
  *      (+ optional bf16 bias) epilogue, dense and grouped (MoE).
+ * Beside it: the W4A8 fallback (MXFP8 activations x the same MXFP4
+ * weights), the smooth pre-scale x * mul_scale fused into the activation
+ * quantizers, and the NVFP4 x NVFP4 GEMM a GPU with native NVFP4 would run
+ * without the requantization (the comparison point).
  *
  * Pages that define the operations (cited by title and section):
  *   [AMD]  "Efficiently Serving NVFP4 Models on AMD Instinct MI350X/MI355X
