@@ -371,6 +371,13 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
     // states that the weights are not written by that kernel, the weight
     // half of the first stages of this CTA's first tile)
     int npre = 0;  // producer thread: stages whose weight half is already in flight
+    // Producer thread: its first work item, decoded before the dependency
+    // wait (a chain of dependent integer operations on the launch parameters,
+    // ~0.5 us on one thread) so that it overlaps the previous kernel.
+    WorkIter first_wi{};
+    Work first_w{};
+    Tile first_t{};
+    bool have_first = false;
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
@@ -384,14 +391,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
         tma_prefetch_map(&tmB);
         tma_prefetch_map(&tmO);
         if constexpr (!kGrouped) {
-            if (p.early_w) {
-                WorkIter wi = work_begin(p, total_tiles);
-                Work w;
-                if (work_next(wi, nkb, w)) {
-                    const Tile T = decode_tile<BN, false>(w.t, p, nullptr);
-                    npre = min(STAGES, w.kb1 - w.kb0);
+            first_wi = work_begin(p, total_tiles);
+            have_first = work_next(first_wi, nkb, first_w);
+            if (have_first) {
+                first_t = decode_tile<BN, false>(first_w.t, p, nullptr);
+                if (p.early_w) {
+                    npre = min(STAGES, first_w.kb1 - first_w.kb0);
                     for (int i = 0; i < npre; ++i)
-                        stage_loads(i, w.kb0 + i, T, kHalfW, true);
+                        stage_loads(i, first_w.kb0 + i, first_t, kHalfW, true);
                 }
             }
         }
@@ -439,10 +446,13 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                 // ------------------------------------------------- TMA producer
                 uint32_t it = 0;
                 bool ok = true;
-                WorkIter wi = work_begin(p, total_tiles);
-                Work w;
-                while (ok && work_next(wi, nkb, w)) {
-                    const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
+                // dense: continue from the first item decoded before the wait
+                WorkIter wi = kGrouped ? work_begin(p, total_tiles) : first_wi;
+                Work w = first_w;
+                bool first = !kGrouped && have_first;
+                while (ok && (first || work_next(wi, nkb, w))) {
+                    const Tile T = first ? first_t : decode_tile<BN, kGrouped>(w.t, p, tiles_before);
+                    first = false;
                     if (!T.valid)
                         continue;
                     for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
