@@ -835,11 +835,16 @@ def cpu_baseline(budget_s=12.0):
         rows = max(128, rows // 128 * 128)
         dt, frac = _oracle_sample(rows, threads)
     full_s = dt / frac
+    # the same oracle on one thread (rows are independent: the results are
+    # identical), on a smaller sample
+    dt1, frac1 = _oracle_sample(128, 1)
     return {"value": round(_decode_flops() / full_s / 1e12, 6), "unit": "TFLOPS", "cores": threads,
             "kind": "oracle",
             "sample": f"{rows} of {N_W} weight rows requantized and multiplied with all {sum(MS)} activation "
                       f"rows, all activations quantized; step time extrapolated by {N_W}/{rows} "
-                      f"({dt:.2f} s measured)"}
+                      f"({dt:.2f} s measured)",
+            "single_thread": {"value": round(_decode_flops() / (dt1 / frac1) / 1e12, 6), "cores": 1,
+                              "sample": f"128 of {N_W} weight rows, extrapolated ({dt1:.2f} s measured)"}}
 
 
 def run_reference(args):
