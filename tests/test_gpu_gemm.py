@@ -234,3 +234,31 @@ def test_end_to_end_tiny_workload(orc, L):
     ref, absum = orc.gemm(ra, ras, rb, rbs)
     ok, ratio = gemm_check(bf16_bits_host(out), ref, absum)
     assert ok, ratio
+
+
+def test_gemm_nan_and_tiny_scales(orc, L):
+    """E8M0 0xFF is NaN: a NaN scale in one block of A row 3 makes output row
+    3 NaN, one in B row 5 makes column 5 NaN.  Scales near the bottom of the
+    range (2^-111 for a whole A row, 2^-112 for one B block) give tiny
+    products that stay normal in float32.  Elsewhere the usual bound holds."""
+    rng = np.random.default_rng(11)
+    M, N, K = 16, 136, 256
+    a = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = rng.integers(120, 134, (M, K // 32), dtype=np.uint8)
+    sb = rng.integers(120, 134, (N, K // 32), dtype=np.uint8)
+    sa[3, 2] = 0xFF
+    sb[5, 7] = 0xFF
+    sa[7, :] = 0x10
+    sb[9, 1] = 0x0F
+    out = _run_gemm(L, a, orc.sf_swizzle(sa), b, orc.sf_swizzle(sb), None, M, N, K)
+    ref, absum = orc.gemm(a, sa, b, sb)
+    from _util import bf16_bits_to_f64
+
+    got = bf16_bits_to_f64(out)
+    nan_ref = np.isnan(ref)
+    assert nan_ref[3, :].all() and nan_ref[:, 5].all() and nan_ref.sum() == N + M - 1
+    assert np.array_equal(np.isnan(got), nan_ref)
+    keep = ~nan_ref
+    ok, ratio = gemm_check(out[keep], ref[keep], absum[keep])
+    assert ok, f"max err/bound = {ratio}"
