@@ -393,6 +393,50 @@ FP4LIN_API fp4_status fp4_gemm_w4a8(const uint8_t* a_e4m3, const uint8_t* sa, co
  * current device (0: not split, or no usable device).                      */
 FP4LIN_API size_t fp4_gemm_w4a8_workspace_size(int64_t M, int64_t N, int64_t K);
 
+/* ------------------------------------------------------------ linear layer */
+
+/* Activation formats of fp4_linear. */
+typedef enum { FP4_ACT_MXFP4 = 0, FP4_ACT_MXFP8 = 1 } fp4_act_format;
+
+/* Options of fp4_linear.  A NULL pointer means {MXFP4, OCP, no smooth
+ * scale, no flags}. */
+typedef struct {
+    int32_t act_format;          /* fp4_act_format; MXFP8 is the W4A8 fallback   */
+    int32_t scale_alg;           /* MXFP4 activations: OCP or UOS; MXFP8: OCP    */
+    const void* mul_scale_bf16;  /* smooth pre-scale [K] bf16 (device), or NULL  */
+    uint32_t gemm_flags;         /* 0 or FP4_GEMM_WEIGHTS_STATIC                 */
+} fp4_linear_opts;
+
+/* Bytes of workspace fp4_linear needs for an M x N x K layer with these
+ * options on the current device (0 for M = 0, invalid options or no usable
+ * device): the split-K scratch of the GEMM, the quantized activations and
+ * their scales.                                                            */
+FP4LIN_API size_t fp4_linear_workspace_size(int64_t M, int64_t N, int64_t K,
+                                 const fp4_linear_opts* opts);
+
+/* The serve-time linear layer in one call: dynamic quantization of the bf16
+ * activations (optionally of x * mul_scale), then the block-scaled GEMM with
+ * the prepared MXFP4 weights, bf16 output (+ bf16 bias) -- [AMD]'s serve-time
+ * path (activations quantized to MXFP4 per batch), [OMNI] Overview / W4A8
+ * fallback / Pre-Quantized Single-Scale Weights (smooth), [SGL] section 6
+ * (bias after the GEMM).  Exactly fp4_quant_act_mxfp4[_smooth] (or
+ * fp4_quant_act_mxfp8[_smooth]) into the workspace followed by
+ * fp4_gemm_mxfp4_ex (or fp4_gemm_w4a8) on the same stream.
+ *   x_bf16     [M, K] bf16; w [N, K/2] MXFP4 codes, sw SWIZZLED E8M0
+ *   workspace  device memory, 256-byte aligned, at least
+ *              fp4_linear_workspace_size(M, N, K, opts) bytes; its first
+ *              bytes are the GEMM's split-K counters: zero them once before
+ *              the first call (every call that finishes without a device
+ *              timeout leaves them zero); calls sharing a workspace must
+ *              not overlap in time.  Owned by the caller.
+ * Errors: FP4_ERR_INVALID_ARG also for an invalid option or a workspace
+ * smaller than the size above.  Shape rules of fp4_gemm_mxfp4; with MXFP8
+ * activations w must be 32-byte aligned.                                   */
+FP4LIN_API fp4_status fp4_linear(const void* x_bf16, const uint8_t* w, const uint8_t* sw,
+                      const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K,
+                      void* workspace, size_t workspace_bytes, const fp4_linear_opts* opts,
+                      void* stream);
+
 /* Grouped (MoE) W4A4 GEMM ([AMD] "Native FP4 matmul": MoE experts on
  * MXFP4): for every expert e and every row m in [row_offsets[e],
  * row_offsets[e+1]):  out[m, :] = A[m, :] . B_e^T (+ bias_e).

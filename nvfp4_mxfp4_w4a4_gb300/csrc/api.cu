@@ -452,6 +452,88 @@ fp4_status fp4_gemm_mxfp4_ex(const uint8_t* a, const uint8_t* sa, const uint8_t*
                        fp4lin::kGemmMx, 1.0f, flags);
 }
 
+// ----------------------------------------------------------- linear layer
+namespace {
+
+struct LinearPlan {
+    int fmt;          // GemmFormat
+    int alg;          // activation scale rule
+    size_t split;     // split-K scratch at offset 0
+    size_t act_off;   // quantized activations
+    size_t sf_off;    // their swizzled scales
+    size_t total;
+};
+
+inline size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+fp4_status linear_plan(int64_t M, int64_t N, int64_t K, const fp4_linear_opts* o, LinearPlan* pl)
+{
+    if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 8 != 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    const int act = o ? o->act_format : FP4_ACT_MXFP4;
+    const int alg = o ? o->scale_alg : FP4_SCALE_OCP;
+    if (act != FP4_ACT_MXFP4 && act != FP4_ACT_MXFP8)
+        return FP4_ERR_INVALID_ARG;
+    if (alg != FP4_SCALE_OCP && alg != FP4_SCALE_UOS)
+        return FP4_ERR_INVALID_ARG;
+    if (act == FP4_ACT_MXFP8 && alg != FP4_SCALE_OCP)
+        return FP4_ERR_INVALID_ARG;  // the A8 path always takes the OCP rule
+    if (o && (o->gemm_flags & ~static_cast<uint32_t>(FP4_GEMM_WEIGHTS_STATIC)))
+        return FP4_ERR_INVALID_ARG;
+    pl->fmt = act == FP4_ACT_MXFP8 ? fp4lin::kGemmW4A8 : fp4lin::kGemmMx;
+    pl->alg = alg;
+    pl->split = current_device(nullptr) == FP4_OK ? round256(fp4lin::gemm_workspace_bytes(M, N, K, pl->fmt)) : 0;
+    pl->act_off = pl->split;
+    const size_t act_bytes = static_cast<size_t>(M) * static_cast<size_t>(act == FP4_ACT_MXFP8 ? K : K / 2);
+    pl->sf_off = pl->act_off + round256(act_bytes);
+    pl->total = pl->sf_off + round256(fp4_sf_bytes(M, K, FP4_SF_SWIZZLED));
+    return FP4_OK;
+}
+
+}  // namespace
+
+size_t fp4_linear_workspace_size(int64_t M, int64_t N, int64_t K, const fp4_linear_opts* opts)
+{
+    LinearPlan pl;
+    if (M <= 0 || linear_plan(M, N, K, opts, &pl) != FP4_OK)
+        return 0;
+    return pl.total;
+}
+
+fp4_status fp4_linear(const void* x_bf16, const uint8_t* w, const uint8_t* sw, const void* bias_bf16, void* out_bf16,
+                      int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                      const fp4_linear_opts* opts, void* stream)
+{
+    LinearPlan pl;
+    fp4_status st = linear_plan(M, N, K, opts, &pl);
+    if (st != FP4_OK)
+        return st;
+    if (M == 0)
+        return FP4_OK;
+    if (!x_bf16 || !w || !sw || !out_bf16 || !workspace)
+        return FP4_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return FP4_ERR_ALIGNMENT;
+    if (pl.fmt == fp4lin::kGemmW4A8 && (reinterpret_cast<uintptr_t>(w) & 31u))
+        return FP4_ERR_ALIGNMENT;
+    if (workspace_bytes < pl.total)
+        return FP4_ERR_INVALID_ARG;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    uint8_t* a = base + pl.act_off;
+    uint8_t* sa = base + pl.sf_off;
+    const void* mul = opts ? opts->mul_scale_bf16 : nullptr;
+    if (pl.fmt == fp4lin::kGemmW4A8)
+        st = act_quant8_common(x_bf16, mul, a, sa, M, K, FP4_SF_SWIZZLED, stream);
+    else {
+        const fp4_quant_opts qo = {pl.alg, FP4_SF_SWIZZLED};
+        st = act_quant_common(x_bf16, mul, a, sa, M, K, &qo, stream);
+    }
+    if (st != FP4_OK)
+        return st;
+    return gemm_common(a, sa, w, sw, bias_bf16, out_bf16, nullptr, 1, M, N, K, pl.split ? base : nullptr, pl.split,
+                       stream, pl.fmt, 1.0f, opts ? opts->gemm_flags : 0u);
+}
+
 fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                                   const void* bias_bf16, void* out_bf16, const int32_t* row_offsets, int32_t E,
                                   int64_t total_M, int64_t N, int64_t K, void* stream)

@@ -37,6 +37,7 @@ SYMBOLS = (
     "fp4_quant_nvfp4_ex", "fp4_sf_bytes_nvfp4", "fp4_sf_swizzle", "fp4_gemm_nvfp4",
     "fp4_quant_act_mxfp8", "fp4_gemm_w4a8", "fp4_gemm_w4a8_workspace_size", "fp4_gemm_mxfp4_ex",
     "fp4_smooth_prepare", "fp4_quant_act_mxfp4_smooth", "fp4_quant_act_mxfp8_smooth",
+    "fp4_linear_workspace_size", "fp4_linear",
 )
 
 
@@ -48,6 +49,15 @@ class Fp4Error(RuntimeError):
 
 class fp4_quant_opts(ctypes.Structure):
     _fields_ = [("scale_alg", ctypes.c_int32), ("sf_layout", ctypes.c_int32)]
+
+
+class fp4_linear_opts(ctypes.Structure):
+    _fields_ = [("act_format", ctypes.c_int32), ("scale_alg", ctypes.c_int32), ("mul_scale_bf16", ctypes.c_void_p),
+                ("gemm_flags", ctypes.c_uint32)]
+
+
+FP4_ACT_MXFP4 = 0
+FP4_ACT_MXFP8 = 1
 
 
 _lib = None
@@ -96,6 +106,9 @@ def load(path: str = LIB_PATH):
             "fp4_quant_act_mxfp4_smooth": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64,
                                                           ctypes.POINTER(fp4_quant_opts), _p]),
             "fp4_quant_act_mxfp8_smooth": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _i32, _p]),
+            "fp4_linear_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, ctypes.POINTER(fp4_linear_opts)]),
+            "fp4_linear": (ctypes.c_int, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, ctypes.c_size_t,
+                                          ctypes.POINTER(fp4_linear_opts), _p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -242,6 +255,28 @@ def fp4_quant_act_mxfp8_smooth(x_bf16, mul_scale_bf16, out_e4m3, out_scale, M, K
     st = load().fp4_quant_act_mxfp8_smooth(_ptr(x_bf16), _ptr(mul_scale_bf16), _ptr(out_e4m3), _ptr(out_scale), M,
                                            K, sf_layout, _stream(stream))
     _check(st, "fp4_quant_act_mxfp8_smooth")
+
+
+def _linear_opts(act_format, scale_alg, mul_scale_bf16, gemm_flags):
+    return fp4_linear_opts(act_format, scale_alg, _ptr(mul_scale_bf16), gemm_flags)
+
+
+def fp4_linear_workspace_size(M, N, K, act_format=FP4_ACT_MXFP4, scale_alg=FP4_SCALE_OCP, mul_scale_bf16=None,
+                              gemm_flags=0) -> int:
+    o = _linear_opts(act_format, scale_alg, mul_scale_bf16, gemm_flags)
+    return load().fp4_linear_workspace_size(M, N, K, ctypes.byref(o))
+
+
+def fp4_linear(x_bf16, w, sw, bias_bf16, out_bf16, M, N, K, workspace, workspace_bytes=None,
+               act_format=FP4_ACT_MXFP4, scale_alg=FP4_SCALE_OCP, mul_scale_bf16=None, gemm_flags=0, stream=None):
+    """y = quant(x [* mul_scale]) . W^T (+ bias) in one call; workspace from
+    fp4_linear_workspace_size, zeroed once before first use."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    o = _linear_opts(act_format, scale_alg, mul_scale_bf16, gemm_flags)
+    st = load().fp4_linear(_ptr(x_bf16), _ptr(w), _ptr(sw), _ptr(bias_bf16), _ptr(out_bf16), M, N, K, _ptr(workspace),
+                           workspace_bytes, ctypes.byref(o), _stream(stream))
+    _check(st, "fp4_linear")
 
 
 def fp4_gemm_w4a8_workspace_size(M, N, K) -> int:

@@ -104,6 +104,20 @@ def test_argument_checks_precede_device_use(L):
     assert raw.fp4_quant_act_mxfp4_smooth(16, None, 16, 16, 4, 32, None, None) == 1             # no scale
     assert raw.fp4_quant_act_mxfp8_smooth(16, None, 16, 16, 4, 32, 0, None) == 1
     assert raw.fp4_quant_act_mxfp4_smooth(16, 24, 16, 16, 4, 32, None, None) == 3               # scale 16 B
+    # linear layer
+    from nvfp4_mxfp4_w4a4_gb300.fp4lin import fp4_linear_opts
+
+    o_bad = fp4_linear_opts(7, 0, None, 0)
+    o_a8_uos = fp4_linear_opts(1, 2, None, 0)
+    o_flag = fp4_linear_opts(0, 0, None, 4)
+    o_ok = fp4_linear_opts(0, 0, None, 0)
+    for o, want in ((o_bad, 1), (o_a8_uos, 1), (o_flag, 1)):
+        assert raw.fp4_linear(256, 256, 256, None, 256, 4, 8, 128, 256, 1 << 20, ctypes.byref(o), None) == want
+    assert raw.fp4_linear(256, 256, 256, None, 256, 4, 8, 192, 256, 1 << 20, ctypes.byref(o_ok), None) == 2  # K
+    assert raw.fp4_linear(256, 256, 256, None, 256, 4, 8, 128, 256, 16, ctypes.byref(o_ok), None) == 1     # ws
+    assert raw.fp4_linear(256, 256, 256, None, 256, 4, 8, 128, 320, 1 << 20, ctypes.byref(o_ok), None) == 3  # align
+    assert raw.fp4_linear(None, None, None, None, None, 0, 8, 128, None, 0, None, None) == 0               # M = 0
+    assert raw.fp4_linear_workspace_size(4, 8, 128, ctypes.byref(o_bad)) == 0
     # W4A8 fallback
     assert raw.fp4_gemm_w4a8(16, 16, 32, 16, None, 16, 1, 8, 192, None, 0, None) == 2           # K % 128
     assert raw.fp4_gemm_w4a8(16, 16, 48, 16, None, 16, 1, 8, 128, None, 0, None) == 3           # b 32 B
