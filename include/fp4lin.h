@@ -437,6 +437,22 @@ FP4LIN_API fp4_status fp4_linear(const void* x_bf16, const uint8_t* w, const uin
                       void* workspace, size_t workspace_bytes, const fp4_linear_opts* opts,
                       void* stream);
 
+/* The MoE form of fp4_linear: grouped activation quantization (MXFP4, OCP
+ * or UOS, rows grouped by expert as row_offsets gives) into the workspace,
+ * then the grouped GEMM against the experts' weights -- exactly
+ * fp4_quant_act_mxfp4_grouped followed by fp4_gemm_mxfp4_grouped on the same
+ * stream ([AMD] "Native FP4 matmul": MoE experts on MXFP4).
+ *   workspace  device memory, 256-byte aligned, at least
+ *              fp4_linear_grouped_workspace_size(total_M, E, K) bytes
+ *   opts       scale rule (sf_layout must be SWIZZLED); NULL = OCP
+ * Otherwise the rules of the two calls.                                    */
+FP4LIN_API size_t fp4_linear_grouped_workspace_size(int64_t total_M, int32_t E, int64_t K);
+FP4LIN_API fp4_status fp4_linear_grouped(const void* x_bf16, const int32_t* row_offsets, int32_t E,
+                              int64_t total_M, const uint8_t* w, const uint8_t* sw,
+                              const void* bias_bf16, void* out_bf16, int64_t N, int64_t K,
+                              void* workspace, size_t workspace_bytes,
+                              const fp4_quant_opts* opts, void* stream);
+
 /* Grouped (MoE) W4A4 GEMM ([AMD] "Native FP4 matmul": MoE experts on
  * MXFP4): for every expert e and every row m in [row_offsets[e],
  * row_offsets[e+1]):  out[m, :] = A[m, :] . B_e^T (+ bias_e).

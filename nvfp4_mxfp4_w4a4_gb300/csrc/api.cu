@@ -534,6 +534,44 @@ fp4_status fp4_linear(const void* x_bf16, const uint8_t* w, const uint8_t* sw, c
                        stream, pl.fmt, 1.0f, opts ? opts->gemm_flags : 0u);
 }
 
+size_t fp4_linear_grouped_workspace_size(int64_t total_M, int32_t E, int64_t K)
+{
+    if (total_M <= 0 || E <= 0 || K <= 0 || K % 32 != 0)
+        return 0;
+    return round256(static_cast<size_t>(total_M) * static_cast<size_t>(K / 2)) +
+           round256(fp4_sf_bytes_grouped(total_M, E, K));
+}
+
+fp4_status fp4_linear_grouped(const void* x_bf16, const int32_t* row_offsets, int32_t E, int64_t total_M,
+                              const uint8_t* w, const uint8_t* sw, const void* bias_bf16, void* out_bf16, int64_t N,
+                              int64_t K, void* workspace, size_t workspace_bytes, const fp4_quant_opts* opts,
+                              void* stream)
+{
+    int alg, swz;
+    fp4_status st = check_opts(opts, &alg, &swz);
+    if (st != FP4_OK)
+        return st;
+    if (opts && !swz)
+        return FP4_ERR_INVALID_ARG;
+    if (E <= 0 || E > fp4lin::kMaxGroupedExperts || total_M < 0 || N <= 0 || K <= 0 || K % 128 != 0 ||
+        N % 8 != 0 || total_M >= kMaxDim || N >= kMaxDim || K >= kMaxDim || static_cast<int64_t>(E) * N >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    if (total_M == 0)
+        return FP4_OK;
+    if (!workspace)
+        return FP4_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return FP4_ERR_ALIGNMENT;
+    if (workspace_bytes < fp4_linear_grouped_workspace_size(total_M, E, K))
+        return FP4_ERR_INVALID_ARG;
+    uint8_t* a = static_cast<uint8_t*>(workspace);
+    uint8_t* sa = a + round256(static_cast<size_t>(total_M) * static_cast<size_t>(K / 2));
+    st = fp4_quant_act_mxfp4_grouped(x_bf16, row_offsets, E, total_M, K, a, sa, opts, stream);
+    if (st != FP4_OK)
+        return st;
+    return fp4_gemm_mxfp4_grouped(a, sa, w, sw, bias_bf16, out_bf16, row_offsets, E, total_M, N, K, stream);
+}
+
 fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                                   const void* bias_bf16, void* out_bf16, const int32_t* row_offsets, int32_t E,
                                   int64_t total_M, int64_t N, int64_t K, void* stream)

@@ -37,7 +37,7 @@ SYMBOLS = (
     "fp4_quant_nvfp4_ex", "fp4_sf_bytes_nvfp4", "fp4_sf_swizzle", "fp4_gemm_nvfp4",
     "fp4_quant_act_mxfp8", "fp4_gemm_w4a8", "fp4_gemm_w4a8_workspace_size", "fp4_gemm_mxfp4_ex",
     "fp4_smooth_prepare", "fp4_quant_act_mxfp4_smooth", "fp4_quant_act_mxfp8_smooth",
-    "fp4_linear_workspace_size", "fp4_linear",
+    "fp4_linear_workspace_size", "fp4_linear", "fp4_linear_grouped_workspace_size", "fp4_linear_grouped",
 )
 
 
@@ -109,6 +109,9 @@ def load(path: str = LIB_PATH):
             "fp4_linear_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, ctypes.POINTER(fp4_linear_opts)]),
             "fp4_linear": (ctypes.c_int, [_p, _p, _p, _p, _p, _i64, _i64, _i64, _p, ctypes.c_size_t,
                                           ctypes.POINTER(fp4_linear_opts), _p]),
+            "fp4_linear_grouped_workspace_size": (ctypes.c_size_t, [_i64, _i32, _i64]),
+            "fp4_linear_grouped": (ctypes.c_int, [_p, _p, _i32, _i64, _p, _p, _p, _p, _i64, _i64, _p, ctypes.c_size_t,
+                                                  ctypes.POINTER(fp4_quant_opts), _p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -277,6 +280,21 @@ def fp4_linear(x_bf16, w, sw, bias_bf16, out_bf16, M, N, K, workspace, workspace
     st = load().fp4_linear(_ptr(x_bf16), _ptr(w), _ptr(sw), _ptr(bias_bf16), _ptr(out_bf16), M, N, K, _ptr(workspace),
                            workspace_bytes, ctypes.byref(o), _stream(stream))
     _check(st, "fp4_linear")
+
+
+def fp4_linear_grouped_workspace_size(total_M, E, K) -> int:
+    return load().fp4_linear_grouped_workspace_size(total_M, E, K)
+
+
+def fp4_linear_grouped(x_bf16, row_offsets, E, total_M, w, sw, bias_bf16, out_bf16, N, K, workspace,
+                       workspace_bytes=None, scale_alg=None, stream=None):
+    """MoE form of fp4_linear: grouped act-quant then grouped GEMM."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    st = load().fp4_linear_grouped(_ptr(x_bf16), _ptr(row_offsets), E, total_M, _ptr(w), _ptr(sw), _ptr(bias_bf16),
+                                   _ptr(out_bf16), N, K, _ptr(workspace), workspace_bytes, _opts(scale_alg, None),
+                                   _stream(stream))
+    _check(st, "fp4_linear_grouped")
 
 
 def fp4_gemm_w4a8_workspace_size(M, N, K) -> int:

@@ -118,6 +118,9 @@ def test_argument_checks_precede_device_use(L):
     assert raw.fp4_linear(256, 256, 256, None, 256, 4, 8, 128, 320, 1 << 20, ctypes.byref(o_ok), None) == 3  # align
     assert raw.fp4_linear(None, None, None, None, None, 0, 8, 128, None, 0, None, None) == 0               # M = 0
     assert raw.fp4_linear_workspace_size(4, 8, 128, ctypes.byref(o_bad)) == 0
+    assert raw.fp4_linear_grouped(256, 256, 0, 8, 256, 256, None, 256, 8, 128, 256, 1 << 20, None, None) == 2  # E
+    assert raw.fp4_linear_grouped(256, 256, 2, 8, 256, 256, None, 256, 8, 128, 256, 16, None, None) == 1     # ws
+    assert raw.fp4_linear_grouped_workspace_size(0, 2, 128) == 0
     # W4A8 fallback
     assert raw.fp4_gemm_w4a8(16, 16, 32, 16, None, 16, 1, 8, 192, None, 0, None) == 2           # K % 128
     assert raw.fp4_gemm_w4a8(16, 16, 48, 16, None, 16, 1, 8, 128, None, 0, None) == 3           # b 32 B

@@ -84,3 +84,31 @@ def test_linear_rejects_small_workspace(L):
     with pytest.raises(L.Fp4Error) as err:
         L.fp4_linear(x, w, sw, None, out, M, N, K, ws, workspace_bytes=need - 1)
     assert err.value.status == L.FP4_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("counts,N,K", [([3, 0, 130, 1, 200], 136, 256), ([40] * 8, 512, 384)])
+@pytest.mark.parametrize("alg", [0, 2])
+def test_linear_grouped_matches_oracle(orc, L, counts, N, K, alg):
+    import torch
+
+    E = len(counts)
+    offsets = np.zeros(E + 1, np.int32)
+    offsets[1:] = np.cumsum(counts)
+    total = int(offsets[-1])
+    X = synth.bf16_normal(total + N, synth.S_ACT, (total, K), 1.0, 0.01, 16.0)
+    bs, sbs, sws = [], [], []
+    for e in range(E):
+        b, sb = _weight(orc, synth.bf16_normal(N * 10 + e, synth.S_WEIGHT, (N, K), 0.02))
+        bs.append(b)
+        sbs.append(sb)
+        sws.append(orc.sf_swizzle(sb))
+    bias = synth.bf16_normal(E + N, synth.S_BIAS, (E, N), 0.01)
+    ws = torch.zeros(L.fp4_linear_grouped_workspace_size(total, E, K), dtype=torch.uint8, device="cuda")
+    out = torch.full((total, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    L.fp4_linear_grouped(dev_bf16(X), dev(offsets), E, total, dev(np.stack(bs)), dev(np.concatenate(sws)),
+                         dev_bf16(bias), out, N, K, ws, scale_alg=alg)
+    assert L.fp4_get_device_status() == 0
+    aq, asf = orc.act_quant(X, alg, threads=THREADS)
+    ref, absum = orc.gemm_grouped(aq, asf, np.stack(bs), np.stack(sbs), bias, offsets, threads=THREADS)
+    ok, ratio = gemm_check(bf16_bits_host(out), ref, absum)
+    assert ok, f"max err/bound = {ratio}"
