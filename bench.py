@@ -9,6 +9,9 @@ W4A4 GEMM(s).  Workloads (seeded synthetic inputs, see synth/):
   prefill W[18432,7168] (~N(0,0.015)); M in {2048, 8192} (0.5 % outliers x16).
   moe     64 experts, gate_up [2048,4096] and down [4096,1024]; 4096 tokens
           routed top-8 -> 32768 grouped rows per projection.
+  stream  the load path instead of a serving step: a 60-layer NVFP4 model
+          streamed from page-locked host memory through the layer loader
+          (one step = the whole load; metric GB/s of source bytes).
 
 Timing: the inputs and outputs of a step are replicated into S buffer sets
 whose total exceeds twice the 129 MB L2, and one CUDA graph runs S
@@ -52,7 +55,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", choices=("decode", "prefill", "moe"), default="decode")
+    ap.add_argument("--workload", choices=("decode", "prefill", "moe", "stream"), default="decode")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--breakdown-reps", type=int, default=200)
@@ -529,6 +532,135 @@ def run_ours(args):
         pg.destroy_process_group()
 
 
+STREAM_DESC = ("layer-streamed load: 60 layers of q,k,v,o [7168,7168] + MLP [18432,7168] NVFP4 from page-locked "
+               "host memory, requantized into MXFP4 destinations allocated up front through one staging buffer; "
+               "layers 0 and 59 FP8-E4M3 pass-through")
+
+
+def run_stream(args):
+    """One step = the whole 60-layer load through the loader (copy-engine
+    upload into the staging buffer overlapped with the requant kernels).
+    The host bytes are generated once before timing: three distinct NVFP4
+    layers served in turn to the 58 requantized layers, one FP8 layer to
+    both pass-through layers.  Afterwards the requant kernels alone are
+    timed at the same shapes (one layer's tensors from the staging buffer
+    into eight layers' destinations, back to back on one stream)."""
+    import torch
+
+    world, rank, local, pg = dist_setup(args)
+    torch.cuda.set_device(local)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import synth
+    from nvfp4_mxfp4_w4a4_gb300 import fp4lin as L
+    from nvfp4_mxfp4_w4a4_gb300.loader import CudaExecutor, LayerSpec, LayerStreamLoader, TensorSpec
+
+    K = synth.HIDDEN4
+    tensors = tuple(TensorSpec(n, N, K) for n, N in synth.TENSORS4)
+    layers = [LayerSpec(i, tensors, i in synth.EXCLUDED4) for i in range(synth.LAYERS4)]
+    req_layers = [ly.index for ly in layers if not ly.excluded]
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    n_distinct = 3
+    host_nv = []
+    for ly in req_layers[:n_distinct]:
+        h = {}
+        for i, (name, _) in enumerate(synth.TENSORS4):
+            d = synth.workload4_tensor(ly, i)
+            h[name] = {"packed": pin(d["packed"]), "scale": pin(d["scale"]), "g": d["g"]}
+        host_nv.append(h)
+    host_fp8 = {name: {"fp8": pin(synth.workload4_tensor(synth.EXCLUDED4[0], i)["fp8"])}
+                for i, (name, _) in enumerate(synth.TENSORS4)}
+    slot_of = {ly: j % n_distinct for j, ly in enumerate(req_layers)}
+
+    def source(layer):
+        return host_fp8 if layer in synth.EXCLUDED4 else host_nv[slot_of[layer]]
+
+    ex = CudaExecutor()
+    ld = LayerStreamLoader(layers, ex, lambda n, k: L.fp4_sf_bytes(n, k))
+    src_bytes = (sum(t.nvfp4_bytes for t in tensors) * len(req_layers) +
+                 sum(t.N * t.K for t in tensors) * len(synth.EXCLUDED4))
+    warm = max(1, min(args.warmup, 3))
+    steps = max(1, min(args.steps, 5))
+    for _ in range(warm):
+        ld.load(source)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(pg)
+    torch.cuda.synchronize()
+    times = []
+    t_wall0 = time.perf_counter()
+    for _ in range(steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e0.record(ex.copy_stream)
+        ld.load(source)
+        e1c = torch.cuda.Event(enable_timing=True)
+        e1k = torch.cuda.Event(enable_timing=True)
+        e1c.record(ex.copy_stream)
+        e1k.record(ex.compute_stream)
+        torch.cuda.synchronize()
+        times.append(max(e0.elapsed_time(e1c), e0.elapsed_time(e1k)))
+    barrier(pg)
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    if L.fp4_get_device_status() != 0:
+        raise RuntimeError("device status reports a timeout")
+    ms = max_over_ranks(pg, statistics.fmean(times), device="cuda")
+    value = world * src_bytes / (ms * 1e-3) / 1e9
+
+    # the requant kernels alone at these shapes
+    st = ex.compute_stream
+    base = ld.staging.data_ptr()
+    g = host_nv[slot_of[req_layers[-1]]]
+    targets = req_layers[:8]
+
+    def requants():
+        for ly in targets:
+            for t in tensors:
+                c_off, s_off = ld.plan.slots[(ly, t.name)]
+                dc, ds = ld.dest[(ly, t.name)]
+                L.fp4_requant_nvfp4_to_mxfp4(base + c_off, base + s_off, g[t.name]["g"], dc, ds, t.N, t.K, stream=st)
+
+    requants()
+    torch.cuda.synchronize()
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 3
+    r0.record(st)
+    for _ in range(reps):
+        requants()
+    r1.record(st)
+    torch.cuda.synchronize()
+    us_layer = r0.elapsed_time(r1) * 1e3 / (reps * len(targets))
+    req_bytes = sum(t.N * t.K for t in tensors) * REQ_B
+    req_gbps = req_bytes / (us_layer * 1e-6) / 1e9
+    hbm_peak, _, peak_kind = peaks()
+    result = {
+        "metric": "layer-streamed load GB/s (NVFP4 + FP8 source bytes from page-locked host memory)",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": warm,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u8 (fp4 / fp8 codes, e4m3 / e8m0 scales)", "data": "synthetic (seeded)",
+        "config": {"workload": STREAM_DESC, "name": "stream",
+                   "host_source": f"{n_distinct} distinct NVFP4 layers served in turn, one FP8 layer for both "
+                                  "pass-through layers, generated before timing",
+                   "parallelism": f"replicas x{world}"},
+        "source_bytes_per_step": src_bytes, "ledger": ld.ledger,
+        "requant_us_per_layer": round(us_layer, 2), "requant_GBps": round(req_gbps, 1),
+        "roofline": {"kernel": "requant_flat_kernel", "bound": "hbm", "achieved": round(req_gbps, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(req_gbps / hbm_peak, 3), "traffic": None,
+                     "peak_source": f"MEASURED_PEAKS hbm_gbs (of {peak_kind})",
+                     "algorithmic": "requant 1.09375 B/element, five tensors of a layer per unit"},
+        "e2e": {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": src_bytes, "d2h_bytes_per_step": 0},
+        "gpu_launches": len(req_layers) * len(tensors) * steps, "clocks": clk,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if rank == 0:
+        print(json.dumps(result))
+    if pg is not None:
+        pg.destroy_process_group()
+
+
 class NvAct:
     """The NVFP4 x NVFP4 path of "[SGLang] FP4 ..." sections 5-6 on the same
     bf16 activations and NVFP4 weight: NVFP4 act-quant with swizzled scales,
@@ -877,5 +1009,7 @@ if __name__ == "__main__":
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.workload == "stream":
+        run_stream(a)
     else:
         run_ours(a)

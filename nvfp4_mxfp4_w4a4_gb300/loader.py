@@ -122,7 +122,9 @@ class LayerStreamLoader:
 
     def load(self, source, start: int = 0):
         """Streams layers [start, n).  `source(layer)` returns, per tensor
-        name, either dict(packed, scale, g) (NVFP4 host arrays) or dict(fp8)."""
+        name, either dict(packed, scale, g) (NVFP4 host arrays) or dict(fp8);
+        with `CudaExecutor` the arrays may also be page-locked uint8 torch
+        tensors, which are uploaded without a host-side copy."""
         self.loaded = start
         for L in self.layers[start:]:
             try:
@@ -174,8 +176,17 @@ class CudaExecutor:
         return t
 
     def _pinned_copy(self, key, arr):
+        """Page-locked bytes of `arr` for an asynchronous upload.  A
+        page-locked contiguous uint8 torch tensor is used as it is (its owner
+        leaves it unchanged until the loader has synchronised); anything else
+        is copied into a page-locked buffer kept per slot."""
         import numpy as np
 
+        torch = self.torch
+        if isinstance(arr, torch.Tensor):
+            if not (arr.is_pinned() and arr.dtype == torch.uint8 and arr.is_contiguous()):
+                raise ValueError("tensor sources must be page-locked, contiguous uint8")
+            return arr.reshape(-1)
         flat = np.ascontiguousarray(arr).reshape(-1).view(np.uint8)
         buf = self._pinned.get(key)
         if buf is None or buf.numel() < flat.size:

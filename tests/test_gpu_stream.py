@@ -119,3 +119,47 @@ def test_full_layer_stream(orc):
     print(f"\nlayer stream: {len(layers)} layers in {wall:.1f} s wall (host generation bound); "
           f"destination {ledger['destination_bytes'] / 1e9:.2f} GB, staging {ledger['staging_bytes'] / 1e6:.1f} MB, "
           f"one layer {one_layer / 1e6:.1f} MB, device free before/after alloc {free0 / 1e9:.1f}/{free1 / 1e9:.1f} GB")
+
+
+def test_page_locked_tensor_source(orc):
+    """Page-locked torch tensors as the source are uploaded without a host
+    copy and load the same bytes as numpy arrays (three layers of 256-row
+    tensors, layer 0 an FP8 pass-through); a pageable tensor is refused."""
+    import torch
+
+    L = lib()
+    from nvfp4_mxfp4_w4a4_gb300.loader import CudaExecutor, LayerSpec, LayerStreamLoader, LoadError, TensorSpec
+
+    rows, K = 256, synth.HIDDEN4
+    tensors = tuple(TensorSpec(n, rows, K) for n, _ in synth.TENSORS4)
+    layers = [LayerSpec(i, tensors, i == 0) for i in range(3)]
+    gen = {ly: {name: synth.workload4_tensor(ly, i, rows=rows) for i, (name, _) in enumerate(synth.TENSORS4)}
+           for ly in range(3)}
+
+    def pinned(ly):
+        return {name: {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() if isinstance(v, np.ndarray) else v
+                       for k, v in d.items()} for name, d in gen[ly].items()}
+
+    loads = []
+    for source in (lambda ly: gen[ly], pinned):
+        ld = LayerStreamLoader(layers, CudaExecutor(), lambda n, k: L.fp4_sf_bytes(n, k))
+        assert ld.load(source) == 3
+        loads.append(ld)
+    assert L.fp4_get_device_status() == 0
+    for key, d in loads[0].dest.items():
+        other = loads[1].dest[key]
+        if isinstance(d, tuple):
+            assert all(torch.equal(x, y) for x, y in zip(d, other)), key
+        else:
+            assert torch.equal(d, other), key
+    # one requantized tensor against the oracle, all rows
+    h = gen[2]["mlp"]
+    p, s = orc.requant(h["packed"], h["scale"], h["g"], threads=THREADS)
+    dc, ds = loads[1].dest[(2, "mlp")]
+    assert np.array_equal(dc.view(rows, K // 2).cpu().numpy(), p)
+    assert np.array_equal(ds.cpu().numpy(), orc.sf_swizzle(s))
+
+    bad = LayerStreamLoader(layers, CudaExecutor(), lambda n, k: L.fp4_sf_bytes(n, k))
+    with pytest.raises(LoadError) as err:
+        bad.load(lambda ly: {name: {"fp8": torch.from_numpy(d["fp8"])} for name, d in gen[0].items()})
+    assert err.value.layer == 0 and isinstance(err.value.cause, ValueError)
