@@ -80,10 +80,21 @@ typedef enum { FP4_SCALE_OCP = 0, FP4_SCALE_UOS = 2 } fp4_scale_alg;
 
 typedef enum { FP4_SF_SWIZZLED = 0, FP4_SF_ROWMAJOR = 1 } fp4_sf_layout;
 
-/* Options for the quantizers.  A NULL pointer means {OCP, SWIZZLED}. */
+/* Quantizer flags.
+ *   FP4_QUANT_BF16_INTERMEDIATE  requantization only: round every decoded
+ *        NVFP4 value to bf16 (nearest, ties to even) before the MX block
+ *        rule, as an implementation that stages the dequantized weight in
+ *        bf16 would.  The pages do not say which precision their
+ *        dequantized intermediate has; the default is float32.  For bf16
+ *        inputs (the activation quantizers) the flag changes nothing.      */
+#define FP4_QUANT_BF16_INTERMEDIATE 1u
+
+/* Options for the quantizers.  A NULL pointer means {OCP, SWIZZLED, 0}.
+ * Unknown flag bits are rejected with FP4_ERR_INVALID_ARG.                */
 typedef struct {
     int32_t scale_alg;   /* fp4_scale_alg */
     int32_t sf_layout;   /* fp4_sf_layout */
+    uint32_t flags;      /* FP4_QUANT_* bits */
 } fp4_quant_opts;
 
 /* ------------------------------------------------------------------ sizes */
@@ -119,7 +130,8 @@ FP4LIN_API fp4_status fp4_get_device_status(void);
  *   out_packed    [N, K/2] u8    MXFP4 codes (device, caller-allocated)
  *   out_scale     E8M0 bytes     fp4_sf_bytes(N, K, layout) (device)
  *
- * Decoding: v = fp32((E2M1(c) * E4M3(s)) * w_global) (one rounding).
+ * Decoding: v = fp32((E2M1(c) * E4M3(s)) * w_global) (one rounding), then
+ * v = bf16(v) when opts->flags has FP4_QUANT_BF16_INTERMEDIATE.
  * Encoding per 32-block: amax, shared exponent by the chosen rule clamped
  * to [-127, 127], codes = nearest E2M1 of v / 2^e with ties to the even
  * code, saturating at +-6, sign always kept (-0 -> 0x8).  A block holding

@@ -60,18 +60,24 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 inline fp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FP4_OK : FP4_ERR_CUDA; }
 
-fp4_status check_opts(const fp4_quant_opts* opts, int* alg, int* swizzled)
+fp4_status check_opts(const fp4_quant_opts* opts, int* alg, int* swizzled, int* bf16 = nullptr)
 {
     *alg = FP4_SCALE_OCP;
     *swizzled = 1;
+    if (bf16)
+        *bf16 = 0;
     if (!opts)
         return FP4_OK;
     if (opts->scale_alg != FP4_SCALE_OCP && opts->scale_alg != FP4_SCALE_UOS)
         return FP4_ERR_INVALID_ARG;
     if (opts->sf_layout != FP4_SF_SWIZZLED && opts->sf_layout != FP4_SF_ROWMAJOR)
         return FP4_ERR_INVALID_ARG;
+    if (opts->flags & ~FP4_QUANT_BF16_INTERMEDIATE)
+        return FP4_ERR_INVALID_ARG;
     *alg = opts->scale_alg;
     *swizzled = opts->sf_layout == FP4_SF_SWIZZLED ? 1 : 0;
+    if (bf16)
+        *bf16 = (opts->flags & FP4_QUANT_BF16_INTERMEDIATE) ? 1 : 0;
     return FP4_OK;
 }
 
@@ -144,8 +150,8 @@ fp4_status fp4_requant_nvfp4_to_mxfp4_ex(const uint8_t* w_packed, const uint8_t*
                                          uint8_t* out_packed, uint8_t* out_scale, int64_t N, int64_t K,
                                          const fp4_quant_opts* opts, void* stream)
 {
-    int alg, swz;
-    fp4_status st = check_opts(opts, &alg, &swz);
+    int alg, swz, bf16;
+    fp4_status st = check_opts(opts, &alg, &swz, &bf16);
     if (st != FP4_OK)
         return st;
     if (!w_packed || !w_scale_e4m3 || !out_packed || !out_scale)
@@ -158,7 +164,7 @@ fp4_status fp4_requant_nvfp4_to_mxfp4_ex(const uint8_t* w_packed, const uint8_t*
     if ((st = current_device(nullptr)) != FP4_OK)
         return st;
     return from_cuda(fp4lin::launch_requant(w_packed, w_scale_e4m3, w_global, out_packed, out_scale, N, K, alg, swz,
-                                            static_cast<cudaStream_t>(stream)));
+                                            bf16, static_cast<cudaStream_t>(stream)));
 }
 
 fp4_status fp4_requant_nvfp4_to_mxfp4(const uint8_t* w_packed, const uint8_t* w_scale_e4m3, float w_global,
@@ -173,8 +179,8 @@ fp4_status fp4_requant_nvfp4_to_mxfp4_grouped(const uint8_t* w_packed, const uin
                                               int32_t E, int64_t N, int64_t K, const fp4_quant_opts* opts,
                                               void* stream)
 {
-    int alg, swz;
-    fp4_status st = check_opts(opts, &alg, &swz);
+    int alg, swz, bf16;
+    fp4_status st = check_opts(opts, &alg, &swz, &bf16);
     if (st != FP4_OK)
         return st;
     if (!w_packed || !w_scale_e4m3 || !w_global || !out_packed || !out_scale)
@@ -188,7 +194,7 @@ fp4_status fp4_requant_nvfp4_to_mxfp4_grouped(const uint8_t* w_packed, const uin
     if ((st = current_device(nullptr)) != FP4_OK)
         return st;
     return from_cuda(fp4lin::launch_requant_grouped(w_packed, w_scale_e4m3, w_global, out_packed, out_scale, E, N, K,
-                                                    alg, swz, static_cast<cudaStream_t>(stream)));
+                                                    alg, swz, bf16, static_cast<cudaStream_t>(stream)));
 }
 
 static fp4_status act_quant_common(const void* x_bf16, const void* mul, uint8_t* out_packed, uint8_t* out_scale,
@@ -525,7 +531,7 @@ fp4_status fp4_linear(const void* x_bf16, const uint8_t* w, const uint8_t* sw, c
     if (pl.fmt == fp4lin::kGemmW4A8)
         st = act_quant8_common(x_bf16, mul, a, sa, M, K, FP4_SF_SWIZZLED, stream);
     else {
-        const fp4_quant_opts qo = {pl.alg, FP4_SF_SWIZZLED};
+        const fp4_quant_opts qo = {pl.alg, FP4_SF_SWIZZLED, 0u};
         st = act_quant_common(x_bf16, mul, a, sa, M, K, &qo, stream);
     }
     if (st != FP4_OK)

@@ -68,13 +68,14 @@ constexpr int kMaxGroupedExperts = 1024;
 // Upper bound of every bounded device wait (nanoseconds of wall time).
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
+// alg: 0 OCP, 2 UOS; bf16: round the decoded values to bf16 first.
 cudaError_t launch_requant(const uint8_t* wp, const uint8_t* ws, float g, uint8_t* op, uint8_t* osf,
-                           int64_t N, int64_t K, int alg, int swizzled, cudaStream_t stream);
+                           int64_t N, int64_t K, int alg, int swizzled, int bf16, cudaStream_t stream);
 
 // E tensors [E][N][K/2] with global scales g_dev[E] (device); needs
 // requant_flat_ok (K % 128 == 0 and aligned arrays).
 cudaError_t launch_requant_grouped(const uint8_t* wp, const uint8_t* ws, const float* g_dev, uint8_t* op,
-                                   uint8_t* osf, int E, int64_t N, int64_t K, int alg, int swizzled,
+                                   uint8_t* osf, int E, int64_t N, int64_t K, int alg, int swizzled, int bf16,
                                    cudaStream_t stream);
 
 bool requant_flat_ok(const uint8_t* wp, const uint8_t* ws, const uint8_t* op, const uint8_t* osf, int64_t K,

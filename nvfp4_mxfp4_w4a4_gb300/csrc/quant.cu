@@ -98,17 +98,21 @@ __device__ __forceinline__ uint2 pack_code_map(uint32_t r1, uint32_t r2, uint32_
 
 // Code maps for one tensor (fixed global scale g).  Entry (s, d) holds the
 // map of a half-block with E4M3 scale byte s (sign cleared) when the block
-// exponent is e = er(s) + d, er(s) the unbiased exponent of P = RN(S |g|),
-// d in [-3, 5].  With S = value(s): the decoded magnitudes are H = RN(S/2 |g|),
-// P, Q = RN(1.5 S |g|) for codes 1..3 and the exact doublings 2P, 2Q, 4P, 4Q
-// for codes 4..7 (their overflow matches that of the direct product);
-// multiplying by 2^-e is exact except in deep underflow, where every code
-// is 0 anyway.  A half whose largest code is m >= 1 has amax >= H, so its
-// block exponent is >= er - 3; at d >= 6 every magnitude is below 2^(e-2)
-// and maps to 0 (entry 9).  A half of zero codes reads 0 from any entry.
-// Exponents outside [-127, 126] never occur for a finite block and stay 0.
-// The doubling codes of entry d are the plain codes of entry d - 1
-// (2 x_d = x_{d-1}), so each further entry costs three roundings.
+// exponent is e = er(s) + d, er(s) the unbiased exponent of P, d in [-3, 5].
+// With S = value(s), the decoded magnitude of code k is D(k) =
+// RN(E2M1(k) S |g|), rounded once more to bf16 when the intermediate is bf16:
+// H, P, Q for codes 1..3.  For codes 4..7, D is 2P, 2Q, 4P, 4Q exactly when
+// S |g| >= 2^-125 (doubling commutes with rounding to a normal float32 or
+// bf16 value, overflow included); below that the products are subnormal,
+// where a doubled rounded value can sit one ulp from the rounded double, so
+// those four are rounded one by one.  Multiplying by 2^-e is exact except in
+// deep underflow, where every code is 0 anyway.  A half whose largest code
+// is m >= 1 has amax >= H, so its block exponent is >= er - 3; at d >= 6
+// every magnitude is below 2^(e-2) and maps to 0 (entry 9).  A half of zero
+// codes reads 0 from any entry.  Exponents outside [-127, 126] never occur
+// for a finite block and stay 0.  Where the doublings hold, the codes 4..7
+// of entry d are the codes 2..5 of entry d - 1 (2 x_d = x_{d-1}), so each
+// further entry costs three roundings.
 constexpr int kMapD = 10;
 constexpr int kMapEntries = 128 * kMapD;
 
@@ -126,20 +130,40 @@ struct RequantTables {
     uint8_t ter[128];
 };
 
-__device__ void build_code_maps(float ag, int uos, RequantTables& tb)
+// Table options: the block rule and the precision of the decoded values.
+constexpr int kRuleUos = 1;   // UOS block rule (else OCP)
+constexpr int kRuleBf16 = 2;  // decoded values rounded to bf16 before the block rule
+
+__device__ __forceinline__ float round_to_bf16(float x)
 {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+__device__ void build_code_maps(float ag, int rule, RequantTables& tb)
+{
+    const int uos = rule & kRuleUos;
+    const bool bf16 = (rule & kRuleBf16) != 0;
+    // decoded magnitude from an exact E2M1 x E4M3 product: one float32
+    // rounding, then bf16 for the bf16 intermediate
+    auto decode = [&](float cs) {
+        const float v = __fmul_rn(cs, ag);
+        return bf16 ? round_to_bf16(v) : v;
+    };
     uint2* __restrict__ map = tb.map;
     for (int i = threadIdx.x; i < 128 * 8; i += blockDim.x) {
         const float S = fabsf(e4m3x2_to_float2(static_cast<uint32_t>(i >> 3)).x);
-        const float amax = __fmul_rn(__fmul_rn(e2m1_mag_value(static_cast<uint32_t>(i & 7)), S), ag);
+        const float amax = decode(__fmul_rn(e2m1_mag_value(static_cast<uint32_t>(i & 7)), S));
         const uint32_t ab = __float_as_uint(amax);
         tb.texp[i] = ab >= 0x7F800000u ? uint8_t(255) : static_cast<uint8_t>(mx_shared_exp(ab, uos) + 127);
     }
     for (int sb = threadIdx.x; sb < 128; sb += blockDim.x) {
         const float S = e4m3x2_to_float2(static_cast<uint32_t>(sb)).x;
-        const float H = __fmul_rn(0.5f * S, ag);
-        const float P = __fmul_rn(S, ag);
-        const float Q = __fmul_rn(1.5f * S, ag);
+        const float H = decode(0.5f * S);
+        const float P = decode(S);
+        const float Q = decode(1.5f * S);
+        // codes 4..7 as doublings of P and Q where that is exact (2^-125 = biased exponent 2)
+        const bool dbl = __fmul_rn(S, ag) >= __uint_as_float(2u << 23);
+        const float P2 = decode(2.0f * S), Q2 = decode(3.0f * S), P4 = decode(4.0f * S), Q4 = decode(6.0f * S);
         tb.ter[sb] = static_cast<uint8_t>(__float_as_uint(P) >> 23);
         const int er = static_cast<int>(__float_as_uint(P) >> 23) - 127;
         uint32_t p2 = 0u, p3 = 0u, p4 = 0u, p5 = 0u;
@@ -154,16 +178,21 @@ __device__ void build_code_maps(float ag, int uos, RequantTables& tb)
                 const uint32_t r2 = __float_as_uint(e2m1_code_scaled<0>(x));
                 const uint32_t r3 = __float_as_uint(e2m1_code_scaled<0>(y));
                 uint32_t r4, r5, r6, r7;
-                if (prev) {
+                if (dbl && prev) {
                     r4 = p2;
                     r5 = p3;
                     r6 = p4;
                     r7 = p5;
-                } else {
+                } else if (dbl) {
                     r4 = __float_as_uint(e2m1_code_scaled<1>(x));
                     r5 = __float_as_uint(e2m1_code_scaled<1>(y));
                     r6 = __float_as_uint(e2m1_code_scaled<2>(x));
                     r7 = __float_as_uint(e2m1_code_scaled<2>(y));
+                } else {
+                    r4 = __float_as_uint(e2m1_code_scaled<0>(__fmul_rn(P2, se)));
+                    r5 = __float_as_uint(e2m1_code_scaled<0>(__fmul_rn(Q2, se)));
+                    r6 = __float_as_uint(e2m1_code_scaled<0>(__fmul_rn(P4, se)));
+                    r7 = __float_as_uint(e2m1_code_scaled<0>(__fmul_rn(Q4, se)));
                 }
                 m = pack_code_map(r1, r2, r3, r4, r5, r6, r7);
                 p2 = r2;
@@ -276,12 +305,12 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const uint8_t* __rest
                                                            const uint8_t* __restrict__ ws, float g,
                                                            uint8_t* __restrict__ op, uint8_t* __restrict__ osf,
                                                            int64_t N, int64_t K, int64_t rows, int kb, int kbp,
-                                                           int nch, int uos, int swizzled)
+                                                           int nch, int rule, int swizzled)
 {
     __shared__ RequantTables tb;
     const float ag = fabsf(g);
     const uint32_t gsign = __float_as_uint(g) >> 31;
-    build_code_maps(ag, uos, tb);  // needs no global memory: overlaps the previous kernel
+    build_code_maps(ag, rule, tb);  // needs no global memory: overlaps the previous kernel
     __syncthreads();
     grid_dependency_wait();
     launch_dependents();
@@ -358,19 +387,19 @@ __global__ void __launch_bounds__(kThreads) requant_flat_kernel(const uint8_t* _
                                                                 uint8_t* __restrict__ op, uint8_t* __restrict__ osf,
                                                                 int64_t N, int64_t K, int64_t rows_pad, int kb,
                                                                 int64_t items, int ctas_per_e, int64_t sf_e_bytes,
-                                                                int uos, int swizzled, DivMagic kb_div, int idx32)
+                                                                int rule, int swizzled, DivMagic kb_div, int idx32)
 {
     __shared__ RequantTables tb;
     const int e = kGrouped ? static_cast<int>(blockIdx.x) / ctas_per_e : 0;
     const int local = kGrouped ? static_cast<int>(blockIdx.x) - e * ctas_per_e : static_cast<int>(blockIdx.x);
     float g = g_dense;
     if (!kGrouped)
-        build_code_maps(fabsf(g), uos, tb);  // needs no global memory: overlaps the previous kernel
+        build_code_maps(fabsf(g), rule, tb);  // needs no global memory: overlaps the previous kernel
     grid_dependency_wait();
     launch_dependents();
     if (kGrouped) {
         g = __ldg(g_dev + e);
-        build_code_maps(fabsf(g), uos, tb);
+        build_code_maps(fabsf(g), rule, tb);
     }
     __syncthreads();
     const float ag = fabsf(g);
@@ -819,13 +848,12 @@ bool requant_flat_ok(const uint8_t* wp, const uint8_t* ws, const uint8_t* op, co
 
 // Flat kernel over E tensors (E = 1: dense, g_dev unused).
 cudaError_t launch_requant_flat(const uint8_t* wp, const uint8_t* ws, float g, const float* g_dev, uint8_t* op,
-                                uint8_t* osf, int E, int64_t N, int64_t K, int alg, int swizzled, cudaStream_t stream)
+                                uint8_t* osf, int E, int64_t N, int64_t K, int rule, int swizzled, cudaStream_t stream)
 {
     const int kb = static_cast<int>(K / 32);
     const int64_t rows_pad = swizzled ? ceil_div(N, 128) * 128 : N;
     const int64_t items = ceil_div(rows_pad * kb, 128);  // warp items per tensor
     const int64_t sf_e_bytes = rows_pad * kb;            // swizzled bytes per tensor (kb % 4 == 0)
-    const int uos = alg == 2 ? 1 : 0;
     const int64_t want = ceil_div(items * 32, kThreads);  // CTAs that give every warp one item
     // a lane's first block index f < items * 128 (pad rows included)
     const int idx32 = items * 128 <= int64_t(UINT32_MAX) ? 1 : 0;
@@ -834,39 +862,45 @@ cudaError_t launch_requant_flat(const uint8_t* wp, const uint8_t* ws, float g, c
         const int64_t blocks = std::min<int64_t>(want, resident_ctas(requant_flat_kernel<false>));
         return launch_pdl(requant_flat_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream,
                           wp, ws, g, static_cast<const float*>(nullptr), op, osf, N, K, rows_pad, kb, items,
-                          static_cast<int>(blocks), sf_e_bytes, uos, swizzled, kb_div, idx32);
+                          static_cast<int>(blocks), sf_e_bytes, rule, swizzled, kb_div, idx32);
     }
     const int64_t per_e = std::max<int64_t>(1, std::min<int64_t>(want, resident_ctas(requant_flat_kernel<true>) / E));
     return launch_pdl(requant_flat_kernel<true>, dim3(static_cast<unsigned>(per_e * E)), dim3(kThreads), 0, stream, wp,
-                      ws, 0.0f, g_dev, op, osf, N, K, rows_pad, kb, items, static_cast<int>(per_e), sf_e_bytes, uos,
+                      ws, 0.0f, g_dev, op, osf, N, K, rows_pad, kb, items, static_cast<int>(per_e), sf_e_bytes, rule,
                       swizzled, kb_div, idx32);
 }
 
+// rule bits for the code maps: the block rule and the decoded-value precision
+static int requant_rule(int alg, int bf16)
+{
+    return (alg == 2 ? kRuleUos : 0) | (bf16 ? kRuleBf16 : 0);
+}
+
 cudaError_t launch_requant(const uint8_t* wp, const uint8_t* ws, float g, uint8_t* op, uint8_t* osf, int64_t N,
-                           int64_t K, int alg, int swizzled, cudaStream_t stream)
+                           int64_t K, int alg, int swizzled, int bf16, cudaStream_t stream)
 {
     const int kb = static_cast<int>(K / 32);
     const int kbp = swizzled ? static_cast<int>(ceil_div(kb, 4) * 4) : kb;
     const int64_t rows = swizzled ? ceil_div(N, 128) * 128 : N;
     const int nch = static_cast<int>(ceil_div(kbp, 128));
     const int64_t warps = rows * nch;
-    const int uos = alg == 2 ? 1 : 0;
+    const int rule = requant_rule(alg, bf16);
     if (requant_flat_ok(wp, ws, op, osf, K, swizzled)) {
-        return launch_requant_flat(wp, ws, g, nullptr, op, osf, 1, N, K, alg, swizzled, stream);
+        return launch_requant_flat(wp, ws, g, nullptr, op, osf, 1, N, K, rule, swizzled, stream);
     } else {
         const int64_t blocks =
             std::min<int64_t>(ceil_div(warps * 32, kThreads), resident_ctas(requant_kernel));
         return launch_pdl(requant_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, wp,
-                          ws, g, op, osf, N, K, rows, kb, kbp, nch, uos, swizzled);
+                          ws, g, op, osf, N, K, rows, kb, kbp, nch, rule, swizzled);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_requant_grouped(const uint8_t* wp, const uint8_t* ws, const float* g_dev, uint8_t* op,
-                                   uint8_t* osf, int E, int64_t N, int64_t K, int alg, int swizzled,
+                                   uint8_t* osf, int E, int64_t N, int64_t K, int alg, int swizzled, int bf16,
                                    cudaStream_t stream)
 {
-    return launch_requant_flat(wp, ws, 0.0f, g_dev, op, osf, E, N, K, alg, swizzled, stream);
+    return launch_requant_flat(wp, ws, 0.0f, g_dev, op, osf, E, N, K, requant_rule(alg, bf16), swizzled, stream);
 }
 
 cudaError_t launch_act_quant(const void* x, uint8_t* op, uint8_t* osf, int64_t M, int64_t K, int alg,

@@ -48,7 +48,10 @@ class Fp4Error(RuntimeError):
 
 
 class fp4_quant_opts(ctypes.Structure):
-    _fields_ = [("scale_alg", ctypes.c_int32), ("sf_layout", ctypes.c_int32)]
+    _fields_ = [("scale_alg", ctypes.c_int32), ("sf_layout", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+FP4_QUANT_BF16_INTERMEDIATE = 1
 
 
 class fp4_linear_opts(ctypes.Structure):
@@ -139,11 +142,11 @@ def _stream(s):
     return s.cuda_stream
 
 
-def _opts(scale_alg, sf_layout):
-    if scale_alg is None and sf_layout is None:
+def _opts(scale_alg, sf_layout, flags=0):
+    if scale_alg is None and sf_layout is None and not flags:
         return None
     o = fp4_quant_opts(FP4_SCALE_OCP if scale_alg is None else scale_alg,
-                       FP4_SF_SWIZZLED if sf_layout is None else sf_layout)
+                       FP4_SF_SWIZZLED if sf_layout is None else sf_layout, flags)
     return ctypes.byref(o)
 
 
@@ -169,24 +172,27 @@ def fp4_get_device_status() -> int:
 
 
 def fp4_requant_nvfp4_to_mxfp4(w_packed, w_scale_e4m3, w_global, out_packed, out_scale, N, K, stream=None,
-                               scale_alg=None, sf_layout=None):
+                               scale_alg=None, sf_layout=None, bf16_intermediate=False):
+    """bf16_intermediate: round each decoded value to bf16 before the block rule."""
     L = load()
-    if scale_alg is None and sf_layout is None:
+    flags = FP4_QUANT_BF16_INTERMEDIATE if bf16_intermediate else 0
+    if scale_alg is None and sf_layout is None and not flags:
         st = L.fp4_requant_nvfp4_to_mxfp4(_ptr(w_packed), _ptr(w_scale_e4m3), float(w_global), _ptr(out_packed),
                                           _ptr(out_scale), N, K, _stream(stream))
     else:
         st = L.fp4_requant_nvfp4_to_mxfp4_ex(_ptr(w_packed), _ptr(w_scale_e4m3), float(w_global),
                                              _ptr(out_packed), _ptr(out_scale), N, K,
-                                             _opts(scale_alg, sf_layout), _stream(stream))
+                                             _opts(scale_alg, sf_layout, flags), _stream(stream))
     _check(st, "fp4_requant_nvfp4_to_mxfp4")
 
 
 def fp4_requant_nvfp4_to_mxfp4_grouped(w_packed, w_scale_e4m3, w_global, out_packed, out_scale, E, N, K,
-                                       stream=None, scale_alg=None, sf_layout=None):
+                                       stream=None, scale_alg=None, sf_layout=None, bf16_intermediate=False):
     """w_global: device array of E float32 global scales."""
+    flags = FP4_QUANT_BF16_INTERMEDIATE if bf16_intermediate else 0
     st = load().fp4_requant_nvfp4_to_mxfp4_grouped(_ptr(w_packed), _ptr(w_scale_e4m3), _ptr(w_global),
                                                    _ptr(out_packed), _ptr(out_scale), E, N, K,
-                                                   _opts(scale_alg, sf_layout), _stream(stream))
+                                                   _opts(scale_alg, sf_layout, flags), _stream(stream))
     _check(st, "fp4_requant_nvfp4_to_mxfp4_grouped")
 
 

@@ -63,6 +63,7 @@ def lib():
                 ("orc_mx_quantize_block", None, [_p, ctypes.c_int, _p, _p]),
                 ("orc_nvfp4_dequant", None, [_p, _p, ctypes.c_float, _i64, _i64, _p]),
                 ("orc_requant", None, [_p, _p, ctypes.c_float, _i64, _i64, _i64, ctypes.c_int, _p, _p]),
+                ("orc_requant_bf16", None, [_p, _p, ctypes.c_float, _i64, _i64, _i64, ctypes.c_int, _p, _p]),
                 ("orc_act_quant", None, [_p, _i64, _i64, _i64, ctypes.c_int, _p, _p]),
                 ("orc_gemm", None, [_p, _p, _p, _p, _p, _i64, _p, _i64, _p, _i64, _p, _p]),
                 ("orc_bf16_encode", ctypes.c_uint16, [ctypes.c_float]),
@@ -155,8 +156,9 @@ def nvfp4_dequant(w_packed: np.ndarray, w_scale: np.ndarray, g: float) -> np.nda
     return out
 
 
-def requant(w_packed, w_scale, g, alg=SCALE_OCP, threads=1):
-    """NVFP4 -> MXFP4; returns (packed [N, K/2] u8, row-major E8M0 [N, K/32] u8)."""
+def requant(w_packed, w_scale, g, alg=SCALE_OCP, threads=1, bf16=False):
+    """NVFP4 -> MXFP4; returns (packed [N, K/2] u8, row-major E8M0 [N, K/32] u8).
+    bf16: round each decoded value to bf16 before the block rule."""
     w_packed = np.ascontiguousarray(w_packed)
     w_scale = np.ascontiguousarray(w_scale)
     N, half = w_packed.shape
@@ -164,8 +166,9 @@ def requant(w_packed, w_scale, g, alg=SCALE_OCP, threads=1):
     out_p = np.empty((N, K // 2), np.uint8)
     out_s = np.empty((N, K // 32), np.uint8)
     L = lib()
-    _parallel(lambda r0, r1: L.orc_requant(_ptr(w_packed), _ptr(w_scale), g, r0, r1, K, alg,
-                                           _ptr(out_p), _ptr(out_s)), N, threads)
+    fn = L.orc_requant_bf16 if bf16 else L.orc_requant
+    _parallel(lambda r0, r1: fn(_ptr(w_packed), _ptr(w_scale), g, r0, r1, K, alg, _ptr(out_p), _ptr(out_s)),
+              N, threads)
     return out_p, out_s
 
 

@@ -55,6 +55,10 @@ void orc_nvfp4_dequant(const uint8_t* w_packed, const uint8_t* w_scale, float g,
 void orc_requant(const uint8_t* w_packed, const uint8_t* w_scale, float g,
                  int64_t row0, int64_t row1, int64_t K, int alg,
                  uint8_t* out_packed, uint8_t* out_sf);
+/* The same with each decoded value rounded to bf16 before the block rule. */
+void orc_requant_bf16(const uint8_t* w_packed, const uint8_t* w_scale, float g,
+                      int64_t row0, int64_t row1, int64_t K, int alg,
+                      uint8_t* out_packed, uint8_t* out_sf);
 /* Dynamic MXFP4 quantization of bf16 activations ([AMD] serve-time path).  */
 void orc_act_quant(const uint16_t* x_bf16, int64_t row0, int64_t row1, int64_t K,
                    int alg, uint8_t* out_packed, uint8_t* out_sf);

@@ -84,6 +84,9 @@ def test_argument_checks_precede_device_use(L):
 
     bad = fp4_quant_opts(1, 0)
     assert raw.fp4_quant_act_mxfp4(16, 16, 16, 4, 32, ctypes.byref(bad), None) == 1
+    bad_flag = fp4_quant_opts(0, 0, 2)                                  # unknown flag bit
+    assert raw.fp4_requant_nvfp4_to_mxfp4_ex(16, 16, 1.0, 16, 16, 4, 32, ctypes.byref(bad_flag), None) == 1
+    assert raw.fp4_quant_act_mxfp4(16, 16, 16, 4, 32, ctypes.byref(bad_flag), None) == 1
     # NVFP4 side path
     assert raw.fp4_gemm_nvfp4(16, 16, 16, 16, 1.0, None, 16, 1, 8, 192, None, 0, None) == 2     # K % 128
     assert raw.fp4_gemm_nvfp4(16, None, 16, 16, 1.0, None, 16, 1, 8, 128, None, 0, None) == 1    # no scales

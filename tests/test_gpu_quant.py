@@ -18,20 +18,20 @@ def L():
     return lib()
 
 
-def _kernel_requant(L, packed, scale, g, alg, layout):
+def _kernel_requant(L, packed, scale, g, alg, layout, bf16=False):
     N, half = packed.shape
     K = 2 * half
     dp, ds = dev(packed), dev(scale)
     op = empty_u8(N * K // 2)
     osf = empty_u8(L.fp4_sf_bytes(N, K, layout))
-    L.fp4_requant_nvfp4_to_mxfp4(dp, ds, g, op, osf, N, K, scale_alg=alg, sf_layout=layout)
+    L.fp4_requant_nvfp4_to_mxfp4(dp, ds, g, op, osf, N, K, scale_alg=alg, sf_layout=layout, bf16_intermediate=bf16)
     assert L.fp4_get_device_status() == 0
     return host(op)[: N * K // 2].reshape(N, K // 2), host(osf)[: L.fp4_sf_bytes(N, K, layout)]
 
 
-def _check_requant(orc, L, packed, scale, g, alg=OCP, layout=SWZ):
-    kp, ks = _kernel_requant(L, packed, scale, g, alg, layout)
-    rp, rs = orc.requant(packed, scale, g, alg, threads=THREADS)
+def _check_requant(orc, L, packed, scale, g, alg=OCP, layout=SWZ, bf16=False):
+    kp, ks = _kernel_requant(L, packed, scale, g, alg, layout, bf16)
+    rp, rs = orc.requant(packed, scale, g, alg, threads=THREADS, bf16=bf16)
     assert np.array_equal(kp, rp), f"codes differ at {np.argwhere(kp != rp)[:5]}"
     expect_sf = orc.sf_swizzle(rs) if layout == SWZ else rs.reshape(-1)
     assert np.array_equal(ks, expect_sf), f"scales differ at {np.argwhere(ks != expect_sf)[:5]}"
@@ -99,7 +99,7 @@ def test_requant_16_byte_aligned_buffers(orc, L):
     assert np.array_equal(host(osf), orc.sf_swizzle(rs))
 
 
-def _check_requant_grouped(orc, L, packed, scale, gs, alg, layout):
+def _check_requant_grouped(orc, L, packed, scale, gs, alg, layout, bf16=False):
     import torch
 
     E, N, half = packed.shape
@@ -109,12 +109,12 @@ def _check_requant_grouped(orc, L, packed, scale, gs, alg, layout):
     osf = empty_u8(E * per)
     gdev = torch.from_numpy(np.asarray(gs, np.float32)).cuda()
     L.fp4_requant_nvfp4_to_mxfp4_grouped(dev(packed), dev(scale), gdev, op, osf, E, N, K, scale_alg=alg,
-                                         sf_layout=layout)
+                                         sf_layout=layout, bf16_intermediate=bf16)
     assert L.fp4_get_device_status() == 0
     hp = host(op)[: E * N * K // 2].reshape(E, N, K // 2)
     hs = host(osf)[: E * per].reshape(E, per)
     for e in range(E):
-        rp, rs = orc.requant(packed[e], scale[e], float(gs[e]), alg, threads=THREADS)
+        rp, rs = orc.requant(packed[e], scale[e], float(gs[e]), alg, threads=THREADS, bf16=bf16)
         assert np.array_equal(hp[e], rp), f"expert {e}: codes differ at {np.argwhere(hp[e] != rp)[:5]}"
         expect = orc.sf_swizzle(rs) if layout == SWZ else rs.reshape(-1)
         assert np.array_equal(hs[e], expect), f"expert {e}: scales differ at {np.argwhere(hs[e] != expect)[:5]}"
@@ -139,6 +139,55 @@ def test_requant_grouped_special_scales(orc, L):
     gs = np.float32([0.0, -0.0, np.inf, np.nan, 3.0e38, 1.0e-45])
     _check_requant_grouped(orc, L, packed, scale, gs, OCP, SWZ)
 
+
+
+# global scales that put S |g| among the float32 subnormals
+SUBNORMAL_G = [float(np.float32(np.ldexp(float(G), -149))) for G in (2796202, 1234567, 7777777, 3, 99991)]
+# a scale where bf16 rounding moves an element onto an E2M1 tie
+BF16_TIE_G = float(np.float32(0.875 * (1 - 2.0 ** -20)))
+
+
+@pytest.mark.parametrize("N,K", [(1, 32), (3, 96), (64, 256), (130, 1024)])
+@pytest.mark.parametrize("alg", [OCP, UOS])
+def test_requant_subnormal_products(orc, L, N, K, alg):
+    """Decoded values among the float32 subnormals, where the codes of
+    magnitudes 4..7 are not the doublings of codes 2..3 (row 0 block 0 is
+    the worked example: code 4 under scale 0.5625 next to the 0.75 tie)."""
+    rng = np.random.default_rng(N * 31 + K + alg)
+    packed, scale = _random_nvfp4(rng, N, K, 0, 0x7F)
+    packed[0, :16] = 0
+    packed[0, 0] = 0x04
+    scale[0, 0:2] = 0x31
+    for g in SUBNORMAL_G:
+        for layout in (SWZ, ROW):
+            _check_requant(orc, L, packed, scale, g, alg, layout)
+
+
+@pytest.mark.parametrize("N,K", [(1, 32), (5, 96), (130, 256), (300, 1024)])
+@pytest.mark.parametrize("alg", [OCP, UOS])
+@pytest.mark.parametrize("layout", [SWZ, ROW])
+def test_requant_bf16_intermediate(orc, L, N, K, alg, layout):
+    """FP4_QUANT_BF16_INTERMEDIATE: every scale byte and code, ordinary,
+    special and subnormal-product global scales; row 0 block 0 is the worked
+    example whose bf16 value lands on the q = 1.75 tie."""
+    rng = np.random.default_rng(N * 17 + K + alg + layout)
+    packed, scale = _random_nvfp4(rng, N, K)
+    packed[0, :16] = 0
+    packed[0, 0] = 0x62
+    scale[0, 0:2] = 0x38
+    for g in (1.0, 0.0037, -0.25, 2.0 ** -20, BF16_TIE_G, 3.0e38, 1.0e-38, float("nan"), SUBNORMAL_G[0]):
+        _check_requant(orc, L, packed, scale, float(np.float32(g)), alg, layout, bf16=True)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_requant_grouped_bf16_and_subnormal_scales(orc, L, bf16):
+    rng = np.random.default_rng(41)
+    E, N, K = 5, 70, 256
+    packed = rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
+    scale = rng.integers(0, 256, (E, N, K // 16), dtype=np.uint8)
+    gs = np.float32([0.0037, SUBNORMAL_G[0], BF16_TIE_G, -0.25, SUBNORMAL_G[2]])
+    for alg in (OCP, UOS):
+        _check_requant_grouped(orc, L, packed, scale, gs, alg, SWZ, bf16=bf16)
 
 # ---------------------------------------------------------------- activations
 def _kernel_act(L, x_bits, alg, layout):

@@ -208,6 +208,97 @@ def test_nvfp4_dequant_matches_float32_products(orc):
         assert np.array_equal(got.view(np.uint32), expect.astype(np.float32).view(np.uint32))
 
 
+
+def _decode_f32_indep(packed, scale, g32):
+    """NVFP4 decode with numpy float32 products over the hand E2M1 table and
+    torch's E4M3 decode (one float32 rounding of the product with g)."""
+    table = _e2m1_table()
+    cval = np.vectorize(lambda c: table[int(c)])(_unpack(packed)).astype(np.float32)
+    sval = _torch_e4m3(scale).astype(np.float32)
+    with np.errstate(over="ignore", invalid="ignore"):
+        return (cval * np.repeat(sval, 16, axis=1)) * np.float32(g32)
+
+
+def test_requant_subnormal_products_worked_example(orc):
+    """A block whose decoded values are float32 subnormals (the products
+    S * g lie below 2^-126): code 4 (2.0) under scale 0.5625 and
+    g = 2796202 * 2^-149 decodes to RN(3145727.25 * 2^-149) = 3145727 * 2^-149;
+    its amax is below 2^-125, so e = -127 (byte 0x00) and q = 3145727 * 2^-22
+    is just below 0.75: code 1 (0.5), not the tie 0.75 that doubling the
+    rounded value of code 2 would give."""
+    g = float(np.float32(np.ldexp(2796202.0, -149)))
+    packed = np.zeros((1, 16), np.uint8)
+    packed[0, 0] = 0x04
+    scale = np.full((1, 2), 0x31, np.uint8)
+    p, s = orc.requant(packed, scale, g)
+    assert p[0, 0] == 0x01 and not p[0, 1:].any() and s[0, 0] == 0x00
+
+
+def test_requant_subnormal_products_decode_then_quantize(orc):
+    """Tiny global scales: requant equals the (brute-force pinned) block
+    quantizer applied to an independent float32 decode, subnormals included."""
+    rng = np.random.default_rng(31)
+    N, K = 8, 128
+    packed = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scale = rng.integers(0, 0x7F, (N, K // 16), dtype=np.uint8)
+    for G in (2796202, 1234567, 7777777, 3, 99991):
+        g32 = np.float32(np.ldexp(float(G), -149))
+        v = _decode_f32_indep(packed, scale, g32)
+        for alg in (orc.SCALE_OCP, orc.SCALE_UOS):
+            p, s = orc.requant(packed, scale, float(g32), alg)
+            for r in range(N):
+                for b in range(K // 32):
+                    bp, bs = orc.mx_quantize_block(v[r, 32 * b:32 * b + 32], alg)
+                    assert np.array_equal(p[r, 16 * b:16 * b + 16], bp.reshape(-1)) and s[r, b] == bs, (G, alg, r, b)
+
+
+def test_requant_bf16_is_act_quant_of_bf16_decode(orc):
+    """The bf16-intermediate requant equals the activation quantizer (pinned
+    above) applied to the decoded values rounded to bf16 by torch."""
+    rng = np.random.default_rng(21)
+    N, K = 6, 256
+    packed = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scale = rng.integers(0, 256, (N, K // 16), dtype=np.uint8)         # negative and NaN scales too
+    for g in (1.0, 0.0037, -0.25, 2.0 ** -20, 3.0e38, 1.0e-38, 2.0 ** -133):
+        g32 = np.float32(g)
+        v = _decode_f32_indep(packed, scale, g32)
+        xb = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        for alg in (orc.SCALE_OCP, orc.SCALE_UOS):
+            want_p, want_s = orc.act_quant(xb, alg)
+            got_p, got_s = orc.requant(packed, scale, float(g32), alg, bf16=True)
+            assert np.array_equal(got_p, want_p) and np.array_equal(got_s, want_s), (g, alg)
+
+
+def test_requant_bf16_equals_float32_path_for_power_of_two_g(orc):
+    """E2M1 x E4M3 products carry at most 6 significant bits, so with g a
+    power of two (and the products normal) every decoded value is a bf16
+    value and both intermediates give the same bytes."""
+    rng = np.random.default_rng(22)
+    N, K = 6, 256
+    packed = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scale = rng.integers(0, 0x7F, (N, K // 16), dtype=np.uint8)
+    scale[:, ::3] |= 0x80
+    for k in (-100, -3, 0, 5, 100):
+        for alg in (orc.SCALE_OCP, orc.SCALE_UOS):
+            a = orc.requant(packed, scale, 2.0 ** k, alg)
+            b = orc.requant(packed, scale, 2.0 ** k, alg, bf16=True)
+            assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]), (k, alg)
+
+
+def test_requant_bf16_worked_example(orc):
+    """Where bf16 rounding crosses an E2M1 threshold: codes 2 (1.0) and 6
+    (4.0) under scale 1.0 with g = 0.875 (1 - 2^-20).  Both paths take
+    amax < 3.5, e = -1 (byte 126); element 0 has q = 1.75 (1 - 2^-20) in
+    float32, code 3 (1.5), but its bf16 value 0.875 gives the tie q = 1.75,
+    which goes to the even code 4 (2.0); element 1 saturates to code 7."""
+    g = float(np.float32(0.875 * (1 - 2.0 ** -20)))
+    packed = np.zeros((1, 16), np.uint8)
+    packed[0, 0] = 0x62
+    scale = np.full((1, 2), 0x38, np.uint8)
+    p32, s32 = orc.requant(packed, scale, g)
+    p16, s16 = orc.requant(packed, scale, g, bf16=True)
+    assert (p32[0, 0], s32[0, 0]) == (0x73, 126) and (p16[0, 0], s16[0, 0]) == (0x74, 126)
+
 # ------------------------------------------------------ invariants
 
 
