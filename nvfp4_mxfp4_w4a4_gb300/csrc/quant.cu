@@ -161,9 +161,6 @@ __device__ void build_code_maps(float ag, int rule, RequantTables& tb)
         const float H = decode(0.5f * S);
         const float P = decode(S);
         const float Q = decode(1.5f * S);
-        // codes 4..7 as doublings of P and Q where that is exact (2^-125 = biased exponent 2)
-        const bool dbl = __fmul_rn(S, ag) >= __uint_as_float(2u << 23);
-        const float P2 = decode(2.0f * S), Q2 = decode(3.0f * S), P4 = decode(4.0f * S), Q4 = decode(6.0f * S);
         tb.ter[sb] = static_cast<uint8_t>(__float_as_uint(P) >> 23);
         const int er = static_cast<int>(__float_as_uint(P) >> 23) - 127;
         uint32_t p2 = 0u, p3 = 0u, p4 = 0u, p5 = 0u;
@@ -178,21 +175,16 @@ __device__ void build_code_maps(float ag, int rule, RequantTables& tb)
                 const uint32_t r2 = __float_as_uint(e2m1_code_scaled<0>(x));
                 const uint32_t r3 = __float_as_uint(e2m1_code_scaled<0>(y));
                 uint32_t r4, r5, r6, r7;
-                if (dbl && prev) {
+                if (prev) {
                     r4 = p2;
                     r5 = p3;
                     r6 = p4;
                     r7 = p5;
-                } else if (dbl) {
+                } else {
                     r4 = __float_as_uint(e2m1_code_scaled<1>(x));
                     r5 = __float_as_uint(e2m1_code_scaled<1>(y));
                     r6 = __float_as_uint(e2m1_code_scaled<2>(x));
                     r7 = __float_as_uint(e2m1_code_scaled<2>(y));
-                } else {
-                    r4 = __float_as_uint(e2m1_code_scaled<0>(__fmul_rn(P2, se)));
-                    r5 = __float_as_uint(e2m1_code_scaled<0>(__fmul_rn(Q2, se)));
-                    r6 = __float_as_uint(e2m1_code_scaled<0>(__fmul_rn(P4, se)));
-                    r7 = __float_as_uint(e2m1_code_scaled<0>(__fmul_rn(Q4, se)));
                 }
                 m = pack_code_map(r1, r2, r3, r4, r5, r6, r7);
                 p2 = r2;
@@ -206,6 +198,24 @@ __device__ void build_code_maps(float ag, int rule, RequantTables& tb)
             map[sb * kMapD + di] = m;
         }
         map[sb * kMapD + 9] = make_uint2(0u, 0u);
+        // S |g| below 2^-125 (biased exponent 2): the doublings above are not
+        // exact there, so the codes of magnitudes 4..7 (the map's second
+        // word) are redone from one-by-one roundings
+        if (!(__fmul_rn(S, ag) >= __uint_as_float(2u << 23))) {
+#pragma unroll 1
+            for (int di = 0; di < 9; ++di) {
+                const int e = er + di - 3;
+                if (e >= -127 && e <= 126) {
+                    const float se = exp2_neg(e);
+                    // codes of the magnitudes 2S, 3S, 4S, 6S (times |g|), one per byte
+                    const uint32_t w = e2m1x8_pack(__fmul_rn(decode(2.0f * S), se), __fmul_rn(decode(3.0f * S), se),
+                                                   __fmul_rn(decode(4.0f * S), se), __fmul_rn(decode(6.0f * S), se),
+                                                   0.0f, 0.0f, 0.0f, 0.0f);
+                    map[sb * kMapD + di].y =
+                        (w & 0xFu) | ((w << 4) & 0xF00u) | ((w << 8) & 0xF0000u) | ((w << 12) & 0xF000000u);
+                }
+            }
+        }
     }
 }
 
@@ -379,9 +389,10 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const uint8_t* __rest
 // swizzled scale array; pad rows get zero scale bytes).  Grouped: E tensors of
 // the same shape stored back to back, each with its own global scale g[e]
 // (device array); a run of ctas_per_e CTAs serves one tensor, so a CTA builds
-// the code maps of one g only.
+// the code maps of one g only.  Launch bound: four CTAs per SM (at most 64
+// registers a thread), the occupancy the kernel is measured at.
 template <bool kGrouped>
-__global__ void __launch_bounds__(kThreads) requant_flat_kernel(const uint8_t* __restrict__ wp,
+__global__ void __launch_bounds__(kThreads, 4) requant_flat_kernel(const uint8_t* __restrict__ wp,
                                                                 const uint8_t* __restrict__ ws, float g_dense,
                                                                 const float* __restrict__ g_dev,
                                                                 uint8_t* __restrict__ op, uint8_t* __restrict__ osf,
