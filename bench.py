@@ -197,6 +197,32 @@ class Weight:
             setattr(c, k, getattr(self, k).clone())
         return c
 
+    def parts(self, n):
+        """About n contiguous pieces for a chunked upload: row ranges in
+        multiples of 128 (one tensor) or expert ranges (E > 1)."""
+        if self.E > 1:
+            step = -(-self.E // n)
+            return [(p, min(p + step, self.E)) for p in range(0, self.E, step)]
+        step = -(-(-(-self.N // n)) // 128) * 128
+        return [(p, min(p + step, self.N)) for p in range(0, self.N, step)]
+
+    def rows(self, p0, p1):
+        return (p0 * self.N, p1 * self.N) if self.E > 1 else (p0, p1)
+
+    def requant_part(self, s, p0, p1):
+        """Requantize one piece of parts(): the same calls on sub-ranges
+        (a 128-row multiple starts a whole swizzled scale tile)."""
+        N, K = self.N, self.K
+        if self.E > 1:
+            self.L.fp4_requant_nvfp4_to_mxfp4_grouped(
+                self.packed[p0 * N:p1 * N], self.scale[p0 * N:p1 * N], self.g_dev[p0:p1],
+                self.b_packed[p0 * N:p1 * N], self.b_scale[p0 * self.sf_bytes:p1 * self.sf_bytes], p1 - p0, N, K,
+                stream=s)
+            return
+        off = (p0 // 128) * (-(-(K // 32) // 4)) * 512
+        self.L.fp4_requant_nvfp4_to_mxfp4(self.packed[p0:p1], self.scale[p0:p1], self.g[0], self.b_packed[p0:p1],
+                                          self.b_scale[off:], p1 - p0, K, stream=s)
+
     def requant(self, s):
         N, K = self.N, self.K
         if self.E > 1:  # all experts in one launch
@@ -271,6 +297,22 @@ class Act:
         else:
             self.L.fp4_quant_act_mxfp4_grouped(self.x, self.offsets, self.E, self.M, self.K, self.a_packed,
                                                self.a_scale, stream=s)
+
+    def _sf_off(self, m0):
+        return (m0 // 128) * (-(-(self.K // 32) // 4)) * 512
+
+    def quant_rows(self, s, m0, m1):
+        """Dense: quantize rows [m0, m1) (m0 a multiple of 128)."""
+        self.L.fp4_quant_act_mxfp4(self.x[m0:m1], self.a_packed[m0:m1], self.a_scale[self._sf_off(m0):], m1 - m0,
+                                   self.K, stream=s)
+
+    def gemm_rows(self, s, m0, m1, static):
+        """Dense: output rows [m0, m1) (m0 a multiple of 128)."""
+        w = self.w
+        ws = gemm_workspace(self.L, self.torch, m1 - m0, w.N, self.K)
+        self.L.fp4_gemm_mxfp4_ex(self.a_packed[m0:m1], self.a_scale[self._sf_off(m0):], w.b_packed, w.b_scale,
+                                 w.bias, self.out[m0:m1], m1 - m0, w.N, self.K, ws,
+                                 flags=self.L.FP4_GEMM_WEIGHTS_STATIC if static else 0, stream=s)
 
     def gemm_static(self, s):
         """The dense GEMM stating that the weights are not written by the
@@ -816,65 +858,98 @@ def _committed_traffic(workload, kernel):
     return None
 
 
-def _e2e(b, torch, L, reps):
+def _e2e(b, torch, L, reps, w_parts=1, m_chunk=2048):
     """The same step through the C ABI with host buffers: H2D of the NVFP4
     weights and the activations from pinned memory, the step, D2H of the
     outputs, all inside the timed events.  The transfers overlap the
-    kernels the way a caller can arrange them with the same calls: the
-    activations are uploaded and quantized on one stream while the weights
-    upload on two copy streams (half of each tensor's rows each); the
-    requant starts when its weight has landed,
-    the GEMMs when both are done, and each output is downloaded as soon as
-    its GEMM has finished."""
+    kernels the way a caller can arrange them with the same calls on
+    sub-ranges: one copy stream uploads, in order, the small activation
+    batches, then each weight (in `w_parts` row or expert pieces, each
+    requantized as soon as it has landed), then the large batches.  A dense
+    batch of more than `m_chunk` rows goes in row chunks, each quantized,
+    multiplied and downloaded on its own, so the downloads of the first
+    chunks overlap the GEMMs of the later ones; every other output is
+    downloaded as soon as its GEMM has finished.  Measured on GB300: weight
+    pieces do not pay (each copy and launch has a fixed cost and the host
+    link is the bound: decode 255 us with one piece, 284 us with eight), the
+    row chunks do (prefill 2.68 ms against 3.24 ms unchunked)."""
     s, side = b.stream, b.side
-    up = [torch.cuda.Stream(), torch.cuda.Stream()]
-    down = torch.cuda.Stream()
-    host_w = [(w.packed.cpu().pin_memory(), w.scale.cpu().pin_memory()) for w in b.weights]
-    host_x = [a.x.cpu().pin_memory() for a in b.acts]
-    host_o = [torch.empty(a.out.shape, dtype=torch.bfloat16).pin_memory() for a in b.acts]
-    h2d = sum(p.numel() + q.numel() for p, q in host_w) + sum(x.numel() * 2 for x in host_x)
-    d2h = sum(o.numel() * 2 for o in host_o)
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
     weights, acts = b.sets[0]
+    with torch.cuda.stream(s):
+        b.step(s, 0)
+    torch.cuda.synchronize()
+    expect = [a.out.cpu() for a in acts]       # the ordinary step's outputs, to check the chunked one
+    host_w = {id(w): (w.packed.cpu().pin_memory(), w.scale.cpu().pin_memory()) for w in weights}
+    host_x = [a.x.cpu().pin_memory() for a in acts]
+    host_o = [torch.empty(a.out.shape, dtype=torch.bfloat16).pin_memory() for a in acts]
+    h2d = sum(p.numel() + q.numel() for p, q in host_w.values()) + sum(x.numel() * 2 for x in host_x)
+    d2h = sum(o.numel() * 2 for o in host_o)
+    small = [j for j, a in enumerate(acts) if a.x.numel() * 2 <= (4 << 20)]
+
+    def mark(st):
+        ev = torch.cuda.Event()
+        ev.record(st)
+        return ev
 
     def once(start):
-        for st in (side, up[0], up[1], down):
+        for st in (side, up, down):
             st.wait_event(start)
-        # activations: upload and quantize on the side stream
-        for a, x in zip(acts, host_x):
-            a.x.copy_(x, non_blocking=True)
-        for a in acts:
-            a.quant(side)
-        x_done = torch.cuda.Event()
-        x_done.record(side)
-        # weights: each tensor's rows split over the two copy streams
-        w_done = []
-        for w, (p, q) in zip(weights, host_w):
-            half = w.packed.shape[0] // 2
-            with torch.cuda.stream(up[0]):
-                w.packed[:half].copy_(p[:half], non_blocking=True)
-                w.scale.copy_(q, non_blocking=True)
-            with torch.cuda.stream(up[1]):
-                w.packed[half:].copy_(p[half:], non_blocking=True)
-            ev = [torch.cuda.Event(), torch.cuda.Event()]
-            ev[0].record(up[0])
-            ev[1].record(up[1])
-            w_done.append(ev)
-        for w, ev in zip(weights, w_done):
-            s.wait_event(ev[0])
-            s.wait_event(ev[1])
-            w.requant(s)
-        s.wait_event(x_done)
+        ready = {}
+        with torch.cuda.stream(up):
+            for j in small:
+                acts[j].x.copy_(host_x[j], non_blocking=True)
+        side.wait_event(mark(up))
+        for j in small:
+            acts[j].quant(side)
+            ready[j] = mark(side)
+        done_w = set()
+        after_gemm = False
         for j, a in enumerate(acts):
-            if j > 0 and a.offsets is None and acts[j - 1].offsets is None:
-                a.gemm_static(s)
-            else:
-                a.gemm(s)
-            g_done = torch.cuda.Event()
-            g_done.record(s)
-            down.wait_event(g_done)
-            with torch.cuda.stream(down):
-                host_o[j].copy_(a.out, non_blocking=True)
+            w = a.w
+            if id(w) not in done_w:
+                hp, hs = host_w[id(w)]
+                for p0, p1 in w.parts(w_parts):
+                    r0, r1 = w.rows(p0, p1)
+                    with torch.cuda.stream(up):
+                        w.packed[r0:r1].copy_(hp[r0:r1], non_blocking=True)
+                        w.scale[r0:r1].copy_(hs[r0:r1], non_blocking=True)
+                    s.wait_event(mark(up))
+                    w.requant_part(s, p0, p1)
+                done_w.add(id(w))
+                after_gemm = False
+            if j in small or a.offsets is not None or a.M <= m_chunk:
+                if j not in small:
+                    with torch.cuda.stream(up):
+                        a.x.copy_(host_x[j], non_blocking=True)
+                    side.wait_event(mark(up))
+                    a.quant(side)
+                    ready[j] = mark(side)
+                s.wait_event(ready[j])
+                if after_gemm and a.offsets is None:
+                    a.gemm_static(s)
+                else:
+                    a.gemm(s)
+                after_gemm = True
+                down.wait_event(mark(s))
+                with torch.cuda.stream(down):
+                    host_o[j].copy_(a.out, non_blocking=True)
+                continue
+            for m0 in range(0, a.M, m_chunk):
+                m1 = min(m0 + m_chunk, a.M)
+                with torch.cuda.stream(up):
+                    a.x[m0:m1].copy_(host_x[j][m0:m1], non_blocking=True)
+                side.wait_event(mark(up))
+                a.quant_rows(side, m0, m1)
+                s.wait_event(mark(side))
+                a.gemm_rows(s, m0, m1, static=after_gemm)
+                after_gemm = True
+                down.wait_event(mark(s))
+                with torch.cuda.stream(down):
+                    host_o[j][m0:m1].copy_(a.out[m0:m1], non_blocking=True)
         s.wait_stream(down)
+        s.wait_stream(side)
+        s.wait_stream(up)
 
     # one step = one CUDA graph launch (as a serving loop replays its step),
     # the transfers inside it; captured from an eager warm-up of the same calls
@@ -904,12 +979,16 @@ def _e2e(b, torch, L, reps):
     for _ in range(3):
         run()
     torch.cuda.synchronize()
+    for o, e in zip(host_o, expect):
+        if not torch.equal(o.view(torch.int16), e.view(torch.int16)):
+            raise RuntimeError("the chunked end-to-end step's outputs differ from the step's")
     ts = [run() for _ in range(reps)]
     ms = statistics.fmean(ts)
     return {"value": round(b.step_flops() / (ms * 1e-3) / 1e12, 4), "unit": "TFLOPS", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "path": "C ABI, pinned host buffers, H2D + step + D2H inside the events (transfers overlapped "
-                    "with the kernels on copy streams; one CUDA graph per step)"}
+            "path": "C ABI, pinned host buffers, H2D + step + D2H inside the events (one copy stream uploading "
+                    f"weights in ~{w_parts} pieces, each requantized on arrival; dense batches over {m_chunk} rows "
+                    "in row chunks; downloads on their own stream; one CUDA graph per step)"}
 
 
 # ------------------------------------------------------------------ CPU oracle
