@@ -151,15 +151,18 @@ class LayerStreamLoader:
 
 
 class CudaExecutor:
-    """Executor over torch device memory and libfp4lin."""
+    """Executor over torch device memory and libfp4lin.  scale_alg picks the
+    MX block rule; bf16_intermediate rounds the decoded NVFP4 values to bf16
+    before it (FP4_QUANT_BF16_INTERMEDIATE)."""
 
-    def __init__(self, scale_alg=0):
+    def __init__(self, scale_alg=0, bf16_intermediate=False):
         import torch
 
         from . import fp4lin as L
 
         self.torch, self.L = torch, L
         self.alg = scale_alg
+        self.bf16 = bool(bf16_intermediate)
         self.copy_stream = torch.cuda.Stream()
         self.compute_stream = torch.cuda.Stream()
         self._allocs = []
@@ -220,7 +223,8 @@ class CudaExecutor:
                 self.compute_stream.wait_event(self._copy_done[(slot, part)])
             base = staging.data_ptr()
             self.L.fp4_requant_nvfp4_to_mxfp4(base + c_off, base + s_off, g, dst_codes, dst_scale, t.N, t.K,
-                                              stream=self.compute_stream, scale_alg=self.alg)
+                                              stream=self.compute_stream, scale_alg=self.alg,
+                                              bf16_intermediate=self.bf16)
             ev = torch.cuda.Event()
             ev.record(self.compute_stream)
         self._readers = [r for r in self._readers if not r[2].query()]

@@ -158,6 +158,13 @@ def test_page_locked_tensor_source(orc):
     dc, ds = loads[1].dest[(2, "mlp")]
     assert np.array_equal(dc.view(rows, K // 2).cpu().numpy(), p)
     assert np.array_equal(ds.cpu().numpy(), orc.sf_swizzle(s))
+    # the bf16-intermediate option through the executor
+    ld16 = LayerStreamLoader(layers, CudaExecutor(bf16_intermediate=True), lambda n, k: L.fp4_sf_bytes(n, k))
+    assert ld16.load(pinned) == 3
+    p16, s16 = orc.requant(h["packed"], h["scale"], h["g"], threads=THREADS, bf16=True)
+    dc, ds = ld16.dest[(2, "mlp")]
+    assert np.array_equal(dc.view(rows, K // 2).cpu().numpy(), p16)
+    assert np.array_equal(ds.cpu().numpy(), orc.sf_swizzle(s16))
 
     bad = LayerStreamLoader(layers, CudaExecutor(), lambda n, k: L.fp4_sf_bytes(n, k))
     with pytest.raises(LoadError) as err:
