@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import synth
-from _util import THREADS, bf16_bits_host, dev, dev_bf16, empty_u8, gemm_check, host, lib
+from _util import THREADS, bf16_bits_host, bf16_bits_to_f64, dev, dev_bf16, empty_u8, gemm_check, host, lib
 
 pytestmark = pytest.mark.gpu
 
@@ -262,3 +262,62 @@ def test_gemm_nan_and_tiny_scales(orc, L):
     keep = ~nan_ref
     ok, ratio = gemm_check(out[keep], ref[keep], absum[keep])
     assert ok, f"max err/bound = {ratio}"
+
+
+# ---------------------------------------------------------------- one token (M = 1)
+@pytest.mark.parametrize("N,K", [(8, 128), (136, 1152), (1024, 4096), (264, 7168), (64, 32768), (16, 33024)])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_one_token_random_codes_nonuniform_scales(orc, L, N, K, with_bias):
+    """One token (the split-K swapped path): every FP4 code on both sides and
+    a different scale per 32-block, K up to 33024, within the GEMM bound."""
+    rng = np.random.default_rng(N + K + with_bias)
+    a = rng.integers(0, 256, (1, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = rng.integers(112, 142, (1, K // 32), dtype=np.uint8)
+    sb = rng.integers(112, 142, (N, K // 32), dtype=np.uint8)
+    bias = synth.bf16_normal(N + K, synth.S_BIAS, (N,), 0.5) if with_bias else None
+    out = _run_gemm(L, a, orc.sf_swizzle(sa), b, orc.sf_swizzle(sb), bias, 1, N, K)
+    ref, absum = orc.gemm(a, sa, b, sb, bias, threads=THREADS)
+    ok, ratio = gemm_check(out, ref, absum)
+    assert ok, f"max err/bound = {ratio}"
+
+
+def test_one_token_one_hot_is_exact(orc, L):
+    """B rows one-hot with code 1.0 under scale 2^0: out[0, n] is one A value
+    times its power-of-two scale, exact in bf16."""
+    rng = np.random.default_rng(21)
+    N, K = 264, 4096
+    a = rng.integers(0, 256, (1, K // 2), dtype=np.uint8)
+    sa = rng.integers(115, 140, (1, K // 32), dtype=np.uint8)
+    sel = rng.integers(0, K, N)
+    codes = np.zeros((N, K), np.uint8)
+    codes[np.arange(N), sel] = 0x2
+    b = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    sb = np.full((N, K // 32), 127, np.uint8)
+    out = _run_gemm(L, a, orc.sf_swizzle(sa), b, orc.sf_swizzle(sb), None, 1, N, K)
+    ref, _ = orc.gemm(a, sa, b, sb)
+    assert np.array_equal(bf16_bits_to_f64(out), ref)
+
+
+def test_one_token_nan_and_tiny_scales(orc, L):
+    """M = 1 with a NaN scale in one B block (that output is NaN), a NaN
+    scale in A (every output NaN) and scales near the bottom of the range."""
+    rng = np.random.default_rng(12)
+    N, K = 136, 1024
+    a = rng.integers(0, 256, (1, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = rng.integers(120, 134, (1, K // 32), dtype=np.uint8)
+    sb = rng.integers(120, 134, (N, K // 32), dtype=np.uint8)
+    sb[5, 7] = 0xFF
+    sb[9, :] = 0x10
+    sb[11, 3] = 0x01
+    out = _run_gemm(L, a, orc.sf_swizzle(sa), b, orc.sf_swizzle(sb), None, 1, N, K)
+    ref, absum = orc.gemm(a, sa, b, sb)
+    got = bf16_bits_to_f64(out)
+    assert np.array_equal(np.isnan(got), np.isnan(ref)) and np.isnan(ref[0, 5]) and np.isnan(ref).sum() == 1
+    keep = ~np.isnan(ref)
+    ok, ratio = gemm_check(out[keep], ref[keep], absum[keep])
+    assert ok, f"max err/bound = {ratio}"
+    sa[0, 2] = 0xFF
+    out = _run_gemm(L, a, orc.sf_swizzle(sa), b, orc.sf_swizzle(sb), None, 1, N, K)
+    assert np.isnan(bf16_bits_to_f64(out)).all()
