@@ -881,7 +881,7 @@ SplitPlan split_plan(int64_t tiles, int64_t nkb, int bn, int sms)
 void swap_config(int64_t M, int64_t K, int* bn, int* kc)
 {
     *kc = K % 256 == 0 ? 2 : 1;
-    *bn = (*kc == 2 && M <= 32) ? 32 : 64;
+    *bn = *kc == 2 ? (M <= 16 ? 16 : M <= 32 ? 32 : 64) : 64;
 }
 
 template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped, int kFmt = kFmtMx>
@@ -996,6 +996,8 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int fmt)
     int bn = 0, kc = 0;
     swap_config(M, K, &bn, &kc);
     int groups = 2 * kc;  // 128-element groups of K per stage
+    if (fmt == kGemmNv && bn == 16)
+        bn = 32;  // launch_gemm_nvfp4 has no 16-token tile
     if (fmt == kGemmW4A8) {
         // launch_gemm_w4a8: two 128-element slabs per stage at any K
         bn = M <= 32 ? 32 : 64;
@@ -1064,6 +1066,8 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream)
     if (a.M <= 64) {
         if (!k256)
             return launch_kernel<64, 8, 1, 4, true, false>(a, stream);
+        if (a.M <= 16)  // the narrower token slab leaves room for a fifth weight stage
+            return launch_kernel<16, 5, 2, 4, true, false>(a, stream);
         return a.M <= 32 ? launch_kernel<32, 4, 2, 4, true, false>(a, stream)
                          : launch_kernel<64, 4, 2, 4, true, false>(a, stream);
     }
