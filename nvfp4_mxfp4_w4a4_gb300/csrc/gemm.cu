@@ -596,6 +596,15 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
             const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
             if (!T.valid)
                 continue;
+            // swapped: this lane's output column has one bias value, an input
+            // the MMAs do not touch -- fetch it before the accumulator wait so
+            // its latency is not added after the last MMA
+            float bias_pre = 0.0f;
+            if constexpr (kSwap) {
+                const int r = quad * 32 + lane;
+                if (p.bias && r < T.rows_valid && w.mode != kPartial)
+                    bias_pre = __bfloat162float(p.bias[static_cast<int64_t>(T.expert) * p.ldo + T.a_row0 + r]);
+            }
             const bool ok = mbar_wait_bounded(accum_full, tcount & 1u, p.status, kStatusTimeout, kWaitLimitNs);
             tc_fence_after_sync();
             uint32_t v[CW];
@@ -673,8 +682,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                 // lane = output column n (weight row); tile columns = tokens.
                 // This warp's 32 columns x CW tokens go out as one box,
                 // staged as [CW tokens][32 n].
-                const int64_t n = T.a_row0 + r;
-                const float bn = (bias && r < T.rows_valid) ? __bfloat162float(bias[n]) : 0.0f;
+                const float bn = bias_pre;
                 __nv_bfloat16* srow = reinterpret_cast<__nv_bfloat16*>(stg) + lane;
 #pragma unroll
                 for (int j = 0; j < CW; ++j) {
