@@ -616,13 +616,17 @@ __global__ void __launch_bounds__(kThreads) smooth_prepare_kernel(const float* _
         atomicAdd(bad, n);
 }
 
-// Tile-prefix of a grouped activation tensor: group e starts at scale row
-// 128 * tiles_before[e].  Computed by one warp into shared memory.
-__device__ void group_tile_prefix(const int32_t* offsets, int E, int32_t* tiles_before)
+// Group of a grouped activation tensor whose padded scale-row range holds
+// scale-row tile `tile` (group e starts at scale row 128 * the sum of
+// ceil(rows_j / 128) over j < e), found by one warp on its own: a running
+// prefix of the groups' tile counts, 32 groups at a time, and a ballot for
+// the group whose range holds the tile.  Returns -1 past the last group;
+// *first_tile is the group's first tile.  Every lane passes the same tile.
+__device__ __forceinline__ int group_of_tile(const int32_t* offsets, int E, int tile, int* first_tile)
 {
     const int lane = threadIdx.x & 31;
     int carry = 0;
-    for (int base = 0; base <= E; base += 32) {
+    for (int base = 0; base < E; base += 32) {
         const int e = base + lane;
         int t = 0;
         if (e < E)
@@ -634,10 +638,16 @@ __device__ void group_tile_prefix(const int32_t* offsets, int E, int32_t* tiles_
             if (lane >= d)
                 incl += n;
         }
-        if (e <= E)
-            tiles_before[e] = carry + incl - t;
+        const int first = carry + incl - t;
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, t > 0 && first <= tile && tile < first + t);
+        if (hit != 0u) {
+            const int src = __ffs(static_cast<int>(hit)) - 1;
+            *first_tile = __shfl_sync(0xFFFFFFFFu, first, src);
+            return base + src;
+        }
         carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
+    return -1;
 }
 
 // Work item = (scale row, chunk of 8*U blocks).  For the dense tensor the
@@ -655,14 +665,8 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
                                                              const int32_t* __restrict__ offsets, int E,
                                                              const uint16_t* __restrict__ mul)
 {
-    extern __shared__ int32_t tiles_before[];
     grid_dependency_wait();
     launch_dependents();
-    if (kGrouped) {
-        if (threadIdx.x < 32)
-            group_tile_prefix(offsets, E, tiles_before);
-        __syncthreads();
-    }
     const int lane = threadIdx.x & 31;
     const int64_t item = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t srow = item / nch;
@@ -671,20 +675,14 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
     int64_t xrow = srow;
     bool row_real = srow < M;
     if (kGrouped) {
-        // locate the group whose padded tile range holds this scale row
-        const int tile = static_cast<int>(srow >> 7);
-        if (tile >= tiles_before[E])
+        // the group whose padded tile range holds this scale row (each warp
+        // finds it itself: no block-wide prefix and barrier)
+        int first_tile = 0;
+        const int grp = group_of_tile(offsets, E, static_cast<int>(srow >> 7), &first_tile);
+        if (grp < 0)
             return;
-        int lo = 0, hi = E;  // invariant: tiles_before[lo] <= tile < tiles_before[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (tiles_before[mid] <= tile)
-                lo = mid;
-            else
-                hi = mid;
-        }
-        const int64_t local = srow - static_cast<int64_t>(tiles_before[lo]) * 128;
-        const int64_t start = __ldg(offsets + lo), rows_e = __ldg(offsets + lo + 1) - start;
+        const int64_t local = srow - static_cast<int64_t>(first_tile) * 128;
+        const int64_t start = __ldg(offsets + grp), rows_e = __ldg(offsets + grp + 1) - start;
         row_real = local < rows_e;
         xrow = start + local;
     }
@@ -967,8 +965,7 @@ cudaError_t launch_act_quant_grouped(const void* x, const int32_t* offsets, int 
     const int64_t blocks = ceil_div(rows * nch * 32, kThreads);
     if (blocks == 0)
         return cudaSuccess;
-    const size_t smem = sizeof(int32_t) * static_cast<size_t>(E + 1);
-    return launch_pdl(act_quant_kernel<U, true, false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), smem, stream,
+    return launch_pdl(act_quant_kernel<U, true, false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream,
                       static_cast<const uint16_t*>(x), op, osf, total_M, K, rows, kb, kbp, nch, alg == 2 ? 1 : 0, 1,
                       offsets, E, static_cast<const uint16_t*>(nullptr));
 }
