@@ -11,7 +11,8 @@
 //
 // Design: one persistent CTA per SM walks output tiles (the MMA-M operand's
 // 128-row tile fastest).  A pipeline stage holds KC slabs of 128 packed
-// bytes (256 elements) of K for both operands.  12 warps:
+// bytes (256 elements) of K for both operands.  12 to 16 warps (the
+// register-split configurations below add two idle warps):
 //   warp 0      TMA producer: per (tile, stage) one tensor-map load per
 //               operand (a 3-D box spanning the KC slabs when KC > 1: the
 //               TMA unit keeps only a few copies in flight per SM, so fewer,
