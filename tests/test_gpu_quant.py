@@ -189,6 +189,39 @@ def test_requant_grouped_bf16_and_subnormal_scales(orc, L, bf16):
     for alg in (OCP, UOS):
         _check_requant_grouped(orc, L, packed, scale, gs, alg, SWZ, bf16=bf16)
 
+
+def _decode_bf16_bits(packed, scale, g):
+    """NVFP4 decode on the host, for the identity below: float32 products of
+    the exact E2M1 and E4M3 values (torch's E4M3 decode) times g, rounded to
+    bf16 by torch (nearest, ties to even)."""
+    import torch
+
+    e2m1 = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6], np.float32)
+    codes = np.stack([packed & 0xF, packed >> 4], axis=-1).reshape(packed.shape[0], -1)
+    s = torch.from_numpy(np.ascontiguousarray(scale)).view(torch.float8_e4m3fn).float().numpy()
+    v = (e2m1[codes] * np.repeat(s, 16, axis=1)) * np.float32(g)
+    return torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("alg", [OCP, UOS])
+def test_requant_equals_act_quant_of_its_decode(L, bf16, alg):
+    """Cross-kernel identity, no oracle: an E2M1 x E4M3 product has at most
+    6 significant bits, so with g a power of two every decoded NVFP4 value is
+    a bf16 value and the requant's bytes equal the activation quantizer's on
+    the decoded tensor; with the bf16 intermediate that holds for any g."""
+    rng = np.random.default_rng(51 + alg)
+    N, K = 130, 1024
+    packed = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scale = rng.integers(0x08, 0x7F, (N, K // 16), dtype=np.uint8)  # normal, finite E4M3
+    scale[:, ::5] |= 0x80
+    for g in ((0.0037, -0.25, 1.7e-3, 2.0 ** -4) if bf16 else (2.0 ** -4, 1.0, -8.0)):
+        g32 = float(np.float32(g))
+        rp, rs = _kernel_requant(L, packed, scale, g32, alg, SWZ, bf16)
+        ap, as_ = _kernel_act(L, _decode_bf16_bits(packed, scale, g32), alg, SWZ)
+        assert np.array_equal(rp, ap), (g, np.argwhere(rp != ap)[:5])
+        assert np.array_equal(rs, as_), g
+
 # ---------------------------------------------------------------- activations
 def _kernel_act(L, x_bits, alg, layout):
     M, K = x_bits.shape
