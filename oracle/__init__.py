@@ -6,7 +6,10 @@ and its Python binding) never touches it.
 
 This module is a thin numpy/ctypes shim over ``oracle.c``: it builds the C
 file with gcc on first use and marshals arrays.  All arithmetic lives in the
-C file, which cites the pages it follows.  Work on row ranges can be spread
+C file, which cites the pages it follows; the one piece of logic here is the
+grouped GEMM's assignment of rows to experts (each row goes to the expert e
+with off[e] <= row < off[e+1]), pinned on its own against a per-expert
+matmul.  Work on row ranges can be spread
 over host threads (ctypes drops the GIL during a call); the result does not
 depend on the thread count because rows are independent.
 """

@@ -423,6 +423,86 @@ def test_gemm_one_hot_selects_columns(orc):
     assert np.array_equal(ref, A[:, sel])
 
 
+# ------------------------------------------------------ grouped (MoE) GEMM
+
+# Experts of a grouped problem ("Efficiently Serving NVFP4 Models ...",
+# "Native FP4 matmul": MoE experts on MXFP4): rows [off[e], off[e+1]) of the
+# activations run against expert e's weight and bias.  The offsets cover an
+# empty first expert, a one-row expert, an empty expert in the middle, an
+# expert ending on the 128-row boundary, one of exactly 128 rows ending on the
+# next, another one-row expert and a ragged last one.
+_GROUPED_OFFSETS = np.array([0, 0, 1, 1, 128, 256, 257, 300], np.int32)
+
+
+def _grouped_case():
+    rng = np.random.default_rng(71)
+    off = _GROUPED_OFFSETS
+    E, total, N, K = len(off) - 1, int(off[-1]), 8, 64
+    a = rng.integers(0, 256, (total, K // 2), dtype=np.uint8)
+    sa = rng.integers(118, 136, (total, K // 32), dtype=np.uint8)
+    b = rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
+    sb = rng.integers(118, 136, (E, N, K // 32), dtype=np.uint8)
+    # a distinct bias per expert (bf16 bits of expert-dependent values)
+    bias_f = (np.arange(E)[:, None] * 4.0 + np.arange(N)[None, :] / 8.0 + 1.0).astype(np.float32)
+    bias = torch.from_numpy(bias_f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return off, a, sa, b, sb, bias
+
+
+def _grouped_expected(off, a, sa, b, sb, bias):
+    """Per expert, a numpy float64 matmul of operands decoded by the E2M1
+    fixture and the E8M0 definition, plus that expert's bias (torch's bf16)."""
+    A = _dequant_indep(a, sa)
+    out = np.full((A.shape[0], b.shape[1]), np.nan)
+    for e in range(len(off) - 1):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 == r0:
+            continue
+        Be = _dequant_indep(b[e], sb[e])
+        be = torch.from_numpy(bias[e].view(np.int16)).view(torch.bfloat16).double().numpy()
+        out[r0:r1] = A[r0:r1] @ Be.T + be
+    return out
+
+
+def _grouped_matches(fn, case):
+    off, a, sa, b, sb, bias = case
+    expect = _grouped_expected(*case)
+    ref, _ = fn(a, sa, b, sb, bias, off)
+    ok = not np.isnan(expect).any() and np.allclose(ref, expect, rtol=1e-12, atol=1e-9)
+    # a row subset that starts on expert boundaries gives the same entries
+    rows = np.array([0, 127, 128, 255, 256, 299])
+    r2, _ = fn(a, sa, b, sb, bias, off, rows=rows)
+    return ok and np.allclose(r2, expect[rows], rtol=1e-12, atol=1e-9)
+
+
+def test_gemm_grouped_matches_per_expert_matmul(orc):
+    assert _grouped_matches(orc.gemm_grouped, _grouped_case())
+
+
+def test_gemm_grouped_pin_catches_planted_mistakes(orc):
+    """Two plausible slips in the row-to-expert mapping, planted in copies of
+    the oracle's grouped GEMM built on its (separately pinned) dense GEMM:
+    rows on an offset assigned with searchsorted side="left", and the bias of
+    the previous expert.  The pin above must reject both."""
+    case = _grouped_case()
+
+    def planted(side, bias_shift):
+        def fn(a, sa, b, sb, bias, off, rows=None):
+            total = int(off[-1])
+            rows = np.arange(total) if rows is None else np.asarray(rows)
+            expert_of = np.searchsorted(off, rows, side=side) - 1
+            ref = np.full((len(rows), b.shape[1]), np.nan)
+            for e in range(len(off) - 1):
+                sel = np.nonzero(expert_of == e)[0]
+                if len(sel):
+                    ref[sel], _ = orc.gemm(a, sa, b[e], sb[e], bias[e - bias_shift], rows=rows[sel])
+            return ref, None
+        return fn
+
+    assert _grouped_matches(planted("right", 0), case)   # the planting harness itself is faithful
+    assert not _grouped_matches(planted("left", 0), case)
+    assert not _grouped_matches(planted("right", 1), case)
+
+
 # ------------------------------------------------------ smooth pre-scale
 
 
