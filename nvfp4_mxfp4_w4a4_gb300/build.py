@@ -6,6 +6,7 @@ library needs no CUDA driver until a call touches the GPU.
 """
 from __future__ import annotations
 
+import hashlib
 import os
 import subprocess
 import sys
@@ -17,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfp4lin.so")
 LIB_PEAK = os.path.join(HERE, "libfp4peak.so")
 ROOT = os.path.dirname(HERE)
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm_noalloc.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm_pair.cu", "gemm_noalloc.cu"]
 PEAK_SOURCES = ["mma_peak.cu"]
 HEADERS = ["ptx.cuh", "formats.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -30,15 +31,39 @@ def _nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def _newest_input() -> float:
+STAMP = os.path.join(BUILD, "sources.sha256")
+
+
+def _source_digest() -> str:
+    """sha256 over every input of the build (sources, headers, the public
+    header, the compiler flags and this machine's architecture): a library is
+    reused only when it was built from exactly these inputs here."""
+    import platform
+
+    h = hashlib.sha256()
+    h.update(" ".join(ARCH + FLAGS).encode())
+    h.update(platform.machine().encode())
     files = [os.path.join(CSRC, f) for f in SOURCES + PEAK_SOURCES + HEADERS] + [os.path.join(ROOT, "include", "fp4lin.h")]
-    return max(os.path.getmtime(f) for f in files)
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def _up_to_date(digest: str) -> bool:
+    if not all(os.path.exists(f) for f in (LIB, LIB_PEAK)) or not os.path.exists(STAMP):
+        return False
+    with open(STAMP) as fh:
+        return fh.read().strip() == digest
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Builds libfp4lin.so (the library) and libfp4peak.so (the FP4 MMA
-    issue-rate probe the benchmark uses)."""
-    if not force and all(os.path.exists(f) and os.path.getmtime(f) >= _newest_input() for f in (LIB, LIB_PEAK)):
+    issue-rate probe the benchmark uses), unless both were built here from
+    the current sources (a stamp of their hash sits beside the objects)."""
+    digest = _source_digest()
+    if not force and _up_to_date(digest):
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
@@ -64,6 +89,10 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, lib)
+    tmp = STAMP + f".tmp{os.getpid()}"
+    with open(tmp, "w") as fh:
+        fh.write(digest + "\n")
+    os.replace(tmp, STAMP)
     return LIB
 
 
