@@ -1,35 +1,54 @@
-"""Measured dense FP4 tensor-core peak: a tcgen05.mma kind::mxf4 issue-rate
-probe (libfp4peak.so) run on every SM at once."""
+"""Measured dense FP4 tensor-core peak: issue-rate probes of the block-scaled
+FP4 MMA forms (libfp4peak.so) run on every SM at once."""
 from __future__ import annotations
 
 import ctypes
-import os
 
-_HERE = os.path.dirname(os.path.abspath(__file__))
+KINDS = {
+    0: "kind::mxf4 scale_vec::2X (UE8M0, block 32)",
+    1: "kind::mxf4nvf4 scale_vec::2X (UE8M0, block 32)",
+    2: "kind::mxf4nvf4 scale_vec::4X (UE8M0, block 16)",
+    3: "kind::mxf4nvf4 scale_vec::4X (UE4M3, block 16)",
+}
+
+_lib = None
 
 
-def measure(n: int = 256, iters: int = 4000, mmas_per_group: int = 4, with_cp: bool = False, reps: int = 3):
-    """Returns dict(tflops, cycles_per_mma, ms) for MMAs of 128 x n x 64 issued
-    back to back by one thread per SM on all SMs."""
+def _probe():
+    global _lib
+    if _lib is None:
+        from . import build as B
+
+        B.build()
+        lib = ctypes.CDLL(B.LIB_PEAK)
+        f = lib.fp4_mma_peak_probe2
+        f.restype = ctypes.c_int
+        f.argtypes = [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        _lib = f
+    return _lib
+
+
+def measure(n: int = 256, iters: int = 4000, mmas_per_group: int = 4, with_cp: bool = False, reps: int = 3,
+            kind: int = 0, ctag: int = 1, alt: bool = False):
+    """Returns dict(tflops, cycles_per_mma, ms, ...) for MMAs of (128 ctag) x n x 64
+    issued back to back by one thread per SM (per SM pair when ctag == 2) on
+    all SMs."""
     import torch
 
-    from . import build as B
-
-    B.build()
-    lib = ctypes.CDLL(B.LIB_PEAK)
-    f = lib.fp4_mma_peak_probe
-    f.restype = ctypes.c_int
-    f.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    f = _probe()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    cycles = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    ctas = sms // ctag * ctag
+    cycles = torch.zeros(ctas // ctag, dtype=torch.int64, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     s = torch.cuda.current_stream()
     best = None
+    cyc = 0.0
     for _ in range(reps):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
-        err = f(n, iters, mmas_per_group, int(with_cp), sms, cycles.data_ptr(), status.data_ptr(), s.cuda_stream)
+        err = f(kind, ctag, n, iters, mmas_per_group, int(with_cp), int(alt), ctas, cycles.data_ptr(),
+                status.data_ptr(), s.cuda_stream)
         b.record()
         torch.cuda.synchronize()
         if err != 0 or int(status.item()) != 0:
@@ -39,6 +58,27 @@ def measure(n: int = 256, iters: int = 4000, mmas_per_group: int = 4, with_cp: b
             best = ms
             cyc = float(cycles.float().mean())
     mmas = iters * mmas_per_group
-    flops = 2.0 * 128 * n * 64 * mmas * sms
-    return {"n": n, "with_cp": with_cp, "tflops": flops / (best * 1e-3) / 1e12, "cycles_per_mma": cyc / mmas,
-            "ms": best, "sms": sms}
+    flops = 2.0 * 128 * ctag * n * 64 * mmas * (ctas // ctag)
+    return {"kind": KINDS[kind], "cta_group": ctag, "n": n, "with_cp": with_cp, "alt_accumulators": alt,
+            "tflops": flops / (best * 1e-3) / 1e12, "cycles_per_mma": cyc / mmas, "ms": best, "sms": ctas}
+
+
+def sweep():
+    """Every form at N = 256 on both CTA groupings, plus N = 128 with one and
+    two accumulators (cta_group::1)."""
+    rows = []
+    for kind in KINDS:
+        for ctag in (1, 2):
+            rows.append(measure(n=256, kind=kind, ctag=ctag))
+        for alt in (False, True):
+            rows.append(measure(n=128, kind=kind, ctag=1, alt=alt))
+    rows.append(measure(n=256, kind=0, ctag=1, with_cp=True))
+    rows.append(measure(n=256, kind=1, ctag=2, with_cp=True))
+    return rows
+
+
+if __name__ == "__main__":
+    import json
+
+    for r in sweep():
+        print(json.dumps({k: (round(v, 2) if isinstance(v, float) else v) for k, v in r.items()}))
