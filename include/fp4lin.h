@@ -115,6 +115,22 @@ FP4LIN_API const char* fp4_status_string(fp4_status s);
  * if the synchronize itself failed).  For tests and diagnostics.           */
 FP4LIN_API fp4_status fp4_get_device_status(void);
 
+/* Test hook for the bounded device waits (no counterpart on the pages: it
+ * exists so that tests can drive the library's failure path without a GPU
+ * fault).  Process-wide, read by each later GEMM call when it is enqueued:
+ *   wait_limit_ns          limit of every bounded wait of the GEMM kernels
+ *                          (0 restores the default of 1 s; otherwise
+ *                          1e3 .. 1e10 ns);
+ *   withhold_split_signal  1: in a split-K launch (see fp4_gemm_mxfp4_ws),
+ *                          the last CTA does not publish its partial sum, so
+ *                          the finishing CTA's bounded wait expires: the call
+ *                          completes, its output is wrong, and
+ *                          fp4_get_device_status() reports FP4_ERR_TIMEOUT;
+ *                          the workspace counters are then left non-zero
+ *                          (fp4_gemm_mxfp4_ws callers re-zero them).  0: off.
+ * Returns FP4_ERR_INVALID_ARG for other values.  Not for production use.    */
+FP4LIN_API fp4_status fp4_debug_set_wait_fault(uint64_t wait_limit_ns, int32_t withhold_split_signal);
+
 /* ------------------------------------------------------- requantization */
 
 /* NVFP4 -> MXFP4 weight requantization ([AMD] online requantization
@@ -336,12 +352,14 @@ FP4LIN_API fp4_status fp4_gemm_mxfp4_ex(const uint8_t* a, const uint8_t* sa, con
  *   FP4_ERR_SHAPE also when the problem's split-K plan needs more than
  *   2 MiB (fp4_gemm_workspace_size(M, N, K) > 2 MiB): use
  *   fp4_gemm_mxfp4_ws with a workspace of that size instead.
- *   The first call on a device looks up the array's device address; make
- *   that first call before starting a stream capture.
+ *   The first call on a device (and the first after a cudaDeviceReset of
+ *   it) looks up the array's device address; make that call before
+ *   starting a stream capture.
  *   Calls on one device must not overlap in time (the array is shared by
- *   every caller in the process).  Each call needs the array's counters
- *   at zero and leaves them zero; after FP4_ERR_TIMEOUT their state is
- *   unknown.                                                                */
+ *   every caller in the process).  A call that uses the array first clears
+ *   its split-K counters on `stream` (a memset of under 1 KB; nothing is
+ *   allocated), so a call made after FP4_ERR_TIMEOUT, which can leave the
+ *   counters set, starts from a clean state.                                */
 FP4LIN_API fp4_status fp4_gemm_mxfp4_noalloc(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
                                   const uint8_t* sb, const void* bias_bf16, void* out_bf16,
                                   int64_t M, int64_t N, int64_t K, void* stream);

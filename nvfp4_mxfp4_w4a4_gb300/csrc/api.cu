@@ -4,10 +4,40 @@
 // fp4_get_device_status, which exists to read the device status word).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/fp4lin.h"
 #include "internal.h"
+
+namespace fp4lin {
+
+unsigned long long current_context_id()
+{
+    typedef CUresult (*GetCurrentFn)(CUcontext*);
+    typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(f);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(f);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+}  // namespace fp4lin
 
 namespace {
 
@@ -20,13 +50,20 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
     bool checked = false;
     bool supported = false;
+    unsigned long long ctx = 0;  // context the status-word address belongs to
     unsigned int* status = nullptr;
 };
 
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
 
-// Resolves the current device's support and status-word address (once).
+// Test hooks (fp4_debug_set_wait_fault): the limit of every bounded device
+// wait of the GEMMs, and whether one split-K partial withholds its signal.
+std::atomic<unsigned long long> g_wait_limit_ns{fp4lin::kWaitLimitNs};
+std::atomic<int> g_withhold_split_signal{0};
+
+// Resolves the current device's support and status-word address (once per
+// device and context: a reset device gets a new context and a new address).
 fp4_status current_device(unsigned int** status)
 {
     int dev = 0;
@@ -34,6 +71,8 @@ fp4_status current_device(unsigned int** status)
         return FP4_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_dev_mutex);
     DeviceInfo& d = g_dev[dev];
+    if (d.checked && d.supported && d.ctx != fp4lin::current_context_id())
+        d.checked = false;
     if (!d.checked) {
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -46,6 +85,7 @@ fp4_status current_device(unsigned int** status)
             if (cudaGetSymbolAddress(&p, g_fp4_device_status) != cudaSuccess)
                 return FP4_ERR_CUDA;
             d.status = static_cast<unsigned int*>(p);
+            d.ctx = fp4lin::current_context_id();  // current now: the lookup initialised it
         }
         d.checked = true;
     }
@@ -144,6 +184,17 @@ fp4_status fp4_get_device_status(void)
     if (cudaMemcpyToSymbol(g_fp4_device_status, &zero, sizeof zero) != cudaSuccess)
         return FP4_ERR_CUDA;
     return (v & fp4lin::kStatusTimeout) ? FP4_ERR_TIMEOUT : FP4_OK;
+}
+
+fp4_status fp4_debug_set_wait_fault(uint64_t wait_limit_ns, int32_t withhold_split_signal)
+{
+    if (wait_limit_ns != 0 && (wait_limit_ns < 1000u || wait_limit_ns > 10000000000ull))
+        return FP4_ERR_INVALID_ARG;
+    if (withhold_split_signal != 0 && withhold_split_signal != 1)
+        return FP4_ERR_INVALID_ARG;
+    g_wait_limit_ns.store(wait_limit_ns ? wait_limit_ns : fp4lin::kWaitLimitNs);
+    g_withhold_split_signal.store(withhold_split_signal);
+    return FP4_OK;
 }
 
 fp4_status fp4_requant_nvfp4_to_mxfp4_ex(const uint8_t* w_packed, const uint8_t* w_scale_e4m3, float w_global,
@@ -302,10 +353,14 @@ fp4_status fp4_sf_swizzle(const uint8_t* in_rowmajor, uint8_t* out, int64_t rows
     return from_cuda(fp4lin::launch_sf_swizzle(in_rowmajor, out, rows, kblocks, static_cast<cudaStream_t>(stream)));
 }
 
-static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
-                              const void* bias, void* out, const int32_t* offsets, int32_t E, int64_t M, int64_t N,
-                              int64_t K, void* workspace, size_t workspace_bytes, void* stream,
-                              int fmt = fp4lin::kGemmMx, float alpha = 1.0f, uint32_t flags = 0)
+}  // extern "C"
+
+namespace fp4lin {
+
+// Host-side checks shared by every GEMM entry point (no CUDA call): shapes,
+// null pointers (only when M > 0) and 16-byte alignment.
+int gemm_check_args(const void* a, const void* sa, const void* b, const void* sb, const void* bias, const void* out,
+                    int64_t M, int64_t N, int64_t K, int32_t E)
 {
     if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 8 != 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
         return FP4_ERR_SHAPE;
@@ -318,8 +373,23 @@ static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t
     if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(out) ||
         (bias && !aligned16(bias)))
         return FP4_ERR_ALIGNMENT;
+    return FP4_OK;
+}
+
+}  // namespace fp4lin
+
+extern "C" {
+
+static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                              const void* bias, void* out, const int32_t* offsets, int32_t E, int64_t M, int64_t N,
+                              int64_t K, void* workspace, size_t workspace_bytes, void* stream,
+                              int fmt = fp4lin::kGemmMx, float alpha = 1.0f, uint32_t flags = 0)
+{
+    fp4_status st = static_cast<fp4_status>(fp4lin::gemm_check_args(a, sa, b, sb, bias, out, M, N, K, E));
+    if (st != FP4_OK || M == 0)
+        return st;
     unsigned int* status = nullptr;
-    fp4_status st = current_device(&status);
+    st = current_device(&status);
     if (st != FP4_OK)
         return st;
     fp4lin::GemmArgs args;
@@ -340,6 +410,8 @@ static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t
     args.fmt = fmt;
     args.alpha = alpha;
     args.early_weights = (flags & FP4_GEMM_WEIGHTS_STATIC) != 0;
+    args.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    args.withhold_split_signal = g_withhold_split_signal.load(std::memory_order_relaxed) != 0;
     return from_cuda(fp4lin::launch_gemm(args, static_cast<cudaStream_t>(stream)));
 }
 

@@ -101,6 +101,8 @@ struct GemmParams {
     int64_t sfb_expert_stride;
     float alpha;                // NVFP4 mode: factor on the accumulator before the bias
     int early_w;                // weights not written by the kernel this one may overlap
+    int withhold_signal;        // test hook: the last CTA of a split launch never publishes its partial
+    unsigned long long wait_ns; // limit of every bounded wait
     unsigned int* status;
 };
 
@@ -464,7 +466,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                             stage_loads(s, kb, T, kHalfX, false);
                             continue;
                         }
-                        if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kStatusTimeout, kWaitLimitNs)) {
+                        if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kStatusTimeout, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -489,7 +491,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                     if (!T.valid)
                         continue;
                     // the epilogue must have drained the accumulator of the previous tile
-                    if (!mbar_wait_bounded(accum_empty, (tcount & 1u) ^ 1u, p.status, kStatusTimeout, kWaitLimitNs)) {
+                    if (!mbar_wait_bounded(accum_empty, (tcount & 1u) ^ 1u, p.status, kStatusTimeout, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -497,8 +499,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                     for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                         const int s = static_cast<int>(it % STAGES);
                         const uint32_t ph = (it / STAGES) & 1u;
-                        if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, kWaitLimitNs) ||
-                            !mbar_wait_bounded(&sf_full[s], ph, p.status, kStatusTimeout, kWaitLimitNs)) {
+                        if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, p.wait_ns) ||
+                            !mbar_wait_bounded(&sf_full[s], ph, p.status, kStatusTimeout, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -553,7 +555,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                     for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                         const int s = static_cast<int>(it % STAGES);
                         const uint32_t ph = (it / STAGES) & 1u;
-                        if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, kWaitLimitNs)) {
+                        if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -606,7 +608,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                 if (p.bias && r < T.rows_valid && w.mode != kPartial)
                     bias_pre = __bfloat162float(p.bias[static_cast<int64_t>(T.expert) * p.ldo + T.a_row0 + r]);
             }
-            const bool ok = mbar_wait_bounded(accum_full, tcount & 1u, p.status, kStatusTimeout, kWaitLimitNs);
+            const bool ok = mbar_wait_bounded(accum_full, tcount & 1u, p.status, kStatusTimeout, p.wait_ns);
             tc_fence_after_sync();
             uint32_t v[CW];
             tmem_load_cols<CW>(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * CW, v);
@@ -633,7 +635,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                     for (int j = 0; j < CW; ++j)
                         __stcg(slot + (half * CW + j) * BM + r, __uint_as_float(v[j]));
                     __syncwarp();
-                    if (lane == 0)
+                    if (lane == 0 && !(p.withhold_signal && blockIdx.x == gridDim.x - 1))
                         red_release_add_gpu(p.flags + blockIdx.x, 1u);  // ready once all 8 warps have added
                     continue;
                 }
@@ -646,7 +648,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                     for (int j = lane; j < nparts; j += 32) {
                         const uint64_t t0 = global_timer_ns();
                         while (ld_acquire_gpu(flags + j) < kEpiWarps) {
-                            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                            if (global_timer_ns() - t0 > p.wait_ns) {
                                 atomicOr(p.status, kStatusTimeout);
                                 break;
                             }
@@ -769,12 +771,15 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
     }
 }
 
+}  // namespace
+
 // --------------------------------------------------------------- host side
+// (tensor-map builders and the SM count are shared with the CTA-pair GEMM)
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn()
+static EncodeTiledFn encode_fn()
 {
     static EncodeTiledFn fn = nullptr;
     static std::once_flag once;
@@ -799,8 +804,6 @@ EncodeTiledFn encode_fn()
 // KC == 1: 2-D boxes of one slab x box_rows.  KC > 1: the rows viewed as
 // slabs (3-D), boxes of one slab x box_rows x KC slabs, which land as KC
 // consecutive [box_rows][128 B] slabs.
-enum : int { kOpFp4Packed = 0, kOpBytes = 1, kOpFp4Expanded = 2 };
-
 bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows, int kc, int kind)
 {
     EncodeTiledFn fn = encode_fn();
@@ -861,6 +864,8 @@ int sm_count()
     }
     return cached[dev];
 }
+
+namespace {
 
 // Split-K plan of a swapped (M <= 64) problem: S CTAs per tile (S < 2: no
 // split) and the workspace that takes.  Split only when at least half the
@@ -937,6 +942,8 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
     p.sfb_expert_stride = ((a.N + 127) / 128) * 128 * (a.K / (kNv ? 16 : 32));
     p.alpha = a.alpha;
     p.early_w = (a.early_weights && !kGrouped) ? 1 : 0;
+    p.withhold_signal = a.withhold_split_signal ? 1 : 0;
+    p.wait_ns = a.wait_ns;
     p.status = a.status;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (tiles == 0)
@@ -959,19 +966,23 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
     auto kern = gemm_fp4_kernel<BN, STAGES, KC, CPW, kSwap, kGrouped, kFmt>;
     // The shared-memory opt-in is a per-device function attribute: set it
     // once per device (and grow it if a larger grouped prefix needs more).
+    // (keyed by context too: a reset device has a new context without it)
     static std::mutex mu;
     static size_t configured[64] = {};
+    static unsigned long long configured_ctx[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess || dev < 0 || dev >= 64)
         return err != cudaSuccess ? err : cudaErrorInvalidDevice;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (configured[dev] < smem) {
+        const unsigned long long ctx = current_context_id();
+        if (configured_ctx[dev] != ctx || configured[dev] < smem) {
             err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
             if (err != cudaSuccess)
                 return err;
             configured[dev] = smem;
+            configured_ctx[dev] = ctx;
         }
         if constexpr (C::SPLIT) {
             // setmaxnreg.inc waits until the registers it asks for are free:
@@ -997,6 +1008,11 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
 }
 
 }  // namespace
+
+size_t gemm_workspace_counter_bytes()
+{
+    return (static_cast<size_t>(sm_count()) * 4 + 255) / 256 * 256;
+}
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int fmt)
 {
@@ -1081,7 +1097,7 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream)
                          : launch_kernel<64, 4, 2, 4, true, false>(a, stream);
     }
     if (wide)
-        return launch_kernel<256, 4, 1, 2, false, false>(a, stream);
+        return a.M >= 256 ? launch_gemm_pair(a, stream) : launch_kernel<256, 4, 1, 2, false, false>(a, stream);
     return k256 ? launch_kernel<128, 3, 2, 4, false, false>(a, stream)
                 : launch_kernel<128, 6, 1, 4, false, false>(a, stream);
 }

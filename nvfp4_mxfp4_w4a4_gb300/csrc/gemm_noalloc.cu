@@ -15,10 +15,10 @@
 //     rejected (FP4_ERR_SHAPE) rather than silently run another way;
 //   * one call at a time per device: two calls in flight at once (other
 //     streams, other threads) would use the same counters and partial tiles;
-//   * the counters must be zero when a call starts.  Static device storage
-//     is zero when the module loads and every call that finishes without a
-//     device timeout leaves the counters zero again; after FP4_ERR_TIMEOUT
-//     their contents are unknown.
+//   * the split-K counters must be zero when a call's kernel starts.  A call
+//     that splits first clears them on its stream (cudaMemsetAsync of the
+//     counter area, less than 1 KB; no allocation), so a call after a device
+//     timeout (which can leave counters behind) starts clean as well.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -34,7 +34,7 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_gemm_scratch[kScratchBytes];
 
 struct ScratchAddr {
-    bool known = false;
+    unsigned long long ctx = 0;  // context the address belongs to (0: not looked up)
     void* ptr = nullptr;
 };
 
@@ -42,8 +42,10 @@ ScratchAddr g_addr[kMaxDevices];
 std::mutex g_addr_mutex;
 
 // Device address of the array on the current device, looked up once per
-// device (the lookup runs with that device current, as the call's own
-// launches do).
+// device and context (the lookup runs with that device current, as the
+// call's own launches do).  A device that was reset has a new context, in
+// which the library's module, and so the array, is loaded again, possibly
+// at another address: the lookup is then repeated.
 fp4_status scratch_address(void** out)
 {
     int dev = 0;
@@ -51,12 +53,13 @@ fp4_status scratch_address(void** out)
         return FP4_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_addr_mutex);
     ScratchAddr& a = g_addr[dev];
-    if (!a.known) {
+    const unsigned long long ctx = fp4lin::current_context_id();
+    if (a.ctx == 0 || a.ctx != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_gemm_scratch) != cudaSuccess || p == nullptr)
             return FP4_ERR_CUDA;
         a.ptr = p;
-        a.known = true;
+        a.ctx = fp4lin::current_context_id();  // current now: the lookup initialised it
     }
     *out = a.ptr;
     return FP4_OK;
@@ -69,6 +72,10 @@ extern "C" {
 fp4_status fp4_gemm_mxfp4_noalloc(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                                   const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, void* stream)
 {
+    // the same host checks as every GEMM entry point, before any CUDA call
+    fp4_status st = static_cast<fp4_status>(fp4lin::gemm_check_args(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, 1));
+    if (st != FP4_OK || M == 0)
+        return st;
     // the plan depends on the current device's SM count; an unusable device
     // reports 0 here and the call below returns its error
     const size_t need = fp4_gemm_workspace_size(M, N, K);
@@ -76,9 +83,13 @@ fp4_status fp4_gemm_mxfp4_noalloc(const uint8_t* a, const uint8_t* sa, const uin
         return FP4_ERR_SHAPE;
     void* scratch = nullptr;
     if (need > 0) {
-        const fp4_status st = scratch_address(&scratch);
+        st = scratch_address(&scratch);
         if (st != FP4_OK)
             return st;
+        // the counters start at zero whatever an earlier call left behind
+        if (cudaMemsetAsync(scratch, 0, fp4lin::gemm_workspace_counter_bytes(), static_cast<cudaStream_t>(stream)) !=
+            cudaSuccess)
+            return FP4_ERR_CUDA;
     }
     return fp4_gemm_mxfp4_ws(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, scratch, scratch ? kScratchBytes : 0,
                              stream);

@@ -2,6 +2,7 @@
 // kernel translation units.  Not part of the public interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -57,6 +58,13 @@ cudaError_t launch_coop(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sm
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
+
+// Identifier of the CUDA context current on the calling thread, unique for
+// the life of the process (0 when no context is current).  Per-device caches
+// of device addresses and function attributes are keyed by it: after a
+// cudaDeviceReset the device gets a new context, with the library's module
+// loaded again and its attributes unset.
+unsigned long long current_context_id();
 
 // Status word bits a kernel sets in the library-owned device status word.
 constexpr unsigned int kStatusTimeout = 1u;
@@ -124,9 +132,32 @@ struct GemmArgs {
     int fmt = 0;                 // GemmFormat
     float alpha = 1.0f;          // NVFP4: factor on the accumulator before the bias
     bool early_weights = false;  // the weights are not written by the preceding kernel in the stream
+    unsigned long long wait_ns = kWaitLimitNs;  // limit of every bounded device wait of the launch
+    bool withhold_split_signal = false;  // test hook: one split-K partial never signals its finisher
 };
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
+
+// Dense MXFP4 GEMM on 256 x 256 output tiles computed by CTA pairs
+// (tcgen05 cta_group::2); used by launch_gemm for large M and N.
+cudaError_t launch_gemm_pair(const GemmArgs& args, cudaStream_t stream);
+
+// Host helpers shared by the GEMM translation units (gemm.cu).
+// Operand kinds of make_operand_map.
+enum : int { kOpFp4Packed = 0, kOpBytes = 1, kOpFp4Expanded = 2 };
+bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows, int kc, int kind);
+bool make_output_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int box_cols, int box_rows,
+                     CUtensorMapSwizzle swizzle);
+int sm_count();
+
+// Host-side argument checks of the GEMM entry points; returns an fp4_status
+// value (FP4_OK = 0), makes no CUDA call.
+int gemm_check_args(const void* a, const void* sa, const void* b, const void* sb, const void* bias, const void* out,
+                    int64_t M, int64_t N, int64_t K, int32_t E);
+
+// Bytes at the start of a split-K workspace that hold the per-CTA counters
+// (zero between calls) on the current device.
+size_t gemm_workspace_counter_bytes();
 
 // Workspace the GEMM uses for split-K on this problem on the current device
 // (0: the problem is not split): a zero-initialised counter per SM (256-byte

@@ -38,6 +38,7 @@ SYMBOLS = (
     "fp4_quant_act_mxfp8", "fp4_gemm_w4a8", "fp4_gemm_w4a8_workspace_size", "fp4_gemm_mxfp4_ex",
     "fp4_smooth_prepare", "fp4_quant_act_mxfp4_smooth", "fp4_quant_act_mxfp8_smooth",
     "fp4_linear_workspace_size", "fp4_linear", "fp4_linear_grouped_workspace_size", "fp4_linear_grouped",
+    "fp4_debug_set_wait_fault",
 )
 
 
@@ -81,6 +82,7 @@ def load(path: str = LIB_PATH):
             "fp4_sf_bytes_grouped": (ctypes.c_size_t, [_i64, _i32, _i64]),
             "fp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "fp4_get_device_status": (ctypes.c_int, []),
+            "fp4_debug_set_wait_fault": (ctypes.c_int, [ctypes.c_uint64, _i32]),
             "fp4_requant_nvfp4_to_mxfp4": (ctypes.c_int, [_p, _p, ctypes.c_float, _p, _p, _i64, _i64, _p]),
             "fp4_requant_nvfp4_to_mxfp4_ex": (ctypes.c_int, [_p, _p, ctypes.c_float, _p, _p, _i64, _i64,
                                                              ctypes.POINTER(fp4_quant_opts), _p]),
@@ -169,6 +171,12 @@ def fp4_sf_bytes_grouped(total_M: int, E: int, K: int) -> int:
 
 def fp4_get_device_status() -> int:
     return load().fp4_get_device_status()
+
+
+def fp4_debug_set_wait_fault(wait_limit_ns: int = 0, withhold_split_signal: int = 0):
+    """Test hook: limit of the GEMMs' bounded device waits (0 = the default
+    1 s) and whether a split-K partial withholds its ready signal."""
+    _check(load().fp4_debug_set_wait_fault(wait_limit_ns, withhold_split_signal), "fp4_debug_set_wait_fault")
 
 
 def fp4_requant_nvfp4_to_mxfp4(w_packed, w_scale_e4m3, w_global, out_packed, out_scale, N, K, stream=None,

@@ -141,3 +141,33 @@ def test_valid_call_without_gpu_reports_cuda_error(L):
     raw = L.load()
     st = raw.fp4_quant_act_mxfp4(16, 16, 16, 4, 32, None, None)
     assert st in (4, 5)   # no usable device: UNSUPPORTED or CUDA, never a silent success
+
+
+def test_no_alloc_argument_checks_match_the_workspace_entry_point(L):
+    """The entry point without allocations runs the same host checks as
+    fp4_gemm_mxfp4_ws, before it touches a device."""
+    raw = L.load()
+    cases = [
+        ((16, 16, 16, 16, None, 16, 1, 8, 100), 2),      # K % 128
+        ((16, 16, 16, 16, None, 16, 1, 12, 128), 2),     # N % 8
+        ((16, 16, 16, 16, None, 16, -1, 8, 128), 2),     # M < 0
+        ((16, 16, 16, 16, None, 16, 1, 0, 128), 2),      # N = 0
+        ((None, 16, 16, 16, None, 16, 1, 8, 128), 1),    # null a
+        ((16, 16, 16, None, None, 16, 1, 8, 128), 1),    # null sb
+        ((16, 16, 16, 16, None, None, 1, 8, 128), 1),    # null out
+        ((17, 16, 16, 16, None, 16, 1, 8, 128), 3),      # a not 16-byte aligned
+        ((16, 16, 16, 16, 24, 16, 1, 8, 128), 3),        # bias not 16-byte aligned
+        ((None, None, None, None, None, None, 0, 8, 128), 0),   # M = 0: no-op
+    ]
+    for args, want in cases:
+        assert raw.fp4_gemm_mxfp4_noalloc(*args, None) == want, args
+        assert raw.fp4_gemm_mxfp4_ws(*args, None, 0, None) == want, args
+
+
+def test_debug_wait_fault_hook_checks_its_arguments(L):
+    raw = L.load()
+    assert raw.fp4_debug_set_wait_fault(10, 0) == 1            # below 1 us
+    assert raw.fp4_debug_set_wait_fault(2 * 10 ** 10, 0) == 1  # above 10 s
+    assert raw.fp4_debug_set_wait_fault(0, 2) == 1
+    assert raw.fp4_debug_set_wait_fault(2_000_000, 1) == 0
+    assert raw.fp4_debug_set_wait_fault(0, 0) == 0             # back to the defaults

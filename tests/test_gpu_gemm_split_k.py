@@ -91,3 +91,30 @@ def test_workspace_entry_without_split_k(orc, L):
         ref, absum = orc.gemm(a, sa, b, sb, threads=THREADS)
         ok, ratio = gemm_check(out, ref, absum)
         assert ok, f"{(M, N, K)}: max err/bound = {ratio}"
+
+
+def test_withheld_partial_expires_the_bounded_wait(orc, L):
+    """Failure path of the split-K hand-over, driven without a GPU fault: with
+    a test hook, the last CTA never publishes its partial, so the finishing
+    CTA's bounded wait (2 ms here) expires.  The call completes, the status
+    word reports FP4_ERR_TIMEOUT (and reading it clears it), the withheld
+    counter is left in the workspace, and once the caller zeroes the
+    workspace again the next call is correct."""
+    import torch
+
+    M, N, K = 32, 1024, 16384
+    a, sa, b, sb = _operands(orc, M, N, K, 11)
+    ws = _workspace(L, M, N, K)
+    good = _run(L, orc, a, sa, b, sb, None, M, N, K, ws)
+    out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    L.fp4_debug_set_wait_fault(2_000_000, 1)
+    try:
+        L.fp4_gemm_mxfp4_ws(dev(a), dev(orc.sf_swizzle(sa)), dev(b), dev(orc.sf_swizzle(sb)), None, out, M, N, K, ws)
+        st = L.fp4_get_device_status()
+    finally:
+        L.fp4_debug_set_wait_fault(0, 0)
+    assert st == L.FP4_ERR_TIMEOUT
+    assert L.fp4_get_device_status() == 0
+    assert int(torch.count_nonzero(ws[: 4 * _sm_count()])) > 0
+    ws.zero_()
+    assert np.array_equal(_run(L, orc, a, sa, b, sb, None, M, N, K, ws), good)
