@@ -4,9 +4,10 @@ One step = one pass of the whole hot path over one batch of a workload:
 requantize the NVFP4 weight(s) to MXFP4, quantize the activations, run the
 W4A4 GEMM(s).  Workloads (seeded synthetic inputs, see synth/):
 
-  decode  (default) W[14336,4096] NVFP4 (bf16 ~N(0,0.02), 4 outlier
-          K-columns x8); M in {1,8,32,64} activation batches ~N(0,1); bias.
-  prefill W[18432,7168] (~N(0,0.015)); M in {2048, 8192} (0.5 % outliers x16).
+  prefill (default) W[18432,7168] NVFP4 (bf16 ~N(0,0.015)); M in {2048, 8192}
+          activation batches ~N(0,1) with 0.5 % outliers x16; no bias.
+  decode  W[14336,4096] (~N(0,0.02), 4 outlier K-columns x8); M in
+          {1,8,32,64}; bias.
   moe     64 experts, gate_up [2048,4096] and down [4096,1024]; 4096 tokens
           routed top-8 -> 32768 grouped rows per projection.
   stream  the load path instead of a serving step: a 60-layer NVFP4 model
@@ -55,7 +56,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", choices=("decode", "prefill", "moe", "stream"), default="decode")
+    ap.add_argument("--workload", choices=("decode", "prefill", "moe", "stream"), default="prefill")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--breakdown-reps", type=int, default=200)
@@ -236,6 +237,50 @@ class Weight:
                                               stream=s)
 
 
+E2M1_VALUES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def requant_error(torch, w, chunk_rows=2048):
+    """Error of the requantized MXFP4 weight against the NVFP4-dequantized
+    weight it came from, over every element of every tensor of `w`:
+    MSE, max |difference|, relative RMS error (against the RMS of the
+    NVFP4-dequantized values).  The NVFP4 decode is the method's
+    (E2M1 code x E4M3 scale, exact, then x g with one float32 rounding);
+    the MXFP4 decode is code x 2^(e8m0 - 127) from the swizzled scale
+    layout.  A reported statistic (torch on the tensors' device, outside
+    every timed region), not a step of the path."""
+    dev = w.packed.device
+    lut = torch.tensor(list(E2M1_VALUES) + [-v for v in E2M1_VALUES], dtype=torch.float32, device=dev)
+    N, K = w.N, w.K
+    kb = K // 32
+    kb4 = -(-kb // 4)
+    c = torch.arange(kb, device=dev)
+    sq = torch.zeros((), dtype=torch.float64, device=dev)
+    ref_sq = torch.zeros((), dtype=torch.float64, device=dev)
+    mx = torch.zeros((), dtype=torch.float64, device=dev)
+    for e in range(w.E):
+        sf = w.b_scale[e * w.sf_bytes:(e + 1) * w.sf_bytes]
+        for r0 in range(0, N, chunk_rows):
+            r1 = min(N, r0 + chunk_rows)
+            rows = torch.arange(r0, r1, device=dev)[:, None]
+            p = w.packed[e * N + r0:e * N + r1]
+            codes = torch.stack([p & 15, p >> 4], dim=-1).reshape(r1 - r0, K).long()
+            s16 = w.scale[e * N + r0:e * N + r1].view(torch.float8_e4m3fn).float().repeat_interleave(16, dim=1)
+            v = ((lut[codes] * s16) * w.g[e]).double()
+            q = w.b_packed[e * N + r0:e * N + r1]
+            qc = torch.stack([q & 15, q >> 4], dim=-1).reshape(r1 - r0, K).long()
+            off = ((rows // 128) * kb4 + c[None, :] // 4) * 512 + (rows % 32) * 16 + ((rows % 128) // 32) * 4 + c[None, :] % 4
+            b = sf[off].double()
+            scale = torch.where(b == 255, torch.full_like(b, float("nan")), torch.exp2(b - 127.0))
+            d = lut[qc].double() * scale.repeat_interleave(32, dim=1) - v
+            sq += (d * d).sum()
+            ref_sq += (v * v).sum()
+            mx = torch.maximum(mx, d.abs().max())
+    n = w.E * N * K
+    return {"vs": "NVFP4-dequantized weight ((E2M1 x E4M3) x g, float32)", "elements": n,
+            "mse": float(sq) / n, "max_abs": float(mx), "rel_rmse": float((sq / ref_sq).sqrt())}
+
+
 _WORKSPACE = {}
 
 
@@ -333,6 +378,13 @@ class Act:
                                           self.offsets, self.E, self.M, w.N, self.K, stream=s)
 
 
+DECODE_DESC = ("decode layer: W[14336,4096] NVFP4->MXFP4 requant + MXFP4 act-quant + W4A4 GEMM (+bias), "
+               "M in {1,8,32,64}")
+PREFILL_DESC = "prefill layer: W[18432,7168] requant + act-quant + W4A4 GEMM, M in {2048, 8192}"
+MOE_DESC = ("MoE: 64 experts gate_up[2048,4096] + down[4096,1024] requant, grouped act-quant and grouped W4A4 "
+            "GEMM over 4096 tokens x top-8 (32768 rows)")
+
+
 def make_workload(name, L, torch):
     import synth
 
@@ -345,15 +397,13 @@ def make_workload(name, L, torch):
         d = synth.workload2()
         w = Weight(L, torch, [d["W"]], 18432, 7168)
         acts = [Act(L, torch, d["X"][M], w) for M in (2048, 8192)]
-        return "prefill layer: W[18432,7168] requant + act-quant + W4A4 GEMM, M in {2048, 8192}", [w], acts
+        return PREFILL_DESC, [w], acts
     d = synth.workload3()
     E = len(d["row_offsets"]) - 1
     wgu = Weight(L, torch, [d["W_gu"][e] for e in range(E)], 2048, 4096)
     wdn = Weight(L, torch, [d["W_down"][e] for e in range(E)], 4096, 1024)
     acts = [Act(L, torch, d["A_gu"], wgu, d["row_offsets"]), Act(L, torch, d["A_down"], wdn, d["row_offsets"])]
-    desc = ("MoE: 64 experts gate_up[2048,4096] + down[4096,1024] requant, grouped act-quant and grouped W4A4 "
-            "GEMM over 4096 tokens x top-8 (32768 rows)")
-    return desc, [wgu, wdn], acts
+    return MOE_DESC, [wgu, wdn], acts
 
 
 class Bench:
@@ -453,6 +503,12 @@ class Bench:
 KERNEL_NAMES = {"gemm": "gemm_fp4_kernel", "requant": "requant_flat_kernel", "act_quant": "act_quant_kernel"}
 
 
+def gemm_kernel_name(workload):
+    """The GEMM kernel the library launches for the workload's batches: the
+    CTA-pair kernel for the prefill batches (M >= 256 filling the GPU)."""
+    return "gemm_pair_kernel" if workload == "prefill" else "gemm_fp4_kernel"
+
+
 def run_ours(args):
     import torch
 
@@ -484,6 +540,8 @@ def run_ours(args):
     if L.fp4_get_device_status() != 0:
         raise RuntimeError("device status reports a timeout")
     times = [total_ms / steps]
+    # requant error of set 0's weights (written by the steps above)
+    req_err = [dict(requant_error(torch, w), weight=f"{w.E} x [{w.N}, {w.K}]") for w in b.weights]
 
     ms = statistics.fmean(times)
     ms_max = max_over_ranks(pg, ms, device="cuda")
@@ -492,6 +550,13 @@ def run_ours(args):
     # per-kernel breakdown: each launch group alone, rotated over the buffer sets in one graph
     hbm_peak, bf16_peak, peak_kind = peaks()
     fp4_peak = bf16_peak * FP4_PER_BF16_NOMINAL
+    try:
+        probe = P.measure(n=256, iters=4000)
+        fp4_probe = {"tflops": round(probe["tflops"], 1), "cycles_per_mma": round(probe["cycles_per_mma"], 1),
+                     "what": "tcgen05.mma 128x256x64 issue-rate probe, all SMs (every block-scaled FP4 form and "
+                             "both CTA groupings measure the same 128 cycles)"}
+    except Exception as exc:  # noqa: BLE001
+        fp4_probe = {"error": str(exc)}
     breakdown, groups = {}, {}
     for group, label, fn, nbytes, flops in b.kernels():
         g = b.graph(fn)
@@ -513,16 +578,19 @@ def run_ours(args):
     shares = {k: round(v["s"] / total, 3) for k, v in groups.items()}
     dom = max(groups, key=lambda k: groups[k]["s"])
     gd = groups[dom]
+    dom_kernel = gemm_kernel_name(args.workload) if dom == "gemm" else KERNEL_NAMES[dom]
     tensor_bound = dom == "gemm" and (gd["flops"] / (fp4_peak * 1e12)) > (gd["bytes"] / (hbm_peak * 1e9))
     if tensor_bound:
         achieved = gd["flops"] / gd["s"] / 1e12
-        roofline = {"kernel": KERNEL_NAMES[dom], "bound": "tensor", "achieved": round(achieved, 1),
+        roofline = {"kernel": dom_kernel, "bound": "tensor", "achieved": round(achieved, 1),
                     "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 3),
-                    "peak_source": f"MEASURED_PEAKS bf16_tflops {bf16_peak} x nominal fp4/bf16 ratio 6 "
-                                   f"(of {peak_kind})"}
+                    "peak_source": f"dense FP4 peak = MEASURED_PEAKS bf16_tflops {bf16_peak} x nominal fp4/bf16 "
+                                   f"ratio 6 (of {peak_kind})"}
+        if "tflops" in fp4_probe:
+            roofline["frac_of_fp4_probe"] = round(achieved / fp4_probe["tflops"], 3)
     else:
         achieved = gd["bytes"] / gd["s"] / 1e9
-        roofline = {"kernel": KERNEL_NAMES[dom], "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
+        roofline = {"kernel": dom_kernel, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak,
                     "unit": "GB/s", "frac": round(achieved / hbm_peak, 3),
                     "peak_source": f"MEASURED_PEAKS hbm_gbs (of {peak_kind})"}
     roofline["traffic"] = _committed_traffic(args.workload, roofline["kernel"])
@@ -530,12 +598,13 @@ def run_ours(args):
     roofline["algorithmic"] = ("bytes: requant 1.09375 B/elem, act-quant 2.53125 B/elem, "
                                "GEMM 0.53125(M+N)K+2MN(+2N bias); flops 2MNK")
 
-    try:
-        probe = P.measure(n=256, iters=4000)
-        fp4_probe = {"tflops": round(probe["tflops"], 1), "cycles_per_mma": round(probe["cycles_per_mma"], 1),
-                     "what": "tcgen05.mma kind::mxf4 128x256x64 issue-rate probe, all SMs"}
-    except Exception as exc:  # noqa: BLE001
-        fp4_probe = {"error": str(exc)}
+    def quant_summary(group):
+        q = groups.get(group)
+        if not q:
+            return None
+        gbps = q["bytes"] / q["s"] / 1e9
+        return {"GBps": round(gbps, 1), "hbm_frac": round(gbps / hbm_peak, 3), "launches": q["n"],
+                "us_total": round(q["s"] * 1e6, 2)}
 
     e2e = _e2e(b, torch, L, min(args.steps, 50))
     nvfp4 = w4a8 = None
@@ -547,7 +616,8 @@ def run_ours(args):
                                     "W4A8 fallback: MXFP8 act-quant + MXFP8 x MXFP4 GEMM (the same requantized "
                                     "weight) vs the MXFP4 path")
 
-    req = [breakdown[k] for k in breakdown if k.startswith("requant")]
+    gemm_q = groups.get("gemm", {"flops": 0.0, "s": 1.0})
+    gemm_tflops = gemm_q["flops"] / gemm_q["s"] / 1e12
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "higher_is_better": True, "scaling": "weak",
@@ -556,18 +626,19 @@ def run_ours(args):
                    "l2": f"inputs larger than L2: {b.n_sets} rotating buffer sets of "
                          f"{b.set_bytes / 2 ** 20:.0f} MiB, one graph of {b.n_sets} consecutive steps",
                    "parallelism": f"replicas x{world}", "cuda_graph": True},
-        "requant_GBps": round(sum(r["GBps"] * r["us"] for r in req) / max(1e-9, sum(r["us"] for r in req)), 1),
         "gemm_TFLOPS": {k: v["TFLOPS"] for k, v in breakdown.items() if "TFLOPS" in v},
-        "pct_fp4_peak_step": {"of_nominal_15PF": round(100 * value / world / FP4_NOMINAL_TFLOPS, 3),
-                              "of_probe": (round(100 * value / world / fp4_probe["tflops"], 3)
-                                           if "tflops" in fp4_probe else None)},
+        "pct_fp4_peak": {"peak_tflops": round(fp4_peak, 1), "peak": roofline.get("peak_source", ""),
+                         "gemm": round(100 * gemm_tflops / fp4_peak, 2),
+                         "step": round(100 * value / world / fp4_peak, 2)},
+        "requant": quant_summary("requant"), "act_quant": quant_summary("act_quant"),
+        "requant_error": req_err,
         "fp4_probe_peak": fp4_probe,
         "breakdown": breakdown, "shares": shares, "roofline": roofline, "e2e": e2e, "nvfp4_path": nvfp4,
         "w4a8_path": w4a8,
         "gpu_launches": b.launches_per_step * steps, "clocks": clk, "wall_s_timed_region": round(t_wall, 3),
     }
-    if rank == 0 and not args.no_cpu_baseline and args.workload == "decode":
-        result["cpu_baseline"] = cpu_baseline(budget_s=12.0)
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        result["cpu_baseline"] = cpu_baseline(args.workload)
     if rank == 0:
         print(json.dumps(result))
     if pg is not None:
@@ -836,25 +907,25 @@ def side_path_comparison(b, L, torch, reps, breakdown, cls, tag_prefix, what):
     return res
 
 
+KERNEL_SOURCES = {"gemm_fp4_kernel": "gemm.cu", "gemm_pair_kernel": "gemm_pair.cu", "requant_kernel": "quant.cu",
+                  "requant_flat_kernel": "quant.cu", "act_quant_kernel": "quant.cu"}
+
+
 def _committed_traffic(workload, kernel):
-    """DRAM bytes per launch of `kernel` on `workload` from profiles/traffic.md
-    (table rows `| workload | kernel | source sha256 prefix | bytes |`), if
-    the kernel's source file still matches the recorded hash; else None."""
+    """DRAM bytes per launch of `kernel` on `workload` from bench_traffic.json
+    (entries captured with ncu, keyed by the kernel's source sha256 prefix),
+    if the kernel's source file still matches the recorded hash; else None."""
     import hashlib
 
-    p = os.path.join(ROOT, "profiles", "traffic.md")
-    src = {"gemm_fp4_kernel": "gemm.cu", "requant_kernel": "quant.cu", "requant_flat_kernel": "quant.cu",
-           "act_quant_kernel": "quant.cu"}.get(kernel)
+    p = os.path.join(ROOT, "bench_traffic.json")
+    src = KERNEL_SOURCES.get(kernel)
     if not os.path.exists(p) or src is None:
         return None
     sha = hashlib.sha256(open(os.path.join(ROOT, "nvfp4_mxfp4_w4a4_gb300", "csrc", src), "rb").read()).hexdigest()
-    for ln in open(p):
-        f = [x.strip() for x in ln.strip().strip("|").split("|")]
-        if len(f) == 4 and f[0] == workload and f[1] == kernel and f[2] and sha.startswith(f[2]):
-            try:
-                return float(f[3])
-            except ValueError:
-                return None
+    for e in json.load(open(p)).get("entries", []):
+        if e.get("workload") == workload and e.get("kernel") == kernel and e.get("sha256_prefix") and \
+                sha.startswith(e["sha256_prefix"]):
+            return float(e["bytes_per_launch"])
     return None
 
 
@@ -992,94 +1063,143 @@ def _e2e(b, torch, L, reps, w_parts=1, m_chunk=2048):
 
 
 # ------------------------------------------------------------------ CPU oracle
-N_W, K_W = 14336, 4096
-MS = (1, 8, 32, 64)
-DECODE_DESC = ("decode layer: W[14336,4096] NVFP4->MXFP4 requant + MXFP4 act-quant + W4A4 GEMM (+bias), "
-               "M in {1,8,32,64}")
+# The oracle (a plain C reference of the method) timed on the host cores on
+# a bounded, proportional sample of a workload's step: for the dense
+# workloads `n` of the weight rows are requantized and multiplied with every
+# activation row, and every activation row is quantized; for MoE `n` of the
+# 64 experts run whole (their weights requantized, their rows quantized and
+# multiplied, both projections).  The sample's throughput (its GEMM FLOPs
+# over its wall time) is the reported value; the inputs (seeded, made by
+# the oracle's own NVFP4 producer) are prepared outside the timing.
 _SAMPLE_CACHE = {}
 
 
-def _decode_flops():
-    return sum(2.0 * M * N_W * K_W for M in MS)
-
-
-def _oracle_inputs(rows_w, threads):
-    """NVFP4 weight rows and activations for the oracle sample (input
-    preparation, not timed).  The global scale is that of the full weight."""
+def _oracle_inputs(workload, n, threads):
     import oracle
     import synth
 
-    if rows_w not in _SAMPLE_CACHE:
-        if "g" not in _SAMPLE_CACHE:
-            full = synth.workload1(rows=None)
-            _SAMPLE_CACHE["g"] = oracle.nvfp4_global_scale(full["W"])
-            del full
-        W = synth.workload1(rows=rows_w)
-        wp, ws = oracle.nvfp4_quantize(W["W"], _SAMPLE_CACHE["g"], threads=threads)
-        _SAMPLE_CACHE[rows_w] = (W, wp, ws)
-    return _SAMPLE_CACHE["g"], _SAMPLE_CACHE[rows_w]
+    key = (workload, n)
+    if key in _SAMPLE_CACHE:
+        return _SAMPLE_CACHE[key]
+    if workload in ("decode", "prefill"):
+        if (workload, "g") not in _SAMPLE_CACHE:
+            full = synth.workload1(rows=None) if workload == "decode" else synth.workload2()
+            _SAMPLE_CACHE[(workload, "g")] = oracle.nvfp4_global_scale(full["W"])
+            _SAMPLE_CACHE[(workload, "X")] = full["X"]
+            _SAMPLE_CACHE[(workload, "W")] = full["W"]
+            _SAMPLE_CACHE[(workload, "bias")] = full["bias"]
+        g = _SAMPLE_CACHE[(workload, "g")]
+        W = _SAMPLE_CACHE[(workload, "W")][:n]
+        wp, ws = oracle.nvfp4_quantize(W, g, threads=threads)
+        bias = _SAMPLE_CACHE[(workload, "bias")]
+        data = {"g": g, "wp": wp, "ws": ws, "X": _SAMPLE_CACHE[(workload, "X")],
+                "bias": None if bias is None else bias[:n], "N": _SAMPLE_CACHE[(workload, "W")].shape[0]}
+    else:
+        experts = list(range(n))
+        d = synth.workload3(experts=experts)
+        off = d["row_offsets"]
+        rows = np.concatenate([np.arange(off[e], off[e + 1]) for e in experts])
+        sub_off = np.zeros(n + 1, np.int32)
+        sub_off[1:] = np.cumsum([off[e + 1] - off[e] for e in experts])
+        proj = []
+        for A, Ws in ((d["A_gu"], d["W_gu"]), (d["A_down"], d["W_down"])):
+            ws_list = []
+            for e in experts:
+                g = oracle.nvfp4_global_scale(Ws[e])
+                wp, wsc = oracle.nvfp4_quantize(Ws[e], g, threads=threads)
+                ws_list.append((g, wp, wsc))
+            proj.append({"A": A[rows], "w": ws_list})
+        data = {"proj": proj, "offsets": sub_off, "E": 64}
+    _SAMPLE_CACHE[key] = data
+    return data
 
 
-def _oracle_sample(rows_w, threads):
-    """The oracle on a bounded sample of the decode step: `rows_w` weight
-    rows are requantized and multiplied with all activation rows
-    (M = 1+8+32+64), and all activations are quantized.  Returns (seconds,
-    fraction of the step)."""
+def _oracle_sample(workload, n, threads):
+    """Runs the oracle on the sample; returns (seconds, sample GEMM FLOPs,
+    full-step GEMM FLOPs)."""
     import oracle
 
-    g, (W, wp, ws) = _oracle_inputs(rows_w, threads)
+    d = _oracle_inputs(workload, n, threads)
+    if workload in ("decode", "prefill"):
+        K = d["wp"].shape[1] * 2
+        t0 = time.perf_counter()
+        bp, bs = oracle.requant(d["wp"], d["ws"], d["g"], threads=threads)
+        for M, X in d["X"].items():
+            ap, as_ = oracle.act_quant(X, threads=threads)
+            oracle.gemm(ap, as_, bp, bs, d["bias"], threads=threads)
+        dt = time.perf_counter() - t0
+        flops = sum(2.0 * M * n * K for M in d["X"])
+        full = sum(2.0 * M * d["N"] * K for M in d["X"])
+        return dt, flops, full
     t0 = time.perf_counter()
-    bp, bs = oracle.requant(wp, ws, g, threads=threads)
-    for M in MS:
-        ap, as_ = oracle.act_quant(W["X"][M], threads=threads)
-        oracle.gemm(ap, as_, bp, bs, W["bias"][:rows_w], threads=threads)
+    flops = 0.0
+    for pj in d["proj"]:
+        bs_, ss_ = [], []
+        for g, wp, wsc in pj["w"]:
+            bp, bs = oracle.requant(wp, wsc, g, threads=threads)
+            bs_.append(bp)
+            ss_.append(bs)
+        ap, as_ = oracle.act_quant(pj["A"], threads=threads)
+        oracle.gemm_grouped(ap, as_, np.stack(bs_), np.stack(ss_), None, d["offsets"], threads=threads)
+        flops += 2.0 * pj["A"].shape[0] * bs_[0].shape[0] * pj["A"].shape[1]
     dt = time.perf_counter() - t0
-    return dt, rows_w / N_W
+    return dt, flops, flops * d["E"] / len(d["offsets"][:-1])
 
 
-def cpu_baseline(budget_s=12.0):
+SAMPLE_UNITS = {"decode": (14336, "weight rows"), "prefill": (18432, "weight rows"), "moe": (64, "experts")}
+
+
+def _sample_text(workload, n):
+    total, unit = SAMPLE_UNITS[workload]
+    if workload == "moe":
+        return (f"{n} of {total} {unit} whole (their gate_up and down weights requantized, their rows quantized "
+                f"and multiplied)")
+    return (f"{n} of {total} {unit} requantized and multiplied with every activation row of the step; every "
+            f"activation row quantized")
+
+
+def cpu_baseline(workload, budget_s=12.0):
     threads = os.cpu_count() or 1
-    rows = 128
-    dt, frac = _oracle_sample(rows, threads)
-    if dt < budget_s / 4:
-        rows = int(min(N_W, rows * max(1.0, budget_s / max(dt, 1e-3))))
-        rows = max(128, rows // 128 * 128)
-        dt, frac = _oracle_sample(rows, threads)
-    full_s = dt / frac
-    # the same oracle on one thread (rows are independent: the results are
-    # identical), on a smaller sample
-    dt1, frac1 = _oracle_sample(128, 1)
-    return {"value": round(_decode_flops() / full_s / 1e12, 6), "unit": "TFLOPS", "cores": threads,
-            "kind": "oracle",
-            "sample": f"{rows} of {N_W} weight rows requantized and multiplied with all {sum(MS)} activation "
-                      f"rows, all activations quantized; step time extrapolated by {N_W}/{rows} "
-                      f"({dt:.2f} s measured)",
-            "single_thread": {"value": round(_decode_flops() / (dt1 / frac1) / 1e12, 6), "cores": 1,
-                              "sample": f"128 of {N_W} weight rows, extrapolated ({dt1:.2f} s measured)"}}
+    n = {"decode": 512, "prefill": 32, "moe": 1}[workload]
+    dt, flops, _ = _oracle_sample(workload, n, threads)
+    if dt < budget_s / 3:
+        total = SAMPLE_UNITS[workload][0]
+        n = int(min(total, n * max(1.0, budget_s / max(dt, 1e-3))))
+        n = max(1, n) if workload == "moe" else max(32, n // 32 * 32)
+        dt, flops, _ = _oracle_sample(workload, n, threads)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+            "sample": f"{_sample_text(workload, n)}; throughput of the sample ({dt:.2f} s measured)"}
+
+
+REF_SAMPLE = {"decode": 2048, "prefill": 64, "moe": 1}
 
 
 def run_reference(args):
     world, rank, local, pg = dist_setup(args)
     if rank != 0:
         return
+    workload = args.workload if args.workload in SAMPLE_UNITS else "prefill"
     threads = os.cpu_count() or 1
-    rows = 256
-    for _ in range(min(args.warmup, 5)):
-        _oracle_sample(rows, threads)
-    ts = []
-    steps = min(args.steps, 20)      # each step is a bounded sample; cap the run at a few minutes
+    n = REF_SAMPLE[workload]
+    _oracle_inputs(workload, n, threads)          # input preparation, not timed
+    for _ in range(min(args.warmup, 1)):
+        _oracle_sample(workload, n, threads)
+    steps = max(1, min(args.steps, 5))            # each step is a bounded sample; the run stays at a few minutes
+    ts, fl = [], 0.0
     for _ in range(steps):
-        dt, frac = _oracle_sample(rows, threads)
-        ts.append(dt / frac)
-    full_s = statistics.fmean(ts)
-    value = _decode_flops() / full_s / 1e12
+        dt, flops, _ = _oracle_sample(workload, n, threads)
+        ts.append(dt)
+        fl = flops
+    sec = statistics.fmean(ts)
+    value = fl / sec / 1e12
+    desc = {"decode": DECODE_DESC, "prefill": PREFILL_DESC, "moe": MOE_DESC}[workload]
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS", "n_gpus": world,
-        "steps": steps, "warmup": args.warmup, "ms_per_step": round(full_s * 1e3, 3), "higher_is_better": True,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
-        "config": {"workload": DECODE_DESC, "name": "decode"},
+        "config": {"workload": desc, "name": workload},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": threads, "kind": "oracle",
-                         "sample": f"{rows} of {N_W} weight rows per step, extrapolated"},
+                         "sample": _sample_text(workload, n) + "; throughput of the sample, per step"},
         "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
