@@ -607,6 +607,7 @@ def run_ours(args):
                 "us_total": round(q["s"] * 1e6, 2)}
 
     e2e = _e2e(b, torch, L, min(args.steps, 50))
+    fused = fused_quant_comparison(b, L, torch, args.breakdown_reps) if args.workload == "decode" else None
     nvfp4 = w4a8 = None
     if not args.no_nvfp4 and all(a.offsets is None for a in b.acts):
         nvfp4 = side_path_comparison(b, L, torch, args.breakdown_reps, breakdown, NvAct, "nv",
@@ -634,7 +635,7 @@ def run_ours(args):
         "requant_error": req_err,
         "fp4_probe_peak": fp4_probe,
         "breakdown": breakdown, "shares": shares, "roofline": roofline, "e2e": e2e, "nvfp4_path": nvfp4,
-        "w4a8_path": w4a8,
+        "w4a8_path": w4a8, "fused_act_quant": fused,
         "gpu_launches": b.launches_per_step * steps, "clocks": clk, "wall_s_timed_region": round(t_wall, 3),
     }
     if rank == 0 and not args.no_cpu_baseline and world == 1:
@@ -830,6 +831,36 @@ class A8Act:
         a, w = self.act, self.w
         self.L.fp4_gemm_w4a8(self.codes, self.scale, w.b_packed, w.b_scale, w.bias, self.out, a.M, w.N, a.K,
                              self.ws, stream=s)
+
+
+def fused_quant_comparison(b, L, torch, reps):
+    """Decode batches through fp4_linear as a chain of back-to-back calls
+    (buffer sets rotated as in the step), with the activation quantizer as
+    its own kernel before the GEMM and with FP4_LINEAR_FUSED_QUANT (the GEMM
+    quantizes the tokens itself); both with FP4_GEMM_WEIGHTS_STATIC (the
+    weights are not written by the kernel before each call)."""
+    res = {}
+    for ai, a0 in enumerate(b.acts):
+        if a0.offsets is not None or a0.M > 64:
+            continue
+        w0 = a0.w
+        ws = torch.zeros(max(256, L.fp4_linear_workspace_size(a0.M, w0.N, a0.K)), dtype=torch.uint8, device="cuda")
+        row = {}
+        for name, flags in (("act_quant_then_gemm", L.FP4_GEMM_WEIGHTS_STATIC),
+                            ("fused", L.FP4_GEMM_WEIGHTS_STATIC | L.FP4_LINEAR_FUSED_QUANT)):
+            def fn(s, i, ai=ai, flags=flags):
+                a = b.sets[i][1][ai]
+                L.fp4_linear(a.x, a.w.b_packed, a.w.b_scale, a.w.bias, a.out, a.M, a.w.N, a.K, ws,
+                             gemm_flags=flags, stream=s)
+            g = b.graph(fn)
+            r = max(1, -(-reps // b.n_sets))
+            b.time_graph(g, 1)
+            row[name + "_us"] = round(b.time_graph(g, r) / (r * b.n_sets) * 1e3, 2)
+        row["fused_gain_us"] = round(row["act_quant_then_gemm_us"] - row["fused_us"], 2)
+        res[f"M{a0.M}"] = row
+    res["what"] = ("fp4_linear per decode batch, back-to-back calls: activation quantizer kernel then GEMM, "
+                   "against one GEMM that quantizes the tokens itself (bit-identical output)")
+    return res
 
 
 def _w4a8_workspace(torch, need):

@@ -434,8 +434,22 @@ typedef struct {
     int32_t act_format;          /* fp4_act_format; MXFP8 is the W4A8 fallback   */
     int32_t scale_alg;           /* MXFP4 activations: OCP or UOS; MXFP8: OCP    */
     const void* mul_scale_bf16;  /* smooth pre-scale [K] bf16 (device), or NULL  */
-    uint32_t gemm_flags;         /* 0 or FP4_GEMM_WEIGHTS_STATIC                 */
+    uint32_t gemm_flags;         /* FP4_GEMM_WEIGHTS_STATIC, FP4_LINEAR_FUSED_QUANT */
 } fp4_linear_opts;
+
+/* fp4_linear flag: for MXFP4 activations and M <= 64, quantize the
+ * activations inside the GEMM kernel instead of in a kernel before it
+ * ([AMD], last section "Fusing activation quantization + GEMM"): the
+ * GEMM's otherwise idle epilogue warps quantize each pipeline stage's bf16
+ * token slab into shared memory with the activation quantizer's block
+ * arithmetic, so the result is bit-identical to the unfused call; the
+ * quantized activations are not written to the workspace.  Other shapes
+ * and formats ignore the flag.  Measured on GB300 (14336 x 4096 weight,
+ * back-to-back calls): no faster than the two-kernel path at M = 1 and
+ * slower at larger M, since every weight-tile CTA quantizes the whole token
+ * tile; the two-kernel path already overlaps its quantizer with the GEMM's
+ * start (programmatic dependent launch, FP4_GEMM_WEIGHTS_STATIC).          */
+#define FP4_LINEAR_FUSED_QUANT 2u
 
 /* Bytes of workspace fp4_linear needs for an M x N x K layer with these
  * options on the current device (0 for M = 0, invalid options or no usable
@@ -451,7 +465,9 @@ FP4LIN_API size_t fp4_linear_workspace_size(int64_t M, int64_t N, int64_t K,
  * fallback / Pre-Quantized Single-Scale Weights (smooth), [SGL] section 6
  * (bias after the GEMM).  Exactly fp4_quant_act_mxfp4[_smooth] (or
  * fp4_quant_act_mxfp8[_smooth]) into the workspace followed by
- * fp4_gemm_mxfp4_ex (or fp4_gemm_w4a8) on the same stream.
+ * fp4_gemm_mxfp4_ex (or fp4_gemm_w4a8) on the same stream (with
+ * FP4_LINEAR_FUSED_QUANT and M <= 64: one GEMM launch that quantizes the
+ * activations itself, bit-identical output).
  *   x_bf16     [M, K] bf16; w [N, K/2] MXFP4 codes, sw SWIZZLED E8M0
  *   workspace  device memory, 256-byte aligned, at least
  *              fp4_linear_workspace_size(M, N, K, opts) bytes; its first

@@ -383,7 +383,8 @@ extern "C" {
 static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                               const void* bias, void* out, const int32_t* offsets, int32_t E, int64_t M, int64_t N,
                               int64_t K, void* workspace, size_t workspace_bytes, void* stream,
-                              int fmt = fp4lin::kGemmMx, float alpha = 1.0f, uint32_t flags = 0)
+                              int fmt = fp4lin::kGemmMx, float alpha = 1.0f, uint32_t flags = 0,
+                              const void* fused_x = nullptr, const void* fused_mul = nullptr, int fused_uos = 0)
 {
     fp4_status st = static_cast<fp4_status>(fp4lin::gemm_check_args(a, sa, b, sb, bias, out, M, N, K, E));
     if (st != FP4_OK || M == 0)
@@ -410,6 +411,9 @@ static fp4_status gemm_common(const uint8_t* a, const uint8_t* sa, const uint8_t
     args.fmt = fmt;
     args.alpha = alpha;
     args.early_weights = (flags & FP4_GEMM_WEIGHTS_STATIC) != 0;
+    args.x_bf16 = fused_x;
+    args.x_mul = fused_mul;
+    args.x_uos = fused_uos;
     args.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     args.withhold_split_signal = g_withhold_split_signal.load(std::memory_order_relaxed) != 0;
     return from_cuda(fp4lin::launch_gemm(args, static_cast<cudaStream_t>(stream)));
@@ -556,7 +560,7 @@ fp4_status linear_plan(int64_t M, int64_t N, int64_t K, const fp4_linear_opts* o
         return FP4_ERR_INVALID_ARG;
     if (act == FP4_ACT_MXFP8 && alg != FP4_SCALE_OCP)
         return FP4_ERR_INVALID_ARG;  // the A8 path always takes the OCP rule
-    if (o && (o->gemm_flags & ~static_cast<uint32_t>(FP4_GEMM_WEIGHTS_STATIC)))
+    if (o && (o->gemm_flags & ~static_cast<uint32_t>(FP4_GEMM_WEIGHTS_STATIC | FP4_LINEAR_FUSED_QUANT)))
         return FP4_ERR_INVALID_ARG;
     pl->fmt = act == FP4_ACT_MXFP8 ? fp4lin::kGemmW4A8 : fp4lin::kGemmMx;
     pl->alg = alg;
@@ -600,6 +604,15 @@ fp4_status fp4_linear(const void* x_bf16, const uint8_t* w, const uint8_t* sw, c
     uint8_t* a = base + pl.act_off;
     uint8_t* sa = base + pl.sf_off;
     const void* mul = opts ? opts->mul_scale_bf16 : nullptr;
+    const uint32_t gflags = opts ? opts->gemm_flags : 0u;
+    if ((gflags & FP4_LINEAR_FUSED_QUANT) && pl.fmt == fp4lin::kGemmMx && M <= 64) {
+        // the GEMM quantizes the activations itself (a and sa are not read)
+        if (!aligned16(x_bf16) || (mul && !aligned16(mul)))
+            return FP4_ERR_ALIGNMENT;
+        return gemm_common(a, sa, w, sw, bias_bf16, out_bf16, nullptr, 1, M, N, K, pl.split ? base : nullptr,
+                           pl.split, stream, fp4lin::kGemmMx, 1.0f, gflags & FP4_GEMM_WEIGHTS_STATIC, x_bf16, mul,
+                           pl.alg == FP4_SCALE_UOS ? 1 : 0);
+    }
     if (pl.fmt == fp4lin::kGemmW4A8)
         st = act_quant8_common(x_bf16, mul, a, sa, M, K, FP4_SF_SWIZZLED, stream);
     else {
@@ -609,7 +622,7 @@ fp4_status fp4_linear(const void* x_bf16, const uint8_t* w, const uint8_t* sw, c
     if (st != FP4_OK)
         return st;
     return gemm_common(a, sa, w, sw, bias_bf16, out_bf16, nullptr, 1, M, N, K, pl.split ? base : nullptr, pl.split,
-                       stream, pl.fmt, 1.0f, opts ? opts->gemm_flags : 0u);
+                       stream, pl.fmt, 1.0f, gflags & FP4_GEMM_WEIGHTS_STATIC);
 }
 
 size_t fp4_linear_grouped_workspace_size(int64_t total_M, int32_t E, int64_t K)

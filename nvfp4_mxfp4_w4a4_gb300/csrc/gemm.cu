@@ -68,6 +68,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "formats.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -102,6 +103,9 @@ struct GemmParams {
     float alpha;                // NVFP4 mode: factor on the accumulator before the bias
     int early_w;                // weights not written by the kernel this one may overlap
     int withhold_signal;        // test hook: the last CTA of a split launch never publishes its partial
+    const uint16_t* x;          // fused activation quantization: bf16 tokens [rows_b, K] (swapped mode)
+    const uint16_t* xmul;       // its smooth pre-scale (bf16 [K]) or null
+    int x_uos;                  // its block rule: UOS (else OCP)
     unsigned long long wait_ns; // limit of every bounded wait
     unsigned int* status;
 };
@@ -316,7 +320,12 @@ __device__ __forceinline__ void load_operand(void* dst, const CUtensorMap* map, 
         tma_load_3d(dst, map, bar, 0, static_cast<int32_t>(row0), kb * KC);
 }
 
-template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped, int kFmt>
+// kFuseX (swapped MXFP4 only): the tokens arrive as bf16 and the epilogue
+// warps, idle during the main loop, quantize each stage's token slab into the
+// stage's B operand and scale chunk themselves (the activation quantizer's
+// block arithmetic, so the codes and scales are the same bytes), instead of
+// a TMA load of tokens quantized by a kernel before this one.
+template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped, int kFmt, bool kFuseX = false>
 __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmO, const GemmParams p)
@@ -324,6 +333,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
     using C = Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>;
     constexpr bool kNv = C::kNv, kA8 = C::kA8;
     constexpr int kFirstEpiWarp = C::FIRST_EPI_WARP;
+    static_assert(!kFuseX || (kSwap && !kGrouped && kFmt == kFmtMx && BN <= 128), "fused quantization: swapped MXFP4");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
@@ -353,7 +363,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
         const int64_t atoms_per_rt = static_cast<int64_t>(p.kb4) * C::APG;  // chunks per 128-row tile
         // boxes past the end of K or of the rows are zero-filled and still counted
         if (expect)
-            mbar_arrive_expect_tx(&full[s], C::A_TX + C::B_TX + sf_bytes * (1u + nsfb));
+            mbar_arrive_expect_tx(&full[s], kFuseX ? C::A_TX + sf_bytes : C::A_TX + C::B_TX + sf_bytes * (1u + nsfb));
         const int a_half = kSwap ? kHalfW : kHalfX;
         if (halves & a_half) {
             load_operand<KC>(smem + C::OFF_A + s * C::A_BYTES, &tmA, &full[s], kb, T.a_row0);
@@ -383,7 +393,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
     bool have_first = false;
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], kFuseX ? 1 + kEpiWarps : 1);  // fused: + one arrival per quantizing warp
             mbar_init(&empty[s], 1);
             mbar_init(&sf_full[s], CPW);
         }
@@ -434,6 +444,16 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
             }
         }
     }
+    if constexpr (kFuseX) {
+        // the quantizing warps write the token rows of each scale chunk; the
+        // other rows of the 128-row chunks stay zero
+        // (and of each stage's token codes: only the real rows are written later)
+        for (int i = threadIdx.x; i < STAGES * C::SFB_BYTES / 16; i += C::THREADS)
+            reinterpret_cast<uint4*>(smem + C::OFF_SFB)[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = threadIdx.x; i < STAGES * C::B_BYTES / 16; i += C::THREADS)
+            reinterpret_cast<uint4*>(smem + C::OFF_B)[i] = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -463,14 +483,15 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                         const uint32_t ph = (it / STAGES) & 1u;
                         if (static_cast<int>(it) < npre) {
                             // weight half issued before the dependency wait (first pass over the ring)
-                            stage_loads(s, kb, T, kHalfX, false);
+                            if constexpr (!kFuseX)
+                                stage_loads(s, kb, T, kHalfX, false);
                             continue;
                         }
                         if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kStatusTimeout, p.wait_ns)) {
                             ok = false;
                             break;
                         }
-                        stage_loads(s, kb, T, kHalfW | kHalfX, true);
+                        stage_loads(s, kb, T, kFuseX ? kHalfW : (kHalfW | kHalfX), true);
                     }
                 }
             }
@@ -592,6 +613,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
         constexpr int CW = C::CW;
         uint8_t* epi = smem + C::OFF_EPI;
         uint32_t tcount = 0;
+        uint32_t qit = 0;     // fused: stages this warp has quantized
+        bool qok = true;
         bool stored = false;  // this thread has bulk stores in flight
         WorkIter wi = work_begin(p, total_tiles);
         Work w;
@@ -599,6 +622,94 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
             const Tile T = decode_tile<BN, kGrouped>(w.t, p, tiles_before);
             if (!T.valid)
                 continue;
+            if constexpr (kFuseX) {
+                // ------------------------------------------ token quantization
+                // Job j of a stage: lane quarter j % 4 of 32-element block
+                // j / 4 (row r, block cl of the stage's K range); 4 consecutive
+                // lanes hold one block, as in the activation quantizer.  Only
+                // the tile's real token rows are processed: the pad rows of
+                // every stage's codes and scale chunks were zeroed at setup
+                // and nothing else writes them.  A stage's token loads are all
+                // issued before the slot wait (and, for tiles of 16 tokens,
+                // one stage ahead), so their latency overlaps.
+                constexpr int kBlocksPerRow = C::GROUPS * 4;
+                constexpr int kJobs = BN * kBlocksPerRow * 4;
+                constexpr int kPer = kJobs / (32 * kEpiWarps);  // jobs per thread per stage
+                constexpr int kCh = BN >= 64 ? 2 : (kPer < 4 ? kPer : 4);  // jobs whose loads are in flight together
+                static_assert(kJobs % (32 * kEpiWarps) == 0 && kPer % kCh == 0, "whole warps per stage");
+                const int et = threadIdx.x - 32 * kFirstEpiWarp;
+                const int kbt = p.K / 32;
+                const int rows_real = min(BN, p.rows_b - T.n0);
+                const int jobs_real = rows_real * kBlocksPerRow * 4;
+                // loads of jobs i0 .. i0 + kCh - 1 of stage kb
+                auto load_jobs = [&](int kb, int i0, uint4 (&v)[kCh]) {
+#pragma unroll
+                    for (int i = 0; i < kCh; ++i) {
+                        const int j = et + (i0 + i) * 32 * kEpiWarps;
+                        const int blk = j >> 2;
+                        const int r = blk / kBlocksPerRow;
+                        const int cg = kb * kBlocksPerRow + (blk - r * kBlocksPerRow);
+                        v[i] = make_uint4(0u, 0u, 0u, 0u);
+                        if (j < jobs_real && cg < kbt)
+                            v[i] = *reinterpret_cast<const uint4*>(p.x + (static_cast<int64_t>(T.n0) + r) * p.K +
+                                                                   static_cast<int64_t>(cg) * 32 + (j & 3) * 8);
+                    }
+                };
+                uint4 vc[kCh], vn[kCh];
+                if (w.kb0 < w.kb1)
+                    load_jobs(w.kb0, 0, vc);
+                for (int kb = w.kb0; kb < w.kb1 && qok; ++kb, ++qit) {
+                    const int s = static_cast<int>(qit % STAGES);
+                    const uint32_t ph = (qit / STAGES) & 1u;
+                    if (!mbar_wait_bounded(&empty[s], ph ^ 1u, p.status, kStatusTimeout, p.wait_ns)) {
+                        qok = false;
+                        break;
+                    }
+                    uint8_t* bst = smem + C::OFF_B + s * C::B_BYTES;
+                    uint8_t* sfb = smem + C::OFF_SFB + s * C::SFB_BYTES;
+#pragma unroll 1
+                    for (int i0 = 0; i0 < kPer; i0 += kCh) {
+                        // the next chunk's loads (or the next stage's first) go out before this one's work
+                        if (i0 + kCh < kPer)
+                            load_jobs(kb, i0 + kCh, vn);
+                        else if (kb + 1 < w.kb1)
+                            load_jobs(kb + 1, 0, vn);
+#pragma unroll
+                        for (int i = 0; i < kCh; ++i) {
+                            const int j0 = (et & ~31) + (i0 + i) * 32 * kEpiWarps;  // this warp's first job
+                            if (j0 < jobs_real) {  // whole warps together (the lane quantizer shuffles)
+                                const int j = j0 + lane;
+                                const int q = j & 3;
+                                const int blk = j >> 2;
+                                const int r = blk / kBlocksPerRow;
+                                const int cl = blk - r * kBlocksPerRow;
+                                const int cg = kb * kBlocksPerRow + cl;
+                                uint4 v = vc[i];
+                                if (p.xmul != nullptr && cg < kbt)
+                                    v = smooth_bf16x8(v, __ldg(reinterpret_cast<const uint4*>(
+                                                             p.xmul + static_cast<int64_t>(cg) * 32 + q * 8)));
+                                uint32_t sf;
+                                const uint32_t codes = act_quant_lane(v, p.x_uos, sf);
+                                if (j < jobs_real && cg < kbt) {
+                                    // 128-byte swizzle of the operand stage: 16-byte unit u of row r at u ^ (r % 8)
+                                    *reinterpret_cast<uint32_t*>(bst + (cl >> 3) * (BN * kSlabBytes) + r * kSlabBytes +
+                                                                 (((cl & 7) ^ (r & 7)) << 4) + q * 4) = codes;
+                                    if (q == 0)
+                                        sfb[(cl >> 2) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (cl & 3)] =
+                                            static_cast<uint8_t>(sf);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < kCh; ++i)
+                            vc[i] = vn[i];
+                    }
+                    fence_proxy_async_smem();  // the MMA and the scale copies read them through the async proxy
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&full[s]);
+                }
+            }
             // swapped: this lane's output column has one bias value, an input
             // the MMAs do not touch -- fetch it before the accumulator wait so
             // its latency is not added after the last MMA
@@ -898,7 +1009,7 @@ void swap_config(int64_t M, int64_t K, int* bn, int* kc)
     *bn = *kc == 2 ? (M <= 16 ? 16 : M <= 32 ? 32 : 64) : 64;
 }
 
-template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped, int kFmt = kFmtMx>
+template <int BN, int STAGES, int KC, int CPW, bool kSwap, bool kGrouped, int kFmt = kFmtMx, bool kFuseX = false>
 cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
 {
     using C = Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>;
@@ -915,7 +1026,9 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
     const int kind_b = kA8 ? (kSwap ? kOpBytes : kOpFp4Expanded) : kOpFp4Packed;
     if (!make_operand_map(&tmA, opA, rows_a, a.K, BM, KC, kind_a))
         return cudaErrorInvalidValue;
-    if (!make_operand_map(&tmB, opB, static_cast<int64_t>(a.E) * rows_b, a.K, BN, KC, kind_b))
+    // fused: there is no quantized token operand; the unused B map points at the weights
+    if (!make_operand_map(&tmB, kFuseX ? opA : opB, kFuseX ? rows_a : static_cast<int64_t>(a.E) * rows_b, a.K,
+                          kFuseX ? BM : BN, KC, kFuseX ? kind_a : kind_b))
         return cudaErrorInvalidValue;
     if (!(kSwap ? make_output_map(&tmO, a.out, a.M, a.N, 32, BN / 2, CU_TENSOR_MAP_SWIZZLE_NONE)
                 : make_output_map(&tmO, a.out, a.M, a.N, C::CHUNK, 32,
@@ -943,6 +1056,9 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
     p.alpha = a.alpha;
     p.early_w = (a.early_weights && !kGrouped) ? 1 : 0;
     p.withhold_signal = a.withhold_split_signal ? 1 : 0;
+    p.x = static_cast<const uint16_t*>(a.x_bf16);
+    p.xmul = static_cast<const uint16_t*>(a.x_mul);
+    p.x_uos = a.x_uos;
     p.wait_ns = a.wait_ns;
     p.status = a.status;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -963,7 +1079,7 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
         }
     }
     const size_t smem = C::SMEM_FIXED + (kGrouped ? sizeof(int32_t) * (a.E + 1) : 0);
-    auto kern = gemm_fp4_kernel<BN, STAGES, KC, CPW, kSwap, kGrouped, kFmt>;
+    auto kern = gemm_fp4_kernel<BN, STAGES, KC, CPW, kSwap, kGrouped, kFmt, kFuseX>;
     // The shared-memory opt-in is a per-device function attribute: set it
     // once per device (and grow it if a larger grouped prefix needs more).
     // (keyed by context too: a reset device has a new context without it)
@@ -1088,6 +1204,14 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream)
     }
     // decode-sized batches: weights on the 128-row MMA side, tokens as N
     // (the choice swap_config describes)
+    if (a.M <= 64 && a.x_bf16 != nullptr) {  // tokens quantized inside the GEMM
+        if (!k256)
+            return launch_kernel<64, 8, 1, 4, true, false, kFmtMx, true>(a, stream);
+        if (a.M <= 16)
+            return launch_kernel<16, 5, 2, 4, true, false, kFmtMx, true>(a, stream);
+        return a.M <= 32 ? launch_kernel<32, 4, 2, 4, true, false, kFmtMx, true>(a, stream)
+                         : launch_kernel<64, 4, 2, 4, true, false, kFmtMx, true>(a, stream);
+    }
     if (a.M <= 64) {
         if (!k256)
             return launch_kernel<64, 8, 1, 4, true, false>(a, stream);

@@ -134,6 +134,11 @@ struct GemmArgs {
     bool early_weights = false;  // the weights are not written by the preceding kernel in the stream
     unsigned long long wait_ns = kWaitLimitNs;  // limit of every bounded device wait of the launch
     bool withhold_split_signal = false;  // test hook: one split-K partial never signals its finisher
+    // M <= 64 MXFP4 only: bf16 activations [M, K] that the GEMM quantizes
+    // itself (a and sa unused), with an optional smooth pre-scale and rule
+    const void* x_bf16 = nullptr;
+    const void* x_mul = nullptr;
+    int x_uos = 0;
 };
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);

@@ -511,37 +511,9 @@ __global__ void __launch_bounds__(kThreads, 4) requant_flat_kernel(const uint8_t
 }
 
 // ------------------------------------------------------- activation quant
-// One lane holds 8 consecutive bf16 of a 32-element block (4 lanes per
-// block).  Returns the packed codes (4 bytes) and, through `sf`, the block's
-// scale byte (the same on all 4 lanes).  q = x * 2^-e is exact in fp32 (a
-// bf16 value times a power of two; e <= 125 for a finite bf16 amax and
-// e >= -127 after the clamp, so 2^-e is a normal fp32), and the hardware
-// pair conversion rounds it to E2M1.
-__device__ __forceinline__ uint32_t act_quant_lane(uint4 v, int uos, uint32_t& sf)
-{
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    // amax as bf16 bit patterns of |x| (NaN above Inf above every finite)
-    const uint32_t a = __vmaxu2(__vmaxu2(w[0] & 0x7FFF7FFFu, w[1] & 0x7FFF7FFFu),
-                                __vmaxu2(w[2] & 0x7FFF7FFFu, w[3] & 0x7FFF7FFFu));
-    uint32_t am = max(a & 0xFFFFu, a >> 16);
-    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
-    const uint32_t ab = am << 16;
-    if (ab >= 0x7F800000u) {
-        sf = 0xFFu;
-        return 0u;
-    }
-    const int e = mx_shared_exp(ab, uos);
-    sf = static_cast<uint32_t>(e + 127);
-    const float se = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
-    float q[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        q[2 * j] = __fmul_rn(__uint_as_float(w[j] << 16), se);
-        q[2 * j + 1] = __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), se);
-    }
-    return e2m1x8_pack(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
-}
+// (act_quant_lane and smooth_bf16x8, the MXFP4 block quantizer of one lane
+// and the smooth pre-scale, live in formats.cuh: the GEMM that quantizes its
+// own activations runs the same code.)
 
 // The same block to MXFP8 (float8_e4m3fn elements) for the W4A8 fallback:
 // OCP exponent e = floor(log2 amax) - 8 (8 = exponent of E4M3's largest
@@ -574,23 +546,6 @@ __device__ __forceinline__ uint2 act_quant_lane8(uint4 v, uint32_t& sf)
         h[j] = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
     }
     return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
-}
-
-// Eight bf16 times eight bf16, each product rounded once to bf16 (the exact
-// float32 product of two bf16 values, then round to nearest even).
-__device__ __forceinline__ uint4 smooth_bf16x8(uint4 x, uint4 m)
-{
-    const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-    const uint32_t mw[4] = {m.x, m.y, m.z, m.w};
-    uint32_t r[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float lo = __fmul_rn(__uint_as_float(xw[j] << 16), __uint_as_float(mw[j] << 16));
-        const float hi = __fmul_rn(__uint_as_float(xw[j] & 0xFFFF0000u), __uint_as_float(mw[j] & 0xFFFF0000u));
-        const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-        r[j] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-    return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
 // Smooth pre-scale preparation: float32 [K] -> bf16 [K] (nearest even) and

@@ -62,6 +62,7 @@ class fp4_linear_opts(ctypes.Structure):
 
 FP4_ACT_MXFP4 = 0
 FP4_ACT_MXFP8 = 1
+FP4_LINEAR_FUSED_QUANT = 2
 
 
 _lib = None
