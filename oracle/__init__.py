@@ -77,6 +77,9 @@ def lib():
                 ("orc_gemm_w4a8", None, [_p, _p, _p, _p, _p, _i64, _p, _i64, _p, _i64, _p, _p]),
                 ("orc_gemm_nvfp4", None,
                  [_p, _p, _p, _p, ctypes.c_double, _p, _i64, _p, _i64, _p, _i64, _p, _p]),
+                ("orc_dual_dequant", None, [_p, _p, _p, _i64, _i64, _p]),
+                ("orc_dual_quantize", None, [_p, _i64, _i64, _i64, _p, _p, _p]),
+                ("orc_gemm_dual", None, [_p, _p, _p, _p, _p, _p, _i64, _p, _i64, _p, _i64, _p, _p]),
                 ("orc_nvfp4_global_scale", ctypes.c_float, [_p, _i64]),
                 ("orc_nvfp4_quantize", None, [_p, ctypes.c_float, _i64, _i64, _i64, _p, _p]),
                 ("orc_sf_swizzled_bytes", _i64, [_i64, _i64]),
@@ -340,6 +343,62 @@ def gemm_grouped(a, sa, b, sb, bias_bf16_bits, row_offsets, rows=None, cols=None
         r, s = gemm(a, sa, b[e], sb[e], bias, rows=rows[sel], cols=cols, threads=threads)
         ref[sel] = r
         absum[sel] = s
+    return ref, absum
+
+
+# ---------------------------------------------------------- DualScale
+def dual_dequant(packed, fine, coarse) -> np.ndarray:
+    """DualScale weight -> float64 [rows, K] (code x 2^(fine-127) x coarse)."""
+    packed = np.ascontiguousarray(packed, np.uint8)
+    fine = np.ascontiguousarray(fine, np.uint8)
+    coarse = np.ascontiguousarray(coarse, np.float32)
+    rows, half = packed.shape
+    out = np.empty((rows, 2 * half), np.float64)
+    lib().orc_dual_dequant(_ptr(packed), _ptr(fine), _ptr(coarse), rows, 2 * half, _ptr(out))
+    return out
+
+
+def dual_quantize(w_bf16_bits, threads=1):
+    """bf16 bits [N, K] (K % 512 == 0) -> (codes [N, K/2] u8, fine E8M0
+    [N, K/32] u8, coarse [N, K/512] float32) by the online dual-level rule."""
+    w = np.ascontiguousarray(w_bf16_bits, np.uint16)
+    N, K = w.shape
+    packed = np.empty((N, K // 2), np.uint8)
+    fine = np.empty((N, K // 32), np.uint8)
+    coarse = np.empty((N, K // 512), np.float32)
+    L = lib()
+    _parallel(lambda r0, r1: L.orc_dual_quantize(_ptr(w), r0, r1, K, _ptr(packed), _ptr(fine), _ptr(coarse)),
+              N, threads)
+    return packed, fine, coarse
+
+
+def gemm_dual(a, sa, b, fine, coarse, bias_bf16_bits=None, rows=None, cols=None, threads=1):
+    """float64 reference: MXFP4 activations x DualScale weights (+ bias)."""
+    a = np.ascontiguousarray(a)
+    sa = np.ascontiguousarray(sa)
+    b = np.ascontiguousarray(b)
+    fine = np.ascontiguousarray(fine, np.uint8)
+    coarse = np.ascontiguousarray(coarse, np.float32)
+    M, half = a.shape
+    N = b.shape[0]
+    K = 2 * half
+    rows = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    cols = np.arange(N, dtype=np.int64) if cols is None else np.ascontiguousarray(cols, np.int64)
+    bias = None if bias_bf16_bits is None else np.ascontiguousarray(bias_bf16_bits, np.uint16)
+    ref = np.empty((len(rows), len(cols)), np.float64)
+    absum = np.empty_like(ref)
+    L = lib()
+
+    def run(r0, r1):
+        sub_rows = np.ascontiguousarray(rows[r0:r1])
+        r = np.empty((r1 - r0, len(cols)), np.float64)
+        s_ = np.empty_like(r)
+        L.orc_gemm_dual(_ptr(a), _ptr(sa), _ptr(b), _ptr(fine), _ptr(coarse), _ptr(bias), K, _ptr(sub_rows),
+                        r1 - r0, _ptr(cols), len(cols), _ptr(r), _ptr(s_))
+        ref[r0:r1] = r
+        absum[r0:r1] = s_
+
+    _parallel(run, len(rows), threads)
     return ref, absum
 
 

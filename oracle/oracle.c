@@ -554,6 +554,100 @@ void orc_nvfp4_quantize(const uint16_t* x_bf16, float g, int64_t row0, int64_t r
 }
 
 /* ------------------------------------------------------------------------
+ * DualScale weights ([OMNI] "mxfp4_dualscale -- DualScale Offline Mode",
+ * "Checkpoint tensor layout": FP4 values, a fine E8M0 block scale per 32
+ * K-elements (weight_scale [N][K/32]) and a coarse float32 block scale per
+ * 512 K-elements (weight_dual_scale [N][K/512][1])).  Reading: an element's
+ * value is  E2M1(code) * 2^(fine - 127) * coarse,  in double (exact: the
+ * first two factors are a binary fraction with 2 significant bits, the
+ * coarse scale a float).
+ * --------------------------------------------------------------------- */
+static void dequant_dual_row(const uint8_t* packed, const uint8_t* fine, const float* coarse, int64_t K,
+                             double* out)
+{
+    for (int64_t k = 0; k < K; ++k) {
+        uint8_t byte = packed[k / 2];
+        unsigned c = (k % 2 == 0) ? (byte & 0xFu) : (byte >> 4);
+        out[k] = orc_e2m1_value(c) * orc_e8m0_value(fine[k / 32]) * (double)coarse[k / 512];
+    }
+}
+
+void orc_dual_dequant(const uint8_t* packed, const uint8_t* fine, const float* coarse, int64_t rows, int64_t K,
+                      double* out)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        dequant_dual_row(packed + r * (K / 2), fine + r * (K / 32), coarse + r * (K / 512), K, out + r * K);
+}
+
+/* Online dual-level quantization of a bf16 weight ([OMNI] "DualScale Online
+ * Mode": both scale levels are computed on the fly from the bf16 weight; the
+ * page only names the operation).  Reading, per row and 512-element group:
+ *   coarse = float32(amax / 6), amax the group's largest finite magnitude
+ *            (coarse = 1 for a group without a nonzero finite element), so
+ *            that the group's largest element lands on E2M1's largest value;
+ *   y      = float32(w / coarse) for every element;
+ * then the single-scale OCP MX block rule on y per 32 elements (fine E8M0
+ * exponent, nearest E2M1 value with ties to the even code, saturating at
+ * 6).  A NaN or Inf element makes only its own 32-element block 0xFF with
+ * zero codes, as in the single-scale rule.  Both divisions are IEEE float32
+ * operations.                                                              */
+void orc_dual_quantize(const uint16_t* w_bf16, int64_t row0, int64_t row1, int64_t K, uint8_t* out_packed,
+                       uint8_t* out_fine, float* out_coarse)
+{
+    float v[32];
+    for (int64_t r = row0; r < row1; ++r)
+        for (int64_t g = 0; g < K / 512; ++g) {
+            const uint16_t* w = w_bf16 + r * K + 512 * g;
+            float amax = 0.0f;
+            for (int i = 0; i < 512; ++i) {
+                float x = (float)orc_bf16_value(w[i]);
+                if (isfinite(x) && fabsf(x) > amax)
+                    amax = fabsf(x);
+            }
+            const float coarse = amax > 0.0f ? amax / 6.0f : 1.0f;
+            out_coarse[r * (K / 512) + g] = coarse;
+            for (int b = 0; b < 16; ++b) {
+                for (int i = 0; i < 32; ++i)
+                    v[i] = (float)orc_bf16_value(w[32 * b + i]) / coarse;
+                orc_mx_quantize_block(v, ORC_SCALE_OCP, out_packed + r * (K / 2) + (512 * g + 32 * b) / 2,
+                                      out_fine + r * (K / 32) + 16 * g + b);
+            }
+        }
+}
+
+/* DualScale GEMM (W4A4 with dual-level weight scales): MXFP4 activations
+ * times DualScale weights, float64 accumulation:
+ *   ref[i][j] = sum_k dq(A)[rows[i]][k] * dqd(B)[cols[j]][k] + bias[cols[j]]
+ *   absum[i][j] = sum_k |dq(A) * dqd(B)|.                                  */
+void orc_gemm_dual(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* fine, const float* coarse,
+                   const uint16_t* bias_bf16, int64_t K, const int64_t* rows, int64_t n_rows, const int64_t* cols,
+                   int64_t n_cols, double* ref, double* absum)
+{
+    double* arows = (double*)malloc(sizeof(double) * (size_t)(n_rows * K));
+    double* brow = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int64_t i = 0; i < n_rows; ++i)
+        dequant_mx_row(a + rows[i] * (K / 2), sa + rows[i] * (K / 32), K, arows + i * K);
+    for (int64_t j = 0; j < n_cols; ++j) {
+        int64_t n = cols[j];
+        dequant_dual_row(b + n * (K / 2), fine + n * (K / 32), coarse + n * (K / 512), K, brow);
+        double bias = bias_bf16 ? orc_bf16_value(bias_bf16[n]) : 0.0;
+        for (int64_t i = 0; i < n_rows; ++i) {
+            const double* arow = arows + i * K;
+            double s = 0.0, sabs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = arow[k] * brow[k];
+                s += p;
+                sabs += fabs(p);
+            }
+            ref[i * n_cols + j] = s + bias;
+            absum[i * n_cols + j] = sabs;
+        }
+    }
+    free(brow);
+    free(arows);
+}
+
+/* ------------------------------------------------------------------------
  * Scale-factor layout read by the block-scaled tensor-core MMA (reading;
  * [SGL] section 5 only names a "swizzle_blockscale" step).  Rows are grouped
  * in tiles of 128 and block columns in groups of 4; each (tile, group) is a

@@ -105,6 +105,18 @@ void orc_gemm_nvfp4(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const
                     const int64_t* rows, int64_t n_rows, const int64_t* cols, int64_t n_cols,
                     double* ref, double* absum);
 
+/* ---- DualScale weights ([OMNI] "mxfp4_dualscale"): E2M1 codes [rows][K/2],
+ * fine E8M0 [rows][K/32], coarse float32 [rows][K/512]; K % 512 == 0.     */
+void orc_dual_dequant(const uint8_t* packed, const uint8_t* fine, const float* coarse, int64_t rows, int64_t K,
+                      double* out);
+/* bf16 weight -> DualScale (online dual-level quantization, stated reading). */
+void orc_dual_quantize(const uint16_t* w_bf16, int64_t row0, int64_t row1, int64_t K, uint8_t* out_packed,
+                       uint8_t* out_fine, float* out_coarse);
+/* MXFP4 activations x DualScale weights, float64 accumulation (as orc_gemm). */
+void orc_gemm_dual(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* fine, const float* coarse,
+                   const uint16_t* bias_bf16, int64_t K, const int64_t* rows, int64_t n_rows, const int64_t* cols,
+                   int64_t n_cols, double* ref, double* absum);
+
 /* ---- input preparation (NVFP4 producer used to build test inputs) ----- */
 float orc_nvfp4_global_scale(const uint16_t* x_bf16, int64_t n);   /* amax/(6*448) */
 void orc_nvfp4_quantize(const uint16_t* x_bf16, float g, int64_t row0, int64_t row1,

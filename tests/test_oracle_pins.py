@@ -503,6 +503,167 @@ def test_gemm_grouped_pin_catches_planted_mistakes(orc):
     assert not _grouped_matches(planted("right", 1), case)
 
 
+# ------------------------------------------------------ DualScale weights
+
+# "W4A4 MXFP4 Quantization", "mxfp4_dualscale -- DualScale Offline Mode",
+# "Checkpoint tensor layout": FP4 values, fine E8M0 per 32 K-elements, coarse
+# float32 per 512 K-elements; value = E2M1 x 2^(fine - 127) x coarse.
+
+
+def _dual_dequant_indep(packed, fine, coarse):
+    """E2M1 fixture x 2^(fine - 127) x coarse, each factor expanded by numpy."""
+    table = _e2m1_table()
+    vals = np.vectorize(lambda c: table[int(c)])(_unpack(packed))
+    return (vals * np.repeat(2.0 ** (fine.astype(np.float64) - 127), 32, axis=1)
+            * np.repeat(coarse.astype(np.float64), 512, axis=1))
+
+
+def _dual_operands(rng, rows, K):
+    packed = rng.integers(0, 256, (rows, K // 2), dtype=np.uint8)
+    fine = rng.integers(112, 140, (rows, K // 32), dtype=np.uint8)
+    coarse = np.exp(rng.normal(-3.0, 1.5, (rows, K // 512))).astype(np.float32)
+    return packed, fine, coarse
+
+
+def test_dual_dequant_matches_numpy(orc):
+    rng = np.random.default_rng(81)
+    packed, fine, coarse = _dual_operands(rng, 5, 1536)
+    assert np.array_equal(orc.dual_dequant(packed, fine, coarse), _dual_dequant_indep(packed, fine, coarse))
+
+
+def test_dual_quantize_properties(orc):
+    """The online dual-level quantizer (stated reading) against what it must
+    satisfy: the group's largest element lands on E2M1's largest value with a
+    unit fine scale, 6 x coarse recovers the group's largest magnitude, every
+    code is the nearest E2M1 value of w / coarse / 2^e (ties to the even code,
+    saturating), the fine exponent obeys the OCP closed form, NaN / Inf poison
+    only their own block, an all-zero group gets coarse 1, and the
+    reconstruction error stays within half a grid step."""
+    import synth
+
+    N, K = 10, 1536
+    W = synth.bf16_normal(83, synth.S_WEIGHT, (N, K), 0.02, 0.01, 8.0)
+    W[0, 512:1024] = 0                                  # an all-zero group
+    W[1, 40] = 0x7FC0                                   # NaN
+    W[2, 700] = 0xFF80                                  # -Inf
+    packed, fine, coarse = orc.dual_quantize(W)
+    w = torch.from_numpy(W.view(np.int16)).view(torch.bfloat16).float().numpy()
+    codes = _unpack(packed)
+    table = _e2m1_table()
+    grid = np.array([table[c] for c in range(16)])
+    for r in range(N):
+        for g in range(K // 512):
+            seg = w[r, 512 * g:512 * (g + 1)]
+            fin = np.isfinite(seg)
+            amax = np.abs(seg[fin]).max()
+            c = coarse[r, g]
+            if amax == 0:
+                assert c == 1.0
+            else:
+                assert abs(6.0 * float(c) - amax) <= 2.0 ** -22 * amax
+                kmax = 512 * g + int(np.argmax(np.where(fin, np.abs(seg), -1)))
+                b0 = kmax // 32 * 32
+                if np.all(np.isfinite(w[r, b0:b0 + 32])):       # (a NaN / Inf block is all zero instead)
+                    assert fine[r, kmax // 32] == 127 and codes[r, kmax] & 7 == 7
+            for b in range(16):
+                k0 = 512 * g + 32 * b
+                blk = w[r, k0:k0 + 32]
+                if not np.all(np.isfinite(blk)):
+                    assert fine[r, k0 // 32] == 0xFF and not codes[r, k0:k0 + 32].any()
+                    continue
+                y = (blk / c).astype(np.float32)                   # float32 division, as the reading states
+                e = int(fine[r, k0 // 32]) - 127
+                ay = float(np.abs(y).max())
+                if ay == 0:
+                    assert e == -127
+                else:
+                    assert 4.0 <= ay / 2.0 ** e < 8.0
+                q = y.astype(np.float64) / 2.0 ** e
+                for i in range(32):
+                    d = np.abs(grid - q[i])
+                    d[np.abs(grid) < 0] = np.inf
+                    best = np.min(np.abs(np.abs(grid[:8]) - min(abs(q[i]), 6.0)))
+                    got = codes[r, k0 + i]
+                    assert abs(abs(grid[got]) - min(abs(q[i]), 6.0)) == best
+                    if best > 0 and np.sum(np.abs(np.abs(grid[:8]) - min(abs(q[i]), 6.0)) == best) > 1:
+                        assert got & 1 == 0                         # a tie goes to the even code
+                    if q[i] != 0:
+                        assert (got >> 3) == (q[i] < 0)
+    # reconstruction error: half a grid step of the scaled grid, or the saturation at 6
+    dq = orc.dual_dequant(packed, fine, coarse)
+    ok = np.isfinite(w)
+    for r in range(N):
+        for k in range(K):
+            if not ok[r, k] or fine[r, k // 32] == 0xFF:
+                continue
+            s = 2.0 ** (int(fine[r, k // 32]) - 127) * float(coarse[r, k // 512])
+            qa = abs(w[r, k]) / s
+            half = (0.25 if qa <= 2 else 0.5 if qa <= 4 else 1.0) * s
+            assert abs(dq[r, k] - w[r, k]) <= max(half, (qa - 6.0) * s) + 2.0 ** -20 * abs(w[r, k])
+
+
+def test_gemm_dual_matches_numpy(orc):
+    rng = np.random.default_rng(85)
+    M, N, K = 6, 9, 2048
+    a = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    sa = rng.integers(112, 140, (M, K // 32), dtype=np.uint8)
+    b, fine, coarse = _dual_operands(rng, N, K)
+    bias = torch.randn(N).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    A = _dequant_indep(a, sa)
+    B = _dual_dequant_indep(b, fine, coarse)
+    bias_f = torch.from_numpy(bias.view(np.int16)).view(torch.bfloat16).double().numpy()
+    ref, absum = orc.gemm_dual(a, sa, b, fine, coarse, bias)
+    prod_abs = np.abs(A) @ np.abs(B).T
+    assert np.allclose(ref, A @ B.T + bias_f, rtol=1e-12, atol=1e-12 * prod_abs + 1e-300)
+    assert np.allclose(absum, prod_abs, rtol=1e-12)
+    rows, cols = np.array([4, 1]), np.array([8, 0, 3])
+    r2, _ = orc.gemm_dual(a, sa, b, fine, coarse, bias, rows=rows, cols=cols)
+    assert np.array_equal(r2, ref[np.ix_(rows, cols)])
+    # two plausible slips, each in a copy of the definition, must fail this pin:
+    # the coarse scale indexed per 1024 elements, the fine scale per 64
+    table = _e2m1_table()
+    vals = np.vectorize(lambda c: table[int(c)])(_unpack(b))
+    wrong_coarse = vals * np.repeat(2.0 ** (fine.astype(np.float64) - 127), 32, axis=1) * \
+        np.repeat(coarse.astype(np.float64), 1024, axis=1)[:, :K]
+    wrong_fine = vals * np.repeat(2.0 ** (fine.astype(np.float64) - 127), 64, axis=1)[:, :K] * \
+        np.repeat(coarse.astype(np.float64), 512, axis=1)
+    for Bw in (wrong_coarse, wrong_fine):
+        assert not np.allclose(A @ Bw.T + bias_f, ref, rtol=1e-6, atol=1e-9)
+
+
+def test_gemm_dual_unit_coarse_equals_mx_gemm(orc):
+    """With every coarse scale 1 a DualScale weight is an MXFP4 weight: the
+    two GEMMs agree bit for bit."""
+    rng = np.random.default_rng(87)
+    M, N, K = 5, 7, 1536
+    a = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    sa = rng.integers(112, 140, (M, K // 32), dtype=np.uint8)
+    b, fine, _ = _dual_operands(rng, N, K)
+    one = np.ones((N, K // 512), np.float32)
+    r1, s1 = orc.gemm_dual(a, sa, b, fine, one)
+    r2, s2 = orc.gemm(a, sa, b, fine)
+    assert np.array_equal(r1, r2) and np.array_equal(s1, s2)
+
+
+def test_gemm_dual_one_hot_selects_scaled_columns(orc):
+    """B rows one-hot with code 1.0 under fine scale 2^0 and a power-of-two
+    coarse scale per group: out[:, n] = A[:, sel[n]] x coarse[n, sel[n] / 512]
+    exactly."""
+    rng = np.random.default_rng(89)
+    M, N, K = 6, 10, 1024
+    a = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    sa = rng.integers(120, 135, (M, K // 32), dtype=np.uint8)
+    sel = rng.integers(0, K, N)
+    codes = np.zeros((N, K), np.uint8)
+    codes[np.arange(N), sel] = 0x2
+    b = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    fine = np.full((N, K // 32), 127, np.uint8)
+    coarse = (2.0 ** rng.integers(-6, 6, (N, K // 512))).astype(np.float32)
+    ref, _ = orc.gemm_dual(a, sa, b, fine, coarse)
+    A = _dequant_indep(a, sa)
+    assert np.array_equal(ref, A[:, sel] * coarse[np.arange(N), sel // 512].astype(np.float64))
+
+
 # ------------------------------------------------------ smooth pre-scale
 
 
