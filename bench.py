@@ -608,7 +608,7 @@ def run_ours(args):
 
     e2e = _e2e(b, torch, L, min(args.steps, 50))
     fused = fused_quant_comparison(b, L, torch, args.breakdown_reps) if args.workload == "decode" else None
-    nvfp4 = w4a8 = None
+    nvfp4 = w4a8 = dual = None
     if not args.no_nvfp4 and all(a.offsets is None for a in b.acts):
         nvfp4 = side_path_comparison(b, L, torch, args.breakdown_reps, breakdown, NvAct, "nv",
                                      "NVFP4 act-quant + NVFP4 x NVFP4 GEMM (alpha = g_x g_w, no requant) "
@@ -616,6 +616,9 @@ def run_ours(args):
         w4a8 = side_path_comparison(b, L, torch, args.breakdown_reps, breakdown, A8Act, "a8",
                                     "W4A8 fallback: MXFP8 act-quant + MXFP8 x MXFP4 GEMM (the same requantized "
                                     "weight) vs the MXFP4 path")
+        dual = side_path_comparison(b, L, torch, args.breakdown_reps, breakdown, DualAct, "dual",
+                                    "DualScale: the bf16 weight quantized with fine E8M0 per 32 and coarse "
+                                    "float32 per 512 elements, MXFP4 act-quant + DualScale GEMM, vs the MXFP4 path")
 
     gemm_q = groups.get("gemm", {"flops": 0.0, "s": 1.0})
     gemm_tflops = gemm_q["flops"] / gemm_q["s"] / 1e12
@@ -635,7 +638,7 @@ def run_ours(args):
         "requant_error": req_err,
         "fp4_probe_peak": fp4_probe,
         "breakdown": breakdown, "shares": shares, "roofline": roofline, "e2e": e2e, "nvfp4_path": nvfp4,
-        "w4a8_path": w4a8, "fused_act_quant": fused,
+        "w4a8_path": w4a8, "dualscale_path": dual, "fused_act_quant": fused,
         "gpu_launches": b.launches_per_step * steps, "clocks": clk, "wall_s_timed_region": round(t_wall, 3),
     }
     if rank == 0 and not args.no_cpu_baseline and world == 1:
@@ -831,6 +834,40 @@ class A8Act:
         a, w = self.act, self.w
         self.L.fp4_gemm_w4a8(self.codes, self.scale, w.b_packed, w.b_scale, w.bias, self.out, a.M, w.N, a.K,
                              self.ws, stream=s)
+
+
+class DualAct:
+    """The DualScale path of "W4A4 MXFP4 Quantization" (mxfp4_dualscale) on
+    the same bf16 activations and weight: the weight quantized once by the
+    online dual-level quantizer (fine E8M0 per 32, coarse float32 per 512;
+    setup, not timed), then per batch the MXFP4 act-quant and the GEMM with
+    DualScale weights."""
+
+    def __init__(self, L, torch, act):
+        dev = torch.device("cuda")
+        w = act.w
+        self.L, self.act, self.w = L, act, w
+        M, K = act.M, act.K
+        if not hasattr(w, "dual_codes"):                   # setup: quantize the bf16 weight once
+            wb = torch.from_numpy(w.bf16_host.view(np.int16)).to(dev).view(torch.bfloat16)
+            w.dual_codes = torch.empty((w.N, K // 2), dtype=torch.uint8, device=dev)
+            w.dual_fine = torch.empty(L.fp4_sf_bytes(w.N, K), dtype=torch.uint8, device=dev)
+            w.dual_coarse = torch.empty((w.N, K // 512), dtype=torch.float32, device=dev)
+            L.fp4_quant_dualscale(wb, w.dual_codes, w.dual_fine, w.dual_coarse, w.N, K)
+        self.packed = torch.empty((M, K // 2), dtype=torch.uint8, device=dev)
+        self.scale = torch.empty(L.fp4_sf_bytes(M, K), dtype=torch.uint8, device=dev)
+        self.out = torch.empty((M, w.N), dtype=torch.bfloat16, device=dev)
+        self.torch = torch
+
+    def quant(self, s):
+        a = self.act
+        self.L.fp4_quant_act_mxfp4(a.x, self.packed, self.scale, a.M, a.K, stream=s)
+
+    def gemm(self, s):
+        a, w = self.act, self.w
+        ws = gemm_workspace(self.L, self.torch, a.M, w.N, a.K)
+        self.L.fp4_gemm_mxfp4_dualscale(self.packed, self.scale, w.dual_codes, w.dual_fine, w.dual_coarse, w.bias,
+                                        self.out, a.M, w.N, a.K, ws, stream=s)
 
 
 def fused_quant_comparison(b, L, torch, reps):

@@ -423,6 +423,44 @@ FP4LIN_API fp4_status fp4_gemm_w4a8(const uint8_t* a_e4m3, const uint8_t* sa, co
  * current device (0: not split, or no usable device).                      */
 FP4LIN_API size_t fp4_gemm_w4a8_workspace_size(int64_t M, int64_t N, int64_t K);
 
+/* ----------------------------------------------------------- DualScale */
+
+/* DualScale weights ([OMNI] "mxfp4_dualscale", Offline Mode, checkpoint
+ * tensor layout): FP4 codes [N, K/2], a fine E8M0 scale per 32 K-elements
+ * and a coarse float32 scale per 512 K-elements (weight_dual_scale
+ * [N, K/512]); an element's value is E2M1 x 2^(fine - 127) x coarse.
+ * K must be a positive multiple of 512 (the page: DualScale needs complete
+ * 512-channel groups); otherwise FP4_ERR_SHAPE.                           */
+
+/* Online dual-level quantization of a bf16 weight ([OMNI] "DualScale Online
+ * Mode"; the page only names the operation, so this is the library's
+ * reading): per row and 512-element group, coarse = float32(amax / 6) over
+ * the group's finite magnitudes (1 if none is above zero), then the OCP MX
+ * rule on float32(w / coarse) per 32 elements (fine exponent, nearest E2M1
+ * code with ties to even, saturating at 6; a NaN/Inf element makes its
+ * 32-element block 0xFF with zero codes).
+ *   w_bf16      [N, K] bf16 (16-byte aligned)
+ *   out_packed  [N, K/2] codes (8-byte aligned)
+ *   out_fine    E8M0: FP4_SF_SWIZZLED (fp4_sf_bytes(N, K, 0), 4-byte
+ *               aligned, pad rows written as 0) or FP4_SF_ROWMAJOR [N, K/32]
+ *   out_coarse  [N, K/512] float32 (4-byte aligned)                         */
+FP4LIN_API fp4_status fp4_quant_dualscale(const void* w_bf16, uint8_t* out_packed, uint8_t* out_fine,
+                               float* out_coarse, int64_t N, int64_t K, int32_t sf_layout, void* stream);
+
+/* W4A4 GEMM with DualScale weights: MXFP4 activations (a, SWIZZLED sa) times
+ * the DualScale weight (b codes, SWIZZLED fine scales sb, coarse [N, K/512]):
+ *   out[m, n] = bf16_rne( sum_j coarse[n, j] * P_j[m, n] + bias[n] ),
+ *   P_j = the fp32 block-scaled dot product over the j-th 512 elements of K,
+ * each group's partial sum taken from the tensor cores and scaled by its
+ * coarse scale before it is added (fp32).  workspace / workspace_bytes:
+ * split-K scratch as for fp4_gemm_mxfp4_ws (size fp4_gemm_workspace_size),
+ * or NULL.  Shape and alignment rules of fp4_gemm_mxfp4, plus K % 512 == 0
+ * and a 4-byte aligned coarse array.                                      */
+FP4LIN_API fp4_status fp4_gemm_mxfp4_dualscale(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
+                                    const uint8_t* sb, const float* coarse, const void* bias_bf16,
+                                    void* out_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------ linear layer */
 
 /* Activation formats of fp4_linear. */

@@ -458,6 +458,66 @@ size_t fp4_gemm_w4a8_workspace_size(int64_t M, int64_t N, int64_t K)
     return fp4lin::gemm_workspace_bytes(M, N, K, fp4lin::kGemmW4A8);
 }
 
+fp4_status fp4_quant_dualscale(const void* w_bf16, uint8_t* out_packed, uint8_t* out_fine, float* out_coarse,
+                               int64_t N, int64_t K, int32_t sf_layout, void* stream)
+{
+    if (N <= 0 || K <= 0 || K % 512 != 0 || N >= kMaxDim || K >= kMaxDim)
+        return FP4_ERR_SHAPE;
+    if (sf_layout != FP4_SF_SWIZZLED && sf_layout != FP4_SF_ROWMAJOR)
+        return FP4_ERR_INVALID_ARG;
+    if (!w_bf16 || !out_packed || !out_fine || !out_coarse)
+        return FP4_ERR_INVALID_ARG;
+    if (!aligned16(w_bf16) || (reinterpret_cast<uintptr_t>(out_packed) & 7u) ||
+        (reinterpret_cast<uintptr_t>(out_coarse) & 3u) ||
+        (sf_layout == FP4_SF_SWIZZLED && (reinterpret_cast<uintptr_t>(out_fine) & 3u)))
+        return FP4_ERR_ALIGNMENT;
+    fp4_status st;
+    if ((st = current_device(nullptr)) != FP4_OK)
+        return st;
+    return from_cuda(fp4lin::launch_dual_quant(w_bf16, out_packed, out_fine, out_coarse, N, K,
+                                               sf_layout == FP4_SF_SWIZZLED ? 1 : 0,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+fp4_status fp4_gemm_mxfp4_dualscale(const uint8_t* a, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
+                                    const float* coarse, const void* bias_bf16, void* out_bf16, int64_t M, int64_t N,
+                                    int64_t K, void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (K <= 0 || K % 512 != 0)
+        return FP4_ERR_SHAPE;
+    if (M > 0 && !coarse)
+        return FP4_ERR_INVALID_ARG;
+    if (coarse && (reinterpret_cast<uintptr_t>(coarse) & 3u))
+        return FP4_ERR_ALIGNMENT;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FP4_ERR_ALIGNMENT;
+    fp4_status st = static_cast<fp4_status>(fp4lin::gemm_check_args(a, sa, b, sb, bias_bf16, out_bf16, M, N, K, 1));
+    if (st != FP4_OK || M == 0)
+        return st;
+    unsigned int* status = nullptr;
+    if ((st = current_device(&status)) != FP4_OK)
+        return st;
+    fp4lin::GemmArgs args;
+    args.a = a;
+    args.sa = sa;
+    args.b = b;
+    args.sb = sb;
+    args.bias = bias_bf16;
+    args.out = out_bf16;
+    args.row_offsets = nullptr;
+    args.E = 1;
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.status = status;
+    args.workspace = workspace;
+    args.workspace_bytes = workspace ? workspace_bytes : 0;
+    args.fmt = fp4lin::kGemmDual;
+    args.coarse = coarse;
+    args.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    return from_cuda(fp4lin::launch_gemm(args, static_cast<cudaStream_t>(stream)));
+}
+
 fp4_status fp4_gemm_w4a8(const uint8_t* a_e4m3, const uint8_t* sa, const uint8_t* b, const uint8_t* sb,
                          const void* bias_bf16, void* out_bf16, int64_t M, int64_t N, int64_t K, void* workspace,
                          size_t workspace_bytes, void* stream)

@@ -80,7 +80,7 @@ constexpr int BM = 128;
 constexpr int kSlabBytes = 128;  // packed bytes of K per row per slab (256 elements)
 constexpr int kEpiWarps = 8;
 
-enum : int { kFmtMx = kGemmMx, kFmtNv = kGemmNv, kFmtA8 = kGemmW4A8 };
+enum : int { kFmtMx = kGemmMx, kFmtNv = kGemmNv, kFmtA8 = kGemmW4A8, kFmtDual = kGemmDual };
 
 struct GemmParams {
     int64_t units;              // split-K: total K-stage units (0: one CTA per whole tile)
@@ -106,6 +106,7 @@ struct GemmParams {
     const uint16_t* x;          // fused activation quantization: bf16 tokens [rows_b, K] (swapped mode)
     const uint16_t* xmul;       // its smooth pre-scale (bf16 [K]) or null
     int x_uos;                  // its block rule: UOS (else OCP)
+    const float* coarse;        // DualScale: coarse weight scales [weight rows][K / 512]
     unsigned long long wait_ns; // limit of every bounded wait
     unsigned int* status;
 };
@@ -114,6 +115,10 @@ template <int BN, int STAGES, int KC, int CPW, bool kSwap, int kFmt>
 struct Cfg {
     static constexpr bool kNv = kFmt == kFmtNv;
     static constexpr bool kA8 = kFmt == kFmtA8;
+    // DualScale: a stage is one 512-element coarse group of K, and its MMAs
+    // write one of two TMEM partial buffers in turn
+    static constexpr bool kDual = kFmt == kFmtDual;
+    static_assert(!kDual || KC == 2, "DualScale: one 512-element group per stage");
     // Four scale warps beside a 256-wide epilogue do not fit the register
     // file at 14 warps: 16 warps then, warps 6-7 idle, and the two non-
     // epilogue warpgroups hand registers to the epilogue ones (setmaxnreg).
@@ -150,14 +155,14 @@ struct Cfg {
     static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
     static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    static constexpr int NUM_BARS = 3 * STAGES + 2;
+    static constexpr int NUM_BARS = 3 * STAGES + 2 + (kDual ? 4 : 0);
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_PREFIX = OFF_TMEM_SLOT + 16;
     static constexpr int SMEM_FIXED = OFF_PREFIX + 1024;  // + 1 KB alignment slack
     static constexpr int SF_COLS_A = 4 * ATOMS;
     static constexpr int SF_COLS_B_ATOM = 4 * SFB_TILES;
     static constexpr int SF_COLS = SF_COLS_A + ATOMS * SF_COLS_B_ATOM;
-    static constexpr int TMEM_USED = BN + STAGES * SF_COLS;  // one scale buffer per smem stage
+    static constexpr int TMEM_USED = (kDual ? 2 : 1) * BN + STAGES * SF_COLS;  // one scale buffer per smem stage
     static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                      : TMEM_USED <= 256 ? 256 : 512;
     static_assert(TMEM_USED <= 512, "TMEM overflow");
@@ -341,6 +346,8 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
     uint64_t* sf_full = empty + STAGES;
     uint64_t* accum_full = sf_full + STAGES;
     uint64_t* accum_empty = accum_full + 1;
+    uint64_t* part_full = accum_empty + 1;  // DualScale: partial buffer b holds a finished group
+    uint64_t* part_empty = part_full + 2;   // DualScale: the epilogue has read partial buffer b
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM_SLOT);
     int32_t* tiles_before = reinterpret_cast<int32_t*>(smem + C::OFF_PREFIX);
 
@@ -399,6 +406,12 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
         }
         mbar_init(accum_full, 1);
         mbar_init(accum_empty, kEpiWarps);
+        if constexpr (C::kDual) {
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&part_full[b], 1);
+                mbar_init(&part_empty[b], kEpiWarps);
+            }
+        }
         fence_mbar_init();
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
@@ -503,7 +516,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                                            : kA8 ? idesc_mxf8f6f4(BM, BN, kSwap ? kTypeE2M1 : kTypeE4M3,
                                                                   kSwap ? kTypeE4M3 : kTypeE2M1)
                                                  : idesc_mxf4(BM, BN);
-                uint32_t it = 0, tcount = 0;
+                uint32_t it = 0, tcount = 0, pc = 0;
                 bool ok = true;
                 WorkIter wi = work_begin(p, total_tiles);
                 Work w;
@@ -512,7 +525,9 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                     if (!T.valid)
                         continue;
                     // the epilogue must have drained the accumulator of the previous tile
-                    if (!mbar_wait_bounded(accum_empty, (tcount & 1u) ^ 1u, p.status, kStatusTimeout, p.wait_ns)) {
+                    // (DualScale: each group's partial buffer is handed over on its own)
+                    if (!C::kDual &&
+                        !mbar_wait_bounded(accum_empty, (tcount & 1u) ^ 1u, p.status, kStatusTimeout, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -527,7 +542,19 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                         }
                         tc_fence_after_sync();
                         const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
-                        const uint32_t sfa_t = tmem_base + BN + s * C::SF_COLS;
+                        uint32_t d_tmem = tmem_base;
+                        if constexpr (C::kDual) {
+                            // this group's partial buffer must have been read by the epilogue
+                            const uint32_t pb = pc & 1u;
+                            if (!mbar_wait_bounded(&part_empty[pb], ((pc >> 1) & 1u) ^ 1u, p.status, kStatusTimeout,
+                                                   p.wait_ns)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after_sync();
+                            d_tmem = tmem_base + pb * BN;
+                        }
+                        const uint32_t sfa_t = tmem_base + (C::kDual ? 2 : 1) * BN + s * C::SF_COLS;
                         const uint32_t sfb_t = sfa_t + C::SF_COLS_A;
                         const uint32_t a_s = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
                         const uint32_t b_s = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
@@ -538,7 +565,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                             const int slab = k >> 2;
                             const uint64_t ad = smem_desc(a_s + slab * (BM * kSlabBytes) + 32 * (k & 3), 16, 1024, 2);
                             const uint64_t bd = smem_desc(b_s + slab * (BN * kSlabBytes) + 32 * (k & 3), 16, 1024, 2);
-                            const uint32_t acc = (kb != w.kb0 || k != 0) ? 1u : 0u;
+                            const uint32_t acc = C::kDual ? (k != 0 ? 1u : 0u) : ((kb != w.kb0 || k != 0) ? 1u : 0u);
                             if constexpr (kNv) {
                                 tc_mma_nvf4(tmem_base, ad, bd, idesc, sfa_t + 4 * k, sfb_t + k * C::SF_COLS_B_ATOM, acc);
                             } else if constexpr (kA8) {
@@ -548,13 +575,18 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                             } else {
                                 const int g = k >> 1;
                                 const uint32_t sf_id = static_cast<uint32_t>(k & 1) * 2u;
-                                tc_mma_mxf4(tmem_base, ad, bd, idesc_with_sf_id(idesc, sf_id), sfa_t + 4 * g,
+                                tc_mma_mxf4(d_tmem, ad, bd, idesc_with_sf_id(idesc, sf_id), sfa_t + 4 * g,
                                             sfb_t + g * C::SF_COLS_B_ATOM, acc);
                             }
                         }
                         tc_commit(&empty[s]);
+                        if constexpr (C::kDual) {
+                            tc_commit(&part_full[pc & 1u]);
+                            ++pc;
+                        }
                     }
-                    tc_commit(accum_full);  // also on the abort path: the epilogue never waits on missing MMAs
+                    if constexpr (!C::kDual)
+                        tc_commit(accum_full);  // also on the abort path: the epilogue never waits on missing MMAs
                     ++tcount;
                 }
             }
@@ -582,7 +614,7 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                         }
                         tc_fence_after_sync();
                         const int atoms = min(C::GROUPS, p.kb4 - C::GROUPS * kb) * C::APG;
-                        const uint32_t sfa_t = tmem_base + BN + s * C::SF_COLS;
+                        const uint32_t sfa_t = tmem_base + (C::kDual ? 2 : 1) * BN + s * C::SF_COLS;
                         const uint32_t sfb_t = sfa_t + C::SF_COLS_A;
                         const uint32_t sfa_s = smem_u32(smem + C::OFF_SFA + s * C::SFA_BYTES);
                         const uint32_t sfb_s = smem_u32(smem + C::OFF_SFB + s * C::SFB_BYTES);
@@ -719,16 +751,62 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                 if (p.bias && r < T.rows_valid && w.mode != kPartial)
                     bias_pre = __bfloat162float(p.bias[static_cast<int64_t>(T.expert) * p.ldo + T.a_row0 + r]);
             }
-            const bool ok = mbar_wait_bounded(accum_full, tcount & 1u, p.status, kStatusTimeout, p.wait_ns);
-            tc_fence_after_sync();
             uint32_t v[CW];
-            tmem_load_cols<CW>(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * CW, v);
-            tmem_ld_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(accum_empty);  // the accumulator is in registers: let the next tile start
-            ++tcount;
+            bool ok = true;
+            if constexpr (C::kDual) {
+                // DualScale: out = sum over 512-element groups of coarse x the group's
+                // partial sum; the partial of group j is read from its TMEM buffer,
+                // released, scaled by the group's coarse scale (per weight row: the
+                // TMEM lane when swapped, else the output column) and added here
+                float accd[CW];
+#pragma unroll
+                for (int j = 0; j < CW; ++j)
+                    accd[j] = 0.0f;
+                const int nch = p.K / 512;
+                const int r = quad * 32 + lane;
+                // swapped: this lane's weight row; normal: lane c holds columns c and c + 32 of the warp's half
+                const int64_t crow = kSwap ? T.a_row0 + r : static_cast<int64_t>(T.n0) + half * CW + lane;
+                const bool crow_ok = kSwap ? r < T.rows_valid : crow < p.ldo;
+                const bool crow2_ok = !kSwap && CW > 32 && crow + 32 < p.ldo;
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++tcount) {
+                    const float c1 = crow_ok ? __ldg(p.coarse + crow * nch + kb) : 0.0f;
+                    const float c2 = crow2_ok ? __ldg(p.coarse + (crow + 32) * nch + kb) : 0.0f;
+                    const uint32_t pb = tcount & 1u;
+                    ok = ok && mbar_wait_bounded(&part_full[pb], (tcount >> 1) & 1u, p.status, kStatusTimeout, p.wait_ns);
+                    tc_fence_after_sync();
+                    // the partial in pieces of at most 32 columns (fewer live registers)
+                    constexpr int kPc = CW < 32 ? CW : 32;
+#pragma unroll
+                    for (int c0 = 0; c0 < CW; c0 += kPc) {
+                        uint32_t pv[kPc];
+                        tmem_load_cols<kPc>(tmem_base + pb * BN + (static_cast<uint32_t>(quad * 32) << 16) + half * CW + c0,
+                                            pv);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < kPc; ++j) {
+                            const float cj = kSwap ? c1 : __shfl_sync(0xFFFFFFFFu, c0 + j < 32 ? c1 : c2, (c0 + j) & 31);
+                            accd[c0 + j] = __fmaf_rn(__uint_as_float(pv[j]), cj, accd[c0 + j]);
+                        }
+                    }
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&part_empty[pb]);
+                }
+#pragma unroll
+                for (int j = 0; j < CW; ++j)
+                    v[j] = __float_as_uint(accd[j]);
+            } else {
+                ok = mbar_wait_bounded(accum_full, tcount & 1u, p.status, kStatusTimeout, p.wait_ns);
+                tc_fence_after_sync();
+                tmem_load_cols<CW>(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + half * CW, v);
+                tmem_ld_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(accum_empty);  // the accumulator is in registers: let the next tile start
+                ++tcount;
+            }
             if (!ok)
                 break;
             const int r = quad * 32 + lane;
@@ -1059,6 +1137,7 @@ cudaError_t launch_kernel(const GemmArgs& a, cudaStream_t stream)
     p.x = static_cast<const uint16_t*>(a.x_bf16);
     p.xmul = static_cast<const uint16_t*>(a.x_mul);
     p.x_uos = a.x_uos;
+    p.coarse = a.coarse;
     p.wait_ns = a.wait_ns;
     p.status = a.status;
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -1184,10 +1263,26 @@ cudaError_t launch_gemm_w4a8(const GemmArgs& a, cudaStream_t stream)
     return launch_kernel<128, 6, 1, 4, false, false, kFmtA8>(a, stream);
 }
 
+// DualScale weights (K % 512 == 0): the MXFP4 tile shapes whose TMEM holds
+// two partial buffers beside the scale columns -- 16 / 32 / 64 tokens for
+// M <= 64 (weights on the MMA-M side), else 128 x 128 tiles.
+cudaError_t launch_gemm_dual(const GemmArgs& a, cudaStream_t stream)
+{
+    if (a.M <= 64) {
+        if (a.M <= 16)
+            return launch_kernel<16, 5, 2, 4, true, false, kFmtDual>(a, stream);
+        return a.M <= 32 ? launch_kernel<32, 4, 2, 4, true, false, kFmtDual>(a, stream)
+                         : launch_kernel<64, 4, 2, 4, true, false, kFmtDual>(a, stream);
+    }
+    return launch_kernel<128, 3, 2, 4, false, false, kFmtDual>(a, stream);
+}
+
 cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream)
 {
     if (a.fmt == kGemmNv)
         return launch_gemm_nvfp4(a, stream);
+    if (a.fmt == kGemmDual)
+        return launch_gemm_dual(a, stream);
     if (a.fmt == kGemmW4A8)
         return launch_gemm_w4a8(a, stream);
     // Stages of two slabs need the 3-D operand view, which needs

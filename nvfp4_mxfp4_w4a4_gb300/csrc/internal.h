@@ -109,9 +109,14 @@ cudaError_t launch_quant_nvfp4(const void* x, float g, uint8_t* op, uint8_t* osf
 // Row-major [rows][kb] scale bytes -> swizzled layout (any block size).
 cudaError_t launch_sf_swizzle(const uint8_t* in, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t stream);
 
+// bf16 [N, K] -> DualScale (K % 512 == 0): codes [N, K/2], fine E8M0 per 32
+// (swizzled or row-major [N, K/32]), coarse float32 [N, K/512].
+cudaError_t launch_dual_quant(const void* w, uint8_t* op, uint8_t* ofine, float* ocoarse, int64_t N, int64_t K,
+                              int swizzled, cudaStream_t stream);
+
 // Operand formats of the GEMM: both MXFP4; both NVFP4 (E4M3 scales per 16
 // elements, alpha); MXFP8 activations (a: [M, K] E4M3 bytes) x MXFP4 weights.
-enum GemmFormat : int { kGemmMx = 0, kGemmNv = 1, kGemmW4A8 = 2 };
+enum GemmFormat : int { kGemmMx = 0, kGemmNv = 1, kGemmW4A8 = 2, kGemmDual = 3 };
 
 // Dense (offsets == nullptr) or grouped GEMM.
 struct GemmArgs {
@@ -131,6 +136,7 @@ struct GemmArgs {
     size_t workspace_bytes;
     int fmt = 0;                 // GemmFormat
     float alpha = 1.0f;          // NVFP4: factor on the accumulator before the bias
+    const float* coarse = nullptr;  // DualScale: float32 coarse weight scales [N, K/512]
     bool early_weights = false;  // the weights are not written by the preceding kernel in the stream
     unsigned long long wait_ns = kWaitLimitNs;  // limit of every bounded device wait of the launch
     bool withhold_split_signal = false;  // test hook: one split-K partial never signals its finisher

@@ -939,6 +939,100 @@ cudaError_t launch_quant_nvfp4(const void* x, float g, uint8_t* op, uint8_t* osf
                       static_cast<const uint16_t*>(x), g, op, osf, halves, M, K, kb, kbp, swizzled);
 }
 
+// ------------------------------------------------ DualScale quantization
+// Online dual-level quantization of a bf16 weight ("W4A4 MXFP4
+// Quantization", mxfp4_dualscale Online Mode; reading): per row and
+// 512-element group, coarse = amax / 6 over the group's finite magnitudes
+// (1 when there is none above zero), then the OCP MX block rule on
+// y = w / coarse per 32 elements.  Both divisions are IEEE float32.  One warp
+// per (row, group); lane i holds elements 16i .. 16i + 15, a lane pair one
+// 32-element block.  Rows past N (the 128-row padding of a swizzled scale
+// array) get zero fine bytes.
+__global__ void __launch_bounds__(kThreads) dual_quant_kernel(const uint16_t* __restrict__ w, uint8_t* __restrict__ op,
+                                                              uint8_t* __restrict__ ofine, float* __restrict__ ocoarse,
+                                                              int64_t N, int64_t K, int64_t rows, int swizzled)
+{
+    grid_dependency_wait();
+    launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t item = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t groups = K / 512;
+    const int64_t row = item / groups;
+    if (row >= rows)
+        return;
+    const int64_t g = item - row * groups;
+    const int kb = static_cast<int>(K / 32);
+    const int64_t kb4 = kb >> 2;
+    const int blk = static_cast<int>(g) * 16 + (lane >> 1);  // this lane's 32-element block
+    uint32_t sf = 0u;
+    if (row < N) {
+        const uint16_t* src = w + row * K + g * 512 + lane * 16;
+        const uint4 a = ld_stream_u4(src), b = ld_stream_u4(src + 8);
+        const uint32_t x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        // largest finite magnitude of the group (bf16 patterns below Inf order as their values)
+        uint32_t m = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = x[i] & 0x7FFFu, hi = (x[i] >> 16) & 0x7FFFu;
+            m = max(m, lo < 0x7F80u ? lo : 0u);
+            m = max(m, hi < 0x7F80u ? hi : 0u);
+        }
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1)
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
+        const float amax = __uint_as_float(m << 16);
+        const float coarse = amax > 0.0f ? __fdiv_rn(amax, 6.0f) : 1.0f;
+        float y[16];
+        uint32_t ya = 0u;  // largest |y| bits of this lane's half block (NaN / Inf above every finite)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            y[2 * i] = __fdiv_rn(__uint_as_float(x[i] << 16), coarse);
+            y[2 * i + 1] = __fdiv_rn(__uint_as_float(x[i] & 0xFFFF0000u), coarse);
+            ya = max(ya, __float_as_uint(y[2 * i]) & 0x7FFFFFFFu);
+            ya = max(ya, __float_as_uint(y[2 * i + 1]) & 0x7FFFFFFFu);
+        }
+        ya = max(ya, __shfl_xor_sync(0xFFFFFFFFu, ya, 1));
+        uint2 codes = make_uint2(0u, 0u);
+        if (ya >= 0x7F800000u) {
+            sf = 0xFFu;  // NaN or Inf in the block: scale 0xFF, zero codes
+        } else {
+            const int e = mx_shared_exp(ya, 0);
+            sf = static_cast<uint32_t>(e + 127);
+            const float se = exp2_neg(e);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                y[i] = __fmul_rn(y[i], se);
+            codes.x = e2m1x8_pack(y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]);
+            codes.y = e2m1x8_pack(y[8], y[9], y[10], y[11], y[12], y[13], y[14], y[15]);
+        }
+        *reinterpret_cast<uint2*>(op + row * (K / 2) + g * 256 + lane * 8) = codes;
+        if (lane == 0)
+            ocoarse[row * groups + g] = coarse;
+    }
+    if (swizzled) {
+        // lane 8i writes the word of blocks 4i .. 4i + 3 (held by lanes 8i, 8i+2, 8i+4, 8i+6)
+        const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, sf, 2);
+        const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, sf, 4);
+        const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, sf, 6);
+        if ((lane & 7) == 0)
+            *reinterpret_cast<uint32_t*>(ofine + sf_swizzled_offset(row, blk, kb4)) = sf | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    } else if (row < N && (lane & 1) == 0) {
+        ofine[row * kb + blk] = static_cast<uint8_t>(sf);
+    }
+}
+
+cudaError_t launch_dual_quant(const void* w, uint8_t* op, uint8_t* ofine, float* ocoarse, int64_t N, int64_t K,
+                              int swizzled, cudaStream_t stream)
+{
+    const int64_t rows = swizzled ? ceil_div(N, 128) * 128 : N;
+    const int64_t warps = rows * (K / 512);
+    const int64_t blocks = ceil_div(warps * 32, kThreads);
+    if (blocks == 0)
+        return cudaSuccess;
+    return launch_pdl(dual_quant_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream,
+                      static_cast<const uint16_t*>(w), op, ofine, ocoarse, N, K, rows, swizzled);
+}
+
 cudaError_t launch_sf_swizzle(const uint8_t* in, uint8_t* out, int64_t rows, int64_t kb, cudaStream_t stream)
 {
     const int64_t kb4 = ceil_div(kb, 4);

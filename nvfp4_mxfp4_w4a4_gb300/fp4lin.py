@@ -38,7 +38,7 @@ SYMBOLS = (
     "fp4_quant_act_mxfp8", "fp4_gemm_w4a8", "fp4_gemm_w4a8_workspace_size", "fp4_gemm_mxfp4_ex",
     "fp4_smooth_prepare", "fp4_quant_act_mxfp4_smooth", "fp4_quant_act_mxfp8_smooth",
     "fp4_linear_workspace_size", "fp4_linear", "fp4_linear_grouped_workspace_size", "fp4_linear_grouped",
-    "fp4_debug_set_wait_fault",
+    "fp4_debug_set_wait_fault", "fp4_quant_dualscale", "fp4_gemm_mxfp4_dualscale",
 )
 
 
@@ -84,6 +84,9 @@ def load(path: str = LIB_PATH):
             "fp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "fp4_get_device_status": (ctypes.c_int, []),
             "fp4_debug_set_wait_fault": (ctypes.c_int, [ctypes.c_uint64, _i32]),
+            "fp4_quant_dualscale": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _i32, _p]),
+            "fp4_gemm_mxfp4_dualscale": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _i64, _i64, _i64, _p,
+                                                        ctypes.c_size_t, _p]),
             "fp4_requant_nvfp4_to_mxfp4": (ctypes.c_int, [_p, _p, ctypes.c_float, _p, _p, _i64, _i64, _p]),
             "fp4_requant_nvfp4_to_mxfp4_ex": (ctypes.c_int, [_p, _p, ctypes.c_float, _p, _p, _i64, _i64,
                                                              ctypes.POINTER(fp4_quant_opts), _p]),
@@ -370,3 +373,20 @@ def fp4_gemm_mxfp4_grouped(a, sa, b, sb, bias_bf16, out_bf16, row_offsets, E, to
     st = load().fp4_gemm_mxfp4_grouped(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(bias_bf16), _ptr(out_bf16),
                                        _ptr(row_offsets), E, total_M, N, K, _stream(stream))
     _check(st, "fp4_gemm_mxfp4_grouped")
+
+
+def fp4_quant_dualscale(w_bf16, out_packed, out_fine, out_coarse, N, K, sf_layout=FP4_SF_SWIZZLED, stream=None):
+    """bf16 weight -> DualScale codes, fine E8M0 scales and coarse float32 scales."""
+    st = load().fp4_quant_dualscale(_ptr(w_bf16), _ptr(out_packed), _ptr(out_fine), _ptr(out_coarse), N, K,
+                                    sf_layout, _stream(stream))
+    _check(st, "fp4_quant_dualscale")
+
+
+def fp4_gemm_mxfp4_dualscale(a, sa, b, sb, coarse, bias_bf16, out_bf16, M, N, K, workspace=None,
+                             workspace_bytes=None, stream=None):
+    """MXFP4 activations x DualScale weights (+ bias), bf16 out."""
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().fp4_gemm_mxfp4_dualscale(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), _ptr(coarse), _ptr(bias_bf16),
+                                         _ptr(out_bf16), M, N, K, _ptr(workspace), workspace_bytes, _stream(stream))
+    _check(st, "fp4_gemm_mxfp4_dualscale")

@@ -171,3 +171,18 @@ def test_debug_wait_fault_hook_checks_its_arguments(L):
     assert raw.fp4_debug_set_wait_fault(0, 2) == 1
     assert raw.fp4_debug_set_wait_fault(2_000_000, 1) == 0
     assert raw.fp4_debug_set_wait_fault(0, 0) == 0             # back to the defaults
+
+
+def test_dualscale_argument_checks(L):
+    raw = L.load()
+    assert raw.fp4_quant_dualscale(16, 16, 16, 16, 4, 1024 + 128, 0, None) == 2     # K % 512
+    assert raw.fp4_quant_dualscale(16, 16, 16, 16, 0, 512, 0, None) == 2            # N = 0
+    assert raw.fp4_quant_dualscale(16, 16, 16, 16, 4, 512, 7, None) == 1            # layout
+    assert raw.fp4_quant_dualscale(None, 16, 16, 16, 4, 512, 0, None) == 1
+    assert raw.fp4_quant_dualscale(24, 16, 16, 16, 4, 512, 0, None) == 3            # w 16 B
+    assert raw.fp4_quant_dualscale(16, 16, 16, 18, 4, 512, 0, None) == 3            # coarse 4 B
+    assert raw.fp4_gemm_mxfp4_dualscale(16, 16, 16, 16, 16, None, 16, 1, 8, 768, None, 0, None) == 2   # K % 512
+    assert raw.fp4_gemm_mxfp4_dualscale(16, 16, 16, 16, None, None, 16, 1, 8, 512, None, 0, None) == 1  # coarse
+    assert raw.fp4_gemm_mxfp4_dualscale(16, 16, 16, 16, 18, None, 16, 1, 8, 512, None, 0, None) == 3    # coarse 4 B
+    assert raw.fp4_gemm_mxfp4_dualscale(16, 16, 16, 16, 16, None, 16, 1, 8, 512, 16, 1 << 20, None) == 3  # ws
+    assert raw.fp4_gemm_mxfp4_dualscale(None, None, None, None, None, None, None, 0, 8, 512, None, 0, None) == 0
