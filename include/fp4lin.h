@@ -173,8 +173,9 @@ FP4LIN_API fp4_status fp4_requant_nvfp4_to_mxfp4_ex(const uint8_t* w_packed, con
  *                 (the per-expert scale layout fp4_gemm_mxfp4_grouped reads)
  * Tensor e is bit-identical to fp4_requant_nvfp4_to_mxfp4_ex on its slices
  * with w_global[e].  Requires 1 <= E <= 4096, N >= 1, K a positive multiple
- * of 128, 32-byte aligned packed pointers, an 8-byte aligned w_scale_e4m3,
- * a 4-byte aligned out_scale (swizzled) and w_global.                       */
+ * of 128 below 2^29 (else FP4_ERR_SHAPE), 32-byte aligned packed pointers,
+ * an 8-byte aligned w_scale_e4m3, a 4-byte aligned out_scale (swizzled) and
+ * w_global.                                                                 */
 FP4LIN_API fp4_status fp4_requant_nvfp4_to_mxfp4_grouped(const uint8_t* w_packed, const uint8_t* w_scale_e4m3,
                                               const float* w_global, uint8_t* out_packed,
                                               uint8_t* out_scale, int32_t E, int64_t N, int64_t K,

@@ -236,7 +236,7 @@ fp4_status fp4_requant_nvfp4_to_mxfp4_grouped(const uint8_t* w_packed, const uin
         return st;
     if (!w_packed || !w_scale_e4m3 || !w_global || !out_packed || !out_scale)
         return FP4_ERR_INVALID_ARG;
-    if (E <= 0 || E > 4096 || N <= 0 || K <= 0 || K % 128 != 0 || N >= kMaxDim || K >= kMaxDim ||
+    if (E <= 0 || E > 4096 || N <= 0 || K <= 0 || K % 128 != 0 || N >= kMaxDim || K >= (int64_t(1) << 29) ||
         static_cast<int64_t>(E) * N >= kMaxDim)
         return FP4_ERR_SHAPE;
     if (!fp4lin::requant_flat_ok(w_packed, w_scale_e4m3, out_packed, out_scale, K, swz) ||

@@ -81,7 +81,7 @@ cudaError_t launch_requant(const uint8_t* wp, const uint8_t* ws, float g, uint8_
                            int64_t N, int64_t K, int alg, int swizzled, int bf16, cudaStream_t stream);
 
 // E tensors [E][N][K/2] with global scales g_dev[E] (device); needs
-// requant_flat_ok (K % 128 == 0 and aligned arrays).
+// requant_flat_ok (K % 128 == 0, K < 2^29 and aligned arrays).
 cudaError_t launch_requant_grouped(const uint8_t* wp, const uint8_t* ws, const float* g_dev, uint8_t* op,
                                    uint8_t* osf, int E, int64_t N, int64_t K, int alg, int swizzled, int bf16,
                                    cudaStream_t stream);

@@ -110,9 +110,9 @@ __device__ __forceinline__ uint2 pack_code_map(uint32_t r1, uint32_t r2, uint32_
 // is m >= 1 has amax >= H, so its block exponent is >= er - 3; at d >= 6
 // every magnitude is below 2^(e-2) and maps to 0 (entry 9).  A half of zero
 // codes reads 0 from any entry.  Exponents outside [-127, 126] never occur
-// for a finite block and stay 0.  Where the doublings hold, the codes 4..7
-// of entry d are the codes 2..5 of entry d - 1 (2 x_d = x_{d-1}), so each
-// further entry costs three roundings.
+// for a finite block and stay 0.  Each entry is built by its own thread:
+// three products scaled by 2^-e and seven code roundings (the doublings for
+// codes 4..7 happen inside the rounding's fused multiply-adds).
 constexpr int kMapD = 10;
 constexpr int kMapEntries = 128 * kMapD;
 
@@ -149,73 +149,42 @@ __device__ void build_code_maps(float ag, int rule, RequantTables& tb)
         const float v = __fmul_rn(cs, ag);
         return bf16 ? round_to_bf16(v) : v;
     };
-    uint2* __restrict__ map = tb.map;
     for (int i = threadIdx.x; i < 128 * 8; i += blockDim.x) {
         const float S = fabsf(e4m3x2_to_float2(static_cast<uint32_t>(i >> 3)).x);
         const float amax = decode(__fmul_rn(e2m1_mag_value(static_cast<uint32_t>(i & 7)), S));
         const uint32_t ab = __float_as_uint(amax);
         tb.texp[i] = ab >= 0x7F800000u ? uint8_t(255) : static_cast<uint8_t>(mx_shared_exp(ab, uos) + 127);
     }
-    for (int sb = threadIdx.x; sb < 128; sb += blockDim.x) {
+    // one thread per entry (scale byte sb, d = di - 3)
+    for (int i = threadIdx.x; i < kMapEntries; i += blockDim.x) {
+        const int sb = i / kMapD, di = i - sb * kMapD;
         const float S = e4m3x2_to_float2(static_cast<uint32_t>(sb)).x;
-        const float H = decode(0.5f * S);
         const float P = decode(S);
-        const float Q = decode(1.5f * S);
-        tb.ter[sb] = static_cast<uint8_t>(__float_as_uint(P) >> 23);
         const int er = static_cast<int>(__float_as_uint(P) >> 23) - 127;
-        uint32_t p2 = 0u, p3 = 0u, p4 = 0u, p5 = 0u;
-        bool prev = false;
-        for (int di = 0; di < 9; ++di) {
-            const int e = er + di - 3;
-            uint2 m = make_uint2(0u, 0u);
-            if (e >= -127 && e <= 126) {
-                const float se = exp2_neg(e);
-                const float h = __fmul_rn(H, se), x = __fmul_rn(P, se), y = __fmul_rn(Q, se);
-                const uint32_t r1 = __float_as_uint(e2m1_code_scaled<0>(h));
-                const uint32_t r2 = __float_as_uint(e2m1_code_scaled<0>(x));
-                const uint32_t r3 = __float_as_uint(e2m1_code_scaled<0>(y));
-                uint32_t r4, r5, r6, r7;
-                if (prev) {
-                    r4 = p2;
-                    r5 = p3;
-                    r6 = p4;
-                    r7 = p5;
-                } else {
-                    r4 = __float_as_uint(e2m1_code_scaled<1>(x));
-                    r5 = __float_as_uint(e2m1_code_scaled<1>(y));
-                    r6 = __float_as_uint(e2m1_code_scaled<2>(x));
-                    r7 = __float_as_uint(e2m1_code_scaled<2>(y));
-                }
-                m = pack_code_map(r1, r2, r3, r4, r5, r6, r7);
-                p2 = r2;
-                p3 = r3;
-                p4 = r4;
-                p5 = r5;
-                prev = true;
-            } else {
-                prev = false;
-            }
-            map[sb * kMapD + di] = m;
-        }
-        map[sb * kMapD + 9] = make_uint2(0u, 0u);
-        // S |g| below 2^-125 (biased exponent 2): the doublings above are not
-        // exact there, so the codes of magnitudes 4..7 (the map's second
-        // word) are redone from one-by-one roundings
-        if (!(__fmul_rn(S, ag) >= __uint_as_float(2u << 23))) {
-#pragma unroll 1
-            for (int di = 0; di < 9; ++di) {
-                const int e = er + di - 3;
-                if (e >= -127 && e <= 126) {
-                    const float se = exp2_neg(e);
-                    // codes of the magnitudes 2S, 3S, 4S, 6S (times |g|), one per byte
-                    const uint32_t w = e2m1x8_pack(__fmul_rn(decode(2.0f * S), se), __fmul_rn(decode(3.0f * S), se),
-                                                   __fmul_rn(decode(4.0f * S), se), __fmul_rn(decode(6.0f * S), se),
-                                                   0.0f, 0.0f, 0.0f, 0.0f);
-                    map[sb * kMapD + di].y =
-                        (w & 0xFu) | ((w << 4) & 0xF00u) | ((w << 8) & 0xF0000u) | ((w << 12) & 0xF000000u);
-                }
+        if (di == 0)
+            tb.ter[sb] = static_cast<uint8_t>(er + 127);
+        const int e = er + di - 3;
+        uint2 m = make_uint2(0u, 0u);
+        if (di < 9 && e >= -127 && e <= 126) {
+            const float se = exp2_neg(e);
+            const float x = __fmul_rn(P, se), y = __fmul_rn(decode(1.5f * S), se);
+            const uint32_t r1 = __float_as_uint(e2m1_code_scaled<0>(__fmul_rn(decode(0.5f * S), se)));
+            const uint32_t r2 = __float_as_uint(e2m1_code_scaled<0>(x));
+            const uint32_t r3 = __float_as_uint(e2m1_code_scaled<0>(y));
+            m = pack_code_map(r1, r2, r3, __float_as_uint(e2m1_code_scaled<1>(x)),
+                              __float_as_uint(e2m1_code_scaled<1>(y)), __float_as_uint(e2m1_code_scaled<2>(x)),
+                              __float_as_uint(e2m1_code_scaled<2>(y)));
+            // S |g| below 2^-125 (biased exponent 2): the doublings are not
+            // exact there, so the codes of magnitudes 4..7 (the map's second
+            // word) come from one-by-one roundings of 2S, 3S, 4S, 6S (times |g|)
+            if (!(__fmul_rn(S, ag) >= __uint_as_float(2u << 23))) {
+                const uint32_t w = e2m1x8_pack(__fmul_rn(decode(2.0f * S), se), __fmul_rn(decode(3.0f * S), se),
+                                               __fmul_rn(decode(4.0f * S), se), __fmul_rn(decode(6.0f * S), se),
+                                               0.0f, 0.0f, 0.0f, 0.0f);
+                m.y = (w & 0xFu) | ((w << 4) & 0xF00u) | ((w << 8) & 0xF0000u) | ((w << 12) & 0xF000000u);
             }
         }
+        tb.map[i] = m;
     }
 }
 
@@ -238,19 +207,25 @@ __device__ __forceinline__ void max_codes(uint32_t m0, uint32_t m0h, uint32_t m1
     mm1 = 31u - __clz(((w >> 8) & 0xFFu) | 1u);
 }
 
-// Applies a magnitude map to 8 codes (m = magnitudes, mh = m >> 16) and
-// restores the signs of w (flipped when the scale times g is negative).
-__device__ __forceinline__ uint32_t apply_map(uint32_t w, uint32_t m, uint32_t mh, uint2 t, uint32_t flip)
+// Applies a magnitude map to the 8 codes of one word (m = magnitudes, mh =
+// m >> 16): the map's bytes for nibbles 0..3 and 4..7 are regrouped into the
+// even and the odd nibbles and packed with one multiply-add; the sign bits
+// come from ws (the input word with its signs flipped where the scale times
+// g is negative).
+__device__ __forceinline__ uint32_t apply_map(uint32_t ws, uint32_t m, uint32_t mh, uint2 t)
 {
     const uint32_t lo = __byte_perm(t.x, t.y, m);
     const uint32_t hi = __byte_perm(t.x, t.y, mh);
-    const uint32_t a = lo | (lo >> 4);
-    const uint32_t b = hi | (hi >> 4);
-    return __byte_perm(a, b, 0x6420u) | ((w & 0x88888888u) ^ flip);
+    const uint32_t ev = __byte_perm(lo, hi, 0x6420u);  // codes of nibbles 0, 2, 4, 6
+    const uint32_t od = __byte_perm(lo, hi, 0x7531u);  // codes of nibbles 1, 3, 5, 7
+    return (od * 16u + ev) | (ws & 0x88888888u);
 }
 
-// One block: codes in 4 words, its two E4M3 scale bytes in `sc` (low byte =
-// elements 0..15).  Returns the scale byte; writes the 4 output words.
+// One block: codes in 4 words, its two E4M3 scale bytes in the low 16 bits of
+// `sc` (low byte = elements 0..15).  Returns the scale byte; writes the 4
+// output words.  kFlip: some scale byte of the warp's blocks is negative or
+// g < 0 (otherwise every element keeps the sign of its code).
+template <bool kFlip>
 __device__ __forceinline__ uint32_t requant_block(const uint32_t* w, uint32_t sc, uint32_t gsign,
                                                   const RequantTables& tb, uint32_t* out)
 {
@@ -265,18 +240,28 @@ __device__ __forceinline__ uint32_t requant_block(const uint32_t* w, uint32_t sc
         out[0] = out[1] = out[2] = out[3] = 0u;
         return 0xFFu;
     }
-    // d + 3 = e - er + 3 = (e + 127) + 3 - biased exponent of RN(S |g|)
-    const int i0 = min(max(eb + 3 - static_cast<int>(tb.ter[s0]), 0), kMapD - 1);
-    const int i1 = min(max(eb + 3 - static_cast<int>(tb.ter[s1]), 0), kMapD - 1);
+    // entry d + 3 = e - er + 3 = (e + 127) + 3 - biased exponent of RN(S |g|).
+    // It is >= 0 for a half with a nonzero code; an all-zero half maps to 0
+    // from any entry, so a negative value (wrapping around as unsigned) and
+    // values past the last entry both take entry 9.
+    const uint32_t i0 = min(static_cast<uint32_t>(eb + 3 - static_cast<int>(tb.ter[s0])), uint32_t(kMapD - 1));
+    const uint32_t i1 = min(static_cast<uint32_t>(eb + 3 - static_cast<int>(tb.ter[s1])), uint32_t(kMapD - 1));
     const uint2 t0 = tb.map[s0 * kMapD + i0];
     const uint2 t1 = tb.map[s1 * kMapD + i1];
-    // element sign = code sign ^ scale sign ^ sign of g
-    const uint32_t f0 = (((sc >> 7) & 1u) ^ gsign) ? 0x88888888u : 0u;
-    const uint32_t f1 = (((sc >> 15) & 1u) ^ gsign) ? 0x88888888u : 0u;
-    out[0] = apply_map(w[0], m0, m0h, t0, f0);
-    out[1] = apply_map(w[1], m1, m1h, t0, f0);
-    out[2] = apply_map(w[2], m2, m2h, t1, f1);
-    out[3] = apply_map(w[3], m3, m3h, t1, f1);
+    uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3];
+    if constexpr (kFlip) {
+        // element sign = code sign ^ scale sign ^ sign of g
+        const uint32_t f0 = (((sc >> 7) ^ gsign) & 1u) * 0x88888888u;
+        const uint32_t f1 = (((sc >> 15) ^ gsign) & 1u) * 0x88888888u;
+        w0 ^= f0;
+        w1 ^= f0;
+        w2 ^= f1;
+        w3 ^= f1;
+    }
+    out[0] = apply_map(w0, m0, m0h, t0);
+    out[1] = apply_map(w1, m1, m1h, t0);
+    out[2] = apply_map(w2, m2, m2h, t1);
+    out[3] = apply_map(w3, m3, m3h, t1);
     return static_cast<uint32_t>(eb);
 }
 
@@ -352,7 +337,7 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const uint8_t* __rest
         uint32_t sfw = 0u;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t sf = requant_block(cur.w + 4 * j, cur.sc[j], gsign, tb, out + 4 * j);
+            const uint32_t sf = requant_block<true>(cur.w + 4 * j, cur.sc[j], gsign, tb, out + 4 * j);
             if (j < nreal)
                 sfw |= sf << (8 * j);
         }
@@ -385,20 +370,28 @@ __global__ void __launch_bounds__(kThreads) requant_kernel(const uint8_t* __rest
 // aligned scales.  Rows are then back to back in memory and a row's block
 // count is a multiple of 4, so a tensor is one run of 32-element blocks and a
 // warp item is 128 consecutive blocks whatever K is (a lane's 4 blocks never
-// straddle rows).  Rows are counted up to rows_pad (the 128-row padding of a
-// swizzled scale array; pad rows get zero scale bytes).  Grouped: E tensors of
-// the same shape stored back to back, each with its own global scale g[e]
-// (device array); a run of ctas_per_e CTAs serves one tensor, so a CTA builds
-// the code maps of one g only.  Launch bound: four CTAs per SM (at most 64
-// registers a thread), the occupancy the kernel is measured at.
-template <bool kGrouped>
-__global__ void __launch_bounds__(kThreads, 4) requant_flat_kernel(const uint8_t* __restrict__ wp,
-                                                                const uint8_t* __restrict__ ws, float g_dense,
-                                                                const float* __restrict__ g_dev,
-                                                                uint8_t* __restrict__ op, uint8_t* __restrict__ osf,
-                                                                int64_t N, int64_t K, int64_t rows_pad, int kb,
-                                                                int64_t items, int ctas_per_e, int64_t sf_e_bytes,
-                                                                int rule, int swizzled, DivMagic kb_div, int idx32)
+// straddle rows).  A launch covers rows [r0, r0 + n_rows) of each tensor,
+// counted up to rows_pad (the 128-row padding of a swizzled scale array; pad
+// rows get zero scale bytes), with every block index of that range below
+// 2^32.  Grouped: E tensors of N rows stored back to back, each with its own
+// global scale g[e] (device array); a run of ctas_per_e CTAs serves one
+// tensor, so a CTA builds the code maps of one g only.  Dense launches use
+// one 1024-thread CTA per SM (one set of code maps per SM, built by all its
+// threads); grouped ones four 256-thread CTAs per SM, so that a tensor's
+// CTAs spread over the SMs.  Both bounds keep a thread at 64 registers.
+// Each warp walks its items two at a time from two register buffers: the
+// next item's loads are in flight while the current one is converted.
+struct FlatLane {
+    uint32_t w[16];  // 4 blocks x 4 code words
+    uint32_t s[2];   // the blocks' 8 E4M3 bytes
+};
+
+template <bool kGrouped, int kT>
+__global__ void __launch_bounds__(kT, kGrouped ? 4 : 1)
+    requant_flat_kernel(const uint8_t* __restrict__ wp, const uint8_t* __restrict__ ws, float g_dense,
+                        const float* __restrict__ g_dev, uint8_t* __restrict__ op, uint8_t* __restrict__ osf,
+                        int64_t N, int64_t K, int64_t r0, uint32_t n_rows, uint32_t rows_pad, int kb, uint32_t items,
+                        int ctas_per_e, int64_t sf_e_bytes, int rule, int swizzled, DivMagic kb_div)
 {
     __shared__ RequantTables tb;
     const int e = kGrouped ? static_cast<int>(blockIdx.x) / ctas_per_e : 0;
@@ -413,100 +406,102 @@ __global__ void __launch_bounds__(kThreads, 4) requant_flat_kernel(const uint8_t
         build_code_maps(fabsf(g), rule, tb);
     }
     __syncthreads();
-    const float ag = fabsf(g);
     const uint32_t gsign = __float_as_uint(g) >> 31;
 
-    const int lane = threadIdx.x & 31;
-    const int64_t stride = static_cast<int64_t>(ctas_per_e) * (kThreads / 32);
-    int64_t item = static_cast<int64_t>(local) * (kThreads / 32) + (threadIdx.x >> 5);
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t stride = static_cast<uint32_t>(ctas_per_e) * (kT / 32);
+    uint32_t item = static_cast<uint32_t>(local) * (kT / 32) + (threadIdx.x >> 5);
     if (item >= items)
         return;
-    const int64_t nblocks = rows_pad * kb;  // blocks of one tensor, pad rows included
-    const int64_t kb4 = kb >> 2;
-    const uint8_t* wpe = wp + static_cast<int64_t>(e) * N * (K / 2);
-    const uint8_t* wse = ws + static_cast<int64_t>(e) * N * (K / 16);
-    uint8_t* ope = op + static_cast<int64_t>(e) * N * (K / 2);
-    uint8_t* osfe = osf + (swizzled ? static_cast<int64_t>(e) * sf_e_bytes : static_cast<int64_t>(e) * N * kb);
-    // lane's first block and whether it holds real data (4 blocks of one row)
-    auto locate = [&](int64_t it, int64_t& f, bool& real) {
-        f = it * 128 + 4 * lane;
-        real = f < N * kb;  // rows are contiguous: the first N*kb blocks are the tensor's
-    };
-    int64_t f;
-    bool real;
-    locate(item, f, real);
-    RequantLane cur;
-    auto load = [&](RequantLane& L, int64_t fb, bool r) {
-        if (r) {
+    const uint32_t nreal = n_rows * static_cast<uint32_t>(kb);    // the range's real blocks come first
+    const uint32_t nblocks = rows_pad * static_cast<uint32_t>(kb);  // pad rows included
+    const uint32_t kb4 = static_cast<uint32_t>(kb) >> 2;
+    const int64_t row0 = static_cast<int64_t>(e) * N + r0;
+    const uint8_t* wpe = wp + row0 * (K / 2);
+    const uint8_t* wse = ws + row0 * (K / 16);
+    uint8_t* ope = op + row0 * (K / 2);
+    uint8_t* osfe = osf + (swizzled ? static_cast<int64_t>(e) * sf_e_bytes : static_cast<int64_t>(e) * N * kb) + r0 * kb;
+
+    auto load = [&](FlatLane& L, uint32_t it) {
+        const uint32_t f = it * 128u + 4u * lane;  // the lane's first block
+        if (f < nreal) {
             uint32_t a[8], b[8];
-            ld_nc_v8(wpe + fb * 16, a);
-            ld_nc_v8(wpe + fb * 16 + 32, b);
+            ld_nc_v8(wpe + static_cast<size_t>(f) * 16, a);
+            ld_nc_v8(wpe + static_cast<size_t>(f) * 16 + 32, b);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 L.w[i] = a[i];
                 L.w[8 + i] = b[i];
             }
-            const uint2 s2 = ld_nc_u64(wse + fb * 2);
-            L.sc[0] = s2.x & 0xFFFFu;
-            L.sc[1] = s2.x >> 16;
-            L.sc[2] = s2.y & 0xFFFFu;
-            L.sc[3] = s2.y >> 16;
+            const uint2 s2 = ld_nc_u64(wse + static_cast<size_t>(f) * 2);
+            L.s[0] = s2.x;
+            L.s[1] = s2.y;
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 L.w[i] = 0u;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                L.sc[j] = 0u;
+            L.s[0] = L.s[1] = 0u;
         }
     };
-    load(cur, f, real);
-    while (true) {
-        const int64_t next = item + stride;
-        int64_t nf = 0;
-        bool nreal = false;
-        RequantLane nxt;
-        const bool more = next < items;
-        if (more) {
-            locate(next, nf, nreal);
-            load(nxt, nf, nreal);
-        }
-        if (f < nblocks) {
-            uint32_t out[16];
-            uint32_t sfw = 0u;
+    auto convert = [&](const FlatLane& L, uint32_t it) {
+        const uint32_t f = it * 128u + 4u * lane;
+        // signs change only where a scale byte is negative or g < 0: one vote
+        // per warp item picks the path
+        const bool flip = __any_sync(0xFFFFFFFFu, (gsign | ((L.s[0] | L.s[1]) & 0x80808080u)) != 0u);
+        if (f >= nblocks)
+            return;
+        const bool real = f < nreal;
+        uint32_t sfw = 0u;
+        // two blocks at a time: convert, then store their 32 bytes
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                sfw |= requant_block(cur.w + 4 * j, cur.sc[j], gsign, tb, out + 4 * j) << (8 * j);
-            // block index -> (row, block column): a multiply-high while the
-            // tensor's block count fits 32 bits
-            const int64_t row = idx32 ? static_cast<int64_t>(div_by_magic(static_cast<uint32_t>(f), kb_div)) : f / kb;
-            const int c0 = static_cast<int>(f - row * kb);
-            if (real) {
-                uint32_t a[8], b[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    a[i] = out[i];
-                    b[i] = out[8 + i];
-                }
-                st_v8(ope + f * 16, a);
-                st_v8(ope + f * 16 + 32, b);
+        for (int h = 0; h < 2; ++h) {
+            uint32_t out[8];
+            const uint32_t sc = L.s[h];
+            if (flip) {
+                sfw |= requant_block<true>(L.w + 8 * h, sc, gsign, tb, out) << (16 * h);
+                sfw |= requant_block<true>(L.w + 8 * h + 4, sc >> 16, gsign, tb, out + 4) << (16 * h + 8);
             } else {
-                sfw = 0u;  // pad rows
+                sfw |= requant_block<false>(L.w + 8 * h, sc, 0u, tb, out) << (16 * h);
+                sfw |= requant_block<false>(L.w + 8 * h + 4, sc >> 16, 0u, tb, out + 4) << (16 * h + 8);
             }
-            if (swizzled) {
-                *reinterpret_cast<uint32_t*>(osfe + sf_swizzled_offset(row, c0, kb4)) = sfw;
-            } else if (real) {
+            if (real)
+                st_v8(ope + static_cast<size_t>(f) * 16 + 32 * h, out);
+        }
+        // block index -> (row, block column) by a multiply-high
+        const uint32_t row = div_by_magic(f, kb_div);
+        const uint32_t c0 = f - row * static_cast<uint32_t>(kb);
+        if (real) {
+            if (!swizzled) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     osfe[f + j] = static_cast<uint8_t>(sfw >> (8 * j));
             }
+        } else {
+            sfw = 0u;  // pad rows
         }
-        if (!more)
+        if (swizzled) {
+            // r0 is a multiple of 128, so the range's swizzled bytes start at r0 * kb
+            const uint32_t off = ((row >> 7) * kb4 + (c0 >> 2)) * 512u + (row & 31u) * 16u + ((row & 127u) >> 5) * 4u;
+            *reinterpret_cast<uint32_t*>(osfe + off) = sfw;
+        }
+    };
+
+    FlatLane A, B;
+    load(A, item);
+    while (true) {
+        const uint32_t i1 = item + stride;
+        if (i1 < items)
+            load(B, i1);
+        convert(A, item);
+        if (i1 >= items)
             break;
-        item = next;
-        f = nf;
-        real = nreal;
-        cur = nxt;
+        const uint32_t i2 = i1 + stride;
+        if (i2 < items)
+            load(A, i2);
+        convert(B, i1);
+        if (i2 >= items)
+            break;
+        item = i2;
     }
 }
 
@@ -783,7 +778,7 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // CTAs of `kern` that fit on the whole GPU at once (per device, cached).
 template <typename Kern>
-int64_t resident_ctas(Kern kern)
+int64_t resident_ctas(Kern kern, int threads = kThreads)
 {
     static std::mutex mu;
     static int64_t cached[64] = {};
@@ -794,7 +789,7 @@ int64_t resident_ctas(Kern kern)
     if (cached[dev] == 0) {
         int sms = 0, per_sm = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
         cached[dev] = std::max<int64_t>(1, static_cast<int64_t>(sms) * std::max(per_sm, 1));
     }
     return cached[dev];
@@ -806,32 +801,50 @@ int64_t resident_ctas(Kern kern)
 bool requant_flat_ok(const uint8_t* wp, const uint8_t* ws, const uint8_t* op, const uint8_t* osf, int64_t K,
                      int swizzled)
 {
-    return K % 128 == 0 && (reinterpret_cast<uintptr_t>(wp) & 31u) == 0 && (reinterpret_cast<uintptr_t>(op) & 31u) == 0 &&
+    return K % 128 == 0 && K < (int64_t(1) << 29) && (reinterpret_cast<uintptr_t>(wp) & 31u) == 0 && (reinterpret_cast<uintptr_t>(op) & 31u) == 0 &&
            (reinterpret_cast<uintptr_t>(ws) & 7u) == 0 && (!swizzled || (reinterpret_cast<uintptr_t>(osf) & 3u) == 0);
 }
 
-// Flat kernel over E tensors (E = 1: dense, g_dev unused).
+// Flat kernel over E tensors (E = 1: dense, g_dev unused), in row ranges
+// whose block indices fit 32 bits (one range unless a tensor has 2^31
+// blocks or more).
 cudaError_t launch_requant_flat(const uint8_t* wp, const uint8_t* ws, float g, const float* g_dev, uint8_t* op,
                                 uint8_t* osf, int E, int64_t N, int64_t K, int rule, int swizzled, cudaStream_t stream)
 {
+    constexpr int kDenseT = 1024, kGroupT = 256;
     const int kb = static_cast<int>(K / 32);
     const int64_t rows_pad = swizzled ? ceil_div(N, 128) * 128 : N;
-    const int64_t items = ceil_div(rows_pad * kb, 128);  // warp items per tensor
-    const int64_t sf_e_bytes = rows_pad * kb;            // swizzled bytes per tensor (kb % 4 == 0)
-    const int64_t want = ceil_div(items * 32, kThreads);  // CTAs that give every warp one item
-    // a lane's first block index f < items * 128 (pad rows included)
-    const int idx32 = items * 128 <= int64_t(UINT32_MAX) ? 1 : 0;
+    const int64_t sf_e_bytes = rows_pad * kb;  // swizzled bytes per tensor (kb % 4 == 0)
+    // rows per launch: a multiple of 128 with at most 2^31 blocks
+    const int64_t chunk = std::max<int64_t>(128, ((int64_t(1) << 31) / kb) / 128 * 128);
     const DivMagic kb_div = div_magic(static_cast<uint32_t>(kb));
-    if (g_dev == nullptr) {
-        const int64_t blocks = std::min<int64_t>(want, resident_ctas(requant_flat_kernel<false>));
-        return launch_pdl(requant_flat_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream,
-                          wp, ws, g, static_cast<const float*>(nullptr), op, osf, N, K, rows_pad, kb, items,
-                          static_cast<int>(blocks), sf_e_bytes, rule, swizzled, kb_div, idx32);
+    for (int64_t r0 = 0; r0 < rows_pad; r0 += chunk) {
+        const int64_t pad = std::min(chunk, rows_pad - r0);
+        const int64_t real = std::max<int64_t>(0, std::min(chunk, N - r0));
+        const int64_t items = ceil_div(pad * kb, 128);  // warp items per tensor and launch
+        cudaError_t err;
+        if (g_dev == nullptr) {
+            const int64_t want = ceil_div(items * 32, kDenseT);  // CTAs that give every warp one item
+            const int64_t blocks = std::min<int64_t>(want, resident_ctas(requant_flat_kernel<false, kDenseT>, kDenseT));
+            err = launch_pdl(requant_flat_kernel<false, kDenseT>, dim3(static_cast<unsigned>(blocks)), dim3(kDenseT),
+                             0, stream, wp, ws, g, static_cast<const float*>(nullptr), op, osf, N, K, r0,
+                             static_cast<uint32_t>(real), static_cast<uint32_t>(pad), kb,
+                             static_cast<uint32_t>(items), static_cast<int>(blocks), sf_e_bytes, rule, swizzled,
+                             kb_div);
+        } else {
+            const int64_t want = ceil_div(items * 32, kGroupT);
+            const int64_t per_e = std::max<int64_t>(
+                1, std::min<int64_t>(want, resident_ctas(requant_flat_kernel<true, kGroupT>, kGroupT) / E));
+            err = launch_pdl(requant_flat_kernel<true, kGroupT>, dim3(static_cast<unsigned>(per_e * E)),
+                             dim3(kGroupT), 0, stream, wp, ws, 0.0f, g_dev, op, osf, N, K, r0,
+                             static_cast<uint32_t>(real), static_cast<uint32_t>(pad), kb,
+                             static_cast<uint32_t>(items), static_cast<int>(per_e), sf_e_bytes, rule, swizzled,
+                             kb_div);
+        }
+        if (err != cudaSuccess)
+            return err;
     }
-    const int64_t per_e = std::max<int64_t>(1, std::min<int64_t>(want, resident_ctas(requant_flat_kernel<true>) / E));
-    return launch_pdl(requant_flat_kernel<true>, dim3(static_cast<unsigned>(per_e * E)), dim3(kThreads), 0, stream, wp,
-                      ws, 0.0f, g_dev, op, osf, N, K, rows_pad, kb, items, static_cast<int>(per_e), sf_e_bytes, rule,
-                      swizzled, kb_div, idx32);
+    return cudaSuccess;
 }
 
 // rule bits for the code maps: the block rule and the decoded-value precision

@@ -69,6 +69,7 @@ def test_argument_checks_precede_device_use(L):
     assert raw.fp4_requant_nvfp4_to_mxfp4(16, 16, 1.0, 16, 16, 0, 32, None) == 2   # N = 0
     assert raw.fp4_requant_nvfp4_to_mxfp4_grouped(32, 32, 32, 32, 32, 2, 4, 96, None, None) == 2   # K % 128
     assert raw.fp4_requant_nvfp4_to_mxfp4_grouped(32, 32, 32, 32, 32, 0, 4, 128, None, None) == 2  # E = 0
+    assert raw.fp4_requant_nvfp4_to_mxfp4_grouped(32, 32, 32, 32, 32, 2, 4, 1 << 29, None, None) == 2  # K >= 2^29
     assert raw.fp4_gemm_mxfp4_grouped(16, 16, 16, 16, None, 16, 16, 1025, 4, 8, 128, None) == 2    # E > 1024
     # null pointers
     assert raw.fp4_gemm_mxfp4(None, 16, 16, 16, None, 16, 1, 8, 128, None) == 1

@@ -80,6 +80,22 @@ def test_requant_flat_shapes(orc, L, N, K, alg, layout):
         _check_requant(orc, L, packed, scale, float(np.float32(g)), alg, layout)
 
 
+@pytest.mark.parametrize("alg", [OCP, UOS])
+def test_requant_flat_several_items_per_warp(orc, L, alg):
+    """A tensor with more 128-block warp items than the GPU has resident
+    warps, so warps walk two and more items through both register buffers;
+    random bytes mix warp items with and without negative scales (the two
+    sign paths) and a ragged last item; positive and negative g."""
+    N, K = 9000, 4224
+    rng = np.random.default_rng(4224)
+    packed, scale = _random_nvfp4(rng, N, K)
+    # rows 0..2999: positive scale bytes only (no sign changes unless g < 0)
+    scale[:3000] &= 0x7F
+    for g in (0.0123, -0.5):
+        _check_requant(orc, L, packed, scale, float(np.float32(g)), alg, SWZ)
+    _check_requant(orc, L, packed, scale, float(np.float32(0.0123)), alg, ROW)
+
+
 def test_requant_16_byte_aligned_buffers(orc, L):
     # codes only 16-byte aligned: the row kernel takes the K % 128 == 0 shape
     import torch
