@@ -423,25 +423,15 @@ __global__ void __launch_bounds__(kT, kGrouped ? 4 : 1)
     uint8_t* osfe = osf + (swizzled ? static_cast<int64_t>(e) * sf_e_bytes : static_cast<int64_t>(e) * N * kb) + r0 * kb;
 
     auto load = [&](FlatLane& L, uint32_t it) {
-        const uint32_t f = it * 128u + 4u * lane;  // the lane's first block
-        if (f < nreal) {
-            uint32_t a[8], b[8];
-            ld_nc_v8(wpe + static_cast<size_t>(f) * 16, a);
-            ld_nc_v8(wpe + static_cast<size_t>(f) * 16 + 32, b);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                L.w[i] = a[i];
-                L.w[8 + i] = b[i];
-            }
-            const uint2 s2 = ld_nc_u64(wse + static_cast<size_t>(f) * 2);
-            L.s[0] = s2.x;
-            L.s[1] = s2.y;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                L.w[i] = 0u;
-            L.s[0] = L.s[1] = 0u;
-        }
+        // the lane's first block; lanes past the range's real blocks load the
+        // last real ones (their results are never stored), so the loads need
+        // no branch
+        const uint32_t f = min(it * 128u + 4u * lane, nreal - 4u);
+        ld_nc_v8(wpe + static_cast<size_t>(f) * 16, *reinterpret_cast<uint32_t(*)[8]>(L.w));
+        ld_nc_v8(wpe + static_cast<size_t>(f) * 16 + 32, *reinterpret_cast<uint32_t(*)[8]>(L.w + 8));
+        const uint2 s2 = ld_nc_u64(wse + static_cast<size_t>(f) * 2);
+        L.s[0] = s2.x;
+        L.s[1] = s2.y;
     };
     auto convert = [&](const FlatLane& L, uint32_t it) {
         const uint32_t f = it * 128u + 4u * lane;
