@@ -396,23 +396,9 @@ __global__ void __launch_bounds__(kT, kGrouped ? 4 : 1)
     __shared__ RequantTables tb;
     const int e = kGrouped ? static_cast<int>(blockIdx.x) / ctas_per_e : 0;
     const int local = kGrouped ? static_cast<int>(blockIdx.x) - e * ctas_per_e : static_cast<int>(blockIdx.x);
-    float g = g_dense;
-    if (!kGrouped)
-        build_code_maps(fabsf(g), rule, tb);  // needs no global memory: overlaps the previous kernel
-    grid_dependency_wait();
-    launch_dependents();
-    if (kGrouped) {
-        g = __ldg(g_dev + e);
-        build_code_maps(fabsf(g), rule, tb);
-    }
-    __syncthreads();
-    const uint32_t gsign = __float_as_uint(g) >> 31;
-
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t stride = static_cast<uint32_t>(ctas_per_e) * (kT / 32);
     uint32_t item = static_cast<uint32_t>(local) * (kT / 32) + (threadIdx.x >> 5);
-    if (item >= items)
-        return;
     const uint32_t nreal = n_rows * static_cast<uint32_t>(kb);    // the range's real blocks come first
     const uint32_t nblocks = rows_pad * static_cast<uint32_t>(kb);  // pad rows included
     const uint32_t kb4 = static_cast<uint32_t>(kb) >> 2;
@@ -433,6 +419,21 @@ __global__ void __launch_bounds__(kT, kGrouped ? 4 : 1)
         L.s[0] = s2.x;
         L.s[1] = s2.y;
     };
+
+    // The first item's loads go out before the code maps are built, so that
+    // building them overlaps the loads' latency.
+    grid_dependency_wait();
+    launch_dependents();
+    FlatLane A, B;
+    if (item < items)
+        load(A, item);
+    const float g = kGrouped ? __ldg(g_dev + e) : g_dense;
+    build_code_maps(fabsf(g), rule, tb);
+    __syncthreads();
+    if (item >= items)
+        return;
+    const uint32_t gsign = __float_as_uint(g) >> 31;
+
     auto convert = [&](const FlatLane& L, uint32_t it) {
         const uint32_t f = it * 128u + 4u * lane;
         // signs change only where a scale byte is negative or g < 0: one vote
@@ -476,8 +477,6 @@ __global__ void __launch_bounds__(kT, kGrouped ? 4 : 1)
         }
     };
 
-    FlatLane A, B;
-    load(A, item);
     while (true) {
         const uint32_t i1 = item + stride;
         if (i1 < items)
