@@ -196,7 +196,10 @@ FP4LIN_API fp4_status fp4_quant_act_mxfp4(const void* x_bf16, uint8_t* out_packe
  * to group e.  Scales are always SWIZZLED; group e's scale rows start at
  * sum_{j<e} ceil(rows_j/128)*128, so every group begins on a 128-row tile.
  *   row_offsets  [E+1] int32 (device), non-decreasing, row_offsets[0] = 0,
- *                row_offsets[E] = total_M
+ *                row_offsets[E] = total_M.  The kernel clamps every offset
+ *                to [0, total_M] (and each end to at least its start), so
+ *                offsets that break this rule give wrong groups but no
+ *                access outside the buffers.
  *   out_scale    fp4_sf_bytes_grouped(total_M, E, K) bytes (device)
  * Only the scale-row tiles a group uses are written (pad rows as 0).       */
 FP4LIN_API fp4_status fp4_quant_act_mxfp4_grouped(const void* x_bf16, const int32_t* row_offsets, int32_t E,
@@ -547,11 +550,14 @@ FP4LIN_API fp4_status fp4_linear_grouped(const void* x_bf16, const int32_t* row_
  *   b            [E][N][K/2] u8; sb: E consecutive SWIZZLED arrays of
  *                fp4_sf_bytes(N, K, 0) bytes each
  *   bias         [E][N] bf16 or NULL
- *   row_offsets  [E+1] int32 (device); the tile walk is derived on the
- *                device, so no host synchronization is needed
+ *   row_offsets  [E+1] int32 (device), the same rule as for
+ *                fp4_quant_act_mxfp4_grouped (and the same clamping); the
+ *                tile walk is derived on the device, so no host
+ *                synchronization is needed
  *   out          [total_M, N] bf16
  * Same shape and alignment rules as fp4_gemm_mxfp4, and 1 <= E <= 1024
- * (FP4_ERR_SHAPE otherwise).                                                */
+ * (FP4_ERR_SHAPE otherwise).  Large problems with E <= 233 run on CTA pairs
+ * (256 x 256 tiles of one expert), the rest on single CTAs.                 */
 FP4LIN_API fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
                                   const uint8_t* sb, const void* bias_bf16, void* out_bf16,
                                   const int32_t* row_offsets, int32_t E, int64_t total_M,

@@ -130,6 +130,18 @@ __device__ __forceinline__ uint32_t div_by_magic(uint32_t n, DivMagic g)
     return (t + ((n - t) >> g.s1)) >> g.s2;
 }
 
+// Rows [start, start + rows) of group e from the row offsets, each offset
+// clamped to [0, total] (and the end to >= the start): offsets that are out
+// of order or out of range can then give wrong groups but never an access
+// outside the total rows.
+__device__ __forceinline__ void group_rows(const int32_t* offsets, int e, int total, int* start, int* rows)
+{
+    const int a = min(max(__ldg(offsets + e), 0), total);
+    const int b = min(max(__ldg(offsets + e + 1), a), total);
+    *start = a;
+    *rows = b - a;
+}
+
 // Scale-factor byte offset of (row r, 32-block c) in the swizzled layout the
 // block-scaled MMA reads; kb4 = ceil(K/32 / 4).
 __device__ __forceinline__ int64_t sf_swizzled_offset(int64_t r, int64_t c, int64_t kb4)

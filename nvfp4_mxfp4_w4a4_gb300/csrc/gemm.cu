@@ -215,12 +215,13 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmParams& p, const in
         const int mt = tiles_before[lo + 1] - tiles_before[lo];  // >= 1: expert lo holds tile t
         const int local = t - tiles_before[lo] * nt;
         const int gl = local % mt;
+        int start, rows_e;
+        group_rows(p.offsets, lo, p.rows_a, &start, &rows_e);
         T.expert = lo;
         T.n0 = (local / mt) * BN;
-        T.sfa_rt = tiles_before[lo] + gl;
-        const int start = __ldg(p.offsets + lo);
+        T.sfa_rt = min(tiles_before[lo] + gl, p.m_tiles - 1);  // inside the scale array whatever the offsets
         T.a_row0 = start + static_cast<int64_t>(gl) * BM;
-        rows = __ldg(p.offsets + lo + 1) - static_cast<int>(T.a_row0);
+        rows = rows_e - gl * BM;
     } else {
         const int g = t % p.m_tiles;
         T.n0 = (t / p.m_tiles) * BN;
@@ -442,8 +443,11 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
             for (int base = 0; base <= p.E; base += 32) {
                 const int e = base + lane;
                 int t = 0;
-                if (e < p.E)
-                    t = (__ldg(p.offsets + e + 1) - __ldg(p.offsets + e) + 127) >> 7;
+                if (e < p.E) {
+                    int start, rows;
+                    group_rows(p.offsets, e, p.rows_a, &start, &rows);
+                    t = (rows + 127) >> 7;
+                }
                 int incl = t;
 #pragma unroll
                 for (int d = 1; d < 32; d <<= 1) {
@@ -1292,6 +1296,8 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream)
         a.row_offsets != nullptr ? (a.M + static_cast<int64_t>(a.E) * 127) / 128 : (a.M + 127) / 128;
     const bool wide = a.N >= 256 && m_tiles * ((a.N + 255) / 256) >= 148;
     if (a.row_offsets != nullptr) {
+        if (wide && a.E <= gemm_pair_max_experts())
+            return launch_gemm_pair(a, stream);
         if (wide)
             return launch_kernel<256, 4, 1, 2, false, true>(a, stream);
         return k256 ? launch_kernel<128, 3, 2, 4, false, true>(a, stream)

@@ -25,7 +25,7 @@
 // 32 KB), the scale factors do not go through the copy engine at all, and
 // the epilogue stores few, large boxes.
 //
-// Per CTA (16 warps, registers split 80 / 176 with setmaxnreg):
+// Per CTA (16 warps, registers split 88 / 168 with setmaxnreg):
 //   warp 0, 6   TMA producers of A and of B: per stage one tensor-map load of
 //               the CTA's 128 rows (KC slabs of 256 K-elements); both CTAs'
 //               loads count on the LEADER's full barrier;
@@ -45,11 +45,23 @@
 //               MMAs start, add bias, round to bf16, TMA-store 32 x 64 boxes.
 // Every wait is bounded; on expiry the kernel records a timeout in the status
 // word and winds down.
+//
+// Grouped (MoE experts, "Efficiently Serving NVFP4 Models ...", "Native FP4
+// matmul": the experts on MXFP4): expert e owns rows [off[e], off[e+1]) of A
+// and its own weight [N, K/2], scale array and bias row.  A pair tile is two
+// consecutive 128-row tiles of one expert (the second may lie past the
+// expert's rows when it has an odd tile count: its MMA rows are computed
+// from whatever rows follow and never stored), walked expert-major.  Each
+// CTA derives the walk from the device offsets after the dependency wait
+// (exclusive prefixes of the experts' 128-row tile and pair-tile counts in
+// shared memory).  An output box whose 32 rows run past the expert's end is
+// stored row by row, so no row of the next expert is written.
 #include <cuda_bf16.h>
 
 #include <algorithm>
 #include <mutex>
 
+#include "formats.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -69,6 +81,11 @@ struct PairParams {
     const uint8_t* sfa;
     const uint8_t* sfb;
     const __nv_bfloat16* bias;
+    __nv_bfloat16* out;         // grouped: rows of partial output boxes are stored directly
+    const int32_t* offsets;     // grouped: [E + 1] row offsets (device)
+    int E;                      // grouped: experts
+    int64_t sfb_expert_stride;  // grouped: scale bytes of one expert's weight
+    int M;                      // dense: rows of A
     int N;
     int kb4;        // K / 128
     int m_pairs;    // 256-row tiles of A
@@ -92,20 +109,69 @@ struct PairCfg {
     static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * EPI_WARP_BYTES;
     static constexpr int NUM_BARS = 3 * STAGES + 2;
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
-    static constexpr int SMEM = OFF_SLOT + 16 + 1024;  // + 1 KB alignment slack
+    static constexpr int OFF_PREFIX = OFF_SLOT + 16;   // grouped: 2 (E + 1) int32
+    static constexpr int SMEM = OFF_PREFIX + 1024;     // + 1 KB alignment slack (+ the prefixes when grouped)
     static constexpr int SF_COLS_A = 4 * GROUPS;       // TMEM scale columns per stage
     static constexpr int SF_COLS_B = 8 * GROUPS;
     static constexpr int SF_COLS = SF_COLS_A + SF_COLS_B;
     static constexpr int TMEM_COLS = 512;
     static constexpr int THREADS = 512;
     static constexpr int FIRST_EPI_WARP = 8;
-    static constexpr int REGS_LOW = 80;
-    static constexpr int REGS_HIGH = 176;
+    static constexpr int REGS_LOW = 88;
+    static constexpr int REGS_HIGH = 168;
     static_assert((REGS_LOW + REGS_HIGH) * 256 == 65536, "register split must fill the register file");
     static_assert(kTileN + STAGES * SF_COLS <= TMEM_COLS, "TMEM overflow");
     static_assert(OFF_EPI % 1024 == 0, "staging alignment (swizzled store boxes)");
     static_assert(SMEM <= 232448, "shared memory budget");
+    // experts whose prefixes still fit
+    static constexpr int MAX_E = (232448 - SMEM) / 8 - 1;
 };
+
+// One CTA's share of a pair tile.
+struct PairTile {
+    int64_t a_row0;  // this CTA's first row of A and of the output
+    int rows_valid;  // of its 128 rows, those inside the problem (grouped: inside the expert); <= 0: none
+    int sfa_rt;      // its 128-row scale tile of A
+    int n0;          // first output column
+    int expert;
+};
+
+template <bool kGrouped>
+__device__ __forceinline__ PairTile pair_tile(int t, int rank, const PairParams& p, const int32_t* tiles_before,
+                                              const int32_t* pairs_before)
+{
+    PairTile T;
+    if constexpr (kGrouped) {
+        // the expert holding pair tile t: pairs_before[lo] * nt <= t < pairs_before[lo + 1] * nt
+        const int nt = p.n_tiles;
+        int lo = 0, hi = p.E;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pairs_before[mid] * nt <= t)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int pt = pairs_before[lo + 1] - pairs_before[lo];
+        const int local = t - pairs_before[lo] * nt;
+        const int gl = 2 * (local % pt) + rank;  // this CTA's 128-row tile of the expert
+        int start, rows;
+        group_rows(p.offsets, lo, p.M, &start, &rows);
+        T.expert = lo;
+        T.n0 = (local / pt) * kTileN;
+        T.a_row0 = start + static_cast<int64_t>(gl) * kRows;
+        T.rows_valid = min(rows - gl * kRows, kRows);
+        T.sfa_rt = min(tiles_before[lo] + gl, p.sfa_tiles - 1);  // inside the scale array whatever the offsets
+    } else {
+        const int mp = t % p.m_pairs;
+        T.expert = 0;
+        T.n0 = (t / p.m_pairs) * kTileN;
+        T.sfa_rt = 2 * mp + rank;
+        T.a_row0 = static_cast<int64_t>(T.sfa_rt) * kRows;
+        T.rows_valid = min(p.M - T.sfa_rt * kRows, kRows);
+    }
+    return T;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
@@ -113,7 +179,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int KC, int STAGES>
+template <int KC, int STAGES, bool kGrouped>
 __global__ void __launch_bounds__(512, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmO, const PairParams p)
@@ -127,6 +193,8 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t* accum_full = sf_full + STAGES;                          // the tile's accumulator is complete
     uint64_t* accum_empty = accum_full + 1;                           // leader: both epilogues hold it
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SLOT);
+    int32_t* tiles_before = reinterpret_cast<int32_t*>(smem + C::OFF_PREFIX);  // grouped: [E + 1]
+    int32_t* pairs_before = tiles_before + (kGrouped ? p.E + 1 : 0);          // grouped: [E + 1]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -134,7 +202,7 @@ __global__ void __launch_bounds__(512, 1)
     const bool leader = rank == 0;
     const int pair = static_cast<int>(blockIdx.x >> 1);
     const int pairs = static_cast<int>(gridDim.x >> 1);
-    const int total = p.m_pairs * p.n_tiles;
+    const int rk = static_cast<int>(rank);
     const int nkb = (p.kb4 + C::GROUPS - 1) / C::GROUPS;  // stages per tile
 
     if (warp == 0 && lane == 0) {
@@ -160,6 +228,45 @@ __global__ void __launch_bounds__(512, 1)
     tc_fence_after_sync();
     grid_dependency_wait();
     launch_dependents();
+    if constexpr (kGrouped) {
+        if (warp == 2) {
+            // exclusive prefixes of the experts' 128-row tile and pair-tile counts
+            int carry_t = 0, carry_p = 0;
+            for (int base = 0; base <= p.E; base += 32) {
+                const int e = base + lane;
+                int mt = 0;
+                if (e < p.E) {
+                    int start, rows;
+                    group_rows(p.offsets, e, p.M, &start, &rows);
+                    mt = (rows + kRows - 1) / kRows;
+                }
+                const int pt = (mt + 1) >> 1;
+                int it = mt, ip = pt;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int vt = __shfl_up_sync(0xFFFFFFFFu, it, d);
+                    const int vp = __shfl_up_sync(0xFFFFFFFFu, ip, d);
+                    if (lane >= d) {
+                        it += vt;
+                        ip += vp;
+                    }
+                }
+                if (e <= p.E) {
+                    tiles_before[e] = carry_t + it - mt;
+                    pairs_before[e] = carry_p + ip - pt;
+                }
+                carry_t += __shfl_sync(0xFFFFFFFFu, it, 31);
+                carry_p += __shfl_sync(0xFFFFFFFFu, ip, 31);
+            }
+        }
+        __syncthreads();
+    }
+    // pair tiles of the problem (grouped: read from shared memory where needed, so
+    // that no extra value stays live into the register-split roles)
+    auto total_tiles = [&]() {
+        return kGrouped ? *reinterpret_cast<volatile int32_t*>(pairs_before + p.E) * p.n_tiles
+                        : p.m_pairs * p.n_tiles;
+    };
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t limit = p.wait_ns;
 
@@ -175,10 +282,9 @@ __global__ void __launch_bounds__(512, 1)
             const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
             uint32_t it = 0;
             bool ok = true;
-            for (int t = pair; t < total && ok; t += pairs) {
-                const int mp = t % p.m_pairs;
-                const int n0 = (t / p.m_pairs) * kTileN;
-                const int row0 = (is_a ? mp * 256 : n0) + kRows * static_cast<int>(rank);
+            for (int t = pair; t < total_tiles() && ok; t += pairs) {
+                const PairTile T = pair_tile<kGrouped>(t, rk, p, tiles_before, pairs_before);
+                const int row0 = is_a ? static_cast<int>(T.a_row0) : T.expert * p.N + T.n0 + kRows * rk;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = static_cast<int>(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -203,7 +309,7 @@ __global__ void __launch_bounds__(512, 1)
                 constexpr uint32_t idesc = idesc_mxf4(2 * kRows, kTileN);
                 uint32_t it = 0, tcount = 0;
                 bool ok = true;
-                for (int t = pair; t < total && ok; t += pairs) {
+                for (int t = pair; t < total_tiles() && ok; t += pairs) {
                     // both epilogues must hold the previous tile's accumulator
                     if (!mbar_wait_bounded(accum_empty, (tcount & 1u) ^ 1u, p.status, kStatusTimeout, limit)) {
                         ok = false;
@@ -251,14 +357,15 @@ __global__ void __launch_bounds__(512, 1)
             const uint32_t sf_full_leader = mapa_shared(smem_u32(sf_full), 0);
             uint32_t it = 0;
             bool ok = true;
-            for (int t = pair; t < total && ok; t += pairs) {
-                const int mp = t % p.m_pairs;
-                const int n0 = (t / p.m_pairs) * kTileN;
-                const int sfa_rt = 2 * mp + static_cast<int>(rank);
-                const bool has_sfa = sfa_rt < p.sfa_tiles;
+            for (int t = pair; t < total_tiles() && ok; t += pairs) {
+                const PairTile T = pair_tile<kGrouped>(t, rk, p, tiles_before, pairs_before);
+                const int n0 = T.n0;
+                // rows past the problem (the expert) get zero scales; their outputs are not stored
+                const bool has_sfa = T.rows_valid > 0;
                 const int nsfb = min(2, p.sfb_tiles - n0 / 128);
-                const uint8_t* sfa = p.sfa + static_cast<int64_t>(has_sfa ? sfa_rt : 0) * p.kb4 * 512 + lane * 16;
-                const uint8_t* sfb0 = p.sfb + static_cast<int64_t>(n0 / 128) * p.kb4 * 512 + lane * 16;
+                const uint8_t* sfa = p.sfa + static_cast<int64_t>(has_sfa ? T.sfa_rt : 0) * p.kb4 * 512 + lane * 16;
+                const uint8_t* sfb0 = p.sfb + T.expert * p.sfb_expert_stride +
+                                      static_cast<int64_t>(n0 / 128) * p.kb4 * 512 + lane * 16;
                 const uint8_t* sfb1 = sfb0 + (nsfb > 1 ? static_cast<int64_t>(p.kb4) * 512 : 0);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = static_cast<int>(it % STAGES);
@@ -309,10 +416,14 @@ __global__ void __launch_bounds__(512, 1)
         const int rot = lane & 7;  // 128-byte swizzle of the store box: 16-byte piece q of row i at q ^ (i % 8)
         uint32_t tcount = 0;
         bool stored = false;
-        for (int t = pair; t < total; t += pairs) {
-            const int mp = t % p.m_pairs;
-            const int n0 = (t / p.m_pairs) * kTileN;
-            const int row0 = mp * 256 + kRows * static_cast<int>(rank) + quad * 32;
+        for (int t = pair; t < total_tiles(); t += pairs) {
+            const PairTile T = pair_tile<kGrouped>(t, rk, p, tiles_before, pairs_before);
+            const int n0 = T.n0;
+            const int row0 = static_cast<int>(T.a_row0) + quad * 32;
+            // rows of this warp's 32 that belong to the expert (dense: rows past M are
+            // clipped by the store itself)
+            const int rv = kGrouped ? T.rows_valid - quad * 32 : 32;
+            const __nv_bfloat16* bias = p.bias ? p.bias + static_cast<int64_t>(T.expert) * p.N : nullptr;
             const bool ok = mbar_wait_bounded(accum_full, tcount & 1u, p.status, kStatusTimeout, limit);
             tc_fence_after_sync();
             uint32_t v[CW];
@@ -327,20 +438,25 @@ __global__ void __launch_bounds__(512, 1)
             ++tcount;
             if (!ok)
                 break;
+            if (rv <= 0)
+                continue;
+            const bool whole = rv >= 32;
 #pragma unroll
             for (int c = 0; c < CW; c += kChunk) {
                 const int col0 = n0 + half * CW + c;
-                if (lane == 0 && stored)
-                    bulk_wait_group_read0();  // the previous box has left the staging area
-                __syncwarp();
+                if (whole) {
+                    if (lane == 0 && stored)
+                        bulk_wait_group_read0();  // the previous box has left the staging area
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int j = 0; j < kChunk; j += 8) {
                     float f[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         f[i] = __uint_as_float(v[c + j + i]);
-                    if (p.bias && col0 + j < p.N) {
-                        const uint4 bb = *reinterpret_cast<const uint4*>(p.bias + col0 + j);
+                    if (bias && col0 + j < p.N) {
+                        const uint4 bb = *reinterpret_cast<const uint4*>(bias + col0 + j);
                         const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
@@ -350,14 +466,19 @@ __global__ void __launch_bounds__(512, 1)
                     }
                     const uint4 o = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                                                pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-                    *reinterpret_cast<uint4*>(my_row + (((j >> 3) ^ rot) << 4)) = o;
+                    if (whole)
+                        *reinterpret_cast<uint4*>(my_row + (((j >> 3) ^ rot) << 4)) = o;
+                    else if (lane < rv && col0 + j < p.N)
+                        *reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(row0 + lane) * p.N + col0 + j) = o;
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&tmO, stg, col0, row0);
-                    bulk_commit_group();
-                    stored = true;
+                if (whole) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmO, stg, col0, row0);
+                        bulk_commit_group();
+                        stored = true;
+                    }
                 }
             }
         }
@@ -375,31 +496,45 @@ __global__ void __launch_bounds__(512, 1)
     }
 }
 
-template <int KC, int STAGES>
+template <int KC, int STAGES, bool kGrouped>
 cudaError_t launch_pair(const GemmArgs& a, cudaStream_t stream)
 {
     using C = PairCfg<KC, STAGES>;
+    const int E = kGrouped ? a.E : 1;
+    if (kGrouped && E > C::MAX_E)
+        return cudaErrorInvalidValue;
     CUtensorMap tmA, tmB, tmO;
     if (!make_operand_map(&tmA, a.a, a.M, a.K, kRows, KC, kOpFp4Packed) ||
-        !make_operand_map(&tmB, a.b, a.N, a.K, kRows, KC, kOpFp4Packed) ||
+        !make_operand_map(&tmB, a.b, static_cast<int64_t>(E) * a.N, a.K, kRows, KC, kOpFp4Packed) ||
         !make_output_map(&tmO, a.out, a.M, a.N, C::CHUNK, 32, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     PairParams p;
     p.sfa = a.sa;
     p.sfb = a.sb;
     p.bias = static_cast<const __nv_bfloat16*>(a.bias);
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.offsets = a.row_offsets;
+    p.E = E;
+    p.sfb_expert_stride = (a.N + 127) / 128 * 128 * (a.K / 32);
+    p.M = static_cast<int>(a.M);
     p.N = static_cast<int>(a.N);
     p.kb4 = static_cast<int>(a.K / 128);
     p.m_pairs = static_cast<int>((a.M + 255) / 256);
     p.n_tiles = static_cast<int>((a.N + kTileN - 1) / kTileN);
-    p.sfa_tiles = static_cast<int>((a.M + 127) / 128);
+    // grouped: the scale row tiles fp4_sf_bytes_grouped provides for
+    p.sfa_tiles = static_cast<int>(kGrouped ? (a.M + static_cast<int64_t>(E) * 127) / 128 : (a.M + 127) / 128);
     p.sfb_tiles = static_cast<int>((a.N + 127) / 128);
     p.wait_ns = a.wait_ns;
     p.status = a.status;
-    const int64_t total = static_cast<int64_t>(p.m_pairs) * p.n_tiles;
+    // grouped: the pair tiles are counted on the device; at most one partial
+    // pair tile per expert beyond the dense count
+    const int64_t total = static_cast<int64_t>(p.m_pairs + (kGrouped ? E : 0)) * p.n_tiles;
     if (total == 0)
         return cudaSuccess;
-    auto kern = gemm_pair_kernel<KC, STAGES>;
+    auto kern = gemm_pair_kernel<KC, STAGES, kGrouped>;
+    // grouped: the shared-memory opt-in covers the prefixes of MAX_E experts
+    constexpr int kSmemMax = C::SMEM + (kGrouped ? 8 * (C::MAX_E + 1) : 0);
+    const int smem = C::SMEM + (kGrouped ? 8 * (E + 1) : 0);
     // per device, once: the shared-memory opt-in, the register split check
     // (setmaxnreg.inc waits until the registers it asks for are free: never
     // launch a split the launch's allocation cannot cover) and the number of
@@ -417,7 +552,7 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t stream)
         const unsigned long long ctx = current_context_id();
         if (resident_pairs[dev] == 0 || configured_ctx[dev] != ctx) {
             configured_ctx[dev] = ctx;
-            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+            err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
             if (err != cudaSuccess)
                 return err;
             cudaFuncAttributes fa;
@@ -430,7 +565,7 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t stream)
             cudaLaunchConfig_t q = {};
             q.gridDim = dim3(2);
             q.blockDim = dim3(C::THREADS);
-            q.dynamicSmemBytes = C::SMEM;
+            q.dynamicSmemBytes = kSmemMax;
             cudaLaunchAttribute qa[1];
             qa[0].id = cudaLaunchAttributeClusterDimension;
             qa[0].val.clusterDim.x = 2;
@@ -449,7 +584,7 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t stream)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -468,9 +603,15 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t stream)
 cudaError_t launch_gemm_pair(const GemmArgs& a, cudaStream_t stream)
 {
     // stages of two slabs need the 3-D operand view (K % 256 == 0)
-    if (FP4_PAIR_KC == 2 && a.K % 256 == 0)
-        return launch_pair<2, 3>(a, stream);
-    return launch_pair<1, 6>(a, stream);
+    const bool kc2 = FP4_PAIR_KC == 2 && a.K % 256 == 0;
+    if (a.row_offsets != nullptr)
+        return kc2 ? launch_pair<2, 3, true>(a, stream) : launch_pair<1, 6, true>(a, stream);
+    return kc2 ? launch_pair<2, 3, false>(a, stream) : launch_pair<1, 6, false>(a, stream);
+}
+
+int gemm_pair_max_experts()
+{
+    return std::min(PairCfg<2, 3>::MAX_E, PairCfg<1, 6>::MAX_E);
 }
 
 }  // namespace fp4lin

@@ -149,9 +149,11 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
 
-// Dense MXFP4 GEMM on 256 x 256 output tiles computed by CTA pairs
-// (tcgen05 cta_group::2); used by launch_gemm for large M and N.
+// MXFP4 GEMM on 256 x 256 output tiles computed by CTA pairs (tcgen05
+// cta_group::2), dense or grouped (row_offsets set, E <= gemm_pair_max_experts());
+// used by launch_gemm for large problems.
 cudaError_t launch_gemm_pair(const GemmArgs& args, cudaStream_t stream);
+int gemm_pair_max_experts();
 
 // Host helpers shared by the GEMM translation units (gemm.cu).
 // Operand kinds of make_operand_map.

@@ -561,15 +561,18 @@ __global__ void __launch_bounds__(kThreads) smooth_prepare_kernel(const float* _
 // prefix of the groups' tile counts, 32 groups at a time, and a ballot for
 // the group whose range holds the tile.  Returns -1 past the last group;
 // *first_tile is the group's first tile.  Every lane passes the same tile.
-__device__ __forceinline__ int group_of_tile(const int32_t* offsets, int E, int tile, int* first_tile)
+__device__ __forceinline__ int group_of_tile(const int32_t* offsets, int E, int total, int tile, int* first_tile)
 {
     const int lane = threadIdx.x & 31;
     int carry = 0;
     for (int base = 0; base < E; base += 32) {
         const int e = base + lane;
         int t = 0;
-        if (e < E)
-            t = (__ldg(offsets + e + 1) - __ldg(offsets + e) + 127) >> 7;
+        if (e < E) {
+            int start, rows;
+            group_rows(offsets, e, total, &start, &rows);
+            t = (rows + 127) >> 7;
+        }
         int incl = t;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -617,11 +620,13 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
         // the group whose padded tile range holds this scale row (each warp
         // finds it itself: no block-wide prefix and barrier)
         int first_tile = 0;
-        const int grp = group_of_tile(offsets, E, static_cast<int>(srow >> 7), &first_tile);
+        const int grp = group_of_tile(offsets, E, static_cast<int>(M), static_cast<int>(srow >> 7), &first_tile);
         if (grp < 0)
             return;
         const int64_t local = srow - static_cast<int64_t>(first_tile) * 128;
-        const int64_t start = __ldg(offsets + grp), rows_e = __ldg(offsets + grp + 1) - start;
+        int start_i, rows_i;
+        group_rows(offsets, grp, static_cast<int>(M), &start_i, &rows_i);
+        const int64_t start = start_i, rows_e = rows_i;
         row_real = local < rows_e;
         xrow = start + local;
     }

@@ -164,6 +164,23 @@ def test_grouped_gemm(orc, L, counts, N, K, with_bias):
     _grouped_case(orc, L, counts, N, K, with_bias, seed=len(counts) + N)
 
 
+@pytest.mark.parametrize("counts,N,K,with_bias", [
+    ([300, 0, 1, 257, 1000, 129, 640, 0, 77, 512], 2048, 512, True),
+    ([256, 130, 513, 0, 700, 1200, 300], 1544, 384, False),
+])
+def test_grouped_gemm_on_cta_pairs(orc, L, counts, N, K, with_bias):
+    """Grouped problems large enough for the CTA-pair path (256 x 256 tiles
+    of one expert on two SMs): experts with an odd number of 128-row tiles
+    (the second CTA of the last pair tile lies past the expert), a one-row
+    expert, empty experts, row counts that end inside a 32-row store box
+    (stored row by row), a ragged last column tile, one- and two-slab
+    stages; every row compared."""
+    E = len(counts)
+    m_tiles = (sum(counts) + E * 127) // 128
+    assert N >= 256 and m_tiles * (-(-N // 256)) >= 148, "shape must take the pair path"
+    _grouped_case(orc, L, counts, N, K, with_bias, seed=E * 1000 + K)
+
+
 # ---------------------------------------------------------------- full sizes
 @pytest.mark.slow
 def test_full_decode_workload_gemm(orc, L):
