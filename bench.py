@@ -505,8 +505,10 @@ KERNEL_NAMES = {"gemm": "gemm_fp4_kernel", "requant": "requant_flat_kernel", "ac
 
 def gemm_kernel_name(workload):
     """The GEMM kernel the library launches for the workload's batches: the
-    CTA-pair kernel for the prefill batches (M >= 256 filling the GPU)."""
-    return "gemm_pair_kernel" if workload == "prefill" else "gemm_fp4_kernel"
+    CTA-pair kernel for the prefill batches (M >= 256 filling the GPU) and
+    for the MoE projections (grouped, 64 experts, filling the GPU); the
+    single-CTA kernel (weights on the MMA-M side) for decode."""
+    return "gemm_pair_kernel" if workload in ("prefill", "moe") else "gemm_fp4_kernel"
 
 
 def run_ours(args):
