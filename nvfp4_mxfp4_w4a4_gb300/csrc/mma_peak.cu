@@ -7,6 +7,8 @@
 //   kind 1  tcgen05.mma kind::mxf4nvf4  scale_vec::2X, UE8M0 scales (block 32)
 //   kind 2  tcgen05.mma kind::mxf4nvf4  scale_vec::4X, UE8M0 scales (block 16)
 //   kind 3  tcgen05.mma kind::mxf4nvf4  scale_vec::4X, UE4M3 scales (block 16, NVFP4)
+// and, for the W4A8 path, kind 4: tcgen05.mma kind::mxf8f6f4 scale_vec::1X
+// with E4M3 A and E2M1 B (UE8M0 scales, block 32; K = 32 per instruction).
 // and two CTA groupings: cta_group::1 (one SM, 128 x N x 64 per instruction)
 // or cta_group::2 (a cluster of two CTAs on two SMs, 256 x N x 64 per
 // instruction, issued by the even CTA).
@@ -97,7 +99,10 @@ template <int KIND, int CTAG>
 __device__ __forceinline__ void probe_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sfa,
                                           uint32_t sfb)
 {
-    if constexpr (CTAG == 1) {
+    if constexpr (KIND == 4) {
+        static_assert(CTAG == 1, "the W4A8 form is probed on one SM");
+        FP4_PROBE_MMA("1", "mxf8f6f4.block_scale.scale_vec::1X");
+    } else if constexpr (CTAG == 1) {
         if constexpr (KIND == 0)
             FP4_PROBE_MMA("1", "mxf4.block_scale.scale_vec::2X");
         else if constexpr (KIND == 1)
@@ -119,6 +124,8 @@ __device__ __forceinline__ void probe_mma(uint32_t d, uint64_t ad, uint64_t bd, 
 // scale type (bit 23: 1 = UE8M0, 0 = UE4M3), M >> 4 (24-28).
 __host__ __device__ constexpr uint32_t probe_idesc(int kind, uint32_t m, uint32_t n)
 {
+    if (kind == 4)  // E4M3 A (type 0), E2M1 B (type 5), UE8M0 scales
+        return (0u << 7) | (5u << 10) | ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24);
     return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((kind == 3 ? 0u : 1u) << 23) | ((m >> 4) << 24);
 }
 
@@ -170,7 +177,9 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int mmas_pe
                 probe_cp<CTAG>(sfb_t + 8 * (it & 1), smem_desc(sf_s + 1024, 0, 128, 0));
             }
             for (int k = 0; k < mmas_per_group; ++k) {
-                const uint32_t sel = KIND >= 2 ? 0u : static_cast<uint32_t>(k & 1) * 2u;
+                // scale selector: two scales per K = 64 step (2X), one per K = 32 step (1X: byte k % 4)
+                const uint32_t sel = KIND == 4 ? static_cast<uint32_t>(k & 3)
+                                               : (KIND >= 2 ? 0u : static_cast<uint32_t>(k & 1) * 2u);
                 const uint32_t d = tmem + ((alt && (k & 1)) ? 128u : 0u);
                 probe_mma<KIND, CTAG>(d, smem_desc(a_s + 32 * (k & 3), 16, 1024, 2),
                                       smem_desc(b_s + 32 * (k & 3), 16, 1024, 2),
@@ -219,7 +228,8 @@ cudaError_t run_probe(int iters, int mmas_per_group, int with_cp, int alt, int n
 }  // namespace
 }  // namespace fp4lin
 
-// kind: 0..3 as above; ctag: 1 or 2; n: 64, 128 or 256.  cycles_dev holds
+// kind: 0..4 as above; ctag: 1 or 2 (kind 4: 1); n: 128 or 256, and 16, 32
+// or 64 for kinds 0 and 4 on one SM (the decode tile widths).  cycles_dev holds
 // one entry per issuing CTA (num_ctas / ctag).  Returns a cudaError_t.
 extern "C" __attribute__((visibility("default"))) int fp4_mma_peak_probe2(int kind, int ctag, int n, int iters,
                                                                         int mmas_per_group, int with_cp, int alt,
@@ -243,6 +253,14 @@ extern "C" __attribute__((visibility("default"))) int fp4_mma_peak_probe2(int ki
     FP4_PEAK_KIND(1)
     FP4_PEAK_KIND(2)
     FP4_PEAK_KIND(3)
+    FP4_PEAK_CASE(0, 1, 16)
+    FP4_PEAK_CASE(0, 1, 32)
+    FP4_PEAK_CASE(0, 1, 64)
+    FP4_PEAK_CASE(4, 1, 16)
+    FP4_PEAK_CASE(4, 1, 32)
+    FP4_PEAK_CASE(4, 1, 64)
+    FP4_PEAK_CASE(4, 1, 128)
+    FP4_PEAK_CASE(4, 1, 256)
 #undef FP4_PEAK_KIND
 #undef FP4_PEAK_CASE
     return static_cast<int>(cudaErrorInvalidValue);

@@ -9,6 +9,7 @@ KINDS = {
     1: "kind::mxf4nvf4 scale_vec::2X (UE8M0, block 32)",
     2: "kind::mxf4nvf4 scale_vec::4X (UE8M0, block 16)",
     3: "kind::mxf4nvf4 scale_vec::4X (UE4M3, block 16)",
+    4: "kind::mxf8f6f4 scale_vec::1X (E4M3 x E2M1, UE8M0, block 32; K = 32)",
 }
 
 _lib = None
@@ -58,22 +59,27 @@ def measure(n: int = 256, iters: int = 4000, mmas_per_group: int = 4, with_cp: b
             best = ms
             cyc = float(cycles.float().mean())
     mmas = iters * mmas_per_group
-    flops = 2.0 * 128 * ctag * n * 64 * mmas * (ctas // ctag)
+    k = 32 if kind == 4 else 64  # K per instruction
+    flops = 2.0 * 128 * ctag * n * k * mmas * (ctas // ctag)
     return {"kind": KINDS[kind], "cta_group": ctag, "n": n, "with_cp": with_cp, "alt_accumulators": alt,
             "tflops": flops / (best * 1e-3) / 1e12, "cycles_per_mma": cyc / mmas, "ms": best, "sms": ctas}
 
 
 def sweep():
     """Every form at N = 256 on both CTA groupings, plus N = 128 with one and
-    two accumulators (cta_group::1)."""
+    two accumulators (cta_group::1); the decode tile widths N = 16, 32, 64
+    for kind::mxf4 and for the W4A8 form kind::mxf8f6f4 (cta_group::1)."""
     rows = []
-    for kind in KINDS:
+    for kind in (0, 1, 2, 3):
         for ctag in (1, 2):
             rows.append(measure(n=256, kind=kind, ctag=ctag))
         for alt in (False, True):
             rows.append(measure(n=128, kind=kind, ctag=1, alt=alt))
     rows.append(measure(n=256, kind=0, ctag=1, with_cp=True))
     rows.append(measure(n=256, kind=1, ctag=2, with_cp=True))
+    for kind in (0, 4):
+        for n in (16, 32, 64) + ((128, 256) if kind == 4 else ()):
+            rows.append(measure(n=n, kind=kind, ctag=1))
     return rows
 
 
