@@ -38,7 +38,8 @@
 //               ahead of time, waits until the stage's TMEM scale columns are
 //               free, writes them into its quarter of the TMEM lanes with
 //               tcgen05.st (the layout a 32x128b.warpx4 copy would produce)
-//               and arrives on the leader's sf_full;
+//               and arrives on the leader's full barrier of the stage, so
+//               that the MMA thread waits once per stage;
 //   warp 7      idle (it completes the 8-warp low-register half);
 //   warps 8-15  epilogue of the CTA's 128 rows: read the accumulator, release
 //               it (arrive on the leader's accum_empty) so the next tile's
@@ -107,7 +108,7 @@ struct PairCfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * EPI_WARP_BYTES;
-    static constexpr int NUM_BARS = 3 * STAGES + 2;
+    static constexpr int NUM_BARS = 2 * STAGES + 2;
     static constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_PREFIX = OFF_SLOT + 16;   // grouped: 2 (E + 1) int32
     static constexpr int SMEM = OFF_PREFIX + 1024;     // + 1 KB alignment slack (+ the prefixes when grouped)
@@ -187,10 +188,10 @@ __global__ void __launch_bounds__(512, 1)
     using C = PairCfg<KC, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);  // leader: A and B of both CTAs landed
-    uint64_t* empty = full + STAGES;                                  // stage consumed by the pair's MMAs
-    uint64_t* sf_full = empty + STAGES;                               // leader: scales in both CTAs' TMEM
-    uint64_t* accum_full = sf_full + STAGES;                          // the tile's accumulator is complete
+    // leader: A and B of both CTAs landed and the scales are in both CTAs' TMEM
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    uint64_t* empty = full + STAGES;       // stage consumed by the pair's MMAs
+    uint64_t* accum_full = empty + STAGES;  // the tile's accumulator is complete
     uint64_t* accum_empty = accum_full + 1;                           // leader: both epilogues hold it
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_SLOT);
     int32_t* tiles_before = reinterpret_cast<int32_t*>(smem + C::OFF_PREFIX);  // grouped: [E + 1]
@@ -207,9 +208,8 @@ __global__ void __launch_bounds__(512, 1)
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 1 + 8);  // the leader's A producer (with the bytes) + 4 scale warps x 2 CTAs
             mbar_init(&empty[s], 1);
-            mbar_init(&sf_full[s], 8);  // 4 scale warps x 2 CTAs
         }
         mbar_init(accum_full, 1);
         mbar_init(accum_empty, 2 * kEpiWarps);
@@ -307,6 +307,8 @@ __global__ void __launch_bounds__(512, 1)
             if (leader && lane == 0) {
                 // --------------------------------------------------- MMA issuer
                 constexpr uint32_t idesc = idesc_mxf4(2 * kRows, kTileN);
+                const uint64_t a_desc = smem_desc(smem_u32(smem + C::OFF_A), 16, 1024, 2);
+                const uint64_t b_desc = smem_desc(smem_u32(smem + C::OFF_B), 16, 1024, 2);
                 uint32_t it = 0, tcount = 0;
                 bool ok = true;
                 for (int t = pair; t < total_tiles() && ok; t += pairs) {
@@ -319,26 +321,35 @@ __global__ void __launch_bounds__(512, 1)
                     for (int kb = 0; kb < nkb; ++kb, ++it) {
                         const int s = static_cast<int>(it % STAGES);
                         const uint32_t ph = (it / STAGES) & 1u;
-                        if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, limit) ||
-                            !mbar_wait_bounded(&sf_full[s], ph, p.status, kStatusTimeout, limit)) {
+                        if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, limit)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after_sync();
-                        const int groups = min(C::GROUPS, p.kb4 - C::GROUPS * kb);
+                        // this one thread's instruction stream paces the tensor pipe:
+                        // descriptors are the stage's base plus constant offsets
                         const uint32_t sfa_t = tmem_base + kTileN + s * C::SF_COLS;
                         const uint32_t sfb_t = sfa_t + C::SF_COLS_A;
-                        const uint32_t a_s = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
-                        const uint32_t b_s = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
-                        for (int k = 0; k < 2 * groups; ++k) {
-                            // k-th MMA (K = 64): slab k / 4, 32-byte column k % 4;
-                            // scale chunk k / 2, bytes 2 (k % 2) and 2 (k % 2) + 1
-                            const int slab = k >> 2;
-                            const int g = k >> 1;
-                            const uint64_t ad = smem_desc(a_s + slab * (kRows * kSlab) + 32 * (k & 3), 16, 1024, 2);
-                            const uint64_t bd = smem_desc(b_s + slab * (kRows * kSlab) + 32 * (k & 3), 16, 1024, 2);
-                            tc_mma_mxf4_pair(tmem_base, ad, bd, idesc_with_sf_id(idesc, static_cast<uint32_t>(k & 1) * 2u),
-                                             sfa_t + 4 * g, sfb_t + 8 * g, (kb | k) != 0 ? 1u : 0u);
+                        const uint64_t ad0 = a_desc + static_cast<uint32_t>((s * C::A_BYTES) >> 4);
+                        const uint64_t bd0 = b_desc + static_cast<uint32_t>((s * C::B_BYTES) >> 4);
+                        if (C::GROUPS * (kb + 1) <= p.kb4) {
+#pragma unroll
+                            for (int k = 0; k < 2 * C::GROUPS; ++k) {
+                                // k-th MMA (K = 64): slab k / 4, 32-byte column k % 4;
+                                // scale chunk k / 2, bytes 2 (k % 2) and 2 (k % 2) + 1
+                                const uint32_t off = ((k >> 2) * (kRows * kSlab) + 32 * (k & 3)) >> 4;
+                                tc_mma_mxf4_pair(tmem_base, ad0 + off, bd0 + off,
+                                                 idesc_with_sf_id(idesc, static_cast<uint32_t>(k & 1) * 2u),
+                                                 sfa_t + 4 * (k >> 1), sfb_t + 8 * (k >> 1), (kb | k) != 0 ? 1u : 0u);
+                            }
+                        } else {
+                            const int groups = p.kb4 - C::GROUPS * kb;  // the last, partial stage of K
+                            for (int k = 0; k < 2 * groups; ++k) {
+                                const uint32_t off = ((k >> 2) * (kRows * kSlab) + 32 * (k & 3)) >> 4;
+                                tc_mma_mxf4_pair(tmem_base, ad0 + off, bd0 + off,
+                                                 idesc_with_sf_id(idesc, static_cast<uint32_t>(k & 1) * 2u),
+                                                 sfa_t + 4 * (k >> 1), sfb_t + 8 * (k >> 1), (kb | k) != 0 ? 1u : 0u);
+                            }
                         }
                         tc_commit_pair_multicast(&empty[s], 0x3);
                     }
@@ -354,7 +365,7 @@ __global__ void __launch_bounds__(512, 1)
             // 32x128b.warpx4 copy would place in each 32-lane quarter.  The
             // chunks of a stage are loaded before the wait for its columns.
             const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-            const uint32_t sf_full_leader = mapa_shared(smem_u32(sf_full), 0);
+            const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
             uint32_t it = 0;
             bool ok = true;
             for (int t = pair; t < total_tiles() && ok; t += pairs) {
@@ -398,7 +409,7 @@ __global__ void __launch_bounds__(512, 1)
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive_cluster(sf_full_leader + 8u * static_cast<uint32_t>(s));
+                        mbar_arrive_cluster(full_leader + 8u * static_cast<uint32_t>(s));
                 }
             }
         }
