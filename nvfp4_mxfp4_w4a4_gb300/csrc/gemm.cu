@@ -520,6 +520,10 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                                            : kA8 ? idesc_mxf8f6f4(BM, BN, kSwap ? kTypeE2M1 : kTypeE4M3,
                                                                   kSwap ? kTypeE4M3 : kTypeE2M1)
                                                  : idesc_mxf4(BM, BN);
+                // this one thread's instruction stream paces the tensor pipe: one
+                // barrier wait per stage, descriptors from the stage's base
+                const uint64_t a_desc = smem_desc(smem_u32(smem + C::OFF_A), 16, 1024, 2);
+                const uint64_t b_desc = smem_desc(smem_u32(smem + C::OFF_B), 16, 1024, 2);
                 uint32_t it = 0, tcount = 0, pc = 0;
                 bool ok = true;
                 WorkIter wi = work_begin(p, total_tiles);
@@ -539,8 +543,9 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                     for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                         const int s = static_cast<int>(it % STAGES);
                         const uint32_t ph = (it / STAGES) & 1u;
-                        if (!mbar_wait_bounded(&full[s], ph, p.status, kStatusTimeout, p.wait_ns) ||
-                            !mbar_wait_bounded(&sf_full[s], ph, p.status, kStatusTimeout, p.wait_ns)) {
+                        // the scale movers copy a stage's scales only after its full
+                        // barrier, so its sf_full barrier implies both
+                        if (!mbar_wait_bounded(&sf_full[s], ph, p.status, kStatusTimeout, p.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -560,16 +565,17 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                         }
                         const uint32_t sfa_t = tmem_base + (C::kDual ? 2 : 1) * BN + s * C::SF_COLS;
                         const uint32_t sfb_t = sfa_t + C::SF_COLS_A;
-                        const uint32_t a_s = smem_u32(smem + C::OFF_A + s * C::A_BYTES);
-                        const uint32_t b_s = smem_u32(smem + C::OFF_B + s * C::B_BYTES);
-                        for (int k = 0; k < C::MMAS_PER_GROUP * groups; ++k) {
-                            // k-th MMA: slab k / 4, 32-byte column k % 4 (64 FP4 or 32 byte
-                            // elements); scale chunk k / 2 (MXFP4: bytes 2 (k % 2), +1 of it),
-                            // k (NVFP4: all four bytes) or k / 4 (W4A8: byte k % 4)
+                        const uint64_t ad0 = a_desc + static_cast<uint32_t>((s * C::A_BYTES) >> 4);
+                        const uint64_t bd0 = b_desc + static_cast<uint32_t>((s * C::B_BYTES) >> 4);
+                        const bool first = C::kDual || kb == w.kb0;
+                        // k-th MMA: slab k / 4, 32-byte column k % 4 (64 FP4 or 32 byte
+                        // elements); scale chunk k / 2 (MXFP4: bytes 2 (k % 2), +1 of it),
+                        // k (NVFP4: all four bytes) or k / 4 (W4A8: byte k % 4)
+                        auto mma = [&](int k) {
                             const int slab = k >> 2;
-                            const uint64_t ad = smem_desc(a_s + slab * (BM * kSlabBytes) + 32 * (k & 3), 16, 1024, 2);
-                            const uint64_t bd = smem_desc(b_s + slab * (BN * kSlabBytes) + 32 * (k & 3), 16, 1024, 2);
-                            const uint32_t acc = C::kDual ? (k != 0 ? 1u : 0u) : ((kb != w.kb0 || k != 0) ? 1u : 0u);
+                            const uint64_t ad = ad0 + static_cast<uint32_t>((slab * (BM * kSlabBytes) + 32 * (k & 3)) >> 4);
+                            const uint64_t bd = bd0 + static_cast<uint32_t>((slab * (BN * kSlabBytes) + 32 * (k & 3)) >> 4);
+                            const uint32_t acc = (first && k == 0) ? 0u : 1u;
                             if constexpr (kNv) {
                                 tc_mma_nvf4(tmem_base, ad, bd, idesc, sfa_t + 4 * k, sfb_t + k * C::SF_COLS_B_ATOM, acc);
                             } else if constexpr (kA8) {
@@ -582,6 +588,14 @@ __global__ void __launch_bounds__(Cfg<BN, STAGES, KC, CPW, kSwap, kFmt>::THREADS
                                 tc_mma_mxf4(d_tmem, ad, bd, idesc_with_sf_id(idesc, sf_id), sfa_t + 4 * g,
                                             sfb_t + g * C::SF_COLS_B_ATOM, acc);
                             }
+                        };
+                        if (groups == C::GROUPS) {
+#pragma unroll
+                            for (int k = 0; k < C::MMAS_PER_GROUP * C::GROUPS; ++k)
+                                mma(k);
+                        } else {
+                            for (int k = 0; k < C::MMAS_PER_GROUP * groups; ++k)
+                                mma(k);
                         }
                         tc_commit(&empty[s]);
                         if constexpr (C::kDual) {
