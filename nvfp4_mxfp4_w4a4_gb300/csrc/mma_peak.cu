@@ -14,11 +14,15 @@
 // instruction, issued by the even CTA).
 //
 // One thread per SM (per pair) issues a long chain of MMAs from shared memory
-// (zero operands, zero scale bytes) into TMEM and times it with the SM clock.
+// (zero operands and scale bytes, or pseudo-random operand bytes with scale
+// bytes 120..134) into TMEM and times it with the SM clock.
 // Optionally a scale-factor copy (tcgen05.cp) is issued before every group of
 // MMAs, as the GEMM main loop does, and optionally the MMAs alternate between
 // two accumulators (N <= 128), which separates the accumulator dependency
-// from the issue rate.
+// from the issue rate.  Optionally the thread also waits, after each group,
+// `waits` times on an mbarrier phase that has already completed and commits
+// to a second barrier, as a GEMM's MMA thread does once per stage: this
+// measures what the issuing thread's own instructions cost the tensor pipe.
 //
 // Exposed through its own small C entry point in a separate library, used
 // only by the benchmark.
@@ -129,9 +133,20 @@ __host__ __device__ constexpr uint32_t probe_idesc(int kind, uint32_t m, uint32_
     return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((kind == 3 ? 0u : 1u) << 23) | ((m >> 4) << 24);
 }
 
+__device__ __forceinline__ uint32_t probe_hash(uint32_t x)
+{
+    x ^= x >> 16;
+    x *= 0x7feb352du;
+    x ^= x >> 15;
+    x *= 0x846ca68bu;
+    x ^= x >> 16;
+    return x;
+}
+
 template <int KIND, int CTAG, int N>
 __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int mmas_per_group, int with_cp, int alt,
-                                                          unsigned long long* cycles, unsigned int* status)
+                                                          int waits, int fill, unsigned long long* cycles,
+                                                          unsigned int* status)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -139,12 +154,28 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int mmas_pe
     uint8_t* b = smem + 16384;                 // N rows x 128 B (cta_group::2: N / 2 rows per CTA)
     uint8_t* sf = smem + 16384 + kMaxN * 128;  // 2 KB of scale chunks
     uint64_t* bar = reinterpret_cast<uint64_t*>(sf + 2048);
-    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
-    for (int i = threadIdx.x; i < kSmemUsed / 4; i += blockDim.x)
-        reinterpret_cast<uint32_t*>(smem)[i] = 0u;
+    uint64_t* done = bar + 1;  // its phase 0 completes before the chain starts
+    uint64_t* sink = bar + 2;  // per-group commits land here; nobody waits on it
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 3);
+    for (int i = threadIdx.x; i < kSmemUsed / 4; i += blockDim.x) {
+        uint32_t v = 0u;
+        if (fill) {
+            v = probe_hash(static_cast<uint32_t>(i) * 2654435761u + blockIdx.x);
+            if (i * 4 >= 16384 + kMaxN * 128) {  // scale bytes: 120 ... 134
+                uint32_t w = 0u;
+                for (int j = 0; j < 4; ++j)
+                    w |= (120u + ((v >> (8 * j)) & 0xFFu) % 15u) << (8 * j);
+                v = w;
+            }
+        }
+        reinterpret_cast<uint32_t*>(smem)[i] = v;
+    }
     if (threadIdx.x == 0) {
         mbar_init(bar, 1);
+        mbar_init(done, 1);
+        mbar_init(sink, 1);
         fence_mbar_init();
+        mbar_arrive(done);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     const int warp = threadIdx.x >> 5;
@@ -185,6 +216,12 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int mmas_pe
                                       smem_desc(b_s + 32 * (k & 3), 16, 1024, 2),
                                       idesc | (sel << 4) | (sel << 29), sfa_t + 4 * (k & 1), sfb_t + 8 * (k & 1));
             }
+            if (waits > 0) {
+                probe_commit<CTAG>(sink);
+                for (int w = 0; w < waits; ++w)
+                    mbar_wait_bounded(done, 0, status, 1u, 1000000000ull);
+                tc_fence_after_sync();
+            }
         }
         probe_commit<CTAG>(bar);
         mbar_wait_bounded(bar, 0, status, 1u, 2000000000ull);
@@ -202,8 +239,8 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int mmas_pe
 }
 
 template <int KIND, int CTAG, int N>
-cudaError_t run_probe(int iters, int mmas_per_group, int with_cp, int alt, int num_ctas, unsigned long long* cycles,
-                      unsigned int* status, cudaStream_t s)
+cudaError_t run_probe(int iters, int mmas_per_group, int with_cp, int alt, int waits, int fill, int num_ctas,
+                      unsigned long long* cycles, unsigned int* status, cudaStream_t s)
 {
     const size_t smem = kSmemUsed + 64 + 1024;
     auto kern = mma_peak_kernel<KIND, CTAG, N>;
@@ -222,18 +259,21 @@ cudaError_t run_probe(int iters, int mmas_per_group, int with_cp, int alt, int n
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, iters, mmas_per_group, with_cp, alt, cycles, status);
+    return cudaLaunchKernelEx(&cfg, kern, iters, mmas_per_group, with_cp, alt, waits, fill, cycles, status);
 }
 
 }  // namespace
 }  // namespace fp4lin
 
 // kind: 0..4 as above; ctag: 1 or 2 (kind 4: 1); n: 128 or 256, and 16, 32
-// or 64 for kinds 0 and 4 on one SM (the decode tile widths).  cycles_dev holds
-// one entry per issuing CTA (num_ctas / ctag).  Returns a cudaError_t.
-extern "C" __attribute__((visibility("default"))) int fp4_mma_peak_probe2(int kind, int ctag, int n, int iters,
+// or 64 for kinds 0 and 4 on one SM (the decode tile widths).  waits: completed
+// barrier waits (plus one commit) per group of MMAs; fill: 1 for pseudo-random
+// operands.  cycles_dev holds one entry per issuing CTA (num_ctas / ctag).
+// Returns a cudaError_t.
+extern "C" __attribute__((visibility("default"))) int fp4_mma_peak_probe3(int kind, int ctag, int n, int iters,
                                                                         int mmas_per_group, int with_cp, int alt,
-                                                                        int num_ctas, unsigned long long* cycles_dev,
+                                                                        int waits, int fill, int num_ctas,
+                                                                        unsigned long long* cycles_dev,
                                                                         unsigned int* status_dev, void* stream)
 {
     using namespace fp4lin;
@@ -242,7 +282,7 @@ extern "C" __attribute__((visibility("default"))) int fp4_mma_peak_probe2(int ki
         return static_cast<int>(cudaErrorInvalidValue);  // two accumulators of n columns must leave room for scales
 #define FP4_PEAK_CASE(K, G, NN)                                                                     \
     if (kind == K && ctag == G && n == NN)                                                          \
-        return static_cast<int>(run_probe<K, G, NN>(iters, mmas_per_group, with_cp, alt, num_ctas, \
+        return static_cast<int>(run_probe<K, G, NN>(iters, mmas_per_group, with_cp, alt, waits, fill, num_ctas, \
                                                     cycles_dev, status_dev, s));
 #define FP4_PEAK_KIND(K)     \
     FP4_PEAK_CASE(K, 1, 128) \
@@ -264,6 +304,16 @@ extern "C" __attribute__((visibility("default"))) int fp4_mma_peak_probe2(int ki
 #undef FP4_PEAK_KIND
 #undef FP4_PEAK_CASE
     return static_cast<int>(cudaErrorInvalidValue);
+}
+
+// Without the per-group waits, zero operands.
+extern "C" __attribute__((visibility("default"))) int fp4_mma_peak_probe2(int kind, int ctag, int n, int iters,
+                                                                        int mmas_per_group, int with_cp, int alt,
+                                                                        int num_ctas, unsigned long long* cycles_dev,
+                                                                        unsigned int* status_dev, void* stream)
+{
+    return fp4_mma_peak_probe3(kind, ctag, n, iters, mmas_per_group, with_cp, alt, 0, 0, num_ctas, cycles_dev,
+                               status_dev, stream);
 }
 
 // The original entry point: kind::mxf4, cta_group::1.

@@ -22,18 +22,19 @@ def _probe():
 
         B.build()
         lib = ctypes.CDLL(B.LIB_PEAK)
-        f = lib.fp4_mma_peak_probe2
+        f = lib.fp4_mma_peak_probe3
         f.restype = ctypes.c_int
-        f.argtypes = [ctypes.c_int] * 8 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        f.argtypes = [ctypes.c_int] * 10 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         _lib = f
     return _lib
 
 
 def measure(n: int = 256, iters: int = 4000, mmas_per_group: int = 4, with_cp: bool = False, reps: int = 3,
-            kind: int = 0, ctag: int = 1, alt: bool = False):
+            kind: int = 0, ctag: int = 1, alt: bool = False, waits: int = 0, random_operands: bool = False):
     """Returns dict(tflops, cycles_per_mma, ms, ...) for MMAs of (128 ctag) x n x 64
     issued back to back by one thread per SM (per SM pair when ctag == 2) on
-    all SMs."""
+    all SMs.  waits: completed-barrier waits (and one commit) the issuing
+    thread adds after each group of mmas_per_group MMAs."""
     import torch
 
     f = _probe()
@@ -48,8 +49,8 @@ def measure(n: int = 256, iters: int = 4000, mmas_per_group: int = 4, with_cp: b
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
-        err = f(kind, ctag, n, iters, mmas_per_group, int(with_cp), int(alt), ctas, cycles.data_ptr(),
-                status.data_ptr(), s.cuda_stream)
+        err = f(kind, ctag, n, iters, mmas_per_group, int(with_cp), int(alt), waits, int(random_operands), ctas,
+                cycles.data_ptr(), status.data_ptr(), s.cuda_stream)
         b.record()
         torch.cuda.synchronize()
         if err != 0 or int(status.item()) != 0:
@@ -62,6 +63,7 @@ def measure(n: int = 256, iters: int = 4000, mmas_per_group: int = 4, with_cp: b
     k = 32 if kind == 4 else 64  # K per instruction
     flops = 2.0 * 128 * ctag * n * k * mmas * (ctas // ctag)
     return {"kind": KINDS[kind], "cta_group": ctag, "n": n, "with_cp": with_cp, "alt_accumulators": alt,
+            "mmas_per_group": mmas_per_group, "waits_per_group": waits, "random_operands": random_operands,
             "tflops": flops / (best * 1e-3) / 1e12, "cycles_per_mma": cyc / mmas, "ms": best, "sms": ctas}
 
 
@@ -80,6 +82,12 @@ def sweep():
     for kind in (0, 4):
         for n in (16, 32, 64) + ((128, 256) if kind == 4 else ()):
             rows.append(measure(n=n, kind=kind, ctag=1))
+    # operand data, and the issuing thread's own per-stage work (a GEMM stage
+    # of 8 MMAs: barrier waits that find their phase complete, one commit)
+    for ctag in (1, 2):
+        for waits in (0, 1, 2, 3, 4):
+            rows.append(measure(n=256, kind=0, ctag=ctag, mmas_per_group=8, iters=2000, waits=waits,
+                                random_operands=True))
     return rows
 
 
