@@ -201,26 +201,76 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int mmas_pe
             probe_cp<CTAG>(sfa_t + 4 * g, smem_desc(sf_s, 0, 128, 0));
         for (int g = 0; g < 8; ++g)
             probe_cp<CTAG>(sfb_t + 4 * g, smem_desc(sf_s, 0, 128, 0));
+        // every operand of the chain is formed before the clock starts, so that the
+        // issuing thread does no arithmetic per MMA (it would otherwise pace
+        // the narrower MMAs)
+        uint64_t ad[4], bd[4];
+        uint32_t id[4];
+        for (int k = 0; k < 4; ++k) {
+            ad[k] = smem_desc(a_s + 32 * k, 16, 1024, 2);
+            bd[k] = smem_desc(b_s + 32 * k, 16, 1024, 2);
+            // scale selector: two scales per K = 64 step (2X), one per K = 32 step (1X: byte k % 4)
+            const uint32_t sel = KIND == 4 ? static_cast<uint32_t>(k) : (KIND >= 2 ? 0u : static_cast<uint32_t>(k & 1) * 2u);
+            id[k] = idesc | (sel << 4) | (sel << 29);
+        }
+        const uint32_t dd[2] = {tmem, tmem + (alt ? 128u : 0u)};
+        const uint32_t sa[2] = {sfa_t, sfa_t + 4};
+        const uint32_t sb[2] = {sfb_t, sfb_t + 8};
+        auto mma = [&](int k) { probe_mma<KIND, CTAG>(dd[k & 1], ad[k & 3], bd[k & 3], id[k & 3], sa[k & 1], sb[k & 1]); };
+        auto generic = [&](int k) {
+            const uint32_t sel = KIND == 4 ? static_cast<uint32_t>(k & 3)
+                                           : (KIND >= 2 ? 0u : static_cast<uint32_t>(k & 1) * 2u);
+            probe_mma<KIND, CTAG>(tmem + ((alt && (k & 1)) ? 128u : 0u), smem_desc(a_s + 32 * (k & 3), 16, 1024, 2),
+                                  smem_desc(b_s + 32 * (k & 3), 16, 1024, 2), idesc | (sel << 4) | (sel << 29),
+                                  sfa_t + 4 * (k & 1), sfb_t + 8 * (k & 1));
+        };
         const long long t0 = clock64();
-        for (int it = 0; it < iters; ++it) {
-            if (with_cp) {
+        // one loop per configuration: code for the options a run does not use
+        // stays out of the loop (a wait the loop merely contains slows it)
+        if (!with_cp && waits == 0 && mmas_per_group == 4) {
+            for (int it = 0; it < iters; ++it) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma(k);
+            }
+        } else if (!with_cp && waits == 0 && mmas_per_group == 8) {
+            for (int it = 0; it < iters; ++it) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma(k);
+            }
+        } else if (waits == 0 && mmas_per_group == 4) {
+            for (int it = 0; it < iters; ++it) {
                 probe_cp<CTAG>(sfa_t + 4 * (it & 1), smem_desc(sf_s + 512, 0, 128, 0));
                 probe_cp<CTAG>(sfb_t + 8 * (it & 1), smem_desc(sf_s + 1024, 0, 128, 0));
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    mma(k);
             }
-            for (int k = 0; k < mmas_per_group; ++k) {
-                // scale selector: two scales per K = 64 step (2X), one per K = 32 step (1X: byte k % 4)
-                const uint32_t sel = KIND == 4 ? static_cast<uint32_t>(k & 3)
-                                               : (KIND >= 2 ? 0u : static_cast<uint32_t>(k & 1) * 2u);
-                const uint32_t d = tmem + ((alt && (k & 1)) ? 128u : 0u);
-                probe_mma<KIND, CTAG>(d, smem_desc(a_s + 32 * (k & 3), 16, 1024, 2),
-                                      smem_desc(b_s + 32 * (k & 3), 16, 1024, 2),
-                                      idesc | (sel << 4) | (sel << 29), sfa_t + 4 * (k & 1), sfb_t + 8 * (k & 1));
-            }
-            if (waits > 0) {
+        } else if (!with_cp && mmas_per_group == 8) {
+            for (int it = 0; it < iters; ++it) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma(k);
                 probe_commit<CTAG>(sink);
                 for (int w = 0; w < waits; ++w)
                     mbar_wait_bounded(done, 0, status, 1u, 1000000000ull);
                 tc_fence_after_sync();
+            }
+        } else {
+            for (int it = 0; it < iters; ++it) {
+                if (with_cp) {
+                    probe_cp<CTAG>(sfa_t + 4 * (it & 1), smem_desc(sf_s + 512, 0, 128, 0));
+                    probe_cp<CTAG>(sfb_t + 8 * (it & 1), smem_desc(sf_s + 1024, 0, 128, 0));
+                }
+                for (int k = 0; k < mmas_per_group; ++k)
+                    generic(k);
+                if (waits > 0) {
+                    probe_commit<CTAG>(sink);
+                    for (int w = 0; w < waits; ++w)
+                        mbar_wait_bounded(done, 0, status, 1u, 1000000000ull);
+                    tc_fence_after_sync();
+                }
             }
         }
         probe_commit<CTAG>(bar);

@@ -69,8 +69,9 @@ def measure(n: int = 256, iters: int = 4000, mmas_per_group: int = 4, with_cp: b
 
 def sweep():
     """Every form at N = 256 on both CTA groupings, plus N = 128 with one and
-    two accumulators (cta_group::1); the decode tile widths N = 16, 32, 64
-    for kind::mxf4 and for the W4A8 form kind::mxf8f6f4 (cta_group::1)."""
+    two accumulators (cta_group::1) and on a pair; the decode tile widths
+    N = 16, 32, 64 for kind::mxf4 and for the W4A8 form kind::mxf8f6f4
+    (cta_group::1)."""
     rows = []
     for kind in (0, 1, 2, 3):
         for ctag in (1, 2):
@@ -82,12 +83,17 @@ def sweep():
     for kind in (0, 4):
         for n in (16, 32, 64) + ((128, 256) if kind == 4 else ()):
             rows.append(measure(n=n, kind=kind, ctag=1))
+    rows.append(measure(n=128, kind=0, ctag=2))
     # operand data, and the issuing thread's own per-stage work (a GEMM stage
     # of 8 MMAs: barrier waits that find their phase complete, one commit)
     for ctag in (1, 2):
         for waits in (0, 1, 2, 3, 4):
             rows.append(measure(n=256, kind=0, ctag=ctag, mmas_per_group=8, iters=2000, waits=waits,
                                 random_operands=True))
+    # narrower MMAs leave a wait exposed
+    for n in (16, 128):
+        for waits in (0, 1):
+            rows.append(measure(n=n, kind=0, ctag=1, mmas_per_group=8, iters=2000, waits=waits, random_operands=True))
     return rows
 
 
