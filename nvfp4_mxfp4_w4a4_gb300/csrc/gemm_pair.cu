@@ -378,6 +378,23 @@ __global__ void __launch_bounds__(512, 1)
                 const uint8_t* sfb0 = p.sfb + T.expert * p.sfb_expert_stride +
                                       static_cast<int64_t>(n0 / 128) * p.kb4 * 512 + lane * 16;
                 const uint8_t* sfb1 = sfb0 + (nsfb > 1 ? static_cast<int64_t>(p.kb4) * 512 : 0);
+                // the weight scales of this tile (first tile only) and of the next
+                // one go to L2 ahead of the stage-by-stage loads, which otherwise find
+                // them in memory one stage before use (both CTAs read the same two B
+                // scale tiles).  Dense problems with many row pairs per column tile
+                // skip it: the pairs then work on a few column tiles at a time, and the
+                // next tile's scales are already being read by the pairs ahead.
+                if (leader && warp == 2 && lane == 0 && (kGrouped || 4 * p.m_pairs <= pairs)) {
+                    if (t == pair)
+                        bulk_prefetch_l2(sfb0, static_cast<uint32_t>(p.kb4) * 512u * static_cast<uint32_t>(nsfb));
+                    if (t + pairs < total_tiles()) {
+                        const PairTile U = pair_tile<kGrouped>(t + pairs, rk, p, tiles_before, pairs_before);
+                        const int un = min(2, p.sfb_tiles - U.n0 / 128);
+                        bulk_prefetch_l2(p.sfb + U.expert * p.sfb_expert_stride +
+                                             static_cast<int64_t>(U.n0 / 128) * p.kb4 * 512,
+                                         static_cast<uint32_t>(p.kb4) * 512u * static_cast<uint32_t>(un));
+                    }
+                }
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = static_cast<int>(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;

@@ -95,6 +95,13 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
+// Asks L2 to fetch `bytes` (a multiple of 16) from global memory starting at
+// the 16-byte aligned `p`; nothing is written and nothing waits for it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // 2-D tiled load of one box into shared memory; completion is signalled as
 // transaction bytes on `bar`.  c0 is the innermost coordinate (bytes here).
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0,
