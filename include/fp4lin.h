@@ -556,7 +556,7 @@ FP4LIN_API fp4_status fp4_linear_grouped(const void* x_bf16, const int32_t* row_
  *                synchronization is needed
  *   out          [total_M, N] bf16
  * Same shape and alignment rules as fp4_gemm_mxfp4, and 1 <= E <= 1024
- * (FP4_ERR_SHAPE otherwise).  Large problems with E <= 233 run on CTA pairs
+ * (FP4_ERR_SHAPE otherwise).  Large problems with E <= 239 run on CTA pairs
  * (256 x 256 tiles of one expert), the rest on single CTAs.                 */
 FP4LIN_API fp4_status fp4_gemm_mxfp4_grouped(const uint8_t* a, const uint8_t* sa, const uint8_t* b,
                                   const uint8_t* sb, const void* bias_bf16, void* out_bf16,

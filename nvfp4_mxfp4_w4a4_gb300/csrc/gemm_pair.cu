@@ -97,13 +97,16 @@ struct PairParams {
     unsigned int* status;
 };
 
-template <int KC, int STAGES>
+// EPI_BUFS: store boxes each epilogue warp may have in flight (staging
+// buffers of one box each).
+template <int KC, int STAGES, int EPI_BUFS = 1>
 struct PairCfg {
     static constexpr int GROUPS = 2 * KC;  // 128-element groups of K per stage
     static constexpr int A_BYTES = kRows * kSlab * KC;
     static constexpr int B_BYTES = kRows * kSlab * KC;
     static constexpr int CHUNK = 64;  // output columns per store box (128-byte rows)
-    static constexpr int EPI_WARP_BYTES = 32 * CHUNK * 2;
+    static constexpr int EPI_BOX_BYTES = 32 * CHUNK * 2;
+    static constexpr int EPI_WARP_BYTES = EPI_BUFS * EPI_BOX_BYTES;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
@@ -180,12 +183,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int KC, int STAGES, bool kGrouped>
+template <int KC, int STAGES, bool kGrouped, int EPI_BUFS = 1>
 __global__ void __launch_bounds__(512, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmO, const PairParams p)
 {
-    using C = PairCfg<KC, STAGES>;
+    using C = PairCfg<KC, STAGES, EPI_BUFS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // leader: A and B of both CTAs landed and the scales are in both CTAs' TMEM
@@ -439,11 +442,10 @@ __global__ void __launch_bounds__(512, 1)
         constexpr int CW = kTileN / 2;  // accumulator columns per warp
         constexpr int kChunk = C::CHUNK;
         const uint32_t accum_empty_leader = mapa_shared(smem_u32(accum_empty), 0);
-        uint8_t* stg = smem + C::OFF_EPI + ew * C::EPI_WARP_BYTES;
-        uint8_t* my_row = stg + lane * (kChunk * 2);
+        uint8_t* stg0 = smem + C::OFF_EPI + ew * C::EPI_WARP_BYTES;
         const int rot = lane & 7;  // 128-byte swizzle of the store box: 16-byte piece q of row i at q ^ (i % 8)
         uint32_t tcount = 0;
-        bool stored = false;
+        uint32_t boxes = 0;  // store boxes this warp has issued
         for (int t = pair; t < total_tiles(); t += pairs) {
             const PairTile T = pair_tile<kGrouped>(t, rk, p, tiles_before, pairs_before);
             const int n0 = T.n0;
@@ -472,9 +474,13 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
             for (int c = 0; c < CW; c += kChunk) {
                 const int col0 = n0 + half * CW + c;
+                // staging buffers in turn; the store that last used this one
+                // (EPI_BUFS boxes ago) must have read it
+                uint8_t* stg = stg0 + (boxes % EPI_BUFS) * C::EPI_BOX_BYTES;
+                uint8_t* my_row = stg + lane * (kChunk * 2);
                 if (whole) {
-                    if (lane == 0 && stored)
-                        bulk_wait_group_read0();  // the previous box has left the staging area
+                    if (lane == 0 && boxes >= EPI_BUFS)
+                        bulk_wait_group_read<EPI_BUFS - 1>();
                     __syncwarp();
                 }
 #pragma unroll
@@ -505,13 +511,13 @@ __global__ void __launch_bounds__(512, 1)
                     if (lane == 0) {
                         tma_store_2d(&tmO, stg, col0, row0);
                         bulk_commit_group();
-                        stored = true;
                     }
+                    ++boxes;
                 }
             }
         }
-        if (stored)
-            bulk_wait_group_read0();  // shared memory stays valid until the last store has read it
+        if (boxes > 0)
+            bulk_wait_group_read<0>();  // shared memory stays valid until the last store has read it
     }
 
     // both CTAs are done with the pair's barriers, shared memory and TMEM
@@ -524,10 +530,10 @@ __global__ void __launch_bounds__(512, 1)
     }
 }
 
-template <int KC, int STAGES, bool kGrouped>
+template <int KC, int STAGES, bool kGrouped, int EPI_BUFS = 1>
 cudaError_t launch_pair(const GemmArgs& a, cudaStream_t stream)
 {
-    using C = PairCfg<KC, STAGES>;
+    using C = PairCfg<KC, STAGES, EPI_BUFS>;
     const int E = kGrouped ? a.E : 1;
     if (kGrouped && E > C::MAX_E)
         return cudaErrorInvalidValue;
@@ -559,7 +565,7 @@ cudaError_t launch_pair(const GemmArgs& a, cudaStream_t stream)
     const int64_t total = static_cast<int64_t>(p.m_pairs + (kGrouped ? E : 0)) * p.n_tiles;
     if (total == 0)
         return cudaSuccess;
-    auto kern = gemm_pair_kernel<KC, STAGES, kGrouped>;
+    auto kern = gemm_pair_kernel<KC, STAGES, kGrouped, EPI_BUFS>;
     // grouped: the shared-memory opt-in covers the prefixes of MAX_E experts
     constexpr int kSmemMax = C::SMEM + (kGrouped ? 8 * (C::MAX_E + 1) : 0);
     const int smem = C::SMEM + (kGrouped ? 8 * (E + 1) : 0);
@@ -632,14 +638,20 @@ cudaError_t launch_gemm_pair(const GemmArgs& a, cudaStream_t stream)
 {
     // stages of two slabs need the 3-D operand view (K % 256 == 0)
     const bool kc2 = FP4_PAIR_KC == 2 && a.K % 256 == 0;
-    if (a.row_offsets != nullptr)
+    if (a.row_offsets != nullptr) {
+        // short K (at most two stages a tile, as in an MoE down projection): the
+        // epilogue's stores, not the operand ring, pace the tiles, so two of the
+        // three stages' shared memory go to a second store box per epilogue warp
+        if (kc2 && a.K <= 1024)
+            return launch_pair<2, 2, true, 2>(a, stream);
         return kc2 ? launch_pair<2, 3, true>(a, stream) : launch_pair<1, 6, true>(a, stream);
+    }
     return kc2 ? launch_pair<2, 3, false>(a, stream) : launch_pair<1, 6, false>(a, stream);
 }
 
 int gemm_pair_max_experts()
 {
-    return std::min(PairCfg<2, 3>::MAX_E, PairCfg<1, 6>::MAX_E);
+    return std::min(std::min(PairCfg<2, 3>::MAX_E, PairCfg<1, 6>::MAX_E), PairCfg<2, 2, 2>::MAX_E);
 }
 
 }  // namespace fp4lin

@@ -147,6 +147,13 @@ __device__ __forceinline__ void bulk_wait_group_read0()
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// At most N committed bulk groups of this thread may still be reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
 // Waits until every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_group0()
 {
