@@ -31,7 +31,11 @@
 //               loads count on the LEADER's full barrier;
 //   warp 1      TMEM: allocated and freed by both CTAs together; in the
 //               leader CTA (even rank) lane 0 issues the pair's MMAs, then a
-//               multicast commit frees the stage in both CTAs;
+//               multicast commit frees the stage in both CTAs.  This thread's
+//               own instructions pace the tensor pipe (a barrier wait costs
+//               it a few hundred cycles even when the phase is complete), so
+//               it waits once per stage and forms descriptors from
+//               precomputed bases;
 //   warps 2-5   scale writers: each loads the stage's scale chunks (its A rows'
 //               tile and both 128-row B tiles: each CTA's TMEM needs the
 //               scales of all 256 B rows) from global memory into registers
@@ -39,11 +43,17 @@
 //               free, writes them into its quarter of the TMEM lanes with
 //               tcgen05.st (the layout a 32x128b.warpx4 copy would produce)
 //               and arrives on the leader's full barrier of the stage, so
-//               that the MMA thread waits once per stage;
+//               that the MMA thread waits once per stage; the leader's warp 2
+//               also asks L2 for the next tile's weight scales;
 //   warp 7      idle (it completes the 8-warp low-register half);
 //   warps 8-15  epilogue of the CTA's 128 rows: read the accumulator, release
 //               it (arrive on the leader's accum_empty) so the next tile's
-//               MMAs start, add bias, round to bf16, TMA-store 32 x 64 boxes.
+//               MMAs start, add bias, round to bf16, TMA-store 32 x 64 boxes
+//               (one or two in flight per warp).
+// Configurations: two-slab stages (K % 256 == 0) in a ring of three, or of
+// two with two store boxes in flight per epilogue warp for grouped problems
+// with K <= 1024 (their tiles are paced by the stores); one-slab stages in a
+// ring of six otherwise.
 // Every wait is bounded; on expiry the kernel records a timeout in the status
 // word and winds down.
 //
