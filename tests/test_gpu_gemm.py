@@ -167,6 +167,10 @@ def test_grouped_gemm(orc, L, counts, N, K, with_bias):
 @pytest.mark.parametrize("counts,N,K,with_bias", [
     ([300, 0, 1, 257, 1000, 129, 640, 0, 77, 512], 2048, 512, True),
     ([256, 130, 513, 0, 700, 1200, 300], 1544, 384, False),
+    # K = 1024: two stages a tile with two store boxes in flight per epilogue warp
+    ([513, 0, 255, 384, 1, 900, 256], 2304, 1024, True),
+    # K = 1280: three-stage ring, the tile's last stage half full
+    ([640, 300, 0, 129, 1000], 2048, 1280, False),
 ])
 def test_grouped_gemm_on_cta_pairs(orc, L, counts, N, K, with_bias):
     """Grouped problems large enough for the CTA-pair path (256 x 256 tiles
@@ -174,7 +178,8 @@ def test_grouped_gemm_on_cta_pairs(orc, L, counts, N, K, with_bias):
     (the second CTA of the last pair tile lies past the expert), a one-row
     expert, empty experts, row counts that end inside a 32-row store box
     (stored row by row), a ragged last column tile, one- and two-slab
-    stages; every row compared."""
+    stages, the short-K configuration and a partial last stage; every row
+    compared."""
     E = len(counts)
     m_tiles = (sum(counts) + E * 127) // 128
     assert N >= 256 and m_tiles * (-(-N // 256)) >= 148, "shape must take the pair path"
