@@ -43,8 +43,9 @@
 //               free, writes them into its quarter of the TMEM lanes with
 //               tcgen05.st (the layout a 32x128b.warpx4 copy would produce)
 //               and arrives on the leader's full barrier of the stage, so
-//               that the MMA thread waits once per stage; the leader's warp 2
-//               also asks L2 for the next tile's weight scales;
+//               that the MMA thread waits once per stage; warp 2 also asks
+//               L2 for the next tile's scales (the leader's: the weight
+//               scales; grouped: each CTA's activation scales);
 //   warp 7      idle (it completes the 8-warp low-register half);
 //   warps 8-15  epilogue of the CTA's 128 rows: read the accumulator, release
 //               it (arrive on the leader's accum_empty) so the next tile's
@@ -397,15 +398,23 @@ __global__ void __launch_bounds__(512, 1)
                 // scale tiles).  Dense problems with many row pairs per column tile
                 // skip it: the pairs then work on a few column tiles at a time, and the
                 // next tile's scales are already being read by the pairs ahead.
-                if (leader && warp == 2 && lane == 0 && (kGrouped || 4 * p.m_pairs <= pairs)) {
-                    if (t == pair)
-                        bulk_prefetch_l2(sfb0, static_cast<uint32_t>(p.kb4) * 512u * static_cast<uint32_t>(nsfb));
+                if (warp == 2 && lane == 0 && (kGrouped || 4 * p.m_pairs <= pairs)) {
+                    const uint32_t tile_bytes = static_cast<uint32_t>(p.kb4) * 512u;
+                    if (leader && t == pair)
+                        bulk_prefetch_l2(sfb0, tile_bytes * static_cast<uint32_t>(nsfb));
                     if (t + pairs < total_tiles()) {
                         const PairTile U = pair_tile<kGrouped>(t + pairs, rk, p, tiles_before, pairs_before);
-                        const int un = min(2, p.sfb_tiles - U.n0 / 128);
-                        bulk_prefetch_l2(p.sfb + U.expert * p.sfb_expert_stride +
-                                             static_cast<int64_t>(U.n0 / 128) * p.kb4 * 512,
-                                         static_cast<uint32_t>(p.kb4) * 512u * static_cast<uint32_t>(un));
+                        if (leader) {
+                            const int un = min(2, p.sfb_tiles - U.n0 / 128);
+                            bulk_prefetch_l2(p.sfb + U.expert * p.sfb_expert_stride +
+                                                 static_cast<int64_t>(U.n0 / 128) * p.kb4 * 512,
+                                             tile_bytes * static_cast<uint32_t>(un));
+                        }
+                        // grouped: each CTA's own activation scale tile too (the
+                        // weights streaming through L2 have evicted it since the
+                        // activation quantizer wrote it)
+                        if (kGrouped && U.rows_valid > 0)
+                            bulk_prefetch_l2(p.sfa + static_cast<int64_t>(U.sfa_rt) * p.kb4 * 512, tile_bytes);
                     }
                 }
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
