@@ -96,10 +96,15 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map)
 }
 
 // Asks L2 to fetch `bytes` (a multiple of 16) from global memory starting at
-// the 16-byte aligned `p`; nothing is written and nothing waits for it.
+// the 16-byte aligned `p`, in requests of at most 32 KB; nothing is written
+// and nothing waits for it.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes)
 {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+    const char* c = static_cast<const char*>(p);
+    for (uint32_t off = 0; off < bytes; off += 32768u) {
+        const uint32_t n = bytes - off < 32768u ? bytes - off : 32768u;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + off), "r"(n) : "memory");
+    }
 }
 
 // 2-D tiled load of one box into shared memory; completion is signalled as

@@ -76,6 +76,23 @@ def test_pair_gemm_random_codes_nonuniform_scales(orc, L, M, N, K):
     assert ok, f"max err/bound = {ratio}"
 
 
+def test_pair_gemm_long_k(orc, L):
+    """K = 16384: 32 stages a tile, and the scale tiles prefetched into L2
+    for the next tile (128 KB) go out as several requests."""
+    M, N, K = 1024, 4864, 16384
+    assert _takes_pair_path(M, N)
+    rng = np.random.default_rng(7)
+    a = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    b = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    sa = rng.integers(116, 138, (M, K // 32), dtype=np.uint8)
+    sb = rng.integers(116, 138, (N, K // 32), dtype=np.uint8)
+    out = _run(L, a, orc.sf_swizzle(sa), b, orc.sf_swizzle(sb), None, M, N, K)
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, M - 1], rng.choice(M, 48, replace=False)]))
+    ref, absum = orc.gemm(a, sa, b, sb, rows=rows, threads=THREADS)
+    ok, ratio = gemm_check(out[rows], ref, absum)
+    assert ok, f"max err/bound = {ratio}"
+
+
 def test_pair_gemm_one_hot_is_exact(orc, L):
     """B rows one-hot with code 1.0 under scale 2^0: out[:, n] = A[:, sel[n]]
     exactly, for every row of both CTAs of every pair and every column."""
