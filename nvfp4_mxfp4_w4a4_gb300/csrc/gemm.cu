@@ -22,7 +22,12 @@
 //   warp 1      TMEM owner and MMA issuer: per stage, 4 * KC tcgen05.mma
 //               kind::mxf4 (K = 64, two E8M0 scales per row each) accumulate
 //               into a 128 x BN fp32 TMEM tile; tcgen05.commit frees the
-//               stage, and at the end of a tile signals the epilogue.
+//               stage, and at the end of a tile signals the epilogue.  This
+//               thread's own instructions pace the narrow decode MMAs (a
+//               barrier wait costs it a few hundred cycles even when the
+//               phase is complete), so it waits once per stage, on the scale
+//               movers' barrier (they copy only after the stage has landed),
+//               and forms descriptors from precomputed bases.
 //   CPW warps   scale movers (warps 2 .. 1+CPW; 4, or 2 where the epilogue
 //               needs the registers): per stage, tcgen05.cp of the scale
 //               chunks from smem into that stage's TMEM scale columns, split
